@@ -1,0 +1,415 @@
+"""Benchmark of the ZeRO-1 local-shard optimizer step on one GB300 (or N, one rank per GPU).
+
+One "step" is the whole hot path over one batch of synthetic gradients:
+  K x zero1_accumulate (bf16 micro-batch gradient -> fp32 grad), zero1_grad_norm,
+  zero1_step (clip + AdamW on fp32 master/m/v + bf16 weight copy).
+Default workload: the Llama-3.1-8B-shaped parameter list sharded over dp=8, rank 0
+(1,003,782,656 local parameters, K=1).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the scalar CPU oracle on this host's cores instead (the
+reference arm); it is a deliberately slow program, reported for context.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "AdamW shard-step params/sec and HBM GB/s (fraction of GB300 peak), 1 GPU"
+STEP_BYTES_PER_ELEM = 30          # adamw_step: grad 4 R, master/m/v 12 R + 12 W, bf16 2 W
+NORM_BYTES_PER_ELEM = 4           # grad_norm: grad 4 R
+
+
+def accumulate_bytes_per_elem(k):
+    # first micro-batch overwrites (2 R + 4 W); each further one is 2 + 4 R + 4 W
+    return 6 + 10 * (k - 1)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profile_traffic(kernel_src, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None if it is
+    missing or was taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "adamw_step_%s.md" % workload)
+    src = os.path.join(ROOT, "zero_sharded_mixed_local_gb300", "csrc", kernel_src)
+    try:
+        text = open(path, encoding="utf-8").read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != digest:
+        return None
+    try:
+        return int(float(fields["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU (oracle)
+def oracle_sample_step(master, m, v, micros, no_decay_split, hp, t):
+    """One oracle step over host arrays (the sample), returning seconds."""
+    import oracle
+    n = master.size
+    grad = np.zeros(n, np.float32)
+    t0 = time.perf_counter()
+    oracle.accumulate_all(grad, micros)
+    s = oracle.sumsq(grad)
+    ok, norm, coef = oracle.clip_coef(s, hp["clip_grad"])
+    oracle.adamw(master, m, v, grad, [no_decay_split, n - no_decay_split], [0, 1], hp, t, coef,
+                 w=np.zeros(n, np.uint16))
+    return time.perf_counter() - t0
+
+
+def host_sample(w, n_sample, seed=0):
+    """A bounded host sample of the workload: n_sample elements drawn like its decayed
+    tensors (master N(0, 0.02), K bf16 gradients N(0, sigma^2), m = v = 0)."""
+    g = torch.Generator().manual_seed(seed)
+    master = (torch.randn(n_sample, generator=g) * 0.02).numpy()
+    micros = [(torch.randn(n_sample, generator=g) * w.grad_sigma).to(torch.bfloat16).view(torch.int16)
+              .numpy().view(np.uint16) for _ in range(w.micro_batches)]
+    return master, np.zeros(n_sample, np.float32), np.zeros(n_sample, np.float32), micros
+
+
+def cpu_baseline(w, target_s=10.0, max_elems=None):
+    """Time the oracle as it stands on a bounded sample sized for about target_s seconds."""
+    probe = 1 << 21
+    m_, mm, vv, mic = host_sample(w, probe)
+    dt = oracle_sample_step(m_, mm, vv, mic, probe, w.hp, 1)
+    per_elem = dt / probe
+    n = int(min(max(probe, target_s / max(per_elem, 1e-12)), max_elems or (1 << 28)))
+    n = n // 8 * 8
+    m_, mm, vv, mic = host_sample(w, n, seed=1)
+    dt = oracle_sample_step(m_, mm, vv, mic, n, w.hp, 1)
+    return {"value": n / dt, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": "%d elements drawn like the workload's decayed tensors, one full step (K=%d accumulate, "
+                      "norm, AdamW + bf16 copy), single-threaded scalar C, %.1f s" % (n, w.micro_batches, dt),
+            "seconds": dt, "elements": n}
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    probe = 1 << 20
+    m_, mm, vv, mic = host_sample(w, probe)
+    per_elem = oracle_sample_step(m_, mm, vv, mic, probe, w.hp, 1) / probe
+    # each step a bounded sample, sized so the whole run stays within a few minutes
+    budget_s = 150.0 / max(1, args.steps + args.warmup)
+    n = max(probe, min(int(budget_s / max(per_elem, 1e-12)), 1 << 27)) // 8 * 8
+    m_, mm, vv, mic = host_sample(w, n, seed=1)
+    for t in range(1, args.warmup + 1):
+        oracle_sample_step(m_, mm, vv, mic, n, w.hp, t)
+    times = [oracle_sample_step(m_, mm, vv, mic, n, w.hp, args.warmup + t) for t in range(1, args.steps + 1)]
+    sec = sum(times) / len(times)
+    value = n / sec
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.description, "sample_elements": n, "micro_batches": w.micro_batches},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d elements drawn like the workload's decayed tensors, per step" % n},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ GPU
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+
+    from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout, get_workload
+    w = get_workload(args.workload)
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+
+    import zero_sharded_mixed_local_gb300 as z
+
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    z.load_library()
+
+    # With N ranks each simulates a different data-parallel shard of the same model.
+    dp_rank = (w.dp_rank + rank) % w.dp_size if world > 1 else w.dp_rank
+    plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, dp_rank)
+    L = plan.layout()
+    gen = InputGenerator(w, Layout(L.counts, L.offsets, L.no_decay, L.arena_numel), dev, seed=w.seed + rank)
+    P = plan.local_numel
+    K = w.micro_batches
+    master = gen.master()
+    m, v, grad = gen.zeros(), gen.zeros(), gen.zeros()
+    wbf = gen.zeros(torch.bfloat16)
+    micros = gen.micro_grads()
+    ws, nout = plan.new_workspace(dev), z.new_norm_out(dev)
+    hp = z.Hparams(**w.hp)
+    group = None
+    if world > 1:
+        import torch.distributed as dist
+        group = dist.group.WORLD
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    t_counter = [0]
+
+    def one_step(record=None):
+        t_counter[0] += 1
+        if record is not None:
+            record["a0"].record(stream)
+        for k in range(K):
+            z.accumulate(plan, grad, micros[k], overwrite_first=(k == 0), stream=stream)
+        if record is not None:
+            record["n0"].record(stream)
+        z.grad_norm(plan, grad, ws, nout, 0.0, stream=stream)
+        if group is not None:
+            z.allreduce_sumsq_(nout, group)
+        if record is not None:
+            record["s0"].record(stream)
+        z.step(plan, master, m, v, grad, wbf, hp, t_counter[0], nout, stream=stream)
+        if record is not None:
+            record["s1"].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    visible = [d for d in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if d.strip()]
+    clocks = ClockSampler(visible[local].strip() if local < len(visible) else local)  # index or UUID
+    clocks.start()
+    recs = [{k: ev() for k in ("a0", "n0", "s0", "s1")} for _ in range(args.steps)]
+    start, end = ev(), ev()
+    torch.cuda.synchronize()
+    barrier(world)
+    start.record(stream)
+    for i in range(args.steps):
+        one_step(recs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    acc_ms = statistics.mean(r["a0"].elapsed_time(r["n0"]) for r in recs)
+    norm_ms = statistics.mean(r["n0"].elapsed_time(r["s0"]) for r in recs)
+    step_ms = statistics.mean(r["s0"].elapsed_time(r["s1"]) for r in recs)
+    z.read_norm(nout, stream)
+
+    peak, peak_kind = measured_peaks()
+    step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9
+    path_bytes = (accumulate_bytes_per_elem(K) + NORM_BYTES_PER_ELEM + STEP_BYTES_PER_ELEM) * P
+    traffic = profile_traffic("adamw_step.cu", args.workload)
+
+    # ---- end to end through the public API: pinned host gradients in, norm record out
+    e2e = None
+    if not args.no_e2e:
+        host_micros = [mb.cpu().pin_memory() for mb in micros]
+        dev_micros = [torch.empty_like(mb) for mb in micros]
+        opt_t = [t_counter[0]]
+
+        def e2e_step():
+            for k in range(K):
+                dev_micros[k].copy_(host_micros[k], non_blocking=True)
+                z.accumulate(plan, grad, dev_micros[k], overwrite_first=(k == 0), stream=stream)
+            z.grad_norm(plan, grad, ws, nout, 0.0, stream=stream)
+            if group is not None:
+                z.allreduce_sumsq_(nout, group)
+            opt_t[0] += 1
+            z.step(plan, master, m, v, grad, wbf, hp, opt_t[0], nout, stream=stream)
+            return z.read_norm(nout, stream)  # device -> host read of the step's result, synchronising
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+        e2e = {"value": world * P / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": sum(mb.numel() * mb.element_size() for mb in micros),
+               "d2h_bytes_per_step": z.NORM_OUT_BYTES}
+        del host_micros, dev_micros
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_baseline_seconds)
+        cpu.pop("seconds", None)
+        cpu.pop("elements", None)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC,
+            "value": world * P / (ms_step * 1e-3),
+            "unit": "params/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": w.description,
+                "local_params_per_gpu": P,
+                "arena_elems": plan.arena_numel,
+                "micro_batches": K,
+                "dp_size": w.dp_size,
+                "dp_rank": dp_rank,
+                "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
+                "l2": "no flush: each step streams %.1f GB, far above the 129 MB L2" % (path_bytes / 1e9),
+            },
+            "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
+            "kernels": {
+                "accumulate": {"ms": acc_ms, "gbs": accumulate_bytes_per_elem(K) * P / (acc_ms * 1e-3) / 1e9,
+                               "launches_per_step": K},
+                "grad_norm": {"ms": norm_ms, "gbs": NORM_BYTES_PER_ELEM * P / (norm_ms * 1e-3) / 1e9,
+                              "launches_per_step": 2},
+                "adamw_step": {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
+            },
+            "roofline": {"bound": "hbm", "kernel": "adamw_step_kernel", "achieved": step_gbs, "peak": peak,
+                         "unit": "GB/s", "frac": step_gbs / peak, "traffic": traffic,
+                         "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
+                         "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "gpu_launches": args.steps * (K + 3),
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

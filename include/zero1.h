@@ -1,0 +1,231 @@
+/*
+ * zero1.h -- C ABI of the ZeRO-1 local-shard optimizer step for GB300 (sm_103a).
+ *
+ * One data-parallel rank's step under ZeRO-1 mixed precision, as the pages
+ * describe it ("ZeRO-1 风格的 Distributed Optimizer", sections 6.2-6.3 and
+ * 6.7; "Nanotron Guide: Minimalist 3D-Parallelism LLM Training", "Memory &
+ * Optimization", item 1; "Distributed Training", sections 0, 2 and 3):
+ *
+ *   1. zero1_accumulate  add K bf16 micro-batch gradients into an fp32 grad buffer
+ *   2. zero1_grad_norm   global L2 norm of the accumulated gradient (for clip_grad)
+ *   3. zero1_step        AdamW on the fp32 master / m / v shard, clip applied on
+ *                        the fly, and the bf16 weight copy the all-gather ships
+ *
+ * preceded once by zero1_plan_create, which cuts every parameter tensor by
+ * numel into dp_size contiguous shards and lays the local shards out in one
+ * flat "arena" per quantity.
+ *
+ * Conventions (all entry points):
+ *   - Plain pointers and sizes only.  Device pointers are CUDA global-memory
+ *     addresses on the current device; host pointers are ordinary memory.
+ *   - The caller allocates and owns every device buffer (grad, master, m, v,
+ *     bf16 copy, micro-batch gradients, norm workspace, norm output).  The
+ *     library allocates no device memory and keeps no pointer after a call
+ *     returns.  A plan owns only host memory.
+ *   - Every device buffer must start on a 16-byte boundary (ZERO1_EALIGN).
+ *   - Compute calls are asynchronous on the given stream (a cudaStream_t
+ *     passed as void*; NULL is the legacy default stream).  They launch
+ *     kernels and return; nothing synchronises except zero1_read_norm.
+ *   - Return value: ZERO1_OK (0) or a negative ZERO1_E* code.  Argument errors
+ *     are detected before any launch and leave every buffer untouched.  No
+ *     call aborts the process, traps or waits on the GPU.
+ *   - Thread safety: a plan is read-only after creation and may be shared by
+ *     threads; buffers may not be shared by concurrent calls.
+ */
+#ifndef ZERO1_H
+#define ZERO1_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define ZERO1_OK 0
+#define ZERO1_EINVAL (-1)     /* null pointer, bad size, rank >= dp_size, t < 1, ... */
+#define ZERO1_EALIGN (-2)     /* a buffer is not 16-byte aligned */
+#define ZERO1_ECUDA (-3)      /* a CUDA call or launch failed; see zero1_last_cuda_error() */
+#define ZERO1_ENONFINITE (-4) /* device status: the gradient norm is inf or NaN */
+#define ZERO1_ENOMEM (-5)     /* host allocation failed while building a plan */
+
+/* Each shard starts on a multiple of this many elements inside an arena, so
+ * that 16-byte vector loads of bf16 (8 elements) never straddle tensors. */
+#define ZERO1_ARENA_ALIGN 8
+/* Tensors are grouped by weight-decay class; group 0 is decayed, group 1 is
+ * excluded from weight decay. */
+#define ZERO1_NUM_GROUPS 2
+/* Most micro-batch gradients one zero1_accumulate call accepts. */
+#define ZERO1_MAX_MICRO 16
+
+typedef struct zero1_plan zero1_plan; /* opaque, host memory only */
+
+/* AdamW hyper-parameters ("ZeRO-1 风格的 Distributed Optimizer", section 6.6:
+ * adam_beta1 0.9, adam_beta2 0.95, adam_eps 1e-8, weight_decay 0.1,
+ * clip_grad 1.0).  Doubles, so decimal settings arrive unrounded; the library
+ * derives the fp32 step scalars once per call.  clip_grad <= 0 disables
+ * clipping. */
+typedef struct zero1_hparams {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;
+    double clip_grad;
+} zero1_hparams;
+
+/* Result of zero1_grad_norm.  Lives in DEVICE memory (24 bytes; 16-byte
+ * alignment is required as for every buffer).  zero1_step reads `sumsq` and
+ * `status` and derives the norm itself, so with several data-parallel ranks
+ * the caller may all-reduce (sum) the `sumsq` double in place between
+ * zero1_grad_norm and zero1_step: that one scalar is the only exchange the
+ * step needs, and a non-finite sum on any rank makes every rank skip. */
+typedef struct zero1_norm_out {
+    double sumsq;     /* local sum of squares + extra_sumsq */
+    double norm;      /* sqrt(sumsq) */
+    int32_t status;   /* ZERO1_OK, or ZERO1_ENONFINITE if sumsq is inf/NaN */
+    int32_t n_partials; /* number of per-tile partial sums that were reduced */
+} zero1_norm_out;
+
+/* ---- plan (host only; no CUDA call) ------------------------------------- */
+
+/* Build the shard plan of rank dp_rank out of dp_size.
+ * "ZeRO-1 风格的 Distributed Optimizer", section 6.3: each parameter is cut on
+ * its own, its total numel split evenly over the dp_size ranks (not one
+ * flattened blob).  Remainder rule (not stated on the page): shards are
+ * contiguous in rank order and the first (numel mod dp_size) ranks get one
+ * extra element, so a tensor with fewer than dp_size elements leaves some
+ * ranks with an empty shard.
+ *   numels[n_tensors]   total elements of each parameter tensor (>= 0), in
+ *                       model order
+ *   no_decay[n_tensors] 1 = excluded from weight decay (norm weights), else 0
+ *   out                 receives the plan; free it with zero1_plan_destroy
+ * Arena layout: the decayed tensors' shards first, then the excluded ones,
+ * each group in model order; every shard starts on a multiple of
+ * ZERO1_ARENA_ALIGN elements.  Arena buffers hold zero1_plan_arena_numel()
+ * elements; the padding elements between shards must be zero when the
+ * buffers are created and the library keeps them zero.
+ * Errors: ZERO1_EINVAL (n_tensors < 0, dp_size < 1, dp_rank outside
+ * [0, dp_size), a negative numel, a no_decay value other than 0/1, a null
+ * pointer with n_tensors > 0, out == NULL), ZERO1_ENOMEM. */
+int zero1_plan_create(const int64_t* numels, const uint8_t* no_decay, int32_t n_tensors,
+                      int32_t dp_size, int32_t dp_rank, zero1_plan** out);
+
+/* Free a plan (NULL is ignored). */
+void zero1_plan_destroy(zero1_plan* plan);
+
+/* Plan queries; on a NULL plan they return -1. */
+int32_t zero1_plan_num_tensors(const zero1_plan* plan);
+int64_t zero1_plan_total_numel(const zero1_plan* plan); /* sum of numels, all ranks */
+int64_t zero1_plan_local_numel(const zero1_plan* plan); /* sum of this rank's shards */
+int64_t zero1_plan_arena_numel(const zero1_plan* plan); /* padded arena length */
+
+/* Tensor i's shard: elements [shard_start, shard_start + shard_numel) of the
+ * flattened tensor, stored at arena[arena_offset ...].  Any output pointer
+ * may be NULL.  ZERO1_EINVAL if plan is NULL or i is out of range. */
+int zero1_plan_tensor(const zero1_plan* plan, int32_t i, int64_t* shard_start,
+                      int64_t* shard_numel, int64_t* arena_offset);
+
+/* Arena element range [begin, end) of weight-decay group g (0 or 1). */
+int zero1_plan_group_range(const zero1_plan* plan, int32_t g, int64_t* begin, int64_t* end);
+
+/* Bytes one rank holds under ZeRO-1 mixed precision ("Distributed Training",
+ * section 0: 2 + 2 + 12 = 16 bytes per parameter; "ZeRO-1 风格的 Distributed
+ * Optimizer", sections 6.1 and 6.3: only the 12 bytes of fp32 master, m and v
+ * are sharded, the bf16 weights and gradients stay whole).
+ *   grad_bytes  2 (bf16 gradient, the 16-byte count) or 4 (fp32 gradient,
+ *               the 18-byte itemisation of the Nanotron guide)
+ *   out[4]      {bf16 weights, gradients, optimizer state of the local shard,
+ *               total}, in bytes */
+int zero1_plan_bytes(const zero1_plan* plan, int32_t grad_bytes, int64_t out[4]);
+
+/* Device workspace zero1_grad_norm needs (one double per 16384-element tile
+ * of the arena); 0 for an empty arena. */
+size_t zero1_workspace_bytes(const zero1_plan* plan);
+
+/* ---- compute (asynchronous on `stream`) ---------------------------------- */
+
+/* Gradient accumulation ("ZeRO-1 风格的 Distributed Optimizer", section 6.7:
+ * micro-batch gradients are added into .grad before the data-parallel
+ * reduction and the optimizer step; "Distributed Training", section 2; the
+ * Nanotron config's accumulate_grad_in_fp32).  Element-wise over the arena:
+ *     grad = bf16->fp32(micro[0])            if overwrite_first
+ *     grad = grad + bf16->fp32(micro[k])     for the other k, in order
+ * every addition a single fp32 rounding; a plain sum (no 1/K).
+ *   grad          device fp32 arena (arena_numel), read and written
+ *   micro_bf16    HOST array of n_micro DEVICE pointers to bf16 arenas (raw
+ *                 bits as uint16), read only
+ *   n_micro       1 .. ZERO1_MAX_MICRO
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_accumulate(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
+                     int32_t n_micro, int32_t overwrite_first, void* stream);
+
+/* Global gradient L2 norm for clipping ("ZeRO-1 风格的 Distributed
+ * Optimizer", section 6.6, clip_grad).  sumsq = sum over the arena of grad^2
+ * (padding adds 0) + extra_sumsq, where extra_sumsq is the other ranks' share
+ * of the global sum (0 when this rank is alone); norm = sqrt(sumsq), in
+ * double.  Per 16384-element tile each thread sums the squares of its (at
+ * most 64) elements in compensated fp32 (the rounding errors of every square
+ * and every addition are carried in a second float), and the thread and tile
+ * sums are added in double, in a fixed order: the result is within a few
+ * double ulps of the exact sum, deterministic, and independent of launch
+ * shape.
+ *   grad        device fp32 arena, read only
+ *   workspace   device scratch of zero1_workspace_bytes(plan) bytes
+ *               (may be NULL when that is 0); contents are overwritten
+ *   d_out       device zero1_norm_out, written (status ZERO1_ENONFINITE if
+ *               the sum is inf or NaN)
+ * Errors: ZERO1_EINVAL (workspace_bytes too small, ...), ZERO1_EALIGN,
+ * ZERO1_ECUDA. */
+int zero1_grad_norm(const zero1_plan* plan, const float* grad, double extra_sumsq,
+                    void* workspace, size_t workspace_bytes, zero1_norm_out* d_out, void* stream);
+
+/* Fused clip + AdamW + bf16 copy over the local shard ("ZeRO-1 风格的
+ * Distributed Optimizer", sections 6.2-6.3: each rank updates only its own
+ * fp32 master / m / v and then all-gathers the updated bf16 weights; section
+ * 6.6 for the hyper-parameters).  Decoupled weight decay applied to p before
+ * the bias-corrected Adam update, eps outside the square root:
+ *     coef = clip/(norm+1e-6) if that is < 1 and clip > 0, else 1
+ *     g = grad*coef;  p = p*dfac;  m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
+ *     d = sqrt(v)/sqrt(1-b2^t) + eps;  p = p - lr/(1-b1^t) * (m/d);  w = bf16_rne(p)
+ * with dfac = 1 - lr*weight_decay for group 0 and 1 for group 1; each fp32
+ * operation is rounded once (IEEE divide and square root), the step scalars
+ * are computed in double and rounded once to fp32.  The clipped gradient is
+ * not written back.
+ *   master, exp_avg, exp_avg_sq   device fp32 arenas, read and written
+ *   grad                          device fp32 arena, read only
+ *   weight_bf16                   device bf16 arena (uint16 bits), written;
+ *                                 may be NULL to skip the copy
+ *   hp                            HOST pointer
+ *   step_t                        1-based step count used by bias correction
+ *   d_norm                        device result of zero1_grad_norm (its
+ *                                 sumsq possibly summed across ranks), or
+ *                                 NULL for no clipping; norm = sqrt(sumsq) in
+ *                                 double; if status is not ZERO1_OK or sumsq
+ *                                 is not finite the kernel writes nothing
+ *                                 (the step is skipped)
+ * Errors: ZERO1_EINVAL (step_t < 1, non-finite or out-of-range
+ * hyper-parameters, ...), ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
+               const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
+               const zero1_norm_out* d_norm, void* stream);
+
+/* Copy a device zero1_norm_out to the host, synchronising `stream` first.
+ * Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
+int zero1_read_norm(const zero1_norm_out* d_norm, void* stream, zero1_norm_out* host_out);
+
+/* ---- diagnostics --------------------------------------------------------- */
+
+/* Static description of a status code. */
+const char* zero1_strerror(int code);
+
+/* Text of the CUDA error behind the calling thread's last ZERO1_ECUDA
+ * ("" if none). */
+const char* zero1_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO1_H */

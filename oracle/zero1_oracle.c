@@ -147,17 +147,28 @@ void oracle_accumulate(float *grad, const uint16_t *micro, int64_t n, int32_t ov
 /* ------------------------------------------------------------------------ */
 /* Sum of squares for the L2 gradient norm ("ZeRO-1 风格的 Distributed        */
 /* Optimizer", section 6.6: clip_grad 1.0; the norm type is not stated, L2  */
-/* is taken).  The product of two floats is exact in double, the running    */
-/* sum is double, in index order.                                            */
+/* is taken).  The value wanted is the exact sum of the squares: the clip   */
+/* coefficient is rounded once to fp32 from it, so it must not depend on a  */
+/* summation order.  The product of two floats is exact in double; the      */
+/* running sum is double in index order with a Neumaier compensation term,  */
+/* which keeps the result within a few double ulps of the exact sum for any */
+/* length (a plain double sum drifts by up to n ulps).                       */
 /* ------------------------------------------------------------------------ */
 double oracle_sumsq(const float *grad, int64_t n)
 {
     double s = 0.0;
+    double comp = 0.0; /* the low-order parts lost by the additions to s */
     for (int64_t j = 0; j < n; ++j) {
         double x = (double)grad[j];
-        s += x * x;
+        double sq = x * x;
+        double t = s + sq;
+        if (fabs(s) >= fabs(sq))
+            comp += (s - t) + sq;
+        else
+            comp += (sq - t) + s;
+        s = t;
     }
-    return s;
+    return s + comp;
 }
 
 /* ------------------------------------------------------------------------ */

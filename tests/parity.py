@@ -1,0 +1,172 @@
+"""GPU-vs-oracle parity harness (test infrastructure).
+
+Runs the CUDA path through the C ABI and the CPU oracle on the same seeded
+inputs and compares them element by element:
+  - fp32 grad arena: bit-exact (same IEEE additions in the same order)
+  - sum of squares / norm: within 1e-5 relative
+  - master, m, v: within 4 fp32 ulp after all steps
+  - bf16 copy: bit-exact against round-to-nearest-even of the GPU master
+The oracle accumulates over the whole arena in host chunks (padding is zero
+and stays zero under every operation, which the comparison checks too) and
+steps either every arena element or, for the full-size workloads, sampled
+arena indices.
+"""
+import numpy as np
+import torch
+
+import oracle
+import zero_sharded_mixed_local_gb300 as z
+from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout, Workload, get_workload
+
+SUMSQ_RTOL = 1e-5     # the stated bar for the gradient norm
+SUMSQ_TIGHT = 1e-12   # both sides sum the exact squares with compensation; they agree far closer
+MAX_ULP = 4
+
+
+def ordered_int(x):
+    i = np.asarray(x, np.float32).view(np.int32).astype(np.int64)
+    return np.where(i < 0, -(i & 0x7FFFFFFF), i)
+
+
+def ulp_diff(a, b):
+    return np.abs(ordered_int(a) - ordered_int(b))
+
+
+def u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rne_of(master_cpu):
+    return master_cpu.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+class Problem:
+    """One workload on the GPU: plan, arenas, generator."""
+
+    def __init__(self, workload, device="cuda", seed=None):
+        self.w = workload if isinstance(workload, Workload) else get_workload(workload)
+        self.dev = torch.device(device)
+        p = self.w.params
+        self.plan = z.Plan(p.numels, p.no_decay, self.w.dp_size, self.w.dp_rank)
+        L = self.plan.layout()
+        self.layout = Layout(L.counts, L.offsets, L.no_decay, L.arena_numel)
+        self.gen = InputGenerator(self.w, self.layout, self.dev, seed)
+        self.n = self.plan.arena_numel
+        self.group1 = self.plan.group_range(1)[0]
+        self.hp = z.Hparams(**self.w.hp)
+        self.master = self.gen.master()
+        self.m = self.gen.zeros()
+        self.v = self.gen.zeros()
+        self.grad = self.gen.zeros()
+        self.wbf = self.gen.zeros(torch.bfloat16)
+        self.ws = self.plan.new_workspace(self.dev)
+        self.nout = z.new_norm_out(self.dev)
+
+    def gpu_step(self, micros, t, extra_sumsq=0.0):
+        z.accumulate(self.plan, self.grad, micros[0], overwrite_first=True)
+        for mb in micros[1:]:
+            z.accumulate(self.plan, self.grad, mb, overwrite_first=False)
+        z.grad_norm(self.plan, self.grad, self.ws, self.nout, extra_sumsq)
+        z.step(self.plan, self.master, self.m, self.v, self.grad, self.wbf, self.hp, t, self.nout)
+        return z.read_norm(self.nout)
+
+
+def oracle_grad(n, micros_u16):
+    g = np.zeros(n, np.float32)
+    oracle.accumulate_all(g, micros_u16)
+    return g
+
+
+def group_counts(idx, group1_begin):
+    k = int(np.searchsorted(idx, group1_begin))
+    return [k, len(idx) - k], [0, 1]
+
+
+CHUNK = 1 << 26  # elements per host pass: bounds host memory on the full-size workloads
+
+
+def oracle_pass(micros, gpu_grad, idx):
+    """Oracle accumulation over the whole arena, chunk by chunk: checks the GPU grad
+    arena bit for bit, returns (oracle grad at idx, oracle sum of squares)."""
+    n = gpu_grad.numel()
+    s = 0.0
+    g_idx = np.empty(idx.size, np.float32)
+    for c0 in range(0, n, CHUNK):
+        c1 = min(n, c0 + CHUNK)
+        g = np.zeros(c1 - c0, np.float32)
+        for k, mb in enumerate(micros):
+            oracle.accumulate(g, u16(mb[c0:c1]), overwrite=(k == 0))
+        gg = gpu_grad[c0:c1].cpu().numpy()
+        if not np.array_equal(gg.view(np.uint32), g.view(np.uint32)):
+            bad = int(np.nonzero(gg.view(np.uint32) != g.view(np.uint32))[0][0]) + c0
+            raise AssertionError("grad arena differs from the oracle at element %d" % bad)
+        s += oracle.sumsq(g)
+        lo, hi = np.searchsorted(idx, [c0, c1])
+        g_idx[lo:hi] = g[idx[lo:hi] - c0]
+    return g_idx, s
+
+
+def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda", seed=None):
+    """Run `steps` steps on GPU and oracle; assert parity.  `sample`: None compares every
+    arena element (padding included), "sampled" the tensor edges, the padding and a
+    million random elements; the grad arena and the bf16 copy are checked in full."""
+    pb = Problem(workload, device, seed)
+    w = pb.w
+    steps = w.steps if steps is None else steps
+    n = pb.n
+    idx = np.arange(n, dtype=np.int64) if sample is None else sample_indices(pb.layout)
+    idx_t = torch.from_numpy(idx).to(pb.dev)
+    counts, flags = group_counts(idx, pb.group1)
+    P = pb.master[idx_t].cpu().numpy().copy()
+    M = np.zeros(idx.size, np.float32)
+    V = np.zeros(idx.size, np.float32)
+
+    micros = None
+    report = []
+    for t in range(1, steps + 1):
+        new_grads = micros is None or fresh_grads
+        if new_grads:
+            micros = pb.gen.micro_grads()
+        got = pb.gpu_step(micros, t)
+        if new_grads:
+            g_idx, ref_sumsq = oracle_pass(micros, pb.grad, idx)
+        assert got["status"] == 0
+        assert abs(got["sumsq"] - ref_sumsq) <= SUMSQ_RTOL * ref_sumsq, (t, got["sumsq"], ref_sumsq)
+        assert abs(got["sumsq"] - ref_sumsq) <= SUMSQ_TIGHT * ref_sumsq, (t, got["sumsq"], ref_sumsq)
+        ok, norm, coef = oracle.clip_coef(ref_sumsq, w.hp["clip_grad"])
+        assert ok
+        oracle.adamw(P, M, V, g_idx, counts, flags, w.hp, t, coef)
+        report.append((t, got["norm"], norm, float(coef)))
+
+    res = {}
+    for name, dev_t, ref in (("master", pb.master, P), ("m", pb.m, M), ("v", pb.v, V)):
+        a = dev_t[idx_t].cpu().numpy()
+        d = ulp_diff(a, ref)
+        res[name] = int(d.max()) if d.size else 0
+        assert res[name] <= MAX_ULP, (name, res[name], int(idx[int(np.argmax(d))]))
+    # bf16 copy: bit-exact round-to-nearest-even of the GPU master (torch's cast), in full
+    for c0 in range(0, n, CHUNK):
+        c1 = min(n, c0 + CHUNK)
+        assert torch.equal(pb.wbf[c0:c1].view(torch.int16), pb.master[c0:c1].to(torch.bfloat16).view(torch.int16)), \
+            "bf16 copy is not the RNE of the GPU master in [%d, %d)" % (c0, c1)
+    res["norms"] = report
+    res["local_numel"] = pb.plan.local_numel
+    res["compared"] = int(idx.size)
+    return res
+
+
+def sample_indices(layout, per_tensor_edge=2048, n_random=1_000_000, seed=0):
+    """First and last `per_tensor_edge` local elements of every tensor, plus random ones."""
+    parts = []
+    for o, c in zip(layout.offsets, layout.counts):
+        o, c = int(o), int(c)
+        if c == 0:
+            continue
+        e = min(c, per_tensor_edge)
+        parts.append(np.arange(o, o + e, dtype=np.int64))
+        parts.append(np.arange(o + c - e, o + c, dtype=np.int64))
+        # the padding after the shard (zero, and it must stay zero)
+        parts.append(np.arange(o + c, (o + c + 7) // 8 * 8, dtype=np.int64))
+    rng = np.random.default_rng(seed)
+    parts.append(rng.integers(0, layout.arena_numel, size=min(n_random, layout.arena_numel), dtype=np.int64))
+    return np.unique(np.concatenate(parts))

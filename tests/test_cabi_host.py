@@ -1,0 +1,161 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+declared entry point, and its plan (shard split, arena layout, byte
+accounting) agrees with the oracle.  Only calls that never touch CUDA are
+made; argument errors return before any CUDA call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from zero_sharded_mixed_local_gb300 import build as zbuild
+from zero_sharded_mixed_local_gb300.workloads import WORKLOADS, get_workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def z():
+    zbuild.build_library()
+    import zero_sharded_mixed_local_gb300 as z
+    z.load_library()
+    return z
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(zero1_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol(z):
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(zbuild.LIB)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_exported_symbols_are_all_declared(z):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", zbuild.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (zero1_\w+)", out))
+    assert exported == set(declared_functions())
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_plan_matches_oracle_for_every_workload(z, name):
+    w = get_workload(name)
+    plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank)
+    start, count, local = oracle.plan(w.params.numels, w.dp_size, w.dp_rank)
+    L = plan.layout()
+    assert np.array_equal(L.shard_start, start) and np.array_equal(L.counts, count)
+    assert plan.local_numel == local and plan.total_numel == w.params.total
+    assert plan.num_tensors == len(w.params)
+    _check_layout(plan, w.params.no_decay)
+    for gb in (2, 4):
+        assert plan.bytes(gb) == oracle.zero1_bytes(w.params.total, local, gb)
+
+
+def _check_layout(plan, no_decay):
+    L = plan.layout()
+    assert plan.arena_numel % 8 == 0
+    assert np.all(L.offsets % 8 == 0)
+    b0, e0 = plan.group_range(0)
+    b1, e1 = plan.group_range(1)
+    assert b0 == 0 and e0 == b1 and e1 == plan.arena_numel
+    nd = np.asarray(no_decay, bool)
+    # each group holds exactly its tensors, in model order, without overlap
+    for g, (b, e) in enumerate(((b0, e0), (b1, e1))):
+        sel = np.nonzero(nd == bool(g))[0]
+        offs, cnts = L.offsets[sel], L.counts[sel]
+        assert np.all(offs >= b) and np.all(offs + cnts <= e)
+        assert np.all(np.diff(offs) >= 0)
+        ends = offs + cnts
+        assert np.all(ends[:-1] <= offs[1:])
+        assert (np.sum((cnts + 7) // 8 * 8) == e - b)
+
+
+def test_small_plan_worked_example(z):
+    # numels 10, 3, 8 over dp=3; tensor 1 is a norm weight
+    plans = [z.Plan([10, 3, 8], [0, 1, 0], 3, r) for r in range(3)]
+    assert [p.layout().counts.tolist() for p in plans] == [[4, 1, 3], [3, 1, 3], [3, 1, 2]]
+    assert [p.layout().shard_start.tolist() for p in plans] == [[0, 0, 0], [4, 1, 3], [7, 2, 6]]
+    # arena of rank 0: tensor 0 at 0 (4 -> pad 8), tensor 2 at 8 (3 -> 8), norm group at 16
+    assert plans[0].layout().offsets.tolist() == [0, 16, 8]
+    assert plans[0].arena_numel == 24 and plans[0].group_range(1) == (16, 24)
+    assert plans[0].workspace_bytes == 8
+
+
+def test_plan_rejects_bad_arguments(z):
+    lib = z.load_library()
+    h = ctypes.c_void_p()
+    n = np.array([4, 4], np.int64)
+    nd = np.array([0, 1], np.uint8)
+    bad_nd = np.array([0, 2], np.uint8)
+    neg = np.array([4, -1], np.int64)
+    cases = [                  # (numels, no_decay, n_tensors, dp_size, dp_rank)
+        (n, nd, 2, 2, 2),      # rank == dp
+        (n, nd, 2, 2, -1),     # negative rank
+        (n, nd, -1, 1, 0),     # negative tensor count
+        (n, nd, 2, -3, 0),     # dp < 1
+        (n, nd, 2, 0, 0),      # dp == 0
+        (n, bad_nd, 2, 1, 0),  # no_decay not 0/1
+        (neg, nd, 2, 1, 0),    # negative numel
+    ]
+    for numels, flags, count, dp, rank in cases:
+        rc = lib.zero1_plan_create(numels.ctypes.data, flags.ctypes.data, count, dp, rank, ctypes.byref(h))
+        assert rc == z.ZERO1_EINVAL, (count, dp, rank)
+        assert not h.value
+    assert lib.zero1_plan_create(n.ctypes.data, nd.ctypes.data, 2, 1, 0, None) == z.ZERO1_EINVAL
+    assert lib.zero1_plan_create(None, None, 2, 1, 0, ctypes.byref(h)) == z.ZERO1_EINVAL
+    assert lib.zero1_plan_create(None, None, 0, 1, 0, ctypes.byref(h)) == z.ZERO1_OK
+    lib.zero1_plan_destroy(h)
+    lib.zero1_plan_destroy(None)
+    assert lib.zero1_plan_arena_numel(None) == -1
+    assert lib.zero1_plan_tensor(None, 0, None, None, None) == z.ZERO1_EINVAL
+
+
+def test_compute_calls_reject_bad_arguments_before_any_launch(z):
+    lib = z.load_library()
+    plan = z.Plan([100, 8], [0, 1], 1, 0)
+    h = plan.handle
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every case fails its checks first
+    odd = ctypes.c_void_p(0x10008)
+    arr = (ctypes.c_void_p * 1)(0x20000)
+    arr_odd = (ctypes.c_void_p * 1)(0x20002)
+    assert lib.zero1_accumulate(h, fake, arr, 0, 1, None) == z.ZERO1_EINVAL
+    assert lib.zero1_accumulate(h, fake, arr, 17, 1, None) == z.ZERO1_EINVAL
+    assert lib.zero1_accumulate(h, None, arr, 1, 1, None) == z.ZERO1_EINVAL
+    assert lib.zero1_accumulate(h, fake, arr_odd, 1, 1, None) == z.ZERO1_EALIGN
+    assert lib.zero1_accumulate(h, odd, arr, 1, 1, None) == z.ZERO1_EALIGN
+    assert plan.workspace_bytes == 8
+    assert lib.zero1_grad_norm(h, fake, 0.0, fake, 4, fake, None) == z.ZERO1_EINVAL  # workspace too small
+    assert lib.zero1_grad_norm(h, fake, 0.0, odd, 64, fake, None) == z.ZERO1_EALIGN
+    assert lib.zero1_grad_norm(h, fake, -1.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_grad_norm(None, fake, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    hp = z.binding._Hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    args = [h, fake, fake, fake, fake, fake]
+    assert lib.zero1_step(*args, ctypes.byref(hp), 0, None, None) == z.ZERO1_EINVAL  # t < 1
+    assert lib.zero1_step(h, fake, fake, fake, odd, fake, ctypes.byref(hp), 1, None, None) == z.ZERO1_EALIGN
+    assert lib.zero1_step(h, fake, fake, fake, fake, odd, ctypes.byref(hp), 1, None, None) == z.ZERO1_EALIGN
+    bad = z.binding._Hparams(3e-4, 1.0, 0.95, 1e-8, 0.1, 1.0)
+    assert lib.zero1_step(*args, ctypes.byref(bad), 1, None, None) == z.ZERO1_EINVAL
+    bad = z.binding._Hparams(float("nan"), 0.9, 0.95, 1e-8, 0.1, 1.0)
+    assert lib.zero1_step(*args, ctypes.byref(bad), 1, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_read_norm(None, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_strerror(z.ZERO1_ENONFINITE).decode().startswith("gradient norm")
+    assert lib.zero1_last_cuda_error().decode() == ""
+
+
+def test_binding_refuses_cpu_tensors(z):
+    import torch
+    plan = z.Plan([64], [0], 1, 0)
+    with pytest.raises(ValueError):
+        z.accumulate(plan, torch.zeros(64), torch.zeros(64, dtype=torch.bfloat16))

@@ -1,0 +1,248 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on a GB300.
+
+Small cases compare every arena element; the full-size workloads compare
+sampled elements (tensor edges, padding, a million random positions) while
+the gradient arena, the norm and the bf16 copy are still checked in full.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_sharded_mixed_local_gb300 as z
+from zero_sharded_mixed_local_gb300.workloads import ParamList, Workload
+
+from parity import MAX_ULP, Problem, oracle_grad, rne_of, run_parity, u16, ulp_diff
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip_grad=1.0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    z.load_library()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _custom(numels, no_decay, dp=1, rank=0, K=2, steps=3, sigma=1e-3, name="custom", hp=None):
+    return Workload(name, name, ParamList(["p%d" % i for i in range(len(numels))], list(numels), list(no_decay)),
+                    dp, rank, K, steps, sigma, hp=dict(hp or HP))
+
+
+# ---------------------------------------------------------------- workloads
+def test_toy_full_parity():
+    res = run_parity("toy")
+    assert res["master"] <= MAX_ULP
+
+
+def test_smollm135m_full_size_sampled():
+    res = run_parity("smollm135m", fresh_grads=False, sample="sampled")
+    assert res["local_numel"] == 134_515_008
+
+
+def test_smollm1p7b_full_size_sampled_clip_active():
+    res = run_parity("smollm1p7b", fresh_grads=False, sample="sampled")
+    assert res["local_numel"] == 213_922_048
+    t, gpu_norm, ref_norm, coef = res["norms"][0]
+    assert 3.0 < ref_norm < 5.0 and coef < 1.0  # the grads were scaled so clipping is active
+
+
+def test_llama8b_full_size_sampled():
+    res = run_parity("llama8b", steps=10, fresh_grads=False, sample="sampled")
+    assert res["local_numel"] == 1_003_782_656
+
+
+def test_ragged_full_size_sampled():
+    res = run_parity("ragged", fresh_grads=False, sample="sampled")
+    _, gpu_norm, ref_norm, coef = res["norms"][0]
+    assert ref_norm > 1.0 and coef < 1.0
+
+
+# ---------------------------------------------------------------- edge cases
+def test_tiny_and_ragged_tensors_all_ranks():
+    numels = list(range(1, 18)) + [0, 1023, 1025, 16384 * 3 + 5]
+    nd = [i % 3 == 0 for i in range(len(numels))]
+    for dp in (1, 2, 3, 4, 8):
+        for r in range(dp):
+            run_parity(_custom(numels, nd, dp, r, K=3, steps=4, sigma=0.05))
+
+
+def test_multi_tile_with_ragged_tail():
+    # several 16384-element norm tiles and a tail that is not a multiple of 16
+    numels = [16384 * 5 + 8 * 3 + 7, 100003, 6]
+    run_parity(_custom(numels, [0, 0, 1], K=2, steps=3, sigma=0.02))
+
+
+def test_empty_plan_is_a_no_op():
+    plan = z.Plan([0, 0, 0], [0, 1, 0], 1, 0)
+    assert plan.arena_numel == 0 and plan.workspace_bytes == 0
+    nout = z.new_norm_out()
+    # zero-length arenas: nothing to launch for the element-wise calls
+    g = torch.zeros(0, device="cuda")
+    z.accumulate(plan, g, torch.zeros(0, dtype=torch.bfloat16, device="cuda"))
+    z.grad_norm(plan, g, torch.zeros(16, dtype=torch.uint8, device="cuda"), nout, extra_sumsq=9.0)
+    r = z.read_norm(nout)
+    assert r["sumsq"] == 9.0 and r["norm"] == 3.0 and r["status"] == 0 and r["n_partials"] == 0
+    z.step(plan, g, g.clone(), g.clone(), g, torch.zeros(0, dtype=torch.bfloat16, device="cuda"), z.Hparams(), 1,
+           nout)
+
+
+def test_shards_with_fewer_elements_than_ranks():
+    # numel < dp: some ranks own nothing of a tensor
+    numels = [1, 2, 3, 5, 7]
+    for r in range(8):
+        plan = z.Plan(numels, [0] * 5, 8, r)
+        _, counts, _ = oracle.plan(numels, 8, r)
+        assert plan.local_numel == int(counts.sum())
+        if plan.arena_numel:
+            run_parity(_custom(numels, [0] * 5, 8, r, K=1, steps=2, sigma=0.1))
+
+
+def test_nonfinite_gradient_skips_the_step():
+    for bad in (float("nan"), float("inf")):
+        pb = Problem(_custom([1000, 64], [0, 1], K=2, steps=1))
+        micros = pb.gen.micro_grads()
+        micros[1][123] = bad
+        before = [t.clone() for t in (pb.master, pb.m, pb.v, pb.wbf)]
+        got = pb.gpu_step(micros, 1)
+        assert got["status"] == z.ZERO1_ENONFINITE
+        for a, b in zip(before, (pb.master, pb.m, pb.v, pb.wbf)):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_clip_below_threshold_equals_no_clip_and_no_norm():
+    outs = []
+    for clip, use_norm in ((1.0, True), (0.0, True), (1.0, False)):
+        pb = Problem(_custom([4096, 512, 33], [0, 1, 0], K=2, steps=1, hp=dict(HP, clip_grad=clip)))
+        micros = pb.gen.micro_grads()
+        z.accumulate(pb.plan, pb.grad, micros)
+        z.grad_norm(pb.plan, pb.grad, pb.ws, pb.nout)
+        assert z.read_norm(pb.nout)["norm"] < 1.0
+        z.step(pb.plan, pb.master, pb.m, pb.v, pb.grad, pb.wbf, pb.hp, 1, pb.nout if use_norm else None)
+        outs.append([t.cpu() for t in (pb.master, pb.m, pb.v, pb.wbf)])
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_zero_gradient_is_pure_decay_bit_exact():
+    pb = Problem(_custom([1000, 256, 77], [0, 1, 0], K=1, steps=1))
+    p0 = pb.master.clone()
+    zero = torch.zeros_like(pb.wbf)
+    pb.gpu_step([zero], 1)
+    dfac = np.float32(1.0 - HP["lr"] * HP["weight_decay"])
+    b = pb.group1
+    exp = p0.cpu().numpy().copy()
+    exp[:b] = exp[:b] * dfac
+    assert np.array_equal(pb.master.cpu().numpy().view(np.uint32), exp.view(np.uint32))
+    assert not pb.m.any() and not pb.v.any()
+
+
+def test_step_without_bf16_copy_matches():
+    pa = Problem(_custom([5000, 31], [0, 1], K=1, steps=1))
+    pb = Problem(_custom([5000, 31], [0, 1], K=1, steps=1))
+    mic = pa.gen.micro_grads()
+    for pr, w in ((pa, pa.wbf), (pb, None)):
+        z.accumulate(pr.plan, pr.grad, mic)
+        z.grad_norm(pr.plan, pr.grad, pr.ws, pr.nout)
+        z.step(pr.plan, pr.master, pr.m, pr.v, pr.grad, w, pr.hp, 1, pr.nout)
+    assert torch.equal(pa.master, pb.master) and torch.equal(pa.m, pb.m) and torch.equal(pa.v, pb.v)
+    assert not pb.wbf.view(torch.int16).any()
+
+
+def test_accumulate_many_micro_batches_in_one_call():
+    pb = Problem(_custom([40000, 17], [0, 1], K=16, steps=1, sigma=0.5))
+    micros = pb.gen.micro_grads()
+    z.accumulate(pb.plan, pb.grad, micros, overwrite_first=True)
+    ref = oracle_grad(pb.n, [u16(m) for m in micros])
+    assert np.array_equal(pb.grad.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    # and without overwrite: grad += sum
+    z.accumulate(pb.plan, pb.grad, micros[:3], overwrite_first=False)
+    for m in micros[:3]:
+        oracle.accumulate(ref, u16(m), overwrite=False)
+    assert np.array_equal(pb.grad.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_norm_is_deterministic_and_extra_sumsq_adds():
+    pb = Problem(_custom([16384 * 7 + 40, 9], [0, 1], K=1, steps=1, sigma=0.3))
+    z.accumulate(pb.plan, pb.grad, pb.gen.micro_grads())
+    vals = []
+    for extra in (0.0, 0.0, 2.5):
+        z.grad_norm(pb.plan, pb.grad, pb.ws, pb.nout, extra)
+        vals.append(z.read_norm(pb.nout))
+    assert vals[0] == vals[1]
+    assert vals[2]["sumsq"] == vals[0]["sumsq"] + 2.5
+    assert vals[0]["n_partials"] == 8
+
+
+def test_shard_concatenation_on_gpu():
+    """All dp ranks stepped on the one GPU, each with the other ranks' sum of squares,
+    reproduce the unsharded step bit for bit."""
+    numels = [1000, 3, 64, 4097, 11, 257]
+    nd = [0, 1, 0, 0, 1, 0]
+    dp = 4
+    N = sum(numels)
+    tstart = np.concatenate([[0], np.cumsum(numels)[:-1]])
+    rng = torch.Generator(device="cuda").manual_seed(5)
+    full_micro = [(torch.randn(N, device="cuda", generator=rng) * 0.2).to(torch.bfloat16) for _ in range(2)]
+    full_p = torch.randn(N, device="cuda", generator=rng) * 0.02
+
+    def run(dp_size, rank, extra=None):
+        plan = z.Plan(numels, nd, dp_size, rank)
+        L = plan.layout()
+        sel = [np.arange(tstart[i] + L.shard_start[i], tstart[i] + L.shard_start[i] + L.counts[i])
+               for i in range(len(numels))]
+        def arena_of(full, dtype):
+            a = plan.new_arena(dtype)
+            for i, s in enumerate(sel):
+                if len(s):
+                    a[int(L.offsets[i]):int(L.offsets[i]) + len(s)] = full[torch.from_numpy(s).cuda()]
+            return a
+        master, m, v, g = arena_of(full_p, torch.float32), plan.new_arena(), plan.new_arena(), plan.new_arena()
+        wbf = plan.new_arena(torch.bfloat16)
+        z.accumulate(plan, g, [arena_of(mb, torch.bfloat16) for mb in full_micro])
+        ws, nout = plan.new_workspace(), z.new_norm_out()
+        z.grad_norm(plan, g, ws, nout, 0.0)
+        local = z.read_norm(nout)["sumsq"]
+        if extra is not None:
+            z.grad_norm(plan, g, ws, nout, extra)
+            z.step(plan, master, m, v, g, wbf, z.Hparams(**HP), 1, nout)
+        return plan, sel, local, (master, m, v, wbf)
+
+    ref_plan, ref_sel, ref_sumsq, ref_out = run(1, 0, 0.0)
+    locals_ = [run(dp, r)[2] for r in range(dp)]
+    for r in range(dp):
+        plan, sel, _, out = run(dp, r, sum(s for q, s in enumerate(locals_) if q != r))
+        L, RL = plan.layout(), ref_plan.layout()
+        for i, s in enumerate(sel):
+            if not len(s):
+                continue
+            o = int(L.offsets[i])
+            ro = int(RL.offsets[i]) + int(L.shard_start[i])
+            for a, b in zip(out, ref_out):
+                assert torch.equal(a[o:o + len(s)].view(torch.uint8) if a.dtype != torch.bfloat16 else
+                                   a[o:o + len(s)].view(torch.int16),
+                                   b[ro:ro + len(s)].view(torch.uint8) if b.dtype != torch.bfloat16 else
+                                   b[ro:ro + len(s)].view(torch.int16))
+
+
+def test_misaligned_and_wrong_size_buffers_are_rejected():
+    plan = z.Plan([100], [0], 1, 0)
+    g = plan.new_arena()
+    n = plan.arena_numel
+    big = torch.zeros(n + 4, device="cuda")
+    mb = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError, match="16-byte"):
+        z.accumulate(plan, big[1:1 + n], mb)  # 4-byte offset
+    with pytest.raises(ValueError, match="elements"):
+        z.accumulate(plan, big, mb)           # wrong size
+    # straight through the C ABI: misalignment is caught before any launch
+    lib = z.load_library()
+    arr = (ctypes.c_void_p * 1)(torch.zeros(112, dtype=torch.bfloat16, device="cuda").data_ptr() + 2)
+    assert lib.zero1_accumulate(plan.handle, ctypes.c_void_p(g.data_ptr()), arr, 1, 1, None) == z.ZERO1_EALIGN

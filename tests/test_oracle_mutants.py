@@ -39,7 +39,8 @@ MUTANTS = {
     "nonfinite_not_detected": ("if (!isfinite(norm))\n        return 0;", "if (norm < 0)\n        return 0;"),
     "shard_remainder_off_by_one": ("*count = q + ((r < rem) ? 1 : 0);", "*count = q + ((r <= rem) ? 1 : 0);"),
     "shard_start_ignores_remainder": ("*start = (int64_t)r * q + extra_before;", "*start = (int64_t)r * q;"),
-    "sumsq_not_squared": ("s += x * x;", "s += fabs(x);"),
+    "sumsq_not_squared": ("double sq = x * x;", "double sq = fabs(x);"),
+    "sumsq_compensation_sign": ("comp += (s - t) + sq;", "comp -= (s - t) + sq;"),
     "accumulate_subtracts": ("grad[j] = overwrite ? g : grad[j] + g;", "grad[j] = overwrite ? g : grad[j] - g;"),
     "accumulate_overwrite_adds_zero": ("grad[j] = overwrite ? g : grad[j] + g;",
                                        "grad[j] = overwrite ? 0.0f + g : grad[j] + g;"),

@@ -194,12 +194,27 @@ def test_sumsq_closed_forms(oracle_mod):
 
 
 def test_sumsq_vs_exactly_rounded_fsum(oracle_mod):
+    """math.fsum gives the correctly rounded sum of the (exact) squares; the oracle
+    must be within a few double ulps of it, at any length and scale mix."""
     rng = np.random.default_rng(4)
-    x = (rng.standard_normal(200_000) * 10.0 ** rng.uniform(-4, 2, 200_000)).astype(np.float32)
-    exact = math.fsum(float(v) * float(v) for v in x)
-    got = oracle_mod.sumsq(x)
-    assert abs(got - exact) <= 1e-12 * exact
+    for n, spread in ((200_000, 6), (1_000_003, 2), (3, 30)):
+        x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-spread / 2, spread / 2, n)).astype(np.float32)
+        exact = math.fsum(float(v) * float(v) for v in x)
+        got = oracle_mod.sumsq(x)
+        assert abs(got - exact) <= 4 * math.ulp(exact), (n, got, exact)
     assert abs(math.sqrt(got) - float(np.linalg.norm(x.astype(np.float64)))) <= 1e-12 * math.sqrt(exact)
+
+
+def test_sumsq_no_drift_on_bf16_structured_squares(oracle_mod):
+    """Squares of sums of bf16 values have structured low bits; summing millions of them
+    must not drift (a plain running sum does, by ~1e-7 relative in fp32)."""
+    rng = np.random.default_rng(12)
+    n = 2_000_000
+    a = _to_bf16_bits(rng.standard_normal(n) * 1e-3).astype(np.uint32) << 16
+    b = _to_bf16_bits(rng.standard_normal(n) * 1e-3).astype(np.uint32) << 16
+    g = (a.view(np.float32) + b.view(np.float32)).astype(np.float32)
+    exact = math.fsum((g.astype(np.float64) ** 2).tolist())
+    assert abs(oracle_mod.sumsq(g) - exact) <= 4 * math.ulp(exact)
 
 
 def test_clip_coef_vs_torch_clip_grad_norm(oracle_mod):

@@ -1,0 +1,19 @@
+"""GB300-native ZeRO-1 local-shard optimizer step (sm_103a).
+
+One data-parallel rank's part of a ZeRO-1 mixed-precision training step, as
+described for nanotron's distributed optimizer: accumulate bf16 micro-batch
+gradients in fp32, take the global gradient L2 norm for clipping, run AdamW
+on the fp32 master / m / v shard and write the bf16 weights the all-gather
+ships.  The work runs in hand-written CUDA kernels behind the C ABI of
+``libzero1.so`` (``include/zero1.h``); this package is its thin binding.
+"""
+from .binding import (ARENA_ALIGN, MAX_MICRO, NORM_OUT_BYTES, NUM_GROUPS, ZERO1_EALIGN, ZERO1_ECUDA,
+                      ZERO1_EINVAL, ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_OK, Hparams, LocalShardAdamW, Plan,
+                      ShardLayout, Zero1Error, accumulate, allreduce_sumsq_, decode_norm, grad_norm, load_library, new_norm_out,
+                      read_norm, step)
+
+__all__ = [
+    "ARENA_ALIGN", "MAX_MICRO", "NORM_OUT_BYTES", "NUM_GROUPS", "ZERO1_EALIGN", "ZERO1_ECUDA", "ZERO1_EINVAL",
+    "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_OK", "Hparams", "LocalShardAdamW", "Plan", "ShardLayout",
+    "Zero1Error", "accumulate", "allreduce_sumsq_", "decode_norm", "grad_norm", "load_library", "new_norm_out", "read_norm", "step",
+]

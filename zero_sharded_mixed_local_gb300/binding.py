@@ -1,0 +1,360 @@
+"""ctypes binding of libzero1.so: argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module checks
+tensors (device, dtype, size, contiguity, 16-byte alignment), turns them into
+raw pointers and forwards the current CUDA stream.  It has no fallback: when
+the library is missing or a call fails it raises.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libzero1.so")
+
+ZERO1_OK = 0
+ZERO1_EINVAL = -1
+ZERO1_EALIGN = -2
+ZERO1_ECUDA = -3
+ZERO1_ENONFINITE = -4
+ZERO1_ENOMEM = -5
+ARENA_ALIGN = 8
+NUM_GROUPS = 2
+MAX_MICRO = 16
+NORM_OUT_BYTES = 24
+
+_lib = None
+
+
+class Zero1Error(RuntimeError):
+    def __init__(self, code, where):
+        lib = load_library()
+        msg = "%s failed: %s" % (where, lib.zero1_strerror(code).decode())
+        if code == ZERO1_ECUDA:
+            msg += " (%s)" % lib.zero1_last_cuda_error().decode()
+        super().__init__(msg)
+        self.code = code
+
+
+class _Hparams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in ("lr", "beta1", "beta2", "eps", "weight_decay", "clip_grad")]
+
+
+class _NormOut(ctypes.Structure):
+    _fields_ = [("sumsq", ctypes.c_double), ("norm", ctypes.c_double), ("status", ctypes.c_int32),
+                ("n_partials", ctypes.c_int32)]
+
+
+def load_library(path=None):
+    """Load libzero1.so (built in-tree by ``build.build_library``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError("libzero1.so is not built (%s); run __graft_entry__.build() first" % path)
+    lib = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    sig = {
+        "zero1_plan_create": (ctypes.c_int, [vp, vp, i32, i32, i32, ctypes.POINTER(vp)]),
+        "zero1_plan_destroy": (None, [vp]),
+        "zero1_plan_num_tensors": (i32, [vp]),
+        "zero1_plan_total_numel": (i64, [vp]),
+        "zero1_plan_local_numel": (i64, [vp]),
+        "zero1_plan_arena_numel": (i64, [vp]),
+        "zero1_plan_tensor": (ctypes.c_int, [vp, i32, i64p, i64p, i64p]),
+        "zero1_plan_group_range": (ctypes.c_int, [vp, i32, i64p, i64p]),
+        "zero1_plan_bytes": (ctypes.c_int, [vp, i32, i64p]),
+        "zero1_workspace_bytes": (ctypes.c_size_t, [vp]),
+        "zero1_accumulate": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, i32, vp]),
+        "zero1_grad_norm": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
+        "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
+        "zero1_read_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(_NormOut)]),
+        "zero1_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "zero1_last_cuda_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(code, where):
+    if code != ZERO1_OK:
+        raise Zero1Error(code, where)
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtype, numel, name, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be on a CUDA device (got %s)" % (name, t.device))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if numel is not None and t.numel() != numel:
+        raise ValueError("%s has %d elements, the plan's arena has %d" % (name, t.numel(), numel))
+    if t.data_ptr() % 16:
+        raise ValueError("%s must start on a 16-byte boundary" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@dataclass
+class Hparams:
+    """AdamW settings of the ZeRO-1 optimizer (adam_w, betas 0.9/0.95, eps 1e-8,
+    weight_decay 0.1, clip_grad 1.0 in nanotron's config)."""
+    lr: float = 3e-4
+    beta1: float = 0.9
+    beta2: float = 0.95
+    eps: float = 1e-8
+    weight_decay: float = 0.1
+    clip_grad: float = 1.0
+
+    def _c(self):
+        return _Hparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.clip_grad)
+
+
+@dataclass
+class ShardLayout:
+    """Per-tensor shard placement of a plan (numpy arrays, model order)."""
+    shard_start: np.ndarray
+    counts: np.ndarray
+    offsets: np.ndarray
+    no_decay: np.ndarray
+    arena_numel: int
+
+
+class Plan:
+    """zero1_plan: every parameter tensor cut by numel into dp_size contiguous
+    shards; this rank's shards laid out in one padded arena per quantity."""
+
+    def __init__(self, numels, no_decay, dp_size=1, dp_rank=0):
+        lib = load_library()
+        numels = np.ascontiguousarray(numels, dtype=np.int64)
+        no_decay = np.ascontiguousarray(no_decay, dtype=np.uint8)
+        if numels.shape != no_decay.shape or numels.ndim != 1:
+            raise ValueError("numels and no_decay must be 1-D and the same length")
+        h = ctypes.c_void_p()
+        _check(lib.zero1_plan_create(numels.ctypes.data, no_decay.ctypes.data, len(numels), int(dp_size),
+                                     int(dp_rank), ctypes.byref(h)), "zero1_plan_create")
+        self._h = h
+        self._lib = lib
+        self.dp_size, self.dp_rank = int(dp_size), int(dp_rank)
+        self._no_decay = no_decay.copy()
+        self._layout = None
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.zero1_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def num_tensors(self):
+        return self._lib.zero1_plan_num_tensors(self._h)
+
+    @property
+    def total_numel(self):
+        return self._lib.zero1_plan_total_numel(self._h)
+
+    @property
+    def local_numel(self):
+        return self._lib.zero1_plan_local_numel(self._h)
+
+    @property
+    def arena_numel(self):
+        return self._lib.zero1_plan_arena_numel(self._h)
+
+    @property
+    def workspace_bytes(self):
+        return self._lib.zero1_workspace_bytes(self._h)
+
+    def tensor(self, i):
+        s, c, o = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.zero1_plan_tensor(self._h, int(i), ctypes.byref(s), ctypes.byref(c), ctypes.byref(o)),
+               "zero1_plan_tensor")
+        return s.value, c.value, o.value
+
+    def group_range(self, g):
+        b, e = ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.zero1_plan_group_range(self._h, int(g), ctypes.byref(b), ctypes.byref(e)),
+               "zero1_plan_group_range")
+        return b.value, e.value
+
+    def bytes(self, grad_bytes=2):
+        out = (ctypes.c_int64 * 4)()
+        _check(self._lib.zero1_plan_bytes(self._h, int(grad_bytes), out), "zero1_plan_bytes")
+        return {"weights": out[0], "grads": out[1], "optimizer": out[2], "total": out[3]}
+
+    def layout(self) -> ShardLayout:
+        if self._layout is None:
+            n = self.num_tensors
+            st, ct, of = np.zeros(n, np.int64), np.zeros(n, np.int64), np.zeros(n, np.int64)
+            for i in range(n):
+                st[i], ct[i], of[i] = self.tensor(i)
+            self._layout = ShardLayout(st, ct, of, self._no_decay.copy(), self.arena_numel)
+        return self._layout
+
+    # -- buffers (the caller owns them; these are conveniences) --
+    def new_arena(self, dtype=torch.float32, device="cuda"):
+        """A zero-filled arena buffer (zero padding, as the layout contract requires)."""
+        return torch.zeros(self.arena_numel, dtype=dtype, device=device)
+
+    def new_workspace(self, device="cuda"):
+        return torch.empty(max(self.workspace_bytes, 16), dtype=torch.uint8, device=device)
+
+    def shard_views(self, arena):
+        """Per-tensor views of an arena, in model order (empty shards give empty views)."""
+        L = self.layout()
+        return [arena[int(o):int(o) + int(c)] for o, c in zip(L.offsets, L.counts)]
+
+
+def new_norm_out(device="cuda"):
+    """Device buffer for a zero1_norm_out (24 bytes, 16-byte aligned)."""
+    return torch.zeros(32, dtype=torch.uint8, device=device)
+
+
+def accumulate(plan, grad, micro, overwrite_first=True, stream=None):
+    """zero1_accumulate: grad (fp32 arena) = [grad +] sum of the bf16 micro-batch arenas."""
+    lib = load_library()
+    micro = [micro] if isinstance(micro, torch.Tensor) else list(micro)
+    if not 1 <= len(micro) <= MAX_MICRO:
+        raise ValueError("1..%d micro-batch gradients per call" % MAX_MICRO)
+    n = plan.arena_numel
+    dev = grad.device
+    gp = _ptr(grad, torch.float32, n, "grad")
+    arr = (ctypes.c_void_p * len(micro))(*[_ptr(mb, torch.bfloat16, n, "micro[%d]" % k, dev).value
+                                           for k, mb in enumerate(micro)])
+    _check(lib.zero1_accumulate(plan.handle, gp, arr, len(micro), 1 if overwrite_first else 0,
+                                _stream_ptr(stream, dev)), "zero1_accumulate")
+
+
+def grad_norm(plan, grad, workspace, norm_out, extra_sumsq=0.0, stream=None):
+    """zero1_grad_norm: device {sumsq, norm, status} of the fp32 grad arena (+ extra_sumsq)."""
+    lib = load_library()
+    dev = norm_out.device
+    gp = _ptr(grad, torch.float32, plan.arena_numel, "grad", dev)
+    wp = _ptr(workspace, torch.uint8, None, "workspace", dev)
+    if workspace.numel() < plan.workspace_bytes:
+        raise ValueError("workspace has %d bytes, the plan needs %d" % (workspace.numel(), plan.workspace_bytes))
+    op = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    if norm_out.numel() < NORM_OUT_BYTES:
+        raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
+    _check(lib.zero1_grad_norm(plan.handle, gp, float(extra_sumsq), wp, workspace.numel(), op,
+                               _stream_ptr(stream, dev)), "zero1_grad_norm")
+
+
+def step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, hparams, step_t, norm_out=None, stream=None):
+    """zero1_step: fused clip + AdamW on the fp32 master/m/v arenas and the bf16 copy."""
+    lib = load_library()
+    n = plan.arena_numel
+    dev = master.device
+    ptrs = [_ptr(master, torch.float32, n, "master", dev), _ptr(exp_avg, torch.float32, n, "exp_avg", dev),
+            _ptr(exp_avg_sq, torch.float32, n, "exp_avg_sq", dev), _ptr(grad, torch.float32, n, "grad", dev)]
+    wp = None if weight_bf16 is None else _ptr(weight_bf16, torch.bfloat16, n, "weight_bf16", dev)
+    npp = None
+    if norm_out is not None:
+        npp = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    hp = hparams._c() if isinstance(hparams, Hparams) else Hparams(**hparams)._c()
+    _check(lib.zero1_step(plan.handle, *ptrs, wp, ctypes.byref(hp), int(step_t), npp, _stream_ptr(stream, dev)),
+           "zero1_step")
+
+
+def read_norm(norm_out, stream=None):
+    """zero1_read_norm: synchronise the stream and return the norm record as a dict."""
+    lib = load_library()
+    out = _NormOut()
+    _check(lib.zero1_read_norm(_ptr(norm_out, torch.uint8, None, "norm_out"),
+                               _stream_ptr(stream, norm_out.device), ctypes.byref(out)), "zero1_read_norm")
+    return {"sumsq": out.sumsq, "norm": out.norm, "status": out.status, "n_partials": out.n_partials}
+
+
+def allreduce_sumsq_(norm_out, group=None):
+    """Sum the ``sumsq`` field of a norm record across the ranks of ``group``, in place.
+
+    This is the step's one exchange: each rank's zero1_grad_norm gives its
+    local sum of squares, and after the all-reduce every rank's zero1_step
+    clips with the same global norm (and skips if any rank saw inf/NaN).
+    Works for a CUDA record with NCCL and a CPU record with gloo.
+    """
+    import torch.distributed as dist
+
+    dist.all_reduce(norm_out[:8].view(torch.float64), op=dist.ReduceOp.SUM, group=group)
+
+
+def decode_norm(norm_out_bytes):
+    """Decode a zero1_norm_out already copied to the host (a uint8 tensor / bytes)."""
+    b = bytes(norm_out_bytes.cpu().numpy().tobytes()) if isinstance(norm_out_bytes, torch.Tensor) else norm_out_bytes
+    o = _NormOut.from_buffer_copy(b[:NORM_OUT_BYTES])
+    return {"sumsq": o.sumsq, "norm": o.norm, "status": o.status, "n_partials": o.n_partials}
+
+
+class LocalShardAdamW:
+    """One data-parallel rank's ZeRO-1 optimizer shard, resident on one GPU.
+
+    Owns the arenas of the local shard (fp32 grad, master, m, v and the bf16
+    copy), the norm workspace and record, and the step counter.  A training
+    loop calls ``accumulate`` once per micro-batch and ``step`` once per
+    global batch; both only launch kernels on the current stream.
+    """
+
+    def __init__(self, numels, no_decay, dp_size=1, dp_rank=0, hparams=None, device="cuda"):
+        self.device = torch.device(device)
+        self.plan = Plan(numels, no_decay, dp_size, dp_rank)
+        self.hp = hparams if isinstance(hparams, Hparams) else Hparams(**(hparams or {}))
+        mk = self.plan.new_arena
+        self.grad = mk(torch.float32, self.device)
+        self.master = mk(torch.float32, self.device)
+        self.exp_avg = mk(torch.float32, self.device)
+        self.exp_avg_sq = mk(torch.float32, self.device)
+        self.weight_bf16 = mk(torch.bfloat16, self.device)
+        self.workspace = self.plan.new_workspace(self.device)
+        self.norm_out = new_norm_out(self.device)
+        self.t = 0
+        self._micro_seen = 0
+
+    def accumulate(self, micro, stream=None):
+        """Add one (or several) bf16 micro-batch gradient arenas; the first call of a step overwrites."""
+        accumulate(self.plan, self.grad, micro, overwrite_first=(self._micro_seen == 0), stream=stream)
+        self._micro_seen += 1 if isinstance(micro, torch.Tensor) else len(micro)
+
+    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None):
+        """Norm + clip + AdamW + bf16 copy; returns nothing (read_norm() syncs).
+
+        With ``group`` (a torch.distributed process group of the data-parallel
+        ranks) the local sum of squares is all-reduced before the update."""
+        grad_norm(self.plan, self.grad, self.workspace, self.norm_out, extra_sumsq, stream=stream)
+        if group is not None:
+            allreduce_sumsq_(self.norm_out, group)
+        self.t += 1
+        hp = self.hp if lr is None else Hparams(**{**self.hp.__dict__, "lr": lr})
+        step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
+             self.norm_out, stream=stream)
+        self._micro_seen = 0
+
+    def read_norm(self, stream=None):
+        return read_norm(self.norm_out, stream=stream)

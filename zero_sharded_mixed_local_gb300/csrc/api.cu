@@ -1,0 +1,151 @@
+// C entry points of the compute calls: argument checks, derivation of the
+// fp32 step scalars, and the kernel launches.  Nothing here allocates device
+// memory or synchronises, except zero1_read_norm.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "zero1_internal.h"
+
+namespace {
+
+thread_local char g_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+    std::snprintf(g_cuda_error, sizeof g_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return ZERO1_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];  // 0 = not queried yet
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (dev < kMaxDevices) g_sm_count[dev] = n;
+    return n;
+}
+
+}  // namespace
+
+namespace zero1 {
+
+int64_t streaming_grid(const void* kernel, int threads, int64_t work_items) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm <= 0)
+        per_sm = 1;
+    const int64_t full = static_cast<int64_t>(sm_count()) * per_sm;
+    const int64_t need = (work_items + threads - 1) / threads;
+    int64_t g = need < full ? need : full;
+    return g < 1 ? 1 : g;
+}
+
+}  // namespace zero1
+
+extern "C" int zero1_accumulate(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
+                                int32_t n_micro, int32_t overwrite_first, void* stream) {
+    if (plan == nullptr || micro_bf16 == nullptr) return ZERO1_EINVAL;
+    if (n_micro < 1 || n_micro > ZERO1_MAX_MICRO) return ZERO1_EINVAL;
+    if (plan->arena_numel == 0) return ZERO1_OK;  // nothing to do; empty buffers may be NULL
+    if (grad == nullptr) return ZERO1_EINVAL;
+    zero1::AccumulateParams p{};
+    p.grad = grad;
+    for (int k = 0; k < n_micro; ++k) {
+        if (micro_bf16[k] == nullptr) return ZERO1_EINVAL;
+        if (!aligned16(micro_bf16[k])) return ZERO1_EALIGN;
+        p.micro[k] = micro_bf16[k];
+    }
+    if (!aligned16(grad)) return ZERO1_EALIGN;
+    p.n_micro = n_micro;
+    p.overwrite_first = overwrite_first ? 1 : 0;
+    p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
+    const cudaError_t e = zero1::launch_accumulate(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+extern "C" int zero1_grad_norm(const zero1_plan* plan, const float* grad, double extra_sumsq, void* workspace,
+                               size_t workspace_bytes, zero1_norm_out* d_out, void* stream) {
+    if (plan == nullptr || d_out == nullptr) return ZERO1_EINVAL;
+    const int64_t n_tiles = zero1::norm_tiles(plan->arena_numel);
+    if (n_tiles > 0) {
+        if (grad == nullptr || workspace == nullptr) return ZERO1_EINVAL;
+        if (workspace_bytes < static_cast<size_t>(n_tiles) * sizeof(double)) return ZERO1_EINVAL;
+        if (!aligned16(grad) || !aligned16(workspace)) return ZERO1_EALIGN;
+    }
+    if (!aligned16(d_out)) return ZERO1_EALIGN;
+    if (std::isnan(extra_sumsq) || extra_sumsq < 0.0) return ZERO1_EINVAL;
+    const cudaError_t e = zero1::launch_grad_norm(grad, plan->arena_numel, static_cast<double*>(workspace), n_tiles,
+                                                  extra_sumsq, d_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
+                          const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                          const zero1_norm_out* d_norm, void* stream) {
+    if (plan == nullptr || hp == nullptr || step_t < 1) return ZERO1_EINVAL;
+    const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+    if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd) || !std::isfinite(hp->clip_grad))
+        return ZERO1_EINVAL;
+    if (!(b1 >= 0.0 && b1 < 1.0) || !(b2 >= 0.0 && b2 < 1.0) || eps < 0.0) return ZERO1_EINVAL;
+    if (plan->arena_numel == 0) return ZERO1_OK;  // nothing to do; empty buffers may be NULL
+    if (master == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || grad == nullptr) return ZERO1_EINVAL;
+    if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) || !aligned16(grad)) return ZERO1_EALIGN;
+    if (weight_bf16 != nullptr && !aligned16(weight_bf16)) return ZERO1_EALIGN;
+    if (d_norm != nullptr && !aligned16(d_norm)) return ZERO1_EALIGN;
+
+    // Step scalars in double, each rounded once to fp32.
+    const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step_t));
+    const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step_t));
+    if (!(bc1 > 0.0) || !(bc2 > 0.0)) return ZERO1_EINVAL;
+
+    zero1::StepParams p{};
+    p.master = master;
+    p.m = exp_avg;
+    p.v = exp_avg_sq;
+    p.grad = grad;
+    p.w = weight_bf16;
+    p.norm = d_norm;
+    p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
+    for (int g = 0; g < ZERO1_NUM_GROUPS; ++g) {
+        p.group_begin_vec[g] = plan->group_begin[g] / ZERO1_ARENA_ALIGN;
+        p.stepsize[g] = static_cast<float>(lr / bc1);
+    }
+    p.dfac[0] = static_cast<float>(1.0 - lr * wd);  // decayed group
+    p.dfac[1] = 1.0f;                               // excluded from weight decay
+    p.b1 = static_cast<float>(b1);
+    p.b2 = static_cast<float>(b2);
+    p.omb1 = static_cast<float>(1.0 - b1);
+    p.omb2 = static_cast<float>(1.0 - b2);
+    p.eps = static_cast<float>(eps);
+    p.sqrtbc2 = static_cast<float>(std::sqrt(bc2));
+    p.clip = hp->clip_grad;
+    const cudaError_t e = zero1::launch_step(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+extern "C" int zero1_read_norm(const zero1_norm_out* d_norm, void* stream, zero1_norm_out* host_out) {
+    if (d_norm == nullptr || host_out == nullptr) return ZERO1_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(host_out, d_norm, sizeof(zero1_norm_out), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+extern "C" const char* zero1_strerror(int code) {
+    switch (code) {
+        case ZERO1_OK: return "ok";
+        case ZERO1_EINVAL: return "invalid argument";
+        case ZERO1_EALIGN: return "buffer not 16-byte aligned";
+        case ZERO1_ECUDA: return "CUDA error";
+        case ZERO1_ENONFINITE: return "gradient norm is not finite; step skipped";
+        case ZERO1_ENOMEM: return "out of host memory";
+        default: return "unknown status";
+    }
+}
+
+extern "C" const char* zero1_last_cuda_error(void) { return g_cuda_error; }

@@ -1,0 +1,67 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "zero1.h"
+
+struct zero1_plan {
+    int32_t n_tensors = 0;
+    int32_t dp_size = 1;
+    int32_t dp_rank = 0;
+    std::vector<int64_t> numel;
+    std::vector<int64_t> shard_start;
+    std::vector<int64_t> shard_numel;
+    std::vector<int64_t> arena_offset;
+    std::vector<uint8_t> group;
+    int64_t total_numel = 0;
+    int64_t local_numel = 0;
+    int64_t arena_numel = 0;
+    int64_t group_begin[ZERO1_NUM_GROUPS] = {};
+    int64_t group_end[ZERO1_NUM_GROUPS] = {};
+};
+
+namespace zero1 {
+
+// Elements per partial sum of the gradient norm; also fixes the reduction order.
+constexpr int64_t kNormTile = 16384;
+
+inline int64_t norm_tiles(int64_t arena_numel) { return (arena_numel + kNormTile - 1) / kNormTile; }
+
+// Launch parameters, passed by value (kernel parameter space).
+struct AccumulateParams {
+    float* grad;
+    const uint16_t* micro[ZERO1_MAX_MICRO];
+    int32_t n_micro;
+    int32_t overwrite_first;
+    int64_t n_vec;  // arena_numel / 8
+};
+
+struct StepParams {
+    float* master;
+    float* m;
+    float* v;
+    const float* grad;
+    uint16_t* w;
+    const zero1_norm_out* norm;  // may be null: no clipping
+    int64_t n_vec;               // arena_numel / 8
+    int64_t group_begin_vec[ZERO1_NUM_GROUPS];  // first 8-element vector of each group
+    float dfac[ZERO1_NUM_GROUPS];
+    float stepsize[ZERO1_NUM_GROUPS];
+    float b1, b2, omb1, omb2, eps, sqrtbc2;
+    double clip;
+};
+
+cudaError_t launch_accumulate(const AccumulateParams& p, cudaStream_t stream);
+cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int64_t n_tiles,
+                             double extra_sumsq, zero1_norm_out* out, cudaStream_t stream);
+cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
+
+// Grid size for a grid-stride streaming kernel: enough blocks to fill every SM
+// at the kernel's occupancy, never more than there is work for.
+int64_t streaming_grid(const void* kernel, int threads, int64_t work_items);
+
+}  // namespace zero1
