@@ -49,6 +49,7 @@ extern "C" {
 #define ZERO1_ECUDA (-3)      /* a CUDA call or launch failed; see zero1_last_cuda_error() */
 #define ZERO1_ENONFINITE (-4) /* device status: the gradient norm is inf or NaN */
 #define ZERO1_ENOMEM (-5)     /* host allocation failed while building a plan */
+#define ZERO1_ETOOBIG (-6)    /* the arena exceeds zero1_grad_norm_static's fixed scratch */
 
 /* Each shard starts on a multiple of this many elements inside an arena, so
  * that 16-byte vector loads of bf16 (8 elements) never straddle tensors. */
@@ -210,6 +211,34 @@ int zero1_grad_norm(const zero1_plan* plan, const float* grad, double extra_sums
 int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
                const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
                const zero1_norm_out* d_norm, void* stream);
+
+/* Largest plan zero1_grad_norm_static serves: its fixed scratch holds one
+ * double per 16384-element tile, 262144 tiles (2 MiB per GPU), i.e. arenas of
+ * up to 2^32 elements. */
+#define ZERO1_STATIC_NORM_MAX_TILES 262144
+#define ZERO1_STATIC_NORM_MAX_NUMEL ((int64_t)ZERO1_STATIC_NORM_MAX_TILES * 16384)
+
+/* zero1_grad_norm without a workspace argument: same result, bit for bit, but
+ * the per-tile partial sums live in a fixed array inside the library, so the
+ * call allocates nothing and the caller needs no scratch buffer.  The pages
+ * have no counterpart of this call; it exists for callers that cannot supply
+ * or allocate device scratch: a plain C program with no device allocator of
+ * its own, a process whose framework allocator already holds nearly all of
+ * the GPU's memory, or a step that must not call cudaMalloc/cudaFree (which
+ * can synchronise the device).
+ *   grad, extra_sumsq, d_out, stream   as for zero1_grad_norm
+ * Limits and sharing: arenas above ZERO1_STATIC_NORM_MAX_NUMEL elements are
+ * rejected with ZERO1_ETOOBIG before any launch.  The 2 MiB array stays
+ * allocated on every GPU that loads the library until the process exits.
+ * All calls on a device share it; nothing in it needs to start at zero
+ * (each call writes every partial it reads first), but calls whose kernels
+ * overlap on the GPU (different streams or threads) race on it, so the
+ * caller must serialise them.  The first call on each device looks up the
+ * array's device address with that device current; make that first call
+ * before any stream capture.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ETOOBIG, ZERO1_ECUDA. */
+int zero1_grad_norm_static(const zero1_plan* plan, const float* grad, double extra_sumsq,
+                           zero1_norm_out* d_out, void* stream);
 
 /* Copy a device zero1_norm_out to the host, synchronising `stream` first.
  * Errors: ZERO1_EINVAL, ZERO1_ECUDA. */

@@ -21,6 +21,8 @@ ZERO1_EALIGN = -2
 ZERO1_ECUDA = -3
 ZERO1_ENONFINITE = -4
 ZERO1_ENOMEM = -5
+ZERO1_ETOOBIG = -6
+STATIC_NORM_MAX_NUMEL = 262144 * 16384
 ARENA_ALIGN = 8
 NUM_GROUPS = 2
 MAX_MICRO = 16
@@ -72,6 +74,7 @@ def load_library(path=None):
         "zero1_workspace_bytes": (ctypes.c_size_t, [vp]),
         "zero1_accumulate": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, i32, vp]),
         "zero1_grad_norm": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
+        "zero1_grad_norm_static": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, vp]),
         "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
         "zero1_read_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(_NormOut)]),
         "zero1_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -266,6 +269,27 @@ def grad_norm(plan, grad, workspace, norm_out, extra_sumsq=0.0, stream=None):
         raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
     _check(lib.zero1_grad_norm(plan.handle, gp, float(extra_sumsq), wp, workspace.numel(), op,
                                _stream_ptr(stream, dev)), "zero1_grad_norm")
+
+
+def grad_norm_static(plan, grad, norm_out, extra_sumsq=0.0, stream=None):
+    """zero1_grad_norm_static: the same norm record as grad_norm(), with no workspace.
+
+    For callers that cannot allocate or supply device scratch: the partial
+    sums go to a fixed 2 MiB array inside the library (arenas up to
+    STATIC_NORM_MAX_NUMEL elements).  Calls that overlap on the GPU share that
+    array and race; the first call on a device should precede any stream
+    capture."""
+    lib = load_library()
+    if plan.arena_numel > STATIC_NORM_MAX_NUMEL:
+        raise ValueError("arena of %d elements exceeds the static norm scratch limit of %d elements"
+                         % (plan.arena_numel, STATIC_NORM_MAX_NUMEL))
+    dev = norm_out.device
+    gp = _ptr(grad, torch.float32, plan.arena_numel, "grad", dev)
+    op = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    if norm_out.numel() < NORM_OUT_BYTES:
+        raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
+    _check(lib.zero1_grad_norm_static(plan.handle, gp, float(extra_sumsq), op, _stream_ptr(stream, dev)),
+           "zero1_grad_norm_static")
 
 
 def step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, hparams, step_t, norm_out=None, stream=None):

@@ -35,6 +35,8 @@ int sm_count() {
 
 namespace zero1 {
 
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 int64_t streaming_grid(const void* kernel, int threads, int64_t work_items) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm <= 0)
@@ -144,6 +146,7 @@ extern "C" const char* zero1_strerror(int code) {
         case ZERO1_ECUDA: return "CUDA error";
         case ZERO1_ENONFINITE: return "gradient norm is not finite; step skipped";
         case ZERO1_ENOMEM: return "out of host memory";
+        case ZERO1_ETOOBIG: return "arena larger than the static norm scratch allows (ZERO1_STATIC_NORM_MAX_NUMEL)";
         default: return "unknown status";
     }
 }

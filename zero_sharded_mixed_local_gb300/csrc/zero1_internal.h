@@ -28,6 +28,7 @@ namespace zero1 {
 
 // Elements per partial sum of the gradient norm; also fixes the reduction order.
 constexpr int64_t kNormTile = 16384;
+static_assert(ZERO1_STATIC_NORM_MAX_NUMEL == ZERO1_STATIC_NORM_MAX_TILES * kNormTile, "static norm limit");
 
 inline int64_t norm_tiles(int64_t arena_numel) { return (arena_numel + kNormTile - 1) / kNormTile; }
 
@@ -59,6 +60,9 @@ cudaError_t launch_accumulate(const AccumulateParams& p, cudaStream_t stream);
 cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int64_t n_tiles,
                              double extra_sumsq, zero1_norm_out* out, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
+
+// Record a CUDA error for zero1_last_cuda_error() and return ZERO1_ECUDA.
+int record_cuda_error(cudaError_t e);
 
 // Grid size for a grid-stride streaming kernel: enough blocks to fill every SM
 // at the kernel's occupancy, never more than there is work for.
