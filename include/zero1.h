@@ -141,8 +141,8 @@ int zero1_plan_group_range(const zero1_plan* plan, int32_t g, int64_t* begin, in
  *               total}, in bytes */
 int zero1_plan_bytes(const zero1_plan* plan, int32_t grad_bytes, int64_t out[4]);
 
-/* Device workspace zero1_grad_norm needs (one double per 16384-element tile
- * of the arena); 0 for an empty arena. */
+/* Device workspace zero1_grad_norm needs (8 bytes, one float pair, per
+ * 16384-element tile of the arena); 0 for an empty arena. */
 size_t zero1_workspace_bytes(const zero1_plan* plan);
 
 /* ---- compute (asynchronous on `stream`) ---------------------------------- */
@@ -166,12 +166,11 @@ int zero1_accumulate(const zero1_plan* plan, float* grad, const uint16_t* const*
  * Optimizer", section 6.6, clip_grad).  sumsq = sum over the arena of grad^2
  * (padding adds 0) + extra_sumsq, where extra_sumsq is the other ranks' share
  * of the global sum (0 when this rank is alone); norm = sqrt(sumsq), in
- * double.  Per 16384-element tile each thread sums the squares of its (at
- * most 64) elements in compensated fp32 (the rounding errors of every square
- * and every addition are carried in a second float), and the thread and tile
- * sums are added in double, in a fixed order: the result is within a few
- * double ulps of the exact sum, deterministic, and independent of launch
- * shape.
+ * double.  Every partial sum is an unevaluated pair of floats (hi + lo) that
+ * carries the exact rounding error of each square and of each addition, so
+ * the total is within ~1e-13 relative of the exact sum of squares; the
+ * reduction order is fixed by 16384-element tiles, so the result is
+ * deterministic and independent of launch shape.
  *   grad        device fp32 arena, read only
  *   workspace   device scratch of zero1_workspace_bytes(plan) bytes
  *               (may be NULL when that is 0); contents are overwritten
@@ -213,8 +212,8 @@ int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp
                const zero1_norm_out* d_norm, void* stream);
 
 /* Largest plan zero1_grad_norm_static serves: its fixed scratch holds one
- * double per 16384-element tile, 262144 tiles (2 MiB per GPU), i.e. arenas of
- * up to 2^32 elements. */
+ * 8-byte partial per 16384-element tile, 262144 tiles (2 MiB per GPU), i.e.
+ * arenas of up to 2^32 elements. */
 #define ZERO1_STATIC_NORM_MAX_TILES 262144
 #define ZERO1_STATIC_NORM_MAX_NUMEL ((int64_t)ZERO1_STATIC_NORM_MAX_TILES * 16384)
 

@@ -9,13 +9,17 @@
 //     d = sqrt(v)/sqrtbc2 + eps;  p = p - stepsize*(m/d);  w = bf16_rne(p)
 //
 // Memory-bound: 16 bytes read (grad, master, m, v) and 14 written (master, m,
-// v, bf16) per element, ~20 fp32 operations.  The arena is streamed flat with
-// 16-byte vector accesses, 8 elements per thread per iteration, from a grid
-// sized to fill every SM once (grid-stride).  The weight-decay group of a
-// vector is found by comparing its index with the group boundaries (groups
-// are contiguous in the arena), so no per-tensor table is read.  The
-// rounding-explicit intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn, __fsqrt_rn)
-// are never contracted into FMAs, which keeps the operation order exact.
+// v, bf16) per element, ~20 fp32 operations.  One thread owns one 8-element
+// vector and the grid covers the whole arena (one wave after another, no
+// grid-stride loop): on GB300 this keeps DRAM busier than a persistent grid,
+// which measured ~20% slower because too few loads were in flight per SM.
+// Each thread issues its eight 16-byte loads before thread 0 derives the clip
+// coefficient from the device-resident norm, so that prologue hides under the
+// load latency.  The weight-decay group of a vector is found by comparing its
+// index with the group boundaries (groups are contiguous in the arena), so no
+// per-tensor table is read.  The rounding-explicit intrinsics (__fmul_rn,
+// __fadd_rn, __fdiv_rn, __fsqrt_rn) are never contracted into FMAs, which
+// keeps the operation order exact.
 #include <cuda_bf16.h>
 
 #include "zero1_internal.h"
@@ -45,9 +49,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 template <bool kWriteBf16>
-__global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_constant__ StepParams P) {
+__global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_constant__ StepParams P, int64_t first_vec) {
     __shared__ float s_coef;
     __shared__ int s_skip;
+    const int64_t i = first_vec + static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x;
+    const bool live = i < P.n_vec;
+
+    // Loads first: they do not depend on the clip coefficient.
+    float4 ga, gb, pa, pb, ma, mb, va, vb;
+    if (live) {
+        const float4* g4 = reinterpret_cast<const float4*>(P.grad) + 2 * i;
+        const float4* p4 = reinterpret_cast<const float4*>(P.master) + 2 * i;
+        const float4* m4 = reinterpret_cast<const float4*>(P.m) + 2 * i;
+        const float4* v4 = reinterpret_cast<const float4*>(P.v) + 2 * i;
+        ga = g4[0];
+        gb = g4[1];
+        pa = p4[0];
+        pb = p4[1];
+        ma = m4[0];
+        mb = m4[1];
+        va = v4[0];
+        vb = v4[1];
+    }
     if (threadIdx.x == 0) {
         // Clip coefficient from the device-resident norm: no host round trip.
         float coef = 1.0f;
@@ -67,70 +90,62 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
         s_skip = skip;
     }
     __syncthreads();
-    if (s_skip) return;  // non-finite gradient norm: leave every buffer as it is
+    if (s_skip || !live) return;  // a non-finite gradient norm leaves every buffer as it is
 
     const float coef = s_coef;
     const StepConsts c{P.b1, P.b2, P.omb1, P.omb2, P.eps, P.sqrtbc2};
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < P.n_vec; i += stride) {
-        float dfac = P.dfac[0];
-        float stepsize = P.stepsize[0];
+    float dfac = P.dfac[0];
+    float stepsize = P.stepsize[0];
 #pragma unroll
-        for (int k = 1; k < ZERO1_NUM_GROUPS; ++k) {
-            if (i >= P.group_begin_vec[k]) {
-                dfac = P.dfac[k];
-                stepsize = P.stepsize[k];
-            }
+    for (int k = 1; k < ZERO1_NUM_GROUPS; ++k) {
+        if (i >= P.group_begin_vec[k]) {
+            dfac = P.dfac[k];
+            stepsize = P.stepsize[k];
         }
-        const float4* g4 = reinterpret_cast<const float4*>(P.grad) + 2 * i;
-        float4* p4 = reinterpret_cast<float4*>(P.master) + 2 * i;
-        float4* m4 = reinterpret_cast<float4*>(P.m) + 2 * i;
-        float4* v4 = reinterpret_cast<float4*>(P.v) + 2 * i;
-        // Issue all eight 16-byte loads before any arithmetic.
-        const float4 ga = g4[0], gb = g4[1];
-        float4 pa = p4[0], pb = p4[1];
-        float4 ma = m4[0], mb = m4[1];
-        float4 va = v4[0], vb = v4[1];
+    }
+    adamw_elem(pa.x, ma.x, va.x, ga.x, coef, dfac, stepsize, c);
+    adamw_elem(pa.y, ma.y, va.y, ga.y, coef, dfac, stepsize, c);
+    adamw_elem(pa.z, ma.z, va.z, ga.z, coef, dfac, stepsize, c);
+    adamw_elem(pa.w, ma.w, va.w, ga.w, coef, dfac, stepsize, c);
+    adamw_elem(pb.x, mb.x, vb.x, gb.x, coef, dfac, stepsize, c);
+    adamw_elem(pb.y, mb.y, vb.y, gb.y, coef, dfac, stepsize, c);
+    adamw_elem(pb.z, mb.z, vb.z, gb.z, coef, dfac, stepsize, c);
+    adamw_elem(pb.w, mb.w, vb.w, gb.w, coef, dfac, stepsize, c);
 
-        adamw_elem(pa.x, ma.x, va.x, ga.x, coef, dfac, stepsize, c);
-        adamw_elem(pa.y, ma.y, va.y, ga.y, coef, dfac, stepsize, c);
-        adamw_elem(pa.z, ma.z, va.z, ga.z, coef, dfac, stepsize, c);
-        adamw_elem(pa.w, ma.w, va.w, ga.w, coef, dfac, stepsize, c);
-        adamw_elem(pb.x, mb.x, vb.x, gb.x, coef, dfac, stepsize, c);
-        adamw_elem(pb.y, mb.y, vb.y, gb.y, coef, dfac, stepsize, c);
-        adamw_elem(pb.z, mb.z, vb.z, gb.z, coef, dfac, stepsize, c);
-        adamw_elem(pb.w, mb.w, vb.w, gb.w, coef, dfac, stepsize, c);
-
-        p4[0] = pa;
-        p4[1] = pb;
-        m4[0] = ma;
-        m4[1] = mb;
-        v4[0] = va;
-        v4[1] = vb;
-        if (kWriteBf16) {
-            uint4 w;
-            w.x = pack_bf16x2(pa.x, pa.y);
-            w.y = pack_bf16x2(pa.z, pa.w);
-            w.z = pack_bf16x2(pb.x, pb.y);
-            w.w = pack_bf16x2(pb.z, pb.w);
-            reinterpret_cast<uint4*>(P.w)[i] = w;
-        }
+    float4* p4 = reinterpret_cast<float4*>(P.master) + 2 * i;
+    float4* m4 = reinterpret_cast<float4*>(P.m) + 2 * i;
+    float4* v4 = reinterpret_cast<float4*>(P.v) + 2 * i;
+    p4[0] = pa;
+    p4[1] = pb;
+    m4[0] = ma;
+    m4[1] = mb;
+    v4[0] = va;
+    v4[1] = vb;
+    if (kWriteBf16) {
+        uint4 w;
+        w.x = pack_bf16x2(pa.x, pa.y);
+        w.y = pack_bf16x2(pa.z, pa.w);
+        w.z = pack_bf16x2(pb.x, pb.y);
+        w.w = pack_bf16x2(pb.z, pb.w);
+        reinterpret_cast<uint4*>(P.w)[i] = w;
     }
 }
 
 }  // namespace
 
 cudaError_t launch_step(const StepParams& p, cudaStream_t stream) {
-    if (p.n_vec == 0) return cudaSuccess;
-    const bool bf16 = p.w != nullptr;
-    const void* fn = bf16 ? reinterpret_cast<const void*>(&adamw_step_kernel<true>)
-                          : reinterpret_cast<const void*>(&adamw_step_kernel<false>);
-    const int64_t grid = streaming_grid(fn, kStepThreads, p.n_vec);
-    if (bf16)
-        adamw_step_kernel<true><<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(p);
-    else
-        adamw_step_kernel<false><<<static_cast<unsigned>(grid), kStepThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    // One thread per 8-element vector; grids beyond the launch limit are split.
+    for (int64_t first = 0; first < p.n_vec; first += kMaxGridVectors(kStepThreads)) {
+        const int64_t n = p.n_vec - first < kMaxGridVectors(kStepThreads) ? p.n_vec - first : kMaxGridVectors(kStepThreads);
+        const unsigned grid = static_cast<unsigned>((n + kStepThreads - 1) / kStepThreads);
+        if (p.w != nullptr)
+            adamw_step_kernel<true><<<grid, kStepThreads, 0, stream>>>(p, first);
+        else
+            adamw_step_kernel<false><<<grid, kStepThreads, 0, stream>>>(p, first);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace zero1

@@ -18,34 +18,11 @@ int cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];  // 0 = not queried yet
-
-int sm_count() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-    if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    if (dev < kMaxDevices) g_sm_count[dev] = n;
-    return n;
-}
-
 }  // namespace
 
 namespace zero1 {
 
 int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
-
-int64_t streaming_grid(const void* kernel, int threads, int64_t work_items) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm <= 0)
-        per_sm = 1;
-    const int64_t full = static_cast<int64_t>(sm_count()) * per_sm;
-    const int64_t need = (work_items + threads - 1) / threads;
-    int64_t g = need < full ? need : full;
-    return g < 1 ? 1 : g;
-}
 
 }  // namespace zero1
 

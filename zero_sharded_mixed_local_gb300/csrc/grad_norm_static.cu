@@ -10,7 +10,7 @@
 // cudaMalloc/cudaFree mid-step because those can synchronise the whole device.
 //
 // Costs and rules:
-//   - The array holds ZERO1_STATIC_NORM_MAX_TILES doubles (2 MiB).  Every GPU
+//   - The array holds ZERO1_STATIC_NORM_MAX_TILES 8-byte partials (2 MiB).  Every GPU
 //     that loads the library keeps it allocated until the process exits.
 //   - It covers arenas of up to ZERO1_STATIC_NORM_MAX_NUMEL elements; larger
 //     plans are rejected with ZERO1_ETOOBIG before anything is launched.

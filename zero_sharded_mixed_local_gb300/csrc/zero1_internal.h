@@ -64,8 +64,7 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
 // Record a CUDA error for zero1_last_cuda_error() and return ZERO1_ECUDA.
 int record_cuda_error(cudaError_t e);
 
-// Grid size for a grid-stride streaming kernel: enough blocks to fill every SM
-// at the kernel's occupancy, never more than there is work for.
-int64_t streaming_grid(const void* kernel, int threads, int64_t work_items);
+// Work items one full-grid launch may cover (2^31 - 1 blocks of `threads`).
+constexpr int64_t kMaxGridVectors(int threads) { return static_cast<int64_t>(0x7fffffff) * threads; }
 
 }  // namespace zero1
