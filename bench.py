@@ -1,8 +1,9 @@
 """Benchmark of the ZeRO-1 local-shard optimizer step on one GB300 (or N, one rank per GPU).
 
 One "step" is the whole hot path over one batch of synthetic gradients:
-  K x zero1_accumulate (bf16 micro-batch gradient -> fp32 grad), zero1_grad_norm,
-  zero1_step (clip + AdamW on fp32 master/m/v + bf16 weight copy).
+  K-1 x zero1_accumulate (bf16 micro-batch gradient -> fp32 grad), zero1_accumulate_norm
+  (the last micro-batch and the gradient norm in one pass), zero1_step (clip + AdamW on
+  fp32 master/m/v + bf16 weight copy).
 Default workload: the Llama-3.1-8B-shaped parameter list sharded over dp=8, rank 0
 (1,003,782,656 local parameters, K=1).  Prints one JSON line (rank 0).
 
@@ -30,7 +31,6 @@ if ROOT not in sys.path:
 
 METRIC = "AdamW shard-step params/sec and HBM GB/s (fraction of GB300 peak), 1 GPU"
 STEP_BYTES_PER_ELEM = 30          # adamw_step: grad 4 R, master/m/v 12 R + 12 W, bf16 2 W
-NORM_BYTES_PER_ELEM = 4           # grad_norm: grad 4 R
 
 
 def accumulate_bytes_per_elem(k):
@@ -278,11 +278,12 @@ def main():
         t_counter[0] += 1
         if record is not None:
             record["a0"].record(stream)
-        for k in range(K):
+        for k in range(K - 1):
             z.accumulate(plan, grad, micros[k], overwrite_first=(k == 0), stream=stream)
         if record is not None:
             record["n0"].record(stream)
-        z.grad_norm(plan, grad, ws, nout, 0.0, stream=stream)
+        # the last micro-batch's accumulation also takes the gradient norm
+        z.accumulate_norm(plan, grad, micros[K - 1], ws, nout, overwrite_first=(K == 1), stream=stream)
         if group is not None:
             z.allreduce_sumsq_(nout, group)
         if record is not None:
@@ -314,14 +315,16 @@ def main():
     total_ms = start.elapsed_time(end)
     total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
-    acc_ms = statistics.mean(r["a0"].elapsed_time(r["n0"]) for r in recs)
-    norm_ms = statistics.mean(r["n0"].elapsed_time(r["s0"]) for r in recs)
+    acc_ms = statistics.mean(r["a0"].elapsed_time(r["n0"]) for r in recs)      # the first K-1 micro-batches
+    accnorm_ms = statistics.mean(r["n0"].elapsed_time(r["s0"]) for r in recs)  # last micro-batch + norm
     step_ms = statistics.mean(r["s0"].elapsed_time(r["s1"]) for r in recs)
     z.read_norm(nout, stream)
 
     peak, peak_kind = measured_peaks()
     step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9
-    path_bytes = (accumulate_bytes_per_elem(K) + NORM_BYTES_PER_ELEM + STEP_BYTES_PER_ELEM) * P
+    # the norm is fused into the last micro-batch's pass: no separate 4-byte read
+    path_bytes = (accumulate_bytes_per_elem(K) + STEP_BYTES_PER_ELEM) * P
+    last_bytes = (6 if K == 1 else 10) * P
     traffic = profile_traffic("adamw_step.cu", args.workload)
 
     # ---- end to end through the public API: pinned host gradients in, norm record out
@@ -334,8 +337,10 @@ def main():
         def e2e_step():
             for k in range(K):
                 dev_micros[k].copy_(host_micros[k], non_blocking=True)
-                z.accumulate(plan, grad, dev_micros[k], overwrite_first=(k == 0), stream=stream)
-            z.grad_norm(plan, grad, ws, nout, 0.0, stream=stream)
+                if k < K - 1:
+                    z.accumulate(plan, grad, dev_micros[k], overwrite_first=(k == 0), stream=stream)
+                else:
+                    z.accumulate_norm(plan, grad, dev_micros[k], ws, nout, overwrite_first=(K == 1), stream=stream)
             if group is not None:
                 z.allreduce_sumsq_(nout, group)
             opt_t[0] += 1
@@ -390,10 +395,10 @@ def main():
             },
             "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
             "kernels": {
-                "accumulate": {"ms": acc_ms, "gbs": accumulate_bytes_per_elem(K) * P / (acc_ms * 1e-3) / 1e9,
-                               "launches_per_step": K},
-                "grad_norm": {"ms": norm_ms, "gbs": NORM_BYTES_PER_ELEM * P / (norm_ms * 1e-3) / 1e9,
-                              "launches_per_step": 2},
+                "accumulate": {"ms": acc_ms, "gbs": (accumulate_bytes_per_elem(K) * P - last_bytes) /
+                               (acc_ms * 1e-3) / 1e9 if K > 1 else None, "launches_per_step": K - 1},
+                "accumulate_norm": {"ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
+                                    "launches_per_step": 2},
                 "adamw_step": {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
             },
             "roofline": {"bound": "hbm", "kernel": "adamw_step_kernel", "achieved": step_gbs, "peak": peak,
@@ -403,7 +408,7 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "gpu_launches": args.steps * (K + 3),
+            "gpu_launches": args.steps * (K + 2),
         }
         print(json.dumps(out), flush=True)
     if world > 1:

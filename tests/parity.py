@@ -62,11 +62,17 @@ class Problem:
         self.ws = self.plan.new_workspace(self.dev)
         self.nout = z.new_norm_out(self.dev)
 
-    def gpu_step(self, micros, t, extra_sumsq=0.0):
-        z.accumulate(self.plan, self.grad, micros[0], overwrite_first=True)
-        for mb in micros[1:]:
-            z.accumulate(self.plan, self.grad, mb, overwrite_first=False)
-        z.grad_norm(self.plan, self.grad, self.ws, self.nout, extra_sumsq)
+    def gpu_step(self, micros, t, extra_sumsq=0.0, fused=True):
+        """One step as bench.py runs it: the last micro-batch's accumulation takes the norm
+        (fused=True), or separate accumulate and grad_norm calls (fused=False)."""
+        last = len(micros) - 1
+        for k, mb in enumerate(micros[:last] if fused else micros):
+            z.accumulate(self.plan, self.grad, mb, overwrite_first=(k == 0))
+        if fused:
+            z.accumulate_norm(self.plan, self.grad, micros[last], self.ws, self.nout, overwrite_first=(last == 0),
+                              extra_sumsq=extra_sumsq)
+        else:
+            z.grad_norm(self.plan, self.grad, self.ws, self.nout, extra_sumsq)
         z.step(self.plan, self.master, self.m, self.v, self.grad, self.wbf, self.hp, t, self.nout)
         return z.read_norm(self.nout)
 
@@ -106,7 +112,7 @@ def oracle_pass(micros, gpu_grad, idx):
     return g_idx, s
 
 
-def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda", seed=None):
+def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda", seed=None, fused=True):
     """Run `steps` steps on GPU and oracle; assert parity.  `sample`: None compares every
     arena element (padding included), "sampled" the tensor edges, the padding and a
     million random elements; the grad arena and the bf16 copy are checked in full."""
@@ -127,7 +133,7 @@ def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda
         new_grads = micros is None or fresh_grads
         if new_grads:
             micros = pb.gen.micro_grads()
-        got = pb.gpu_step(micros, t)
+        got = pb.gpu_step(micros, t, fused=fused)
         if new_grads:
             g_idx, ref_sumsq = oracle_pass(micros, pb.grad, idx)
         assert got["status"] == 0

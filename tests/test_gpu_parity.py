@@ -41,6 +41,43 @@ def test_toy_full_parity():
     assert res["master"] <= MAX_ULP
 
 
+def test_toy_full_parity_unfused_calls():
+    run_parity("toy", fused=False)
+
+
+def test_fused_accumulate_norm_equals_separate_calls():
+    """zero1_accumulate_norm writes the same gradient and the same norm record, bit for bit,
+    as zero1_accumulate followed by zero1_grad_norm (same tiles, same summation order)."""
+    for numels, K in (([16384 * 3 + 8 * 5 + 3, 1000, 77], 1), ([40000, 17, 16384], 3), ([9], 2)):
+        pb = Problem(_custom(numels, [0, 1, 0][:len(numels)], K=K, steps=1, sigma=0.1))
+        micros = pb.gen.micro_grads()
+        recs = []
+        grads = []
+        for fused in (False, True):
+            if fused:
+                for k, mb in enumerate(micros[:-1]):
+                    z.accumulate(pb.plan, pb.grad, mb, overwrite_first=(k == 0))
+                z.accumulate_norm(pb.plan, pb.grad, micros[-1], pb.ws, pb.nout, overwrite_first=(K == 1),
+                                  extra_sumsq=0.5)
+            else:
+                for k, mb in enumerate(micros):
+                    z.accumulate(pb.plan, pb.grad, mb, overwrite_first=(k == 0))
+                z.grad_norm(pb.plan, pb.grad, pb.ws, pb.nout, 0.5)
+            recs.append(z.read_norm(pb.nout))
+            grads.append(pb.grad.clone())
+        assert recs[0] == recs[1]
+        assert torch.equal(grads[0].view(torch.int32), grads[1].view(torch.int32))
+    # several micro-batches in the fused call itself
+    pb = Problem(_custom([33333, 64], [0, 1], K=4, steps=1, sigma=0.3))
+    micros = pb.gen.micro_grads()
+    z.accumulate_norm(pb.plan, pb.grad, micros, pb.ws, pb.nout, overwrite_first=True)
+    r1 = z.read_norm(pb.nout)
+    g1 = pb.grad.clone()
+    z.accumulate(pb.plan, pb.grad, micros, overwrite_first=True)
+    z.grad_norm(pb.plan, pb.grad, pb.ws, pb.nout)
+    assert z.read_norm(pb.nout) == r1 and torch.equal(g1, pb.grad)
+
+
 def test_smollm135m_full_size_sampled():
     res = run_parity("smollm135m", fresh_grads=False, sample="sampled")
     assert res["local_numel"] == 134_515_008

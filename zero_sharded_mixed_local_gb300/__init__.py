@@ -9,11 +9,11 @@ ships.  The work runs in hand-written CUDA kernels behind the C ABI of
 """
 from .binding import (ARENA_ALIGN, MAX_MICRO, NORM_OUT_BYTES, NUM_GROUPS, ZERO1_EALIGN, ZERO1_ECUDA,
                       ZERO1_EINVAL, ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, LocalShardAdamW, Plan,
-                      ShardLayout, Zero1Error, accumulate, allreduce_sumsq_, decode_norm, grad_norm, grad_norm_static, load_library, new_norm_out,
+                      ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, grad_norm, grad_norm_static, load_library, new_norm_out,
                       read_norm, step)
 
 __all__ = [
     "ARENA_ALIGN", "MAX_MICRO", "NORM_OUT_BYTES", "NUM_GROUPS", "ZERO1_EALIGN", "ZERO1_ECUDA", "ZERO1_EINVAL",
     "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_ETOOBIG", "ZERO1_OK", "Hparams", "LocalShardAdamW", "Plan", "ShardLayout",
-    "Zero1Error", "accumulate", "allreduce_sumsq_", "decode_norm", "grad_norm", "grad_norm_static", "load_library", "new_norm_out", "read_norm", "step",
+    "Zero1Error", "accumulate", "accumulate_norm", "allreduce_sumsq_", "decode_norm", "grad_norm", "grad_norm_static", "load_library", "new_norm_out", "read_norm", "step",
 ]

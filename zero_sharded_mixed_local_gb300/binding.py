@@ -73,6 +73,8 @@ def load_library(path=None):
         "zero1_plan_bytes": (ctypes.c_int, [vp, i32, i64p]),
         "zero1_workspace_bytes": (ctypes.c_size_t, [vp]),
         "zero1_accumulate": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, i32, vp]),
+        "zero1_accumulate_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, i32, ctypes.c_double, vp,
+                                                 ctypes.c_size_t, vp, vp]),
         "zero1_grad_norm": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
         "zero1_grad_norm_static": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, vp]),
         "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
@@ -256,6 +258,31 @@ def accumulate(plan, grad, micro, overwrite_first=True, stream=None):
                                 _stream_ptr(stream, dev)), "zero1_accumulate")
 
 
+def _micro_array(plan, micro, dev):
+    micro = [micro] if isinstance(micro, torch.Tensor) else list(micro)
+    if not 1 <= len(micro) <= MAX_MICRO:
+        raise ValueError("1..%d micro-batch gradients per call" % MAX_MICRO)
+    return micro, (ctypes.c_void_p * len(micro))(*[_ptr(mb, torch.bfloat16, plan.arena_numel, "micro[%d]" % k, dev).value
+                                                   for k, mb in enumerate(micro)])
+
+
+def accumulate_norm(plan, grad, micro, workspace, norm_out, overwrite_first=True, extra_sumsq=0.0, stream=None):
+    """zero1_accumulate_norm: accumulate the last micro-batch(es) and take the norm in one pass."""
+    lib = load_library()
+    dev = grad.device
+    gp = _ptr(grad, torch.float32, plan.arena_numel, "grad")
+    micro, arr = _micro_array(plan, micro, dev)
+    wp = _ptr(workspace, torch.uint8, None, "workspace", dev)
+    if workspace.numel() < plan.workspace_bytes:
+        raise ValueError("workspace has %d bytes, the plan needs %d" % (workspace.numel(), plan.workspace_bytes))
+    op = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    if norm_out.numel() < NORM_OUT_BYTES:
+        raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
+    _check(lib.zero1_accumulate_norm(plan.handle, gp, arr, len(micro), 1 if overwrite_first else 0,
+                                     float(extra_sumsq), wp, workspace.numel(), op, _stream_ptr(stream, dev)),
+           "zero1_accumulate_norm")
+
+
 def grad_norm(plan, grad, workspace, norm_out, extra_sumsq=0.0, stream=None):
     """zero1_grad_norm: device {sumsq, norm, status} of the fp32 grad arena (+ extra_sumsq)."""
     lib = load_library()
@@ -361,17 +388,28 @@ class LocalShardAdamW:
         self.t = 0
         self._micro_seen = 0
 
-    def accumulate(self, micro, stream=None):
-        """Add one (or several) bf16 micro-batch gradient arenas; the first call of a step overwrites."""
-        accumulate(self.plan, self.grad, micro, overwrite_first=(self._micro_seen == 0), stream=stream)
+    def accumulate(self, micro, last=False, extra_sumsq=0.0, stream=None):
+        """Add one (or several) bf16 micro-batch gradient arenas; the first call of a step
+        overwrites.  ``last=True`` marks the step's final micro-batch: the gradient norm
+        is taken in the same pass and step() will not read the gradient for it again."""
+        first = self._micro_seen == 0
+        if last:
+            accumulate_norm(self.plan, self.grad, micro, self.workspace, self.norm_out, overwrite_first=first,
+                            extra_sumsq=extra_sumsq, stream=stream)
+        else:
+            accumulate(self.plan, self.grad, micro, overwrite_first=first, stream=stream)
         self._micro_seen += 1 if isinstance(micro, torch.Tensor) else len(micro)
+        self._norm_ready = bool(last)
 
     def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None):
         """Norm + clip + AdamW + bf16 copy; returns nothing (read_norm() syncs).
 
-        With ``group`` (a torch.distributed process group of the data-parallel
-        ranks) the local sum of squares is all-reduced before the update."""
-        grad_norm(self.plan, self.grad, self.workspace, self.norm_out, extra_sumsq, stream=stream)
+        The norm is taken here unless the last accumulate() already did.  With
+        ``group`` (a torch.distributed process group of the data-parallel ranks)
+        the local sum of squares is all-reduced before the update."""
+        if not getattr(self, "_norm_ready", False):
+            grad_norm(self.plan, self.grad, self.workspace, self.norm_out, extra_sumsq, stream=stream)
+        self._norm_ready = False
         if group is not None:
             allreduce_sumsq_(self.norm_out, group)
         self.t += 1

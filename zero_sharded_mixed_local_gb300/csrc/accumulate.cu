@@ -10,7 +10,14 @@
 // read when not overwriting).  Flat over the arena, one 8-element vector per
 // thread and a grid that covers the whole arena: one 16-byte load per
 // micro-batch, two 16-byte fp32 accesses.
-#include "zero1_internal.h"
+//
+// accumulate_norm_kernel fuses the last micro-batch's pass with the gradient
+// norm: each block owns one 16384-element norm tile, writes the accumulated
+// gradient and adds its squares into float pairs with exactly the mapping and
+// order of sumsq_tiles_kernel, so the norm record is bit-identical to
+// zero1_grad_norm's while the gradient is never read back (4 bytes per element
+// saved).
+#include "pair_sum.cuh"
 
 namespace zero1 {
 namespace {
@@ -56,7 +63,88 @@ __global__ void __launch_bounds__(kAccThreads)
     g4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
+// One vector's accumulation, in the same operation order as accumulate_kernel.
+__device__ __forceinline__ void accumulate_vec(const AccumulateParams& P, int64_t i, float (&acc)[8]) {
+    int k = 0;
+    if (P.overwrite_first) {
+        widen8(reinterpret_cast<const uint4*>(P.micro[0])[i], acc);
+        k = 1;
+    } else {
+        const float4* g4 = reinterpret_cast<const float4*>(P.grad) + 2 * i;
+        const float4 a = g4[0], b = g4[1];
+        acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+        acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+    }
+    for (; k < P.n_micro; ++k) {
+        float f[8];
+        widen8(reinterpret_cast<const uint4*>(P.micro[k])[i], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], f[j]);
+    }
+}
+
+__global__ void __launch_bounds__(kTileThreads)
+    accumulate_norm_kernel(const __grid_constant__ AccumulateParams P, float2* __restrict__ partials, int64_t first_tile) {
+    __shared__ float2 s_warp[kTileThreads / 32];
+    const int64_t tile = first_tile + blockIdx.x;
+    const int64_t v0 = tile * kVecsPerTile;
+    const int64_t nv = P.n_vec - v0 < kVecsPerTile ? P.n_vec - v0 : kVecsPerTile;
+    SquarePairs sq;
+    if (P.overwrite_first && P.n_micro == 1) {
+        // The common case (one micro-batch per call, first of the step): all
+        // eight 16-byte loads in flight before any conversion.
+        uint4 raw[kVecsPerThread];
+#pragma unroll
+        for (int r = 0; r < kVecsPerThread; ++r) {
+            const int v = threadIdx.x + r * kTileThreads;
+            raw[r] = v < nv ? reinterpret_cast<const uint4*>(P.micro[0])[v0 + v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int r = 0; r < kVecsPerThread; ++r) {
+            const int v = threadIdx.x + r * kTileThreads;
+            float acc[8];
+            widen8(raw[r], acc);
+            const float4 a = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            const float4 b = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (v < nv) {
+                float4* g4 = reinterpret_cast<float4*>(P.grad) + 2 * (v0 + v);
+                g4[0] = a;
+                g4[1] = b;
+            }
+            sq.add_vec(a, b);  // out-of-range vectors are zeros, as in sumsq_tiles_kernel
+        }
+    } else {
+#pragma unroll 2
+        for (int r = 0; r < kVecsPerThread; ++r) {
+            const int v = threadIdx.x + r * kTileThreads;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (v < nv) {
+                accumulate_vec(P, v0 + v, acc);
+                float4* g4 = reinterpret_cast<float4*>(P.grad) + 2 * (v0 + v);
+                g4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                g4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+            sq.add_vec(make_float4(acc[0], acc[1], acc[2], acc[3]), make_float4(acc[4], acc[5], acc[6], acc[7]));
+        }
+    }
+    sq.fold();
+    block_pair_sum<kTileThreads>(sq.s[0], sq.c[0], s_warp);
+    if (threadIdx.x == 0) partials[tile] = make_float2(sq.s[0], sq.c[0]);
+}
+
 }  // namespace
+
+cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, int64_t n_tiles, double extra_sumsq,
+                                   zero1_norm_out* out, cudaStream_t stream) {
+    float2* pairs = reinterpret_cast<float2*>(partials);
+    for (int64_t first = 0; first < n_tiles; first += 0x7fffffff) {
+        const int64_t nb = n_tiles - first < 0x7fffffff ? n_tiles - first : 0x7fffffff;
+        accumulate_norm_kernel<<<static_cast<unsigned>(nb), kTileThreads, 0, stream>>>(p, pairs, first);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return launch_norm_final(pairs, n_tiles, extra_sumsq, out, stream);
+}
 
 cudaError_t launch_accumulate(const AccumulateParams& p, cudaStream_t stream) {
     for (int64_t first = 0; first < p.n_vec; first += kMaxGridVectors(kAccThreads)) {

@@ -47,6 +47,34 @@ extern "C" int zero1_accumulate(const zero1_plan* plan, float* grad, const uint1
     return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
 }
 
+extern "C" int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
+                                     int32_t n_micro, int32_t overwrite_first, double extra_sumsq, void* workspace,
+                                     size_t workspace_bytes, zero1_norm_out* d_out, void* stream) {
+    if (plan == nullptr || micro_bf16 == nullptr || d_out == nullptr) return ZERO1_EINVAL;
+    if (n_micro < 1 || n_micro > ZERO1_MAX_MICRO) return ZERO1_EINVAL;
+    if (std::isnan(extra_sumsq) || extra_sumsq < 0.0) return ZERO1_EINVAL;
+    if (!aligned16(d_out)) return ZERO1_EALIGN;
+    const int64_t n_tiles = zero1::norm_tiles(plan->arena_numel);
+    zero1::AccumulateParams p{};
+    if (n_tiles > 0) {
+        if (grad == nullptr || workspace == nullptr) return ZERO1_EINVAL;
+        if (workspace_bytes < static_cast<size_t>(n_tiles) * sizeof(double)) return ZERO1_EINVAL;
+        for (int k = 0; k < n_micro; ++k) {
+            if (micro_bf16[k] == nullptr) return ZERO1_EINVAL;
+            if (!aligned16(micro_bf16[k])) return ZERO1_EALIGN;
+            p.micro[k] = micro_bf16[k];
+        }
+        if (!aligned16(grad) || !aligned16(workspace)) return ZERO1_EALIGN;
+    }
+    p.grad = grad;
+    p.n_micro = n_micro;
+    p.overwrite_first = overwrite_first ? 1 : 0;
+    p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
+    const cudaError_t e = zero1::launch_accumulate_norm(p, static_cast<double*>(workspace), n_tiles, extra_sumsq,
+                                                        d_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
 extern "C" int zero1_grad_norm(const zero1_plan* plan, const float* grad, double extra_sumsq, void* workspace,
                                size_t workspace_bytes, zero1_norm_out* d_out, void* stream) {
     if (plan == nullptr || d_out == nullptr) return ZERO1_EINVAL;

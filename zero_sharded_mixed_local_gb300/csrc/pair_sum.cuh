@@ -1,0 +1,101 @@
+// Sums of squares kept as unevaluated float pairs (hi + lo), shared by the
+// norm kernels.  The rounding error of every square (an FMA) and of every
+// addition of high parts (TwoSum) goes into the low part, so a pair stays
+// within ~1e-13 relative of the exact sum while all arithmetic runs on the
+// fp32 pipes (GB300's FP64 rate is a small fraction of its fp32 rate).
+//
+// Tile mapping (fixes the summation order, hence bit-identical results in
+// every kernel that uses it): a tile is kNormTile = 16384 elements, i.e.
+// 2048 vectors of 8; thread t of a 256-thread block owns vectors t, t + 256,
+// ..., t + 7*256 and adds each vector's elements 0..7 into its four pairs in
+// the order (0,1,2,3,4,5,6,7) -> pairs (0,1,2,3,0,1,2,3).
+#pragma once
+
+#include "zero1_internal.h"
+
+namespace zero1 {
+
+constexpr int kTileThreads = 256;
+constexpr int kVecsPerTile = static_cast<int>(kNormTile / 8);          // 2048
+constexpr int kVecsPerThread = kVecsPerTile / kTileThreads;            // 8
+static_assert(kVecsPerThread * kTileThreads * 8 == kNormTile, "tile mapping");
+
+// s + e = a + b exactly (Knuth's TwoSum, six rounded operations).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// (s, c) += g*g: the square's rounding error and the addition's go into c.
+__device__ __forceinline__ void add_square(float& s, float& c, float g) {
+    const float p = __fmul_rn(g, g);
+    const float pe = __fmaf_rn(g, g, -p);  // g*g - p, exactly
+    float t, e;
+    two_sum(s, p, t, e);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(e, pe));
+}
+
+// (s, c) += (t, d)
+__device__ __forceinline__ void add_pair(float& s, float& c, float t, float d) {
+    float h, e;
+    two_sum(s, t, h, e);
+    s = h;
+    c = __fadd_rn(c, __fadd_rn(d, e));
+}
+
+// A thread's four running pairs over its vectors.
+struct SquarePairs {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+
+    __device__ __forceinline__ void add_vec(const float4& a, const float4& b) {
+        add_square(s[0], c[0], a.x);
+        add_square(s[1], c[1], a.y);
+        add_square(s[2], c[2], a.z);
+        add_square(s[3], c[3], a.w);
+        add_square(s[0], c[0], b.x);
+        add_square(s[1], c[1], b.y);
+        add_square(s[2], c[2], b.z);
+        add_square(s[3], c[3], b.w);
+    }
+
+    // Fold the four pairs into (s[0], c[0]) in a fixed order.
+    __device__ __forceinline__ void fold() {
+        add_pair(s[0], c[0], s[1], c[1]);
+        add_pair(s[2], c[2], s[3], c[3]);
+        add_pair(s[0], c[0], s[2], c[2]);
+    }
+};
+
+__device__ __forceinline__ void warp_pair_sum(float& s, float& c) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float t = __shfl_down_sync(0xffffffffu, s, off);
+        const float d = __shfl_down_sync(0xffffffffu, c, off);
+        add_pair(s, c, t, d);
+    }
+}
+
+// Sum of the threads' pairs over the block in a fixed order; valid in thread 0.
+template <int kThreads>
+__device__ __forceinline__ void block_pair_sum(float& s, float& c, float2* s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    warp_pair_sum(s, c);
+    if (lane == 0) s_warp[warp] = make_float2(s, c);
+    __syncthreads();
+    if (warp == 0) {
+        const float2 x = lane < kThreads / 32 ? s_warp[lane] : make_float2(0.f, 0.f);
+        s = x.x;
+        c = x.y;
+        warp_pair_sum(s, c);
+    }
+}
+
+// Second kernel of every norm: adds the per-tile pairs in a fixed order,
+// converts to double, adds the other ranks' share and writes the record.
+cudaError_t launch_norm_final(const float2* partials, int64_t n_tiles, double extra_sumsq, zero1_norm_out* out,
+                              cudaStream_t stream);
+
+}  // namespace zero1

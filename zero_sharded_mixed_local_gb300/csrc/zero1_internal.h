@@ -59,6 +59,8 @@ struct StepParams {
 cudaError_t launch_accumulate(const AccumulateParams& p, cudaStream_t stream);
 cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int64_t n_tiles,
                              double extra_sumsq, zero1_norm_out* out, cudaStream_t stream);
+cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, int64_t n_tiles, double extra_sumsq,
+                                   zero1_norm_out* out, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
 
 // Record a CUDA error for zero1_last_cuda_error() and return ZERO1_ECUDA.
