@@ -155,10 +155,16 @@ size_t zero1_workspace_bytes(const zero1_plan* plan);
  *     grad = grad + bf16->fp32(micro[k])     for the other k, in order
  * every addition a single fp32 rounding; a plain sum (no 1/K).
  *   grad          device fp32 arena (arena_numel), read and written
- *   micro_bf16    HOST array of n_micro DEVICE pointers to bf16 arenas (raw
- *                 bits as uint16), read only
+ *   micro_bf16    HOST array of n_micro pointers to bf16 arenas (raw bits as
+ *                 uint16), read only.  Each may be device memory, or host
+ *                 memory the device can read: pinned/registered memory
+ *                 always, ordinary pageable memory where the device reads
+ *                 host page tables (Grace-based GB300 nodes).  Host arenas
+ *                 are read by the kernel itself over the CPU-GPU link, with
+ *                 no staging copy.
  *   n_micro       1 .. ZERO1_MAX_MICRO
- * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+ * Errors: ZERO1_EINVAL (including a host pointer this device cannot read),
+ * ZERO1_EALIGN, ZERO1_ECUDA. */
 int zero1_accumulate(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
                      int32_t n_micro, int32_t overwrite_first, void* stream);
 

@@ -269,6 +269,25 @@ def test_shard_concatenation_on_gpu():
                                    b[ro:ro + len(s)].view(torch.int16))
 
 
+def test_micro_batches_read_from_pinned_host_memory():
+    """Pinned host arenas are read by the kernels directly (no staging copy): same gradient
+    and norm record, bit for bit, as from device memory."""
+    pb = Problem(_custom([40000, 1000, 17], [0, 1, 0], K=3, steps=1, sigma=0.2))
+    micros = pb.gen.micro_grads()
+    host = [m.cpu().pin_memory() for m in micros]
+    outs = []
+    for src in (micros, host):
+        z.accumulate(pb.plan, pb.grad, src[0], overwrite_first=True)
+        z.accumulate(pb.plan, pb.grad, src[1], overwrite_first=False)
+        z.accumulate_norm(pb.plan, pb.grad, src[2], pb.ws, pb.nout, overwrite_first=False)
+        outs.append((pb.grad.clone(), z.read_norm(pb.nout)))
+    assert torch.equal(outs[0][0].view(torch.int32), outs[1][0].view(torch.int32))
+    assert outs[0][1] == outs[1][1]
+    # a plain (pageable) CPU tensor is refused by the binding
+    with pytest.raises(ValueError, match="pinned"):
+        z.accumulate(pb.plan, pb.grad, micros[0].cpu())
+
+
 def test_misaligned_and_wrong_size_buffers_are_rejected():
     plan = z.Plan([100], [0], 1, 0)
     g = plan.new_arena()

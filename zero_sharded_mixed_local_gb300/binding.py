@@ -101,12 +101,16 @@ def _stream_ptr(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _ptr(t, dtype, numel, name, device=None):
+def _ptr(t, dtype, numel, name, device=None, host_ok=False):
+    """Raw pointer of a checked tensor.  With host_ok, a pinned CPU tensor is accepted too:
+    kernels read it directly over the CPU-GPU link."""
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
-    if t.device.type != "cuda":
-        raise ValueError("%s must be on a CUDA device (got %s)" % (name, t.device))
-    if device is not None and t.device != device:
+    pinned_host = host_ok and t.device.type == "cpu" and t.is_pinned()
+    if t.device.type != "cuda" and not pinned_host:
+        raise ValueError("%s must be on a CUDA device%s (got %s)" % (name, " or pinned host memory" if host_ok else "",
+                                                                   t.device))
+    if device is not None and t.device.type == "cuda" and t.device != device:
         raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
     if t.dtype != dtype:
         raise TypeError("%s must be %s (got %s)" % (name, dtype, t.dtype))
@@ -244,16 +248,15 @@ def new_norm_out(device="cuda"):
 
 
 def accumulate(plan, grad, micro, overwrite_first=True, stream=None):
-    """zero1_accumulate: grad (fp32 arena) = [grad +] sum of the bf16 micro-batch arenas."""
+    """zero1_accumulate: grad (fp32 arena) = [grad +] sum of the bf16 micro-batch arenas.
+
+    A micro-batch arena may be a CUDA tensor or a pinned CPU tensor; the kernel reads a
+    pinned one directly over the CPU-GPU link (no staging copy)."""
     lib = load_library()
-    micro = [micro] if isinstance(micro, torch.Tensor) else list(micro)
-    if not 1 <= len(micro) <= MAX_MICRO:
-        raise ValueError("1..%d micro-batch gradients per call" % MAX_MICRO)
     n = plan.arena_numel
     dev = grad.device
     gp = _ptr(grad, torch.float32, n, "grad")
-    arr = (ctypes.c_void_p * len(micro))(*[_ptr(mb, torch.bfloat16, n, "micro[%d]" % k, dev).value
-                                           for k, mb in enumerate(micro)])
+    micro, arr = _micro_array(plan, micro, dev)
     _check(lib.zero1_accumulate(plan.handle, gp, arr, len(micro), 1 if overwrite_first else 0,
                                 _stream_ptr(stream, dev)), "zero1_accumulate")
 
@@ -262,8 +265,8 @@ def _micro_array(plan, micro, dev):
     micro = [micro] if isinstance(micro, torch.Tensor) else list(micro)
     if not 1 <= len(micro) <= MAX_MICRO:
         raise ValueError("1..%d micro-batch gradients per call" % MAX_MICRO)
-    return micro, (ctypes.c_void_p * len(micro))(*[_ptr(mb, torch.bfloat16, plan.arena_numel, "micro[%d]" % k, dev).value
-                                                   for k, mb in enumerate(micro)])
+    return micro, (ctypes.c_void_p * len(micro))(*[_ptr(mb, torch.bfloat16, plan.arena_numel, "micro[%d]" % k, dev,
+                                                        host_ok=True).value for k, mb in enumerate(micro)])
 
 
 def accumulate_norm(plan, grad, micro, workspace, norm_out, overwrite_first=True, extra_sumsq=0.0, stream=None):

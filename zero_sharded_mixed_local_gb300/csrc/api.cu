@@ -18,6 +18,24 @@ int cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Can kernels on the current device read `p`?  Device and managed memory,
+// and pinned or registered host memory (unified addressing), always; plain
+// pageable host memory only where the device reads host page tables (ATS on
+// Grace-based systems such as GB300).  Returns ZERO1_OK, ZERO1_EINVAL, or
+// ZERO1_ECUDA if the query itself fails.
+int check_readable(const void* p) {
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged || a.type == cudaMemoryTypeHost)
+        return ZERO1_OK;
+    int dev = 0, pageable = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return pageable ? ZERO1_OK : ZERO1_EINVAL;
+}
+
 }  // namespace
 
 namespace zero1 {
@@ -40,6 +58,10 @@ extern "C" int zero1_accumulate(const zero1_plan* plan, float* grad, const uint1
         p.micro[k] = micro_bf16[k];
     }
     if (!aligned16(grad)) return ZERO1_EALIGN;
+    for (int k = 0; k < n_micro; ++k) {
+        const int rc = check_readable(micro_bf16[k]);
+        if (rc != ZERO1_OK) return rc;
+    }
     p.n_micro = n_micro;
     p.overwrite_first = overwrite_first ? 1 : 0;
     p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
@@ -65,6 +87,10 @@ extern "C" int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const 
             p.micro[k] = micro_bf16[k];
         }
         if (!aligned16(grad) || !aligned16(workspace)) return ZERO1_EALIGN;
+        for (int k = 0; k < n_micro; ++k) {
+            const int rc = check_readable(micro_bf16[k]);
+            if (rc != ZERO1_OK) return rc;
+        }
     }
     p.grad = grad;
     p.n_micro = n_micro;
