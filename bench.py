@@ -234,10 +234,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    ap.add_argument("--unfused", action="store_true",
+                    help="take the norm in its own pass (zero1_grad_norm) instead of fusing it into the last "
+                         "micro-batch's accumulation")
+    ap.add_argument("--micro-batches", type=int, default=None,
+                    help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
     args = ap.parse_args()
 
     from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout, get_workload
     w = get_workload(args.workload)
+    if args.micro_batches is not None:
+        w.micro_batches = args.micro_batches
+        w.description += " (K overridden to %d)" % args.micro_batches
 
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
@@ -282,8 +290,12 @@ def main():
             z.accumulate(plan, grad, micros[k], overwrite_first=(k == 0), stream=stream)
         if record is not None:
             record["n0"].record(stream)
-        # the last micro-batch's accumulation also takes the gradient norm
-        z.accumulate_norm(plan, grad, micros[K - 1], ws, nout, overwrite_first=(K == 1), stream=stream)
+        if args.unfused:
+            z.accumulate(plan, grad, micros[K - 1], overwrite_first=(K == 1), stream=stream)
+            z.grad_norm(plan, grad, ws, nout, 0.0, stream=stream)
+        else:
+            # the last micro-batch's accumulation also takes the gradient norm
+            z.accumulate_norm(plan, grad, micros[K - 1], ws, nout, overwrite_first=(K == 1), stream=stream)
         if group is not None:
             z.allreduce_sumsq_(nout, group)
         if record is not None:
@@ -322,9 +334,10 @@ def main():
 
     peak, peak_kind = measured_peaks()
     step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9
-    # the norm is fused into the last micro-batch's pass: no separate 4-byte read
-    path_bytes = (accumulate_bytes_per_elem(K) + STEP_BYTES_PER_ELEM) * P
-    last_bytes = (6 if K == 1 else 10) * P
+    # fused: the norm rides on the last micro-batch's pass (no separate 4-byte read)
+    norm_bytes = 4 * P if args.unfused else 0
+    path_bytes = (accumulate_bytes_per_elem(K) + STEP_BYTES_PER_ELEM) * P + norm_bytes
+    last_bytes = (6 if K == 1 else 10) * P + norm_bytes
     traffic = profile_traffic("adamw_step.cu", args.workload)
 
     # ---- end to end through the public API: host gradients in, norm record out.  Every
@@ -420,14 +433,16 @@ def main():
                 "dp_size": w.dp_size,
                 "dp_rank": dp_rank,
                 "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
+                "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
                 "l2": "no flush: each step streams %.1f GB, far above the 129 MB L2" % (path_bytes / 1e9),
             },
             "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
             "kernels": {
                 "accumulate": {"ms": acc_ms, "gbs": (accumulate_bytes_per_elem(K) * P - last_bytes) /
                                (acc_ms * 1e-3) / 1e9 if K > 1 else None, "launches_per_step": K - 1},
-                "accumulate_norm": {"ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
-                                    "launches_per_step": 2},
+                ("accumulate+grad_norm" if args.unfused else "accumulate_norm"): {
+                    "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
+                    "launches_per_step": 3 if args.unfused else 2},
                 "adamw_step": {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
             },
             "roofline": {"bound": "hbm", "kernel": "adamw_step_kernel", "achieved": step_gbs, "peak": peak,
@@ -437,7 +452,7 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "gpu_launches": args.steps * (K + 2),
+            "gpu_launches": args.steps * (K + 2 + (1 if args.unfused else 0)),
         }
         print(json.dumps(out), flush=True)
     if world > 1:
