@@ -390,6 +390,14 @@ def main():
 
         e2e_steps(2)
         torch.cuda.synchronize()
+        # the host link's own speed on this machine, for reading the e2e number: one plain copy
+        c0, c1 = ev(), ev()
+        c0.record(stream)
+        for k in range(K):
+            stage[0][k].copy_(host_micros[k], non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = sum(mb.numel() * mb.element_size() for mb in host_micros) / (c0.elapsed_time(c1) * 1e-3) / 1e9
         barrier(world)
         e0, e1 = ev(), ev()
         e0.record(stream)
@@ -400,7 +408,7 @@ def main():
         assert all(r["status"] == 0 for r in seen)
         e2e = {"value": world * P / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(mb.numel() * mb.element_size() for mb in host_micros),
-               "d2h_bytes_per_step": z.NORM_OUT_BYTES,
+               "d2h_bytes_per_step": z.NORM_OUT_BYTES, "h2d_copy_gbs": h2d_gbs,
                "how": "pinned host gradients copied by the DMA engines on a side stream into two staging "
                       "buffers, overlapping the previous step's kernels; norm record read back every step"}
         del host_micros, stage

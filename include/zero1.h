@@ -54,9 +54,10 @@ extern "C" {
 /* Each shard starts on a multiple of this many elements inside an arena, so
  * that 16-byte vector loads of bf16 (8 elements) never straddle tensors. */
 #define ZERO1_ARENA_ALIGN 8
-/* Tensors are grouped by weight-decay class; group 0 is decayed, group 1 is
- * excluded from weight decay. */
-#define ZERO1_NUM_GROUPS 2
+/* Tensors are grouped (at most ZERO1_MAX_GROUPS groups); each group has its
+ * own learning-rate and weight-decay multipliers.  zero1_plan_create's
+ * no_decay flags make group 0 (decayed) and group 1 (excluded). */
+#define ZERO1_MAX_GROUPS 8
 /* Most micro-batch gradients one zero1_accumulate call accepts. */
 #define ZERO1_MAX_MICRO 16
 
@@ -113,6 +114,28 @@ typedef struct zero1_norm_out {
 int zero1_plan_create(const int64_t* numels, const uint8_t* no_decay, int32_t n_tensors,
                       int32_t dp_size, int32_t dp_rank, zero1_plan** out);
 
+/* zero1_plan_create with parameter groups ("Nanotron Guide", "3. Spectral
+ * muTransfer": learning rates scaled per layer class, eta_hidden = eta_0 /
+ * d_model; torch-style param groups with their own lr and weight decay).
+ *   group[n_tensors]            group of each tensor, 0 .. ZERO1_MAX_GROUPS-1
+ *   lr_scale[ZERO1_MAX_GROUPS]  per-group multiplier of hparams.lr, or NULL
+ *                               for all 1
+ *   wd_scale[ZERO1_MAX_GROUPS]  per-group multiplier of hparams.weight_decay,
+ *                               or NULL for 1 everywhere except group 1 (0)
+ * Group g then steps with lr_g = lr*lr_scale[g] and wd_g = weight_decay *
+ * wd_scale[g] (decay factor 1 - lr_g*wd_g).  The arena holds the groups in
+ * increasing group order, each in model order.  Scales must be finite and
+ * >= 0.  zero1_plan_create(numels, no_decay, ...) is this call with
+ * group = no_decay and both scale arrays NULL.
+ * Errors: as zero1_plan_create, plus ZERO1_EINVAL for a group id out of range
+ * or a bad scale. */
+int zero1_plan_create_grouped(const int64_t* numels, const uint8_t* group, int32_t n_tensors,
+                              const double* lr_scale, const double* wd_scale, int32_t dp_size,
+                              int32_t dp_rank, zero1_plan** out);
+
+/* Multipliers of group g (either output may be NULL). */
+int zero1_plan_group_scales(const zero1_plan* plan, int32_t g, double* lr_scale, double* wd_scale);
+
 /* Free a plan (NULL is ignored). */
 void zero1_plan_destroy(zero1_plan* plan);
 
@@ -128,7 +151,8 @@ int64_t zero1_plan_arena_numel(const zero1_plan* plan); /* padded arena length *
 int zero1_plan_tensor(const zero1_plan* plan, int32_t i, int64_t* shard_start,
                       int64_t* shard_numel, int64_t* arena_offset);
 
-/* Arena element range [begin, end) of weight-decay group g (0 or 1). */
+/* Arena element range [begin, end) of group g (0 .. ZERO1_MAX_GROUPS-1;
+ * empty for a group with no tensors). */
 int zero1_plan_group_range(const zero1_plan* plan, int32_t g, int64_t* begin, int64_t* end);
 
 /* Bytes one rank holds under ZeRO-1 mixed precision ("Distributed Training",
@@ -208,10 +232,11 @@ int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const uint16_t* c
  *     coef = clip/(norm+1e-6) if that is < 1 and clip > 0, else 1
  *     g = grad*coef;  p = p*dfac;  m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
  *     d = sqrt(v)/sqrt(1-b2^t) + eps;  p = p - lr/(1-b1^t) * (m/d);  w = bf16_rne(p)
- * with dfac = 1 - lr*weight_decay for group 0 and 1 for group 1; each fp32
- * operation is rounded once (IEEE divide and square root), the step scalars
- * are computed in double and rounded once to fp32.  The clipped gradient is
- * not written back.
+ * where each parameter group g uses lr_g = lr*lr_scale[g] in place of lr and
+ * dfac = 1 - lr_g*weight_decay*wd_scale[g] (by default group 0 decays and
+ * group 1 does not); each fp32 operation is rounded once (IEEE divide and
+ * square root), the step scalars are computed in double and rounded once to
+ * fp32.  The clipped gradient is not written back.
  *   master, exp_avg, exp_avg_sq   device fp32 arenas, read and written
  *   grad                          device fp32 arena, read only
  *   weight_bf16                   device bf16 arena (uint16 bits), written;

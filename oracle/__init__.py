@@ -48,6 +48,8 @@ def _load():
         lib.oracle_clip_coef.restype = ctypes.c_int32
         lib.oracle_adamw.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32,
                                      ctypes.POINTER(_HP), ctypes.c_int64, ctypes.c_float]
+        lib.oracle_adamw_scaled.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32,
+                                            ctypes.POINTER(_HP), ctypes.c_int64, ctypes.c_float]
         _lib = lib
     return _lib
 
@@ -146,6 +148,27 @@ def adamw(p, m, v, grad, counts, no_decay, hp, t, coef, w=None):
     h = _HP(*(float(hp[k]) for k in ("lr", "beta1", "beta2", "eps", "weight_decay")))
     _load().oracle_adamw(_ptr(p), _ptr(m), _ptr(v), _ptr(grad), _ptr(w), _ptr(counts), _ptr(no_decay),
                          len(counts), ctypes.byref(h), int(t), float(coef))
+
+
+def adamw_scaled(p, m, v, grad, counts, lr_scale, wd_scale, hp, t, coef, w=None):
+    """AdamW with a per-tensor lr multiplier and weight-decay multiplier (in place)."""
+    for a, nme in ((p, "p"), (m, "m"), (v, "v"), (grad, "grad")):
+        _check(a, np.float32, nme)
+    counts = np.ascontiguousarray(counts, dtype=np.int64)
+    lr_scale = np.ascontiguousarray(lr_scale, dtype=np.float64)
+    wd_scale = np.ascontiguousarray(wd_scale, dtype=np.float64)
+    n = int(counts.sum())
+    if not (p.size == m.size == v.size == grad.size == n) or not (len(lr_scale) == len(wd_scale) == len(counts)):
+        raise ValueError("size mismatch")
+    if w is not None:
+        _check(w, np.uint16, "w")
+        if w.size != n:
+            raise ValueError("size mismatch")
+    if t < 1:
+        raise ValueError("t starts at 1")
+    h = _HP(*(float(hp[k]) for k in ("lr", "beta1", "beta2", "eps", "weight_decay")))
+    _load().oracle_adamw_scaled(_ptr(p), _ptr(m), _ptr(v), _ptr(grad), _ptr(w), _ptr(counts), _ptr(lr_scale),
+                                _ptr(wd_scale), len(counts), ctypes.byref(h), int(t), float(coef))
 
 
 def full_step(p, m, v, micros, counts, no_decay, hp, t, clip, extra_sumsq=0.0, w=None, grad=None):

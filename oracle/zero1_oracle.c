@@ -214,6 +214,49 @@ typedef struct {
     double lr, beta1, beta2, eps, weight_decay;
 } oracle_adamw_hp;
 
+/* AdamW with a learning-rate and a weight-decay multiplier per tensor (the
+ * "Nanotron Guide", "3. Spectral muTransfer": learning rates scaled per
+ * layer class, e.g. eta_hidden = eta_0 / d_model).  Tensor i steps with
+ * lr_i = lr * lr_scale[i] and wd_i = weight_decay * wd_scale[i]; every
+ * scalar derived from them is computed in double and rounded once, then the
+ * per-element update is the one of oracle_adamw below. */
+void oracle_adamw_scaled(float *p, float *m, float *v, const float *grad, uint16_t *w,
+                         const int64_t *counts, const double *lr_scale, const double *wd_scale,
+                         int32_t n_tensors, const oracle_adamw_hp *hp, int64_t t, float coef)
+{
+    double bc1 = 1.0 - pow(hp->beta1, (double)t);
+    double bc2 = 1.0 - pow(hp->beta2, (double)t);
+    const float sqrtbc2 = (float)sqrt(bc2);
+    const float b1 = (float)hp->beta1;
+    const float b2 = (float)hp->beta2;
+    const float omb1 = (float)(1.0 - hp->beta1);
+    const float omb2 = (float)(1.0 - hp->beta2);
+    const float eps = (float)hp->eps;
+
+    int64_t j = 0;
+    for (int32_t i = 0; i < n_tensors; ++i) {
+        const double lr_i = hp->lr * lr_scale[i];
+        const double wd_i = hp->weight_decay * wd_scale[i];
+        const float stepsize = (float)(lr_i / bc1);
+        const float dfac = (float)(1.0 - lr_i * wd_i);
+        for (int64_t e = 0; e < counts[i]; ++e, ++j) {
+            float g = grad[j] * coef;
+            float pj = p[j] * dfac;
+            float mj = b1 * m[j] + omb1 * g;
+            float gg = g * g;
+            float vj = b2 * v[j] + omb2 * gg;
+            float d = sqrtf(vj) / sqrtbc2 + eps;
+            float upd = mj / d;
+            pj = pj - stepsize * upd;
+            p[j] = pj;
+            m[j] = mj;
+            v[j] = vj;
+            if (w)
+                w[j] = oracle_bf16_rne(pj);
+        }
+    }
+}
+
 void oracle_adamw(float *p, float *m, float *v, const float *grad, uint16_t *w,
                   const int64_t *counts, const uint8_t *no_decay, int32_t n_tensors,
                   const oracle_adamw_hp *hp, int64_t t, float coef)

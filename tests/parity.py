@@ -47,7 +47,7 @@ class Problem:
         self.w = workload if isinstance(workload, Workload) else get_workload(workload)
         self.dev = torch.device(device)
         p = self.w.params
-        self.plan = z.Plan(p.numels, p.no_decay, self.w.dp_size, self.w.dp_rank)
+        self.plan = z.Plan(p.numels, dp_size=self.w.dp_size, dp_rank=self.w.dp_rank, **self.w.plan_kwargs())
         L = self.plan.layout()
         self.layout = Layout(L.counts, L.offsets, L.no_decay, L.arena_numel)
         self.gen = InputGenerator(self.w, self.layout, self.dev, seed)
@@ -83,9 +83,11 @@ def oracle_grad(n, micros_u16):
     return g
 
 
-def group_counts(idx, group1_begin):
-    k = int(np.searchsorted(idx, group1_begin))
-    return [k, len(idx) - k], [0, 1]
+def group_counts(idx, plan):
+    """Number of the sorted arena indices idx in each parameter group's arena range."""
+    bounds = [plan.group_range(g)[0] for g in range(1, z.MAX_GROUPS)]
+    cuts = np.searchsorted(idx, bounds)
+    return np.diff(np.concatenate([[0], cuts, [len(idx)]])).astype(np.int64)
 
 
 CHUNK = 1 << 26  # elements per host pass: bounds host memory on the full-size workloads
@@ -122,7 +124,8 @@ def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda
     n = pb.n
     idx = np.arange(n, dtype=np.int64) if sample is None else sample_indices(pb.layout)
     idx_t = torch.from_numpy(idx).to(pb.dev)
-    counts, flags = group_counts(idx, pb.group1)
+    counts = group_counts(idx, pb.plan)
+    lr_scale, wd_scale = w.group_scales()  # from the workload's own definition
     P = pb.master[idx_t].cpu().numpy().copy()
     M = np.zeros(idx.size, np.float32)
     V = np.zeros(idx.size, np.float32)
@@ -141,7 +144,7 @@ def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda
         assert abs(got["sumsq"] - ref_sumsq) <= SUMSQ_TIGHT * ref_sumsq, (t, got["sumsq"], ref_sumsq)
         ok, norm, coef = oracle.clip_coef(ref_sumsq, w.hp["clip_grad"])
         assert ok
-        oracle.adamw(P, M, V, g_idx, counts, flags, w.hp, t, coef)
+        oracle.adamw_scaled(P, M, V, g_idx, counts, lr_scale, wd_scale, w.hp, t, coef)
         report.append((t, got["norm"], norm, float(coef)))
 
     res = {}

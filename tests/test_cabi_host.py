@@ -159,3 +159,60 @@ def test_binding_refuses_cpu_tensors(z):
     plan = z.Plan([64], [0], 1, 0)
     with pytest.raises(ValueError):
         z.accumulate(plan, torch.zeros(64), torch.zeros(64, dtype=torch.bfloat16))
+
+
+def test_grouped_plan_layout_and_scales(z):
+    numels = [10, 20, 30, 40, 50]
+    groups = [4, 0, 4, 2, 0]
+    lr = [1.0, 2.0, 0.5, 1.0, 0.25, 1.0, 1.0, 1.0]
+    wd = [1.0, 1.0, 0.0, 1.0, 0.5, 1.0, 1.0, 1.0]
+    plan = z.Plan(numels, groups=groups, lr_scale=lr, wd_scale=wd)
+    L = plan.layout()
+    # arena order: group 0 (tensors 1, 4: 20 -> 24, 50 -> 56), group 2 (tensor 3: 40),
+    # group 4 (tensors 0, 2: 10 -> 16, 30 -> 32); every shard padded to a multiple of 8
+    assert L.offsets.tolist() == [120, 0, 136, 80, 24]
+    assert plan.group_range(0) == (0, 80) and plan.group_range(2) == (80, 120) and plan.group_range(4) == (120, 168)
+    assert plan.group_range(1) == (80, 80) and plan.group_range(7) == (168, 168)
+    for g in range(8):
+        assert plan.group_scales(g) == (lr[g], wd[g])
+    # defaults: lr 1 everywhere, no decay only in group 1
+    d = z.Plan(numels, groups=groups)
+    assert [d.group_scales(g) for g in range(3)] == [(1.0, 1.0), (1.0, 0.0), (1.0, 1.0)]
+    assert z.Plan(numels, [0, 1, 0, 1, 0]).layout().no_decay.tolist() == [0, 1, 0, 1, 0]
+
+
+def test_grouped_plan_rejects_bad_groups_and_scales(z):
+    with pytest.raises(z.Zero1Error):
+        z.Plan([4, 4], groups=[0, 8])
+    with pytest.raises(z.Zero1Error):
+        z.Plan([4, 4], groups=[0, 1], lr_scale=[1.0] * 7 + [-1.0])
+    with pytest.raises(z.Zero1Error):
+        z.Plan([4, 4], groups=[0, 1], wd_scale=[float("nan")] + [1.0] * 7)
+    with pytest.raises(ValueError):
+        z.Plan([4, 4], no_decay=[0, 1], groups=[0, 1])
+
+
+def test_lr_schedule_closed_forms(z):
+    lr, wu, dec, mn = 3e-3, 2000, 100000, 3e-4  # the Nanotron guide's scheduler settings
+    assert z.lr_at(1, lr, wu, dec, mn) == lr / wu
+    assert z.lr_at(wu, lr, wu, dec, mn) == lr
+    assert abs(z.lr_at(wu + dec // 2, lr, wu, dec, mn) - (lr + mn) / 2) < 1e-15
+    assert z.lr_at(wu + dec, lr, wu, dec, mn) == mn and z.lr_at(wu + dec + 5, lr, wu, dec, mn) == mn
+    assert abs(z.lr_at(wu + dec // 4, lr, wu, dec, mn, "linear") - (mn + 0.75 * (lr - mn))) < 1e-15
+    assert z.lr_at(wu + 7, lr, wu, dec, mn, "constant") == lr
+    vals = [z.lr_at(t, lr, wu, dec, mn) for t in range(wu, wu + dec + 1, 997)]
+    assert all(a >= b for a, b in zip(vals, vals[1:]))
+    with pytest.raises(ValueError):
+        z.lr_at(0, lr, wu, dec, mn)
+
+
+def test_mup_groups_follow_the_hidden_width_rule(z):
+    from zero_sharded_mixed_local_gb300.workloads import get_workload
+    names = get_workload("smollm135m").params.names
+    groups, lr_scale, wd_scale = z.mup_groups(names, d_model=576)
+    kinds = dict(zip(names, groups))
+    assert kinds["embed_tokens.weight"] == 2 and kinds["norm.weight"] == 1
+    assert kinds["layers.3.mlp.up_proj.weight"] == 0 and kinds["layers.0.input_layernorm.weight"] == 1
+    assert lr_scale[0] == 1 / 576 and lr_scale[1] == lr_scale[2] == 1.0  # eta_hidden = eta_0 / d_model
+    assert wd_scale[1] == 0.0 and wd_scale[0] == wd_scale[2] == 1.0
+    assert z.mup_groups(names, d_model=576, base_d_model=64)[1][0] == 64 / 576

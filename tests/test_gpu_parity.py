@@ -30,9 +30,29 @@ def _gpu():
     torch.cuda.empty_cache()
 
 
-def _custom(numels, no_decay, dp=1, rank=0, K=2, steps=3, sigma=1e-3, name="custom", hp=None):
+def _custom(numels, no_decay, dp=1, rank=0, K=2, steps=3, sigma=1e-3, name="custom", hp=None, groups=None,
+            lr_scale=None, wd_scale=None):
     return Workload(name, name, ParamList(["p%d" % i for i in range(len(numels))], list(numels), list(no_decay)),
-                    dp, rank, K, steps, sigma, hp=dict(hp or HP))
+                    dp, rank, K, steps, sigma, hp=dict(hp or HP), groups=groups, lr_scale=lr_scale,
+                    wd_scale=wd_scale)
+
+
+def test_parameter_groups_with_lr_and_wd_scales():
+    """Eight tensors in five groups (two empty groups in between), each group with its own
+    lr and weight-decay multiplier, clip active, every arena element compared."""
+    numels = [5000, 17, 16384 + 3, 64, 1, 999, 4096, 40]
+    groups = [3, 0, 3, 7, 1, 0, 5, 1]
+    lr_scale = [1.0, 0.5, 1.0, 1 / 64, 1.0, 2.0, 1.0, 1 / 576]
+    wd_scale = [1.0, 0.0, 1.0, 0.25, 1.0, 0.0, 1.0, 3.0]
+    for dp, r in ((1, 0), (3, 2)):
+        res = run_parity(_custom(numels, [0] * 8, dp, r, K=2, steps=4, sigma=0.05, groups=groups,
+                                 lr_scale=lr_scale, wd_scale=wd_scale))
+        assert res["master"] <= MAX_ULP
+
+
+def test_smollm135m_mup_groups_full_size_sampled():
+    res = run_parity("smollm135m_mup", fresh_grads=False, sample="sampled")
+    assert res["local_numel"] > 67_000_000
 
 
 # ---------------------------------------------------------------- workloads

@@ -476,3 +476,70 @@ def test_shard_concatenation_invariant(oracle_mod):
             P[idx], M[idx], V[idx], W[idx] = pp, mm, vv, ww
         for a, b in ((P, p), (M, m), (V, v), (W, w)):
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), dp
+
+
+# --------------------------------------------------------------------------
+# Per-tensor learning-rate / weight-decay multipliers.
+# --------------------------------------------------------------------------
+def test_adamw_scaled_step1_moves_each_tensor_by_its_own_lr(oracle_mod):
+    """From zero state, step 1 moves every element by lr_i*g/(|g|+eps) after decay by 1-lr_i*wd_i."""
+    counts = np.array([5, 4, 3], np.int64)
+    lr_scale = np.array([1.0, 1.0 / 64, 4.0])
+    wd_scale = np.array([1.0, 0.0, 0.5])
+    g = np.array([0.3, -0.2, 1.0, 2e-3, -4.0, 0.7, 0.1, 1e-2, -1e-3, 3.0, -0.5, 0.25], np.float32)
+    p0 = np.linspace(-0.03, 0.03, g.size).astype(np.float32)
+    p, m, v = p0.copy(), np.zeros(g.size, np.float32), np.zeros(g.size, np.float32)
+    oracle_mod.adamw_scaled(p, m, v, g.copy(), counts, lr_scale, wd_scale, HP, 1, np.float32(1.0))
+    lr_i = np.repeat(HP["lr"] * lr_scale, counts)
+    wd_i = np.repeat(HP["weight_decay"] * wd_scale, counts)
+    g64 = g.astype(np.float64)
+    expect = p0 * (1 - lr_i * wd_i) - lr_i * g64 / (np.abs(g64) + HP["eps"])
+    np.testing.assert_allclose(p, expect, rtol=0, atol=1e-6 * lr_i.max())
+    np.testing.assert_allclose(np.abs((p0 * (1 - lr_i * wd_i)) - p) / lr_i, 1.0, rtol=1e-4)
+
+
+def test_adamw_scaled_reduces_to_no_decay_flags(oracle_mod):
+    rng = np.random.default_rng(13)
+    counts = np.array([100, 7, 64, 1], np.int64)
+    nd = np.array([0, 1, 0, 1], np.uint8)
+    n = int(counts.sum())
+    p0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    outs = []
+    for scaled in (False, True):
+        p, m, v, w = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)
+        for t in (1, 2, 3):
+            if scaled:
+                oracle_mod.adamw_scaled(p, m, v, g.copy(), counts, np.ones(4), 1.0 - nd, HP, t, np.float32(0.5), w=w)
+            else:
+                oracle_mod.adamw(p, m, v, g.copy(), counts, nd, HP, t, np.float32(0.5), w=w)
+        outs.append((p, m, v, w))
+    for a, b in zip(*outs):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_adamw_scaled_vs_torch_param_groups(oracle_mod):
+    """torch.optim.AdamW with one param group per (lr, weight decay) pair."""
+    rng = np.random.default_rng(14)
+    counts = np.array([200, 33, 128], np.int64)
+    lr_scale = np.array([1.0, 0.125, 2.0])
+    wd_scale = np.array([1.0, 0.0, 0.25])
+    n = int(counts.sum())
+    p0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    splits = np.cumsum(counts)[:-1]
+    tparams = [torch.nn.Parameter(torch.from_numpy(x.copy())) for x in np.split(p0, splits)]
+    groups = [{"params": [tp], "lr": HP["lr"] * ls, "weight_decay": HP["weight_decay"] * ws}
+              for tp, ls, ws in zip(tparams, lr_scale, wd_scale)]
+    opt = torch.optim.AdamW(groups, lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"],
+                            foreach=False, fused=False)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    lr_el = np.repeat(HP["lr"] * lr_scale, counts)
+    for t in range(1, 8):
+        g = (rng.standard_normal(n) * 10.0 ** rng.uniform(-4, -1, n)).astype(np.float32)
+        for tp, gg in zip(tparams, np.split(g, splits)):
+            tp.grad = torch.from_numpy(gg.copy())
+        opt.step()
+        oracle_mod.adamw_scaled(p, m, v, g, counts, lr_scale, wd_scale, HP, t, np.float32(1.0))
+    tp_all = np.concatenate([tp.detach().numpy() for tp in tparams])
+    bound = 4 * np.spacing(np.abs(tp_all)) + 1e-5 * lr_el * 7
+    assert np.all(np.abs(p - tp_all) <= bound)

@@ -7,13 +7,17 @@ on the fp32 master / m / v shard and write the bf16 weights the all-gather
 ships.  The work runs in hand-written CUDA kernels behind the C ABI of
 ``libzero1.so`` (``include/zero1.h``); this package is its thin binding.
 """
-from .binding import (ARENA_ALIGN, MAX_MICRO, NORM_OUT_BYTES, NUM_GROUPS, ZERO1_EALIGN, ZERO1_ECUDA,
+from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_EALIGN, ZERO1_ECUDA,
                       ZERO1_EINVAL, ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, LocalShardAdamW, Plan,
                       ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, grad_norm, grad_norm_static, load_library, new_norm_out,
                       read_norm, step)
 
 __all__ = [
-    "ARENA_ALIGN", "MAX_MICRO", "NORM_OUT_BYTES", "NUM_GROUPS", "ZERO1_EALIGN", "ZERO1_ECUDA", "ZERO1_EINVAL",
+    "ARENA_ALIGN", "MAX_GROUPS", "MAX_MICRO", "NORM_OUT_BYTES", "ZERO1_EALIGN", "ZERO1_ECUDA", "ZERO1_EINVAL",
     "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_ETOOBIG", "ZERO1_OK", "Hparams", "LocalShardAdamW", "Plan", "ShardLayout",
     "Zero1Error", "accumulate", "accumulate_norm", "allreduce_sumsq_", "decode_norm", "grad_norm", "grad_norm_static", "load_library", "new_norm_out", "read_norm", "step",
 ]
+
+from .schedules import lr_at, mup_groups  # noqa: E402
+
+__all__ += ["lr_at", "mup_groups"]

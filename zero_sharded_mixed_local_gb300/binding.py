@@ -24,7 +24,7 @@ ZERO1_ENOMEM = -5
 ZERO1_ETOOBIG = -6
 STATIC_NORM_MAX_NUMEL = 262144 * 16384
 ARENA_ALIGN = 8
-NUM_GROUPS = 2
+MAX_GROUPS = 8
 MAX_MICRO = 16
 NORM_OUT_BYTES = 24
 
@@ -63,6 +63,9 @@ def load_library(path=None):
     i64p = ctypes.POINTER(ctypes.c_int64)
     sig = {
         "zero1_plan_create": (ctypes.c_int, [vp, vp, i32, i32, i32, ctypes.POINTER(vp)]),
+        "zero1_plan_create_grouped": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, i32, ctypes.POINTER(vp)]),
+        "zero1_plan_group_scales": (ctypes.c_int, [vp, i32, ctypes.POINTER(ctypes.c_double),
+                                                   ctypes.POINTER(ctypes.c_double)]),
         "zero1_plan_destroy": (None, [vp]),
         "zero1_plan_num_tensors": (i32, [vp]),
         "zero1_plan_total_numel": (i64, [vp]),
@@ -144,27 +147,53 @@ class ShardLayout:
     shard_start: np.ndarray
     counts: np.ndarray
     offsets: np.ndarray
-    no_decay: np.ndarray
+    no_decay: np.ndarray   # 1 where the tensor's group has a weight-decay scale of 0
     arena_numel: int
+    groups: np.ndarray = None
 
 
 class Plan:
     """zero1_plan: every parameter tensor cut by numel into dp_size contiguous
-    shards; this rank's shards laid out in one padded arena per quantity."""
+    shards; this rank's shards laid out in one padded arena per quantity.
 
-    def __init__(self, numels, no_decay, dp_size=1, dp_rank=0):
+    Either ``no_decay`` flags (group 0 decays, group 1 does not) or ``groups``
+    (0..MAX_GROUPS-1) with optional per-group ``lr_scale`` / ``wd_scale``
+    (length MAX_GROUPS) multipliers of the step's lr and weight decay."""
+
+    def __init__(self, numels, no_decay=None, dp_size=1, dp_rank=0, groups=None, lr_scale=None, wd_scale=None):
         lib = load_library()
         numels = np.ascontiguousarray(numels, dtype=np.int64)
-        no_decay = np.ascontiguousarray(no_decay, dtype=np.uint8)
-        if numels.shape != no_decay.shape or numels.ndim != 1:
-            raise ValueError("numels and no_decay must be 1-D and the same length")
+        if (no_decay is None) == (groups is None):
+            raise ValueError("give exactly one of no_decay and groups")
+        grp = np.ascontiguousarray(no_decay if groups is None else groups, dtype=np.uint8)
+        if numels.shape != grp.shape or numels.ndim != 1:
+            raise ValueError("numels and no_decay/groups must be 1-D and the same length")
         h = ctypes.c_void_p()
-        _check(lib.zero1_plan_create(numels.ctypes.data, no_decay.ctypes.data, len(numels), int(dp_size),
-                                     int(dp_rank), ctypes.byref(h)), "zero1_plan_create")
+        if groups is None:
+            if lr_scale is not None or wd_scale is not None:
+                raise ValueError("per-group scales need groups=")
+            _check(lib.zero1_plan_create(numels.ctypes.data, grp.ctypes.data, len(numels), int(dp_size),
+                                         int(dp_rank), ctypes.byref(h)), "zero1_plan_create")
+        else:
+            scales = []
+            for sc in (lr_scale, wd_scale):
+                if sc is None:
+                    scales.append(None)
+                else:
+                    a = np.ascontiguousarray(sc, dtype=np.float64)
+                    if a.shape != (MAX_GROUPS,):
+                        raise ValueError("per-group scales need %d entries" % MAX_GROUPS)
+                    scales.append(a)
+            self._scales = scales
+            _check(lib.zero1_plan_create_grouped(numels.ctypes.data, grp.ctypes.data, len(numels),
+                                                 None if scales[0] is None else scales[0].ctypes.data,
+                                                 None if scales[1] is None else scales[1].ctypes.data,
+                                                 int(dp_size), int(dp_rank), ctypes.byref(h)),
+                   "zero1_plan_create_grouped")
         self._h = h
         self._lib = lib
         self.dp_size, self.dp_rank = int(dp_size), int(dp_rank)
-        self._no_decay = no_decay.copy()
+        self._groups = grp.copy()
         self._layout = None
 
     def close(self):
@@ -214,6 +243,12 @@ class Plan:
                "zero1_plan_group_range")
         return b.value, e.value
 
+    def group_scales(self, g):
+        lr, wd = ctypes.c_double(), ctypes.c_double()
+        _check(self._lib.zero1_plan_group_scales(self._h, int(g), ctypes.byref(lr), ctypes.byref(wd)),
+               "zero1_plan_group_scales")
+        return lr.value, wd.value
+
     def bytes(self, grad_bytes=2):
         out = (ctypes.c_int64 * 4)()
         _check(self._lib.zero1_plan_bytes(self._h, int(grad_bytes), out), "zero1_plan_bytes")
@@ -225,7 +260,9 @@ class Plan:
             st, ct, of = np.zeros(n, np.int64), np.zeros(n, np.int64), np.zeros(n, np.int64)
             for i in range(n):
                 st[i], ct[i], of[i] = self.tensor(i)
-            self._layout = ShardLayout(st, ct, of, self._no_decay.copy(), self.arena_numel)
+            wd_zero = np.array([self.group_scales(g)[1] == 0.0 for g in range(MAX_GROUPS)])
+            self._layout = ShardLayout(st, ct, of, wd_zero[self._groups].astype(np.uint8), self.arena_numel,
+                                       self._groups.copy())
         return self._layout
 
     # -- buffers (the caller owns them; these are conveniences) --

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
     float dfac = P.dfac[0];
     float stepsize = P.stepsize[0];
 #pragma unroll
-    for (int k = 1; k < ZERO1_NUM_GROUPS; ++k) {
+    for (int k = 1; k < ZERO1_MAX_GROUPS; ++k) {
         if (i >= P.group_begin_vec[k]) {
             dfac = P.dfac[k];
             stepsize = P.stepsize[k];

@@ -144,12 +144,13 @@ extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg,
     p.w = weight_bf16;
     p.norm = d_norm;
     p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
-    for (int g = 0; g < ZERO1_NUM_GROUPS; ++g) {
+    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) {
+        const double lr_g = lr * plan->lr_scale[g];
+        const double wd_g = wd * plan->wd_scale[g];
         p.group_begin_vec[g] = plan->group_begin[g] / ZERO1_ARENA_ALIGN;
-        p.stepsize[g] = static_cast<float>(lr / bc1);
+        p.stepsize[g] = static_cast<float>(lr_g / bc1);
+        p.dfac[g] = static_cast<float>(1.0 - lr_g * wd_g);
     }
-    p.dfac[0] = static_cast<float>(1.0 - lr * wd);  // decayed group
-    p.dfac[1] = 1.0f;                               // excluded from weight decay
     p.b1 = static_cast<float>(b1);
     p.b2 = static_cast<float>(b2);
     p.omb1 = static_cast<float>(1.0 - b1);

@@ -6,6 +6,7 @@
 // master, m and v for its own part.  The remainder goes to the lowest ranks,
 // one element each (the page leaves this open).
 #include <algorithm>
+#include <cmath>
 #include <new>
 
 #include "zero1_internal.h"
@@ -18,12 +19,30 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 extern "C" int zero1_plan_create(const int64_t* numels, const uint8_t* no_decay, int32_t n_tensors,
                                  int32_t dp_size, int32_t dp_rank, zero1_plan** out) {
+    if (n_tensors > 0 && no_decay != nullptr) {
+        for (int32_t i = 0; i < n_tensors; ++i) {
+            if (no_decay[i] > 1) {
+                if (out) *out = nullptr;
+                return ZERO1_EINVAL;
+            }
+        }
+    }
+    return zero1_plan_create_grouped(numels, no_decay, n_tensors, nullptr, nullptr, dp_size, dp_rank, out);
+}
+
+extern "C" int zero1_plan_create_grouped(const int64_t* numels, const uint8_t* group, int32_t n_tensors,
+                                         const double* lr_scale, const double* wd_scale, int32_t dp_size,
+                                         int32_t dp_rank, zero1_plan** out) {
     if (out == nullptr) return ZERO1_EINVAL;
     *out = nullptr;
     if (n_tensors < 0 || dp_size < 1 || dp_rank < 0 || dp_rank >= dp_size) return ZERO1_EINVAL;
-    if (n_tensors > 0 && (numels == nullptr || no_decay == nullptr)) return ZERO1_EINVAL;
+    if (n_tensors > 0 && (numels == nullptr || group == nullptr)) return ZERO1_EINVAL;
     for (int32_t i = 0; i < n_tensors; ++i) {
-        if (numels[i] < 0 || no_decay[i] > 1) return ZERO1_EINVAL;
+        if (numels[i] < 0 || group[i] >= ZERO1_MAX_GROUPS) return ZERO1_EINVAL;
+    }
+    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) {
+        if (lr_scale && !(std::isfinite(lr_scale[g]) && lr_scale[g] >= 0.0)) return ZERO1_EINVAL;
+        if (wd_scale && !(std::isfinite(wd_scale[g]) && wd_scale[g] >= 0.0)) return ZERO1_EINVAL;
     }
 
     zero1_plan* p = new (std::nothrow) zero1_plan;
@@ -31,7 +50,7 @@ extern "C" int zero1_plan_create(const int64_t* numels, const uint8_t* no_decay,
     try {
         const size_t n = static_cast<size_t>(n_tensors);
         p->numel.assign(numels, numels + n);
-        p->group.assign(no_decay, no_decay + n);
+        p->group.assign(group, group + n);
         p->shard_start.resize(n);
         p->shard_numel.resize(n);
         p->arena_offset.resize(n);
@@ -42,6 +61,10 @@ extern "C" int zero1_plan_create(const int64_t* numels, const uint8_t* no_decay,
     p->n_tensors = n_tensors;
     p->dp_size = dp_size;
     p->dp_rank = dp_rank;
+    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) {
+        p->lr_scale[g] = lr_scale ? lr_scale[g] : 1.0;
+        p->wd_scale[g] = wd_scale ? wd_scale[g] : (g == 1 ? 0.0 : 1.0);
+    }
 
     const int64_t dp = dp_size, r = dp_rank;
     for (int32_t i = 0; i < n_tensors; ++i) {
@@ -54,11 +77,11 @@ extern "C" int zero1_plan_create(const int64_t* numels, const uint8_t* no_decay,
         p->local_numel += p->shard_numel[i];
     }
 
-    // Group-contiguous arena: decayed shards, then the excluded ones, each
-    // group in model order.  One weight-decay factor per contiguous range
+    // Group-contiguous arena: group 0's shards, then group 1's, ..., each
+    // group in model order.  One set of step scalars per contiguous range
     // lets the step kernel stream the arena flat, with no per-tensor table.
     int64_t off = 0;
-    for (int g = 0; g < ZERO1_NUM_GROUPS; ++g) {
+    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) {
         p->group_begin[g] = off;
         for (int32_t i = 0; i < n_tensors; ++i) {
             if (p->group[i] != g) continue;
@@ -89,9 +112,16 @@ extern "C" int zero1_plan_tensor(const zero1_plan* plan, int32_t i, int64_t* sha
 }
 
 extern "C" int zero1_plan_group_range(const zero1_plan* plan, int32_t g, int64_t* begin, int64_t* end) {
-    if (plan == nullptr || g < 0 || g >= ZERO1_NUM_GROUPS) return ZERO1_EINVAL;
+    if (plan == nullptr || g < 0 || g >= ZERO1_MAX_GROUPS) return ZERO1_EINVAL;
     if (begin) *begin = plan->group_begin[g];
     if (end) *end = plan->group_end[g];
+    return ZERO1_OK;
+}
+
+extern "C" int zero1_plan_group_scales(const zero1_plan* plan, int32_t g, double* lr_scale, double* wd_scale) {
+    if (plan == nullptr || g < 0 || g >= ZERO1_MAX_GROUPS) return ZERO1_EINVAL;
+    if (lr_scale) *lr_scale = plan->lr_scale[g];
+    if (wd_scale) *wd_scale = plan->wd_scale[g];
     return ZERO1_OK;
 }
 

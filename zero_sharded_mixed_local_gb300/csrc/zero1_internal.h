@@ -20,8 +20,10 @@ struct zero1_plan {
     int64_t total_numel = 0;
     int64_t local_numel = 0;
     int64_t arena_numel = 0;
-    int64_t group_begin[ZERO1_NUM_GROUPS] = {};
-    int64_t group_end[ZERO1_NUM_GROUPS] = {};
+    int64_t group_begin[ZERO1_MAX_GROUPS] = {};
+    int64_t group_end[ZERO1_MAX_GROUPS] = {};
+    double lr_scale[ZERO1_MAX_GROUPS] = {};
+    double wd_scale[ZERO1_MAX_GROUPS] = {};
 };
 
 namespace zero1 {
@@ -49,9 +51,9 @@ struct StepParams {
     uint16_t* w;
     const zero1_norm_out* norm;  // may be null: no clipping
     int64_t n_vec;               // arena_numel / 8
-    int64_t group_begin_vec[ZERO1_NUM_GROUPS];  // first 8-element vector of each group
-    float dfac[ZERO1_NUM_GROUPS];
-    float stepsize[ZERO1_NUM_GROUPS];
+    int64_t group_begin_vec[ZERO1_MAX_GROUPS];  // first 8-element vector of each group
+    float dfac[ZERO1_MAX_GROUPS];
+    float stepsize[ZERO1_MAX_GROUPS];
     float b1, b2, omb1, omb2, eps, sqrtbc2;
     double clip;
 };

@@ -87,6 +87,21 @@ class Workload:
     hp: dict = field(default_factory=lambda: dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8,
                                                   weight_decay=0.1, clip_grad=1.0))
     seed: int = 0
+    # optional parameter groups (0..7) with per-group lr / weight-decay multipliers
+    groups: Optional[list] = None
+    lr_scale: Optional[list] = None
+    wd_scale: Optional[list] = None
+
+    def plan_kwargs(self):
+        if self.groups is None:
+            return {"no_decay": self.params.no_decay}
+        return {"groups": self.groups, "lr_scale": self.lr_scale, "wd_scale": self.wd_scale}
+
+    def group_scales(self):
+        """(lr_scale[8], wd_scale[8]) the step applies per group."""
+        if self.groups is None:
+            return [1.0] * 8, [1.0, 0.0] + [1.0] * 6
+        return list(self.lr_scale or [1.0] * 8), list(self.wd_scale or [1.0, 0.0] + [1.0] * 6)
 
 
 def _toy():
@@ -119,6 +134,14 @@ def get_workload(name: str) -> Workload:
     if name == "llama8b":
         return Workload("llama8b", "Llama-3.1-8B-shaped list (untied), dp8 rank0 "
                         "(1,003,782,656 local params), K=1", _llama8b(), 8, 0, 1, 20, 1e-3)
+    if name == "smollm135m_mup":
+        # hidden matrices in group 0 at lr * 64/576 (a muP transfer from a width-64 proxy),
+        # norm weights in group 1 (no decay), embedding in group 2 at the base lr and half decay
+        pl = _smollm135m()
+        grp = [1 if "norm" in n else (2 if "embed" in n else 0) for n in pl.names]
+        return Workload("smollm135m_mup", "SmolLM-135M-shaped list with muP groups (hidden lr x 64/576), dp2 "
+                        "rank1, K=2", pl, 2, 1, 2, 5, 1e-3, groups=grp,
+                        lr_scale=[64 / 576, 1.0, 1.0] + [1.0] * 5, wd_scale=[1.0, 0.0, 0.5] + [1.0] * 5)
     if name == "ragged":
         return Workload("ragged", "ragged stress list: 20,000 tensors log-uniform in [1, 2^22], 10% "
                         "no-decay, dp2 rank1, K=4", ragged_list(), 2, 1, 4, 5, 1e-2)
