@@ -287,6 +287,49 @@ int zero1_grad_norm_static(const zero1_plan* plan, const float* grad, double ext
  * Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
 int zero1_read_norm(const zero1_norm_out* d_norm, void* stream, zero1_norm_out* host_out);
 
+/* ---- model layout <-> arena (the exchanges around the step) -------------- */
+
+/* The data movement on either side of the local step ("ZeRO-1 风格的
+ * Distributed Optimizer", section 6.3: after backward, gradients are
+ * reduce-scattered to the rank that owns each shard; after the step, the
+ * updated bf16 weights are all-gathered).  The "model layout" holds every
+ * parameter whole, concatenated in model order without padding (tensor i at
+ * [sum of earlier numels, + numel_i)), zero1_plan_total_numel() elements.
+ *
+ * Packing a reduce-scatter: for each rank r, zero1_shard_gather with rank
+ * r's plan copies that rank's shard of the full gradient into chunk r of the
+ * send buffer (chunks of the largest arena size).  Unpacking an all-gather:
+ * zero1_shard_scatter with each rank's plan copies chunk r back into the
+ * full bf16 weights.  The same calls move optimizer state between a
+ * checkpoint in model layout and any dp_size's shards (resharding). */
+
+/* Device bytes of the plan's copy table (24 per run of up to 16384 shard
+ * elements); 0 for an empty shard. */
+size_t zero1_layout_table_bytes(const zero1_plan* plan);
+
+/* Copy the plan's table into caller-owned device memory d_table (16-byte
+ * aligned, at least zero1_layout_table_bytes bytes).  Asynchronous on
+ * `stream`; the plan may be destroyed once the call returns.  The table is
+ * valid only for this plan.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_layout_table_upload(const zero1_plan* plan, void* d_table, size_t table_bytes, void* stream);
+
+/* arena[arena_offset_i + k] = full[model_offset_i + shard_start_i + k] for
+ * every tensor i and k < shard_numel_i; padding is not written.
+ *   d_table     this plan's uploaded table
+ *   full        device buffer in model layout (total_numel elements),
+ *               aligned to elem_bytes
+ *   arena       device arena (arena_numel elements), 16-byte aligned
+ *   elem_bytes  2 (bf16 or any 16-bit type) or 4 (fp32); the bits are copied
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_shard_gather(const zero1_plan* plan, const void* d_table, const void* full, void* arena,
+                       int32_t elem_bytes, void* stream);
+
+/* The reverse: full[model_offset_i + shard_start_i + k] = arena[arena_offset_i
+ * + k]; elements of full outside this rank's shard are not written. */
+int zero1_shard_scatter(const zero1_plan* plan, const void* d_table, const void* arena, void* full,
+                        int32_t elem_bytes, void* stream);
+
 /* ---- diagnostics --------------------------------------------------------- */
 
 /* Static description of a status code. */

@@ -216,3 +216,26 @@ def test_mup_groups_follow_the_hidden_width_rule(z):
     assert lr_scale[0] == 1 / 576 and lr_scale[1] == lr_scale[2] == 1.0  # eta_hidden = eta_0 / d_model
     assert wd_scale[1] == 0.0 and wd_scale[0] == wd_scale[2] == 1.0
     assert z.mup_groups(names, d_model=576, base_d_model=64)[1][0] == 64 / 576
+
+
+@pytest.mark.parametrize("name", ["toy", "llama8b", "ragged"])
+def test_layout_table_covers_the_shard_in_16k_runs(z, name):
+    w = get_workload(name)
+    plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank)
+    _, count, _ = oracle.plan(w.params.numels, w.dp_size, w.dp_rank)
+    runs = int(np.sum((count + 16383) // 16384))
+    assert z.load_library().zero1_layout_table_bytes(plan.handle) == 24 * runs
+
+
+def test_layout_calls_reject_bad_arguments_before_any_launch(z):
+    lib = z.load_library()
+    plan = z.Plan([100, 8], [0, 1], 1, 0)
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.zero1_shard_gather(plan.handle, fake, fake, fake, 3, None) == z.ZERO1_EINVAL      # elem_bytes
+    assert lib.zero1_shard_gather(plan.handle, None, fake, fake, 4, None) == z.ZERO1_EINVAL      # no table
+    assert lib.zero1_shard_gather(plan.handle, fake, fake, ctypes.c_void_p(0x10004), 4, None) == z.ZERO1_EALIGN
+    assert lib.zero1_shard_scatter(plan.handle, fake, fake, ctypes.c_void_p(0x10001), 2, None) == z.ZERO1_EALIGN
+    assert lib.zero1_layout_table_upload(plan.handle, fake, 8, None) == z.ZERO1_EINVAL           # too small
+    empty = z.Plan([0], [0], 1, 0)
+    assert lib.zero1_layout_table_bytes(empty.handle) == 0
+    assert lib.zero1_shard_gather(empty.handle, None, None, None, 4, None) == z.ZERO1_OK

@@ -9,15 +9,18 @@ ships.  The work runs in hand-written CUDA kernels behind the C ABI of
 """
 from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_EALIGN, ZERO1_ECUDA,
                       ZERO1_EINVAL, ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, LocalShardAdamW, Plan,
-                      ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, grad_norm, grad_norm_static, load_library, new_norm_out,
+                      ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, exchange_chunk_numel, grad_norm, grad_norm_static, load_library,
+                      pack_reduce_scatter, shard_gather, shard_scatter, unpack_all_gather, new_norm_out,
                       read_norm, step)
 
 __all__ = [
     "ARENA_ALIGN", "MAX_GROUPS", "MAX_MICRO", "NORM_OUT_BYTES", "ZERO1_EALIGN", "ZERO1_ECUDA", "ZERO1_EINVAL",
     "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_ETOOBIG", "ZERO1_OK", "Hparams", "LocalShardAdamW", "Plan", "ShardLayout",
-    "Zero1Error", "accumulate", "accumulate_norm", "allreduce_sumsq_", "decode_norm", "grad_norm", "grad_norm_static", "load_library", "new_norm_out", "read_norm", "step",
+    "Zero1Error", "accumulate", "accumulate_norm", "allreduce_sumsq_", "decode_norm", "exchange_chunk_numel", "grad_norm", "grad_norm_static", "load_library",
+    "pack_reduce_scatter", "shard_gather", "shard_scatter", "unpack_all_gather", "new_norm_out", "read_norm", "step",
 ]
 
+from . import checkpoint  # noqa: E402
 from .schedules import lr_at, mup_groups  # noqa: E402
 
-__all__ += ["lr_at", "mup_groups"]
+__all__ += ["checkpoint", "lr_at", "mup_groups"]

@@ -82,6 +82,10 @@ def load_library(path=None):
         "zero1_grad_norm_static": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, vp]),
         "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
         "zero1_read_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(_NormOut)]),
+        "zero1_layout_table_bytes": (ctypes.c_size_t, [vp]),
+        "zero1_layout_table_upload": (ctypes.c_int, [vp, vp, ctypes.c_size_t, vp]),
+        "zero1_shard_gather": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
+        "zero1_shard_scatter": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
         "zero1_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "zero1_last_cuda_error": (ctypes.c_char_p, []),
     }
@@ -194,6 +198,7 @@ class Plan:
         self._lib = lib
         self.dp_size, self.dp_rank = int(dp_size), int(dp_rank)
         self._groups = grp.copy()
+        self.numels = numels.copy()
         self._layout = None
 
     def close(self):
@@ -264,6 +269,20 @@ class Plan:
             self._layout = ShardLayout(st, ct, of, wd_zero[self._groups].astype(np.uint8), self.arena_numel,
                                        self._groups.copy())
         return self._layout
+
+    def layout_table(self, device="cuda", stream=None):
+        """Device copy of this plan's model-layout <-> arena copy table (made once per device)."""
+        device = torch.device(device)
+        if device.index is None:
+            device = torch.device("cuda", torch.cuda.current_device())
+        cache = self.__dict__.setdefault("_tables", {})
+        if device not in cache:
+            nbytes = self._lib.zero1_layout_table_bytes(self._h)
+            t = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+            _check(self._lib.zero1_layout_table_upload(self._h, ctypes.c_void_p(t.data_ptr()), t.numel(),
+                                                       _stream_ptr(stream, device)), "zero1_layout_table_upload")
+            cache[device] = t
+        return cache[device]
 
     # -- buffers (the caller owns them; these are conveniences) --
     def new_arena(self, dtype=torch.float32, device="cuda"):
@@ -382,6 +401,65 @@ def read_norm(norm_out, stream=None):
     _check(lib.zero1_read_norm(_ptr(norm_out, torch.uint8, None, "norm_out"),
                                _stream_ptr(stream, norm_out.device), ctypes.byref(out)), "zero1_read_norm")
     return {"sumsq": out.sumsq, "norm": out.norm, "status": out.status, "n_partials": out.n_partials}
+
+
+_ELEM_BYTES = {torch.float32: 4, torch.int32: 4, torch.bfloat16: 2, torch.float16: 2, torch.int16: 2}
+
+
+def _layout_args(plan, full, arena, name_full):
+    if full.dtype != arena.dtype or full.dtype not in _ELEM_BYTES:
+        raise TypeError("full and arena must share a 2- or 4-byte dtype")
+    eb = _ELEM_BYTES[full.dtype]
+    dev = arena.device
+    ap = _ptr(arena, arena.dtype, plan.arena_numel, "arena", dev)
+    if full.device != dev or not full.is_contiguous() or full.numel() != plan.total_numel:
+        raise ValueError("%s must be a contiguous %d-element tensor on %s" % (name_full, plan.total_numel, dev))
+    return eb, dev, ap, ctypes.c_void_p(full.data_ptr())
+
+
+def shard_gather(plan, full, arena, stream=None):
+    """zero1_shard_gather: this rank's shard of a model-layout tensor into its arena."""
+    eb, dev, ap, fp = _layout_args(plan, full, arena, "full")
+    tp = ctypes.c_void_p(plan.layout_table(dev).data_ptr())
+    _check(load_library().zero1_shard_gather(plan.handle, tp, fp, ap, eb, _stream_ptr(stream, dev)),
+           "zero1_shard_gather")
+
+
+def shard_scatter(plan, arena, full, stream=None):
+    """zero1_shard_scatter: an arena back into this rank's positions of a model-layout tensor."""
+    eb, dev, ap, fp = _layout_args(plan, full, arena, "full")
+    tp = ctypes.c_void_p(plan.layout_table(dev).data_ptr())
+    _check(load_library().zero1_shard_scatter(plan.handle, tp, ap, fp, eb, _stream_ptr(stream, dev)),
+           "zero1_shard_scatter")
+
+
+def exchange_chunk_numel(plans):
+    """Per-rank chunk length of a reduce-scatter / all-gather buffer: the largest arena."""
+    return max(p.arena_numel for p in plans)
+
+
+def pack_reduce_scatter(plans, full_grad, send, stream=None):
+    """Lay a model-layout gradient out for a reduce-scatter: chunk r of ``send``
+    (``len(plans)`` x ``exchange_chunk_numel(plans)`` elements) receives rank r's
+    shard in rank r's arena layout, zero-padded."""
+    chunk = exchange_chunk_numel(plans)
+    if send.numel() != chunk * len(plans):
+        raise ValueError("send must hold %d x %d elements" % (len(plans), chunk))
+    send.zero_()
+    flat = send.view(-1)
+    for r, pl in enumerate(plans):
+        shard_gather(pl, full_grad, flat[r * chunk:r * chunk + pl.arena_numel], stream=stream)
+
+
+def unpack_all_gather(plans, recv, full, stream=None):
+    """Write every rank's arena (chunk r of an all-gather receive buffer) back into the
+    model-layout tensor ``full``."""
+    chunk = exchange_chunk_numel(plans)
+    if recv.numel() != chunk * len(plans):
+        raise ValueError("recv must hold %d x %d elements" % (len(plans), chunk))
+    flat = recv.view(-1)
+    for r, pl in enumerate(plans):
+        shard_scatter(pl, flat[r * chunk:r * chunk + pl.arena_numel], full, stream=stream)
 
 
 def allreduce_sumsq_(norm_out, group=None):

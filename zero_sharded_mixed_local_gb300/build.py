@@ -16,7 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "zero1")
 LIB = os.path.join(PKG, "libzero1.so")
 
-SOURCES = ["plan.cpp", "api.cu", "accumulate.cu", "grad_norm.cu", "adamw_step.cu", "grad_norm_static.cu"]
+SOURCES = ["plan.cpp", "api.cu", "accumulate.cu", "grad_norm.cu", "adamw_step.cu", "grad_norm_static.cu",
+           "layout.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-Wall",
                      "-I", INCLUDE, "-I", CSRC]

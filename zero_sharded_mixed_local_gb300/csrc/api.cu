@@ -162,6 +162,49 @@ extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg,
     return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
 }
 
+extern "C" int zero1_layout_table_upload(const zero1_plan* plan, void* d_table, size_t table_bytes, void* stream) {
+    if (plan == nullptr) return ZERO1_EINVAL;
+    const size_t need = plan->layout_chunks.size() * sizeof(LayoutChunk);
+    if (need == 0) return ZERO1_OK;
+    if (d_table == nullptr || table_bytes < need) return ZERO1_EINVAL;
+    if (!aligned16(d_table)) return ZERO1_EALIGN;
+    // A pageable source: the call returns once the bytes are staged, so the
+    // plan may be destroyed right after it.
+    const cudaError_t e = cudaMemcpyAsync(d_table, plan->layout_chunks.data(), need, cudaMemcpyHostToDevice,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+namespace {
+
+int layout_copy(const zero1_plan* plan, const void* d_table, const void* src, void* dst, int32_t elem_bytes,
+                bool to_arena, void* stream) {
+    if (plan == nullptr) return ZERO1_EINVAL;
+    if (elem_bytes != 2 && elem_bytes != 4) return ZERO1_EINVAL;
+    const int64_t n_chunks = static_cast<int64_t>(plan->layout_chunks.size());
+    if (n_chunks == 0) return ZERO1_OK;
+    if (d_table == nullptr || src == nullptr || dst == nullptr) return ZERO1_EINVAL;
+    const void* arena = to_arena ? dst : src;
+    const void* full = to_arena ? src : dst;
+    if (!aligned16(d_table) || !aligned16(arena)) return ZERO1_EALIGN;
+    if (reinterpret_cast<uintptr_t>(full) % static_cast<uintptr_t>(elem_bytes)) return ZERO1_EALIGN;
+    const cudaError_t e = zero1::launch_layout_copy(static_cast<const LayoutChunk*>(d_table), n_chunks, src, dst,
+                                                    elem_bytes, to_arena, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int zero1_shard_gather(const zero1_plan* plan, const void* d_table, const void* full, void* arena,
+                                  int32_t elem_bytes, void* stream) {
+    return layout_copy(plan, d_table, full, arena, elem_bytes, true, stream);
+}
+
+extern "C" int zero1_shard_scatter(const zero1_plan* plan, const void* d_table, const void* arena, void* full,
+                                   int32_t elem_bytes, void* stream) {
+    return layout_copy(plan, d_table, arena, full, elem_bytes, false, stream);
+}
+
 extern "C" int zero1_read_norm(const zero1_norm_out* d_norm, void* stream, zero1_norm_out* host_out) {
     if (d_norm == nullptr || host_out == nullptr) return ZERO1_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -1,0 +1,59 @@
+// Copies between the model layout and a rank's arena: the data movement on
+// either side of the local step ("ZeRO-1 风格的 Distributed Optimizer",
+// section 6.3: after backward the gradients are reduce-scattered to the rank
+// that owns each shard, and after the step the updated bf16 weights are
+// all-gathered).
+//
+// Model layout: every parameter whole, concatenated in model order, no
+// padding; tensor i occupies [model_offset_i, model_offset_i + numel_i).
+// Rank r's shard of tensor i is the contiguous run [model_offset_i +
+// shard_start_i, + shard_numel_i), which sits at arena[arena_offset_i ...].
+// Every run is cut into chunks of at most 16384 elements; one block copies
+// one chunk, so the grid covers the whole shard whatever the tensor sizes.
+// The chunk table lives in a caller-provided device buffer (the library
+// allocates no device memory).  Memory-bound: elem_bytes read + elem_bytes
+// written per element; the model-side offsets are arbitrary, so accesses are
+// element-wide (coalesced across a warp) rather than 16-byte vectors.
+#include "zero1_internal.h"
+
+namespace zero1 {
+namespace {
+
+constexpr int kLayoutThreads = 256;
+
+template <typename T, bool kToArena>
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_copy_kernel(const LayoutChunk* __restrict__ table, const T* __restrict__ src, T* __restrict__ dst,
+                       int64_t first_chunk) {
+    const LayoutChunk ch = table[first_chunk + blockIdx.x];
+    const T* s = src + (kToArena ? ch.model_offset : ch.arena_offset);
+    T* d = dst + (kToArena ? ch.arena_offset : ch.model_offset);
+#pragma unroll 8
+    for (int j = threadIdx.x; j < ch.len; j += kLayoutThreads) d[j] = s[j];
+}
+
+template <typename T, bool kToArena>
+cudaError_t launch_typed(const LayoutChunk* table, int64_t n_chunks, const void* src, void* dst, cudaStream_t stream) {
+    for (int64_t first = 0; first < n_chunks; first += 0x7fffffff) {
+        const int64_t nb = n_chunks - first < 0x7fffffff ? n_chunks - first : 0x7fffffff;
+        layout_copy_kernel<T, kToArena><<<static_cast<unsigned>(nb), kLayoutThreads, 0, stream>>>(
+            table, static_cast<const T*>(src), static_cast<T*>(dst), first);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_layout_copy(const LayoutChunk* table, int64_t n_chunks, const void* src, void* dst,
+                               int elem_bytes, bool to_arena, cudaStream_t stream) {
+    if (n_chunks == 0) return cudaSuccess;
+    if (elem_bytes == 2)
+        return to_arena ? launch_typed<uint16_t, true>(table, n_chunks, src, dst, stream)
+                        : launch_typed<uint16_t, false>(table, n_chunks, src, dst, stream);
+    return to_arena ? launch_typed<uint32_t, true>(table, n_chunks, src, dst, stream)
+                    : launch_typed<uint32_t, false>(table, n_chunks, src, dst, stream);
+}
+
+}  // namespace zero1

@@ -91,6 +91,22 @@ extern "C" int zero1_plan_create_grouped(const int64_t* numels, const uint8_t* g
         p->group_end[g] = off;
     }
     p->arena_numel = off;
+
+    // Runs of the shard for the model-layout <-> arena copies.
+    try {
+        int64_t model_offset = 0;
+        for (int32_t i = 0; i < n_tensors; ++i) {
+            for (int64_t k = 0; k < p->shard_numel[i]; k += zero1::kLayoutChunk) {
+                const int64_t len = std::min<int64_t>(zero1::kLayoutChunk, p->shard_numel[i] - k);
+                p->layout_chunks.push_back(
+                    {model_offset + p->shard_start[i] + k, p->arena_offset[i] + k, static_cast<int32_t>(len), 0});
+            }
+            model_offset += p->numel[i];
+        }
+    } catch (const std::bad_alloc&) {
+        delete p;
+        return ZERO1_ENOMEM;
+    }
     *out = p;
     return ZERO1_OK;
 }
@@ -143,4 +159,9 @@ extern "C" int zero1_plan_bytes(const zero1_plan* plan, int32_t grad_bytes, int6
 extern "C" size_t zero1_workspace_bytes(const zero1_plan* plan) {
     if (plan == nullptr) return 0;
     return static_cast<size_t>(zero1::norm_tiles(plan->arena_numel)) * sizeof(double);
+}
+
+extern "C" size_t zero1_layout_table_bytes(const zero1_plan* plan) {
+    if (plan == nullptr) return 0;
+    return plan->layout_chunks.size() * sizeof(LayoutChunk);
 }

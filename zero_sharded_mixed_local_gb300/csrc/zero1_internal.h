@@ -8,6 +8,15 @@
 
 #include "zero1.h"
 
+// One contiguous run of a shard, as the model-layout <-> arena copies see it.
+struct LayoutChunk {
+    int64_t model_offset;  // first element in the model layout
+    int64_t arena_offset;  // first element in the arena
+    int32_t len;           // elements, 1 .. kLayoutChunk
+    int32_t reserved;
+};
+static_assert(sizeof(LayoutChunk) == 24, "LayoutChunk is 24 bytes");
+
 struct zero1_plan {
     int32_t n_tensors = 0;
     int32_t dp_size = 1;
@@ -24,6 +33,7 @@ struct zero1_plan {
     int64_t group_end[ZERO1_MAX_GROUPS] = {};
     double lr_scale[ZERO1_MAX_GROUPS] = {};
     double wd_scale[ZERO1_MAX_GROUPS] = {};
+    std::vector<LayoutChunk> layout_chunks;  // the shard's runs, cut at kLayoutChunk elements
 };
 
 namespace zero1 {
@@ -33,6 +43,9 @@ constexpr int64_t kNormTile = 16384;
 static_assert(ZERO1_STATIC_NORM_MAX_NUMEL == ZERO1_STATIC_NORM_MAX_TILES * kNormTile, "static norm limit");
 
 inline int64_t norm_tiles(int64_t arena_numel) { return (arena_numel + kNormTile - 1) / kNormTile; }
+
+// Most elements one layout-copy block moves.
+constexpr int64_t kLayoutChunk = 16384;
 
 // Launch parameters, passed by value (kernel parameter space).
 struct AccumulateParams {
@@ -64,6 +77,9 @@ cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int
 cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, int64_t n_tiles, double extra_sumsq,
                                    zero1_norm_out* out, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
+
+cudaError_t launch_layout_copy(const LayoutChunk* table, int64_t n_chunks, const void* src, void* dst,
+                               int elem_bytes, bool to_arena, cudaStream_t stream);
 
 // Record a CUDA error for zero1_last_cuda_error() and return ZERO1_ECUDA.
 int record_cuda_error(cudaError_t e);
