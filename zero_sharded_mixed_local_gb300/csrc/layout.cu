@@ -12,8 +12,12 @@
 // one chunk, so the grid covers the whole shard whatever the tensor sizes.
 // The chunk table lives in a caller-provided device buffer (the library
 // allocates no device memory).  Memory-bound: elem_bytes read + elem_bytes
-// written per element; the model-side offsets are arbitrary, so accesses are
-// element-wide (coalesced across a warp) rather than 16-byte vectors.
+// written per element.  Model-side offsets are arbitrary in general, so a
+// chunk whose two ends are both 16-byte aligned (every chunk of a model whose
+// tensor sizes are multiples of 8, i.e. every real one) moves 16-byte
+// vectors plus an element-wise tail; any other chunk moves element by
+// element (coalesced across the warp).  Element-wise bf16 copies measured
+// 5.8 TB/s on a 1.0B-element shard: two bytes per instruction bound them.
 #include "zero1_internal.h"
 
 namespace zero1 {
@@ -28,8 +32,17 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const LayoutChunk ch = table[first_chunk + blockIdx.x];
     const T* s = src + (kToArena ? ch.model_offset : ch.arena_offset);
     T* d = dst + (kToArena ? ch.arena_offset : ch.model_offset);
-#pragma unroll 8
-    for (int j = threadIdx.x; j < ch.len; j += kLayoutThreads) d[j] = s[j];
+    int done = 0;
+    if (((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d)) & 15u) == 0) {
+        constexpr int kPerVec = 16 / sizeof(T);
+        const int nv = ch.len / kPerVec;
+        const uint4* s4 = reinterpret_cast<const uint4*>(s);
+        uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll 4
+        for (int j = threadIdx.x; j < nv; j += kLayoutThreads) d4[j] = s4[j];
+        done = nv * kPerVec;
+    }
+    for (int j = done + threadIdx.x; j < ch.len; j += kLayoutThreads) d[j] = s[j];
 }
 
 template <typename T, bool kToArena>
