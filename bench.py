@@ -359,8 +359,9 @@ def main():
         step_done = [torch.cuda.Event(), torch.cuda.Event()]
         opt_t = [t_counter[0]]
         seen = []
+        copy_ev = []
 
-        def e2e_steps(n_steps, first_event=None):
+        def e2e_steps(n_steps, first_event=None, time_copies=False):
             for t in range(n_steps):
                 b = t % 2
                 with torch.cuda.stream(side):
@@ -368,8 +369,13 @@ def main():
                         side.wait_event(step_done[b])  # staging buffer b is free once step t-2 is done
                     elif first_event is not None:
                         side.wait_event(first_event)
+                    if time_copies:
+                        copy_ev.append((ev(), ev()))
+                        copy_ev[-1][0].record(side)
                     for k in range(K):
                         stage[b][k].copy_(host_micros[k], non_blocking=True)
+                    if time_copies:
+                        copy_ev[-1][1].record(side)
                     copied[b].record(side)
                 stream.wait_event(copied[b])
                 for k in range(K - 1):
@@ -401,14 +407,18 @@ def main():
         barrier(world)
         e0, e1 = ev(), ev()
         e0.record(stream)
-        e2e_steps(args.steps, first_event=e0)
+        e2e_steps(args.steps, first_event=e0, time_copies=True)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+        copy_ms = statistics.mean(a.elapsed_time(b) for a, b in copy_ev)
         assert all(r["status"] == 0 for r in seen)
         e2e = {"value": world * P / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(mb.numel() * mb.element_size() for mb in host_micros),
-               "d2h_bytes_per_step": z.NORM_OUT_BYTES, "h2d_copy_gbs": h2d_gbs,
+               "d2h_bytes_per_step": z.NORM_OUT_BYTES, "h2d_copy_gbs_before": h2d_gbs,
+               "h2d_copy_ms_in_loop": copy_ms,
+               "h2d_copy_gbs_in_loop": sum(mb.numel() * mb.element_size() for mb in host_micros) /
+                                        (copy_ms * 1e-3) / 1e9,
                "how": "pinned host gradients copied by the DMA engines on a side stream into two staging "
                       "buffers, overlapping the previous step's kernels; norm record read back every step"}
         del host_micros, stage
