@@ -322,3 +322,79 @@ def test_misaligned_and_wrong_size_buffers_are_rejected():
     lib = z.load_library()
     arr = (ctypes.c_void_p * 1)(torch.zeros(112, dtype=torch.bfloat16, device="cuda").data_ptr() + 2)
     assert lib.zero1_accumulate(plan.handle, ctypes.c_void_p(g.data_ptr()), arr, 1, 1, None) == z.ZERO1_EALIGN
+
+
+def test_no_call_writes_outside_its_buffers():
+    """Every buffer sits between two guard zones filled with a pattern; after every entry point has
+    run on it, the guards are unchanged."""
+    numels = [1000, 7, 16384 + 9, 33]
+    nd = [0, 1, 0, 1]
+    plan = z.Plan(numels, nd, 3, 1)
+    n, total = plan.arena_numel, plan.total_numel
+    G = 64  # guard elements (a multiple of 8 keeps the buffers 16-byte aligned)
+
+    def guarded(count, dtype):
+        buf = torch.empty(count + 2 * G, dtype=dtype, device="cuda")
+        buf.view(torch.uint8).fill_(0xA5)
+        return buf, buf[G:G + count]
+
+    def zero_mid(pair):
+        pair[1].zero_()
+        return pair
+
+    bufs = {k: zero_mid(guarded(n, torch.float32)) for k in ("grad", "master", "m", "v")}
+    bufs["w"] = zero_mid(guarded(n, torch.bfloat16))
+    bufs["mb"] = zero_mid(guarded(n, torch.bfloat16))
+    bufs["ws"] = guarded(max(plan.workspace_bytes, 16), torch.uint8)
+    bufs["nout"] = guarded(32, torch.uint8)
+    bufs["full32"] = guarded(total, torch.float32)
+    bufs["full16"] = guarded(total, torch.bfloat16)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    L = plan.layout()
+    for o, c in zip(L.offsets, L.counts):
+        bufs["mb"][1][int(o):int(o) + int(c)] = (torch.randn(int(c), device="cuda", generator=g) * 0.1).to(torch.bfloat16)
+        bufs["master"][1][int(o):int(o) + int(c)] = torch.randn(int(c), device="cuda", generator=g) * 0.02
+    bufs["full32"][1].normal_(generator=g)
+    bufs["full16"][1].normal_(generator=g)
+    B = {k: v[1] for k, v in bufs.items()}
+    z.accumulate(plan, B["grad"], B["mb"])
+    z.accumulate(plan, B["grad"], [B["mb"], B["mb"]], overwrite_first=False)
+    z.accumulate_norm(plan, B["grad"], B["mb"], B["ws"], B["nout"], overwrite_first=False)
+    z.grad_norm(plan, B["grad"], B["ws"], B["nout"])
+    z.grad_norm_static(plan, B["grad"], B["nout"])
+    z.step(plan, B["master"], B["m"], B["v"], B["grad"], B["w"], z.Hparams(), 1, B["nout"])
+    z.shard_gather(plan, B["full32"], B["master"])
+    z.shard_scatter(plan, B["master"], B["full32"])
+    z.shard_gather(plan, B["full16"], B["w"])
+    z.shard_scatter(plan, B["w"], B["full16"])
+    torch.cuda.synchronize()
+    for k, (buf, mid) in bufs.items():
+        raw = buf.view(torch.uint8)
+        eb = buf.element_size()
+        head, tail = raw[:G * eb], raw[(G + mid.numel()) * eb:]
+        assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), k
+
+
+def test_other_hyperparameters_and_late_steps():
+    """lr 1e-2, betas (0.8, 0.999), eps 1e-6, weight decay 0.01, clip 0.5, steps 1000-1003
+    (bias corrections near 1) and steps 1-4, every element compared."""
+    hp = dict(lr=1e-2, beta1=0.8, beta2=0.999, eps=1e-6, weight_decay=0.01, clip_grad=0.5)
+    w = _custom([5000, 3, 16384 + 40, 100], [0, 1, 0, 1], dp=2, rank=1, K=3, steps=4, sigma=0.02, hp=hp)
+    res = run_parity(w)
+    assert res["master"] <= MAX_ULP
+    pb = Problem(w)
+    P = pb.master.cpu().numpy().copy()
+    M = np.zeros(pb.n, np.float32)
+    V = np.zeros(pb.n, np.float32)
+    from parity import group_counts, oracle_pass
+    idx = np.arange(pb.n, dtype=np.int64)
+    counts = group_counts(idx, pb.plan)
+    lr_s, wd_s = w.group_scales()
+    for t in (1000, 1001, 1002, 1003):
+        micros = pb.gen.micro_grads()
+        got = pb.gpu_step(micros, t)
+        g_idx, ref = oracle_pass(micros, pb.grad, idx)
+        ok, norm, coef = oracle.clip_coef(ref, hp["clip_grad"])
+        oracle.adamw_scaled(P, M, V, g_idx, counts, lr_s, wd_s, hp, t, coef)
+    for a, b in ((pb.master, P), (pb.m, M), (pb.v, V)):
+        assert ulp_diff(a.cpu().numpy(), b).max() <= MAX_ULP

@@ -115,3 +115,43 @@ def test_sumsq_allreduce_two_ranks_equals_unsharded_step():
 def test_nonfinite_on_one_rank_makes_every_rank_skip():
     results = _run(2, nan_rank=1)
     assert [ok for _, ok, *_ in results] == [False, False]
+
+
+def _worker_drops_out(rank, world, port, q):
+    import sys
+    import datetime
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import torch.distributed as dist
+    from zero_sharded_mixed_local_gb300.binding import allreduce_sumsq_
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=5))
+    def leave(msg):
+        q.put((rank, msg))
+        q.close()
+        q.join_thread()  # flush the message before the hard exit
+        os._exit(0)
+
+    if rank == 1:
+        leave("left")  # this rank dies between steps: it never joins the exchange
+    record = torch.zeros(32, dtype=torch.uint8)
+    try:
+        allreduce_sumsq_(record)
+        msg = "no error"
+    except Exception as e:  # the survivor learns of it instead of hanging
+        msg = "error: " + type(e).__name__
+    leave(msg)
+
+
+def test_a_rank_that_drops_out_is_detected_not_waited_for():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_drops_out, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+    assert out[1] == "left"
+    assert out[0].startswith("error"), out[0]
