@@ -237,6 +237,8 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="take the norm in its own pass (zero1_grad_norm) instead of fusing it into the last "
                          "micro-batch's accumulation")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the step as a CUDA graph (StepGraph) instead of eager calls; one GPU only")
     ap.add_argument("--micro-batches", type=int, default=None,
                     help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
     args = ap.parse_args()
@@ -304,6 +306,22 @@ def main():
         if record is not None:
             record["s1"].record(stream)
 
+    sgraph = None
+    if args.graph:
+        if world > 1:
+            raise SystemExit("--graph runs one rank (the captured step holds no all-reduce)")
+        from types import SimpleNamespace
+        state = SimpleNamespace(plan=plan, grad=grad, workspace=ws, norm_out=nout, master=master, exp_avg=m,
+                                exp_avg_sq=v, weight_bf16=wbf, hp=hp, t=0, device=dev)
+        sgraph = z.StepGraph(state, micros)
+
+        def one_step(record=None):  # noqa: F811  (the graph replaces the eager calls)
+            if record is not None:
+                record["a0"].record(stream)
+            sgraph.replay()
+            if record is not None:
+                record["s1"].record(stream)
+
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
@@ -327,13 +345,16 @@ def main():
     total_ms = start.elapsed_time(end)
     total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
-    acc_ms = statistics.mean(r["a0"].elapsed_time(r["n0"]) for r in recs)      # the first K-1 micro-batches
-    accnorm_ms = statistics.mean(r["n0"].elapsed_time(r["s0"]) for r in recs)  # last micro-batch + norm
-    step_ms = statistics.mean(r["s0"].elapsed_time(r["s1"]) for r in recs)
+    if sgraph is None:
+        acc_ms = statistics.mean(r["a0"].elapsed_time(r["n0"]) for r in recs)      # the first K-1 micro-batches
+        accnorm_ms = statistics.mean(r["n0"].elapsed_time(r["s0"]) for r in recs)  # last micro-batch + norm
+        step_ms = statistics.mean(r["s0"].elapsed_time(r["s1"]) for r in recs)
+    else:  # one graph launch per step: no per-kernel events inside it
+        acc_ms = accnorm_ms = step_ms = float("nan")
     z.read_norm(nout, stream)
 
     peak, peak_kind = measured_peaks()
-    step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9
+    step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9 if sgraph is None else None
     # fused: the norm rides on the last micro-batch's pass (no separate 4-byte read)
     norm_bytes = 4 * P if args.unfused else 0
     path_bytes = (accumulate_bytes_per_elem(K) + STEP_BYTES_PER_ELEM) * P + norm_bytes
@@ -347,7 +368,7 @@ def main():
     # loop logs it.  Two staging buffers and two gradient arenas let step t+1's transfer
     # (link-bound, on DMA engines) overlap step t's kernels (HBM-bound, on the SMs).
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and sgraph is None:
         host_micros = [mb.cpu().pin_memory() for mb in micros]
         stage = [micros, [torch.empty_like(mb) for mb in micros]]
         grads = [grad, plan.new_arena(torch.float32, dev)]
@@ -452,25 +473,26 @@ def main():
                 "dp_rank": dp_rank,
                 "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
                 "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
+                "launch": "one CUDA graph per step (StepGraph)" if sgraph is not None else "eager calls",
                 "l2": "no flush: each step streams %.1f GB, far above the 129 MB L2" % (path_bytes / 1e9),
             },
             "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
-            "kernels": {
+            "kernels": ({
                 "accumulate": {"ms": acc_ms, "gbs": (accumulate_bytes_per_elem(K) * P - last_bytes) /
                                (acc_ms * 1e-3) / 1e9 if K > 1 else None, "launches_per_step": K - 1},
                 ("accumulate+grad_norm" if args.unfused else "accumulate_norm"): {
                     "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
                     "launches_per_step": 3 if args.unfused else 2},
                 "adamw_step": {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
-            },
-            "roofline": {"bound": "hbm", "kernel": "adamw_step_kernel", "achieved": step_gbs, "peak": peak,
+            }) if sgraph is None else None,
+            "roofline": ({"bound": "hbm", "kernel": "adamw_step_kernel", "achieved": step_gbs, "peak": peak,
                          "unit": "GB/s", "frac": step_gbs / peak, "traffic": traffic,
                          "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
-                         "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P},
+                         "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P}) if sgraph is None else None,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "gpu_launches": args.steps * (K + 2 + (1 if args.unfused else 0)),
+            "gpu_launches": args.steps * (K + 2 + (1 if args.unfused else 0)),  # also inside each graph
         }
         print(json.dumps(out), flush=True)
     if world > 1:

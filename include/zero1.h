@@ -283,6 +283,36 @@ int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp
 int zero1_grad_norm_static(const zero1_plan* plan, const float* grad, double extra_sumsq,
                            zero1_norm_out* d_out, void* stream);
 
+/* ---- the step with its scalars in device memory (for CUDA graphs) ------- */
+
+/* The fp32 scalars zero1_step derives from (hparams, plan groups, step_t):
+ * per group the step size lr_g/(1-beta1^t) and the decay factor
+ * 1 - lr_g*wd_g, then beta1, beta2, 1-beta1, 1-beta2, eps, sqrt(1-beta2^t)
+ * (each computed in double and rounded once), and clip_grad. */
+typedef struct zero1_step_scalars {
+    float stepsize[ZERO1_MAX_GROUPS];
+    float dfac[ZERO1_MAX_GROUPS];
+    float b1, b2, omb1, omb2, eps, sqrtbc2;
+    double clip;
+} zero1_step_scalars; /* 96 bytes */
+
+/* Host only: the scalars zero1_step would use for (plan, hp, step_t).
+ * Errors: ZERO1_EINVAL, as zero1_step's hyper-parameter checks. */
+int zero1_step_scalars_fill(const zero1_plan* plan, const zero1_hparams* hp, int64_t step_t,
+                            zero1_step_scalars* out);
+
+/* zero1_step with the scalars read from DEVICE memory (d_scalars, 16-byte
+ * aligned) when the kernel runs, not passed at launch.  A CUDA graph that
+ * captured this call can therefore replay every step: the caller writes the
+ * next step's scalars (zero1_step_scalars_fill) where a captured copy picks
+ * them up.  Same arithmetic and results as zero1_step.  The pages have no
+ * counterpart of this call; it exists so the local step can be replayed as
+ * one graph launch.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_step_dev(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
+                   const float* grad, uint16_t* weight_bf16, const zero1_step_scalars* d_scalars,
+                   const zero1_norm_out* d_norm, void* stream);
+
 /* Copy a device zero1_norm_out to the host, synchronising `stream` first.
  * Errors: ZERO1_EINVAL, ZERO1_ECUDA. */
 int zero1_read_norm(const zero1_norm_out* d_norm, void* stream, zero1_norm_out* host_out);

@@ -239,3 +239,20 @@ def test_layout_calls_reject_bad_arguments_before_any_launch(z):
     empty = z.Plan([0], [0], 1, 0)
     assert lib.zero1_layout_table_bytes(empty.handle) == 0
     assert lib.zero1_shard_gather(empty.handle, None, None, None, 4, None) == z.ZERO1_OK
+
+
+def test_step_scalars_on_the_host(z):
+    import struct
+    plan = z.Plan([100, 8], groups=[0, 3], lr_scale=[1, 1, 1, 0.5, 1, 1, 1, 1], wd_scale=[1, 1, 1, 0, 1, 1, 1, 1])
+    v = struct.unpack("<16f6fd", z.step_scalars(plan, z.Hparams(lr=1e-3, beta1=0.9, beta2=0.99, eps=1e-8,
+                                                                weight_decay=0.1, clip_grad=2.0), 1))
+    stepsize, dfac, rest, clip = v[:8], v[8:16], v[16:22], v[22]
+    f32 = lambda x: struct.unpack("<f", struct.pack("<f", x))[0]  # noqa: E731
+    assert stepsize[0] == f32(1e-3 / (1 - 0.9)) and stepsize[3] == f32(0.5e-3 / (1 - 0.9))
+    assert dfac[0] == f32(1 - 1e-3 * 0.1) and dfac[3] == 1.0
+    assert rest == (f32(0.9), f32(0.99), f32(1 - 0.9), f32(1 - 0.99), f32(1e-8), f32((1 - 0.99) ** 0.5))
+    assert clip == 2.0
+    with pytest.raises(z.Zero1Error):
+        z.step_scalars(plan, z.Hparams(beta1=1.0), 1)
+    with pytest.raises(z.Zero1Error):
+        z.step_scalars(plan, z.Hparams(), 0)

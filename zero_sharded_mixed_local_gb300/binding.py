@@ -45,6 +45,15 @@ class _Hparams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_double) for n in ("lr", "beta1", "beta2", "eps", "weight_decay", "clip_grad")]
 
 
+class _StepScalars(ctypes.Structure):
+    _fields_ = [("stepsize", ctypes.c_float * 8), ("dfac", ctypes.c_float * 8)] + \
+               [(n, ctypes.c_float) for n in ("b1", "b2", "omb1", "omb2", "eps", "sqrtbc2")] + \
+               [("clip", ctypes.c_double)]
+
+
+STEP_SCALARS_BYTES = 96
+
+
 class _NormOut(ctypes.Structure):
     _fields_ = [("sumsq", ctypes.c_double), ("norm", ctypes.c_double), ("status", ctypes.c_int32),
                 ("n_partials", ctypes.c_int32)]
@@ -82,6 +91,8 @@ def load_library(path=None):
         "zero1_grad_norm_static": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, vp]),
         "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
         "zero1_read_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(_NormOut)]),
+        "zero1_step_scalars_fill": (ctypes.c_int, [vp, ctypes.POINTER(_Hparams), i64, ctypes.POINTER(_StepScalars)]),
+        "zero1_step_dev": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "zero1_layout_table_bytes": (ctypes.c_size_t, [vp]),
         "zero1_layout_table_upload": (ctypes.c_int, [vp, vp, ctypes.c_size_t, vp]),
         "zero1_shard_gather": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
@@ -394,6 +405,31 @@ def step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, hparams, step_t, 
            "zero1_step")
 
 
+def step_scalars(plan, hparams, step_t):
+    """zero1_step_scalars_fill: the 96 bytes of fp32 step scalars for (plan, hparams, step_t)."""
+    hp = hparams._c() if isinstance(hparams, Hparams) else Hparams(**hparams)._c()
+    out = _StepScalars()
+    _check(load_library().zero1_step_scalars_fill(plan.handle, ctypes.byref(hp), int(step_t), ctypes.byref(out)),
+           "zero1_step_scalars_fill")
+    return bytes(out)
+
+
+def step_dev(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, d_scalars, norm_out=None, stream=None):
+    """zero1_step_dev: the step with its scalars read from device memory (a uint8 tensor of at
+    least 96 bytes holding step_scalars()), so the call can be captured in a CUDA graph."""
+    lib = load_library()
+    n = plan.arena_numel
+    dev = master.device
+    ptrs = [_ptr(master, torch.float32, n, "master", dev), _ptr(exp_avg, torch.float32, n, "exp_avg", dev),
+            _ptr(exp_avg_sq, torch.float32, n, "exp_avg_sq", dev), _ptr(grad, torch.float32, n, "grad", dev)]
+    wp = None if weight_bf16 is None else _ptr(weight_bf16, torch.bfloat16, n, "weight_bf16", dev)
+    sp = _ptr(d_scalars, torch.uint8, None, "d_scalars", dev)
+    if d_scalars.numel() < STEP_SCALARS_BYTES:
+        raise ValueError("d_scalars needs %d bytes" % STEP_SCALARS_BYTES)
+    npp = None if norm_out is None else _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    _check(lib.zero1_step_dev(plan.handle, *ptrs, wp, sp, npp, _stream_ptr(stream, dev)), "zero1_step_dev")
+
+
 def read_norm(norm_out, stream=None):
     """zero1_read_norm: synchronise the stream and return the norm record as a dict."""
     lib = load_library()
@@ -538,3 +574,71 @@ class LocalShardAdamW:
 
     def read_norm(self, stream=None):
         return read_norm(self.norm_out, stream=stream)
+
+
+class StepGraph:
+    """The whole local step of a LocalShardAdamW captured as CUDA graphs.
+
+    One replay runs what accumulate(..., last=True) + step() launch: the
+    accumulation of the micro-batch buffers given here (their contents at
+    replay time), the fused norm, and the AdamW pass.  The step's scalars
+    (which change with t and lr) are not baked into the graph: before each
+    replay the host writes them into a pinned buffer that a captured copy
+    moves to the device.  Two graphs over two pinned buffers alternate, so
+    the host may write step t+1's scalars while step t still runs; it waits
+    only for step t-1.  No collective is captured: use it where the sum of
+    squares needs no all-reduce (one rank, or a caller that all-reduces the
+    norm record in its own graph).
+    """
+
+    def __init__(self, opt, micro_buffers):
+        self.opt = opt
+        self.micro = list(micro_buffers)
+        if not self.micro:
+            raise ValueError("at least one micro-batch buffer")
+        dev = opt.device
+        self.h = [torch.zeros(128, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.d = [torch.zeros(128, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self._warm_kernels(dev)
+        self.graphs = [self._capture(b) for b in range(2)]
+
+    def _warm_kernels(self, dev):
+        # Load every kernel the graph uses (lazy module loading) on a throwaway one-tensor plan,
+        # so the capture itself launches nothing for the first time.
+        tiny = Plan([16], [0])
+        a = [tiny.new_arena(torch.float32, dev) for _ in range(4)]
+        w = tiny.new_arena(torch.bfloat16, dev)
+        mbs = [tiny.new_arena(torch.bfloat16, dev) for _ in self.micro]
+        ws, nout = tiny.new_workspace(dev), new_norm_out(dev)
+        for k, mb in enumerate(mbs[:-1]):
+            accumulate(tiny, a[0], mb, overwrite_first=(k == 0))
+        accumulate_norm(tiny, a[0], mbs[-1], ws, nout, overwrite_first=(len(mbs) == 1))
+        sc = torch.frombuffer(bytearray(step_scalars(tiny, self.opt.hp, 1)), dtype=torch.uint8).to(dev)
+        step_dev(tiny, a[1], a[2], a[3], a[0], w, sc, nout)
+        torch.cuda.synchronize(dev)
+
+    def _capture(self, b):
+        o = self.opt
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.d[b].copy_(self.h[b], non_blocking=True)
+            for k, mb in enumerate(self.micro[:-1]):
+                accumulate(o.plan, o.grad, mb, overwrite_first=(k == 0))
+            accumulate_norm(o.plan, o.grad, self.micro[-1], o.workspace, o.norm_out,
+                            overwrite_first=(len(self.micro) == 1))
+            step_dev(o.plan, o.master, o.exp_avg, o.exp_avg_sq, o.grad, o.weight_bf16, self.d[b], o.norm_out)
+        return g
+
+    def replay(self, lr=None):
+        """One local step at t = opt.t + 1 (lr overrides the optimizer's lr for this step)."""
+        o = self.opt
+        t = o.t + 1
+        b = t % 2
+        self.done[b].synchronize()  # the replay that last read pinned buffer b (step t-2) is done
+        hp = o.hp if lr is None else Hparams(**{**o.hp.__dict__, "lr": lr})
+        self.h[b][:STEP_SCALARS_BYTES].copy_(torch.frombuffer(bytearray(step_scalars(o.plan, hp, t)),
+                                                              dtype=torch.uint8))
+        self.graphs[b].replay()
+        self.done[b].record()
+        o.t = t

@@ -48,10 +48,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <bool kWriteBf16>
+// kDevScalars: the scalars come from P.dev_scalars (read by thread 0 into
+// shared memory after the loads are issued) rather than from P.sc.
+template <bool kWriteBf16, bool kDevScalars>
 __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_constant__ StepParams P, int64_t first_vec) {
     __shared__ float s_coef;
     __shared__ int s_skip;
+    __shared__ zero1_step_scalars s_sc;
     const int64_t i = first_vec + static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x;
     const bool live = i < P.n_vec;
 
@@ -72,6 +75,11 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
         vb = v4[1];
     }
     if (threadIdx.x == 0) {
+        double clip = P.sc.clip;
+        if (kDevScalars) {
+            s_sc = *P.dev_scalars;
+            clip = s_sc.clip;
+        }
         // Clip coefficient from the device-resident norm: no host round trip.
         float coef = 1.0f;
         int skip = 0;
@@ -81,8 +89,8 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
             const double sumsq = P.norm->sumsq;
             if (P.norm->status != ZERO1_OK || !isfinite(sumsq)) {
                 skip = 1;
-            } else if (P.clip > 0.0) {
-                const double q = P.clip / (sqrt(sumsq) + 1e-6);
+            } else if (clip > 0.0) {
+                const double q = clip / (sqrt(sumsq) + 1e-6);
                 if (q < 1.0) coef = static_cast<float>(q);
             }
         }
@@ -93,14 +101,15 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
     if (s_skip || !live) return;  // a non-finite gradient norm leaves every buffer as it is
 
     const float coef = s_coef;
-    const StepConsts c{P.b1, P.b2, P.omb1, P.omb2, P.eps, P.sqrtbc2};
-    float dfac = P.dfac[0];
-    float stepsize = P.stepsize[0];
+    const zero1_step_scalars& S = kDevScalars ? s_sc : P.sc;
+    const StepConsts c{S.b1, S.b2, S.omb1, S.omb2, S.eps, S.sqrtbc2};
+    float dfac = S.dfac[0];
+    float stepsize = S.stepsize[0];
 #pragma unroll
     for (int k = 1; k < ZERO1_MAX_GROUPS; ++k) {
         if (i >= P.group_begin_vec[k]) {
-            dfac = P.dfac[k];
-            stepsize = P.stepsize[k];
+            dfac = S.dfac[k];
+            stepsize = S.stepsize[k];
         }
     }
     adamw_elem(pa.x, ma.x, va.x, ga.x, coef, dfac, stepsize, c);
@@ -138,10 +147,16 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t stream) {
     for (int64_t first = 0; first < p.n_vec; first += kMaxGridVectors(kStepThreads)) {
         const int64_t n = p.n_vec - first < kMaxGridVectors(kStepThreads) ? p.n_vec - first : kMaxGridVectors(kStepThreads);
         const unsigned grid = static_cast<unsigned>((n + kStepThreads - 1) / kStepThreads);
-        if (p.w != nullptr)
-            adamw_step_kernel<true><<<grid, kStepThreads, 0, stream>>>(p, first);
-        else
-            adamw_step_kernel<false><<<grid, kStepThreads, 0, stream>>>(p, first);
+        if (p.dev_scalars != nullptr) {
+            if (p.w != nullptr)
+                adamw_step_kernel<true, true><<<grid, kStepThreads, 0, stream>>>(p, first);
+            else
+                adamw_step_kernel<false, true><<<grid, kStepThreads, 0, stream>>>(p, first);
+        } else if (p.w != nullptr) {
+            adamw_step_kernel<true, false><<<grid, kStepThreads, 0, stream>>>(p, first);
+        } else {
+            adamw_step_kernel<false, false><<<grid, kStepThreads, 0, stream>>>(p, first);
+        }
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -117,25 +117,47 @@ extern "C" int zero1_grad_norm(const zero1_plan* plan, const float* grad, double
     return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
 }
 
-extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
-                          const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
-                          const zero1_norm_out* d_norm, void* stream) {
-    if (plan == nullptr || hp == nullptr || step_t < 1) return ZERO1_EINVAL;
+namespace zero1 {
+
+int fill_step_scalars(const zero1_plan* plan, const zero1_hparams* hp, int64_t step_t, zero1_step_scalars* sc) {
+    if (plan == nullptr || hp == nullptr || sc == nullptr || step_t < 1) return ZERO1_EINVAL;
     const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
     if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd) || !std::isfinite(hp->clip_grad))
         return ZERO1_EINVAL;
     if (!(b1 >= 0.0 && b1 < 1.0) || !(b2 >= 0.0 && b2 < 1.0) || eps < 0.0) return ZERO1_EINVAL;
+    // Step scalars in double, each rounded once to fp32.
+    const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step_t));
+    const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step_t));
+    if (!(bc1 > 0.0) || !(bc2 > 0.0)) return ZERO1_EINVAL;
+    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) {
+        const double lr_g = lr * plan->lr_scale[g];
+        const double wd_g = wd * plan->wd_scale[g];
+        sc->stepsize[g] = static_cast<float>(lr_g / bc1);
+        sc->dfac[g] = static_cast<float>(1.0 - lr_g * wd_g);
+    }
+    sc->b1 = static_cast<float>(b1);
+    sc->b2 = static_cast<float>(b2);
+    sc->omb1 = static_cast<float>(1.0 - b1);
+    sc->omb2 = static_cast<float>(1.0 - b2);
+    sc->eps = static_cast<float>(eps);
+    sc->sqrtbc2 = static_cast<float>(std::sqrt(bc2));
+    sc->clip = hp->clip_grad;
+    return ZERO1_OK;
+}
+
+}  // namespace zero1
+
+namespace {
+
+// Checks shared by zero1_step and zero1_step_dev, and the launch.
+int launch_checked_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq, const float* grad,
+                        uint16_t* weight_bf16, const zero1_step_scalars* sc, const zero1_step_scalars* d_scalars,
+                        const zero1_norm_out* d_norm, void* stream) {
     if (plan->arena_numel == 0) return ZERO1_OK;  // nothing to do; empty buffers may be NULL
     if (master == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || grad == nullptr) return ZERO1_EINVAL;
     if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) || !aligned16(grad)) return ZERO1_EALIGN;
     if (weight_bf16 != nullptr && !aligned16(weight_bf16)) return ZERO1_EALIGN;
     if (d_norm != nullptr && !aligned16(d_norm)) return ZERO1_EALIGN;
-
-    // Step scalars in double, each rounded once to fp32.
-    const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step_t));
-    const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step_t));
-    if (!(bc1 > 0.0) || !(bc2 > 0.0)) return ZERO1_EINVAL;
-
     zero1::StepParams p{};
     p.master = master;
     p.m = exp_avg;
@@ -144,22 +166,36 @@ extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg,
     p.w = weight_bf16;
     p.norm = d_norm;
     p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
-    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) {
-        const double lr_g = lr * plan->lr_scale[g];
-        const double wd_g = wd * plan->wd_scale[g];
-        p.group_begin_vec[g] = plan->group_begin[g] / ZERO1_ARENA_ALIGN;
-        p.stepsize[g] = static_cast<float>(lr_g / bc1);
-        p.dfac[g] = static_cast<float>(1.0 - lr_g * wd_g);
-    }
-    p.b1 = static_cast<float>(b1);
-    p.b2 = static_cast<float>(b2);
-    p.omb1 = static_cast<float>(1.0 - b1);
-    p.omb2 = static_cast<float>(1.0 - b2);
-    p.eps = static_cast<float>(eps);
-    p.sqrtbc2 = static_cast<float>(std::sqrt(bc2));
-    p.clip = hp->clip_grad;
+    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) p.group_begin_vec[g] = plan->group_begin[g] / ZERO1_ARENA_ALIGN;
+    if (sc != nullptr) p.sc = *sc;
+    p.dev_scalars = d_scalars;
     const cudaError_t e = zero1::launch_step(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
+                          const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                          const zero1_norm_out* d_norm, void* stream) {
+    zero1_step_scalars sc{};
+    const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
+    if (rc != ZERO1_OK) return rc;
+    return launch_checked_step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, &sc, nullptr, d_norm, stream);
+}
+
+extern "C" int zero1_step_scalars_fill(const zero1_plan* plan, const zero1_hparams* hp, int64_t step_t,
+                                       zero1_step_scalars* out) {
+    return zero1::fill_step_scalars(plan, hp, step_t, out);
+}
+
+extern "C" int zero1_step_dev(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
+                              const float* grad, uint16_t* weight_bf16, const zero1_step_scalars* d_scalars,
+                              const zero1_norm_out* d_norm, void* stream) {
+    if (plan == nullptr || d_scalars == nullptr) return ZERO1_EINVAL;
+    if (!aligned16(d_scalars)) return ZERO1_EALIGN;
+    return launch_checked_step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, nullptr, d_scalars, d_norm,
+                               stream);
 }
 
 extern "C" int zero1_layout_table_upload(const zero1_plan* plan, void* d_table, size_t table_bytes, void* stream) {

@@ -65,11 +65,13 @@ struct StepParams {
     const zero1_norm_out* norm;  // may be null: no clipping
     int64_t n_vec;               // arena_numel / 8
     int64_t group_begin_vec[ZERO1_MAX_GROUPS];  // first 8-element vector of each group
-    float dfac[ZERO1_MAX_GROUPS];
-    float stepsize[ZERO1_MAX_GROUPS];
-    float b1, b2, omb1, omb2, eps, sqrtbc2;
-    double clip;
+    zero1_step_scalars sc;                      // the step's scalars, at launch
+    const zero1_step_scalars* dev_scalars;      // or read from device memory when the kernel runs
 };
+static_assert(sizeof(zero1_step_scalars) == 96, "zero1_step_scalars is 96 bytes");
+
+// The fp32 step scalars for (plan, hp, t); ZERO1_OK or ZERO1_EINVAL.
+int fill_step_scalars(const zero1_plan* plan, const zero1_hparams* hp, int64_t step_t, zero1_step_scalars* sc);
 
 cudaError_t launch_accumulate(const AccumulateParams& p, cudaStream_t stream);
 cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int64_t n_tiles,
