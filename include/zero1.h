@@ -215,14 +215,21 @@ int zero1_grad_norm(const zero1_plan* plan, const float* grad, double extra_sums
  * of a step ("ZeRO-1 风格的 Distributed Optimizer", section 6.7: the norm is
  * taken once all micro-batch gradients are in .grad).  The gradient written
  * is bit-identical to zero1_accumulate's and the norm record to
- * zero1_grad_norm's (same tiles, same summation order), but the gradient is
+ * zero1_grad_norm's (same tiles, same summation order; with grad_divisor 1),
+ * but the gradient is
  * not read back for the norm: 4 bytes per element less traffic.
  *   grad, micro_bf16, n_micro, overwrite_first   as for zero1_accumulate
+ *   grad_divisor  after the last addition each element is divided by this
+ *                 (rounded to fp32; one IEEE division), before its square is
+ *                 taken: the average over data-parallel ranks that FSDP2
+ *                 runs as a single divide kernel after the fp32
+ *                 reduce-scatter ("TorchTitan 生产级预训练方案", appendix B.1).
+ *                 1 keeps the plain sum (no division); must be finite > 0
  *   extra_sumsq, workspace, workspace_bytes, d_out  as for zero1_grad_norm
  * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
 int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
-                          int32_t n_micro, int32_t overwrite_first, double extra_sumsq, void* workspace,
-                          size_t workspace_bytes, zero1_norm_out* d_out, void* stream);
+                          int32_t n_micro, int32_t overwrite_first, double grad_divisor, double extra_sumsq,
+                          void* workspace, size_t workspace_bytes, zero1_norm_out* d_out, void* stream);
 
 /* Fused clip + AdamW + bf16 copy over the local shard ("ZeRO-1 风格的
  * Distributed Optimizer", sections 6.2-6.3: each rank updates only its own

@@ -41,6 +41,7 @@ def _load():
         lib.oracle_bf16_rne.restype = ctypes.c_uint16
         lib.oracle_bf16_rne_array.argtypes = [vp, vp, ctypes.c_int64]
         lib.oracle_accumulate.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int32]
+        lib.oracle_divide.argtypes = [vp, ctypes.c_int64, ctypes.c_float]
         lib.oracle_sumsq.argtypes = [vp, ctypes.c_int64]
         lib.oracle_sumsq.restype = ctypes.c_double
         lib.oracle_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double,
@@ -112,6 +113,12 @@ def accumulate_all(grad, micros):
     """Accumulate every micro-batch in order, the first one overwriting."""
     for k, mb in enumerate(micros):
         accumulate(grad, mb, overwrite=(k == 0))
+
+
+def divide(grad, divisor):
+    """grad (float32, in place) /= divisor (rounded to fp32), one IEEE division per element."""
+    _check(grad, np.float32, "grad")
+    _load().oracle_divide(_ptr(grad), grad.size, float(np.float32(divisor)))
 
 
 def sumsq(grad):

@@ -144,6 +144,16 @@ void oracle_accumulate(float *grad, const uint16_t *micro, int64_t n, int32_t ov
     }
 }
 
+/* The average over data-parallel ranks ("TorchTitan 生产级预训练方案",       */
+/* appendix B.1: FSDP2 runs a single divide kernel that divides the local   */
+/* fp32 reduce-scattered gradient by the world size).  grad[j] = grad[j] /  */
+/* divisor, one IEEE fp32 division per element, after the last addition.    */
+void oracle_divide(float *grad, int64_t n, float divisor)
+{
+    for (int64_t j = 0; j < n; ++j)
+        grad[j] = grad[j] / divisor;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Sum of squares for the L2 gradient norm ("ZeRO-1 风格的 Distributed        */
 /* Optimizer", section 6.6: clip_grad 1.0; the norm type is not stated, L2  */

@@ -101,7 +101,7 @@ int main(int argc, char** argv) {
     check_cuda(cudaStreamCreate(&stream), "stream");
     const uint16_t* micro[1] = {d_g};
     zero1_hparams hp = {3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0};
-    check(zero1_accumulate_norm(plan, d_grad, micro, 1, 1, 0.0, d_ws, ws_bytes, d_norm, stream),
+    check(zero1_accumulate_norm(plan, d_grad, micro, 1, 1, 1.0, 0.0, d_ws, ws_bytes, d_norm, stream),
           "zero1_accumulate_norm");
     check(zero1_step(plan, d_p, d_m, d_v, d_grad, d_w, &hp, 1, d_norm, stream), "zero1_step");
     zero1_norm_out rec;

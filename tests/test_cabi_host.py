@@ -256,3 +256,13 @@ def test_step_scalars_on_the_host(z):
         z.step_scalars(plan, z.Hparams(beta1=1.0), 1)
     with pytest.raises(z.Zero1Error):
         z.step_scalars(plan, z.Hparams(), 0)
+
+
+def test_fused_pass_rejects_a_bad_divisor_before_any_launch(z):
+    lib = z.load_library()
+    plan = z.Plan([100, 8], [0, 1], 1, 0)
+    fake = ctypes.c_void_p(0x10000)
+    arr = (ctypes.c_void_p * 1)(0x20000)
+    for d in (0.0, -2.0, float("nan"), float("inf")):
+        rc = lib.zero1_accumulate_norm(plan.handle, fake, arr, 1, 1, d, 0.0, fake, 64, fake, None)
+        assert rc == z.ZERO1_EINVAL, d

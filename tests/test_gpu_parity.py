@@ -398,3 +398,76 @@ def test_other_hyperparameters_and_late_steps():
         oracle.adamw_scaled(P, M, V, g_idx, counts, lr_s, wd_s, hp, t, coef)
     for a, b in ((pb.master, P), (pb.m, M), (pb.v, V)):
         assert ulp_diff(a.cpu().numpy(), b).max() <= MAX_ULP
+
+
+def test_fused_pass_divides_by_the_world_size():
+    """zero1_accumulate_norm with grad_divisor d: grad = (sum of micro-batches) / d, one IEEE
+    division per element after the last addition, bit for bit against the oracle; the norm is
+    the norm of the divided gradient."""
+    for K, d in ((1, 2.0), (3, 3.0), (2, 8.0), (4, 7.0)):
+        pb = Problem(_custom([16384 * 2 + 13, 77, 1000], [0, 1, 0], K=K, steps=1, sigma=0.3))
+        micros = pb.gen.micro_grads()
+        for k, mb in enumerate(micros[:-1]):
+            z.accumulate(pb.plan, pb.grad, mb, overwrite_first=(k == 0))
+        z.accumulate_norm(pb.plan, pb.grad, micros[-1], pb.ws, pb.nout, overwrite_first=(K == 1), divisor=d)
+        got = z.read_norm(pb.nout)
+        ref = oracle_grad(pb.n, [u16(m) for m in micros])
+        oracle.divide(ref, d)
+        assert np.array_equal(pb.grad.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (K, d)
+        s = oracle.sumsq(ref)
+        assert abs(got["sumsq"] - s) <= 1e-12 * s
+
+
+def test_data_parallel_average_emulated_on_one_gpu():
+    """dp=4 ranks reduce-scatter their gradients and divide by the world size in the fused pass
+    (the FSDP2-style average), take the global norm and step: equal to one rank stepping on the
+    average of all ranks' gradients, bit for bit."""
+    from zero_sharded_mixed_local_gb300.workloads import get_workload
+    w = get_workload("toy")
+    numels, nd = w.params.numels, w.params.no_decay
+    total, dp = sum(numels), 4
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    master_full = torch.randn(total, device="cuda", generator=gen) * 0.02
+    plans = [z.Plan(numels, nd, dp, r) for r in range(dp)]
+    ref_plan = z.Plan(numels, nd, 1, 0)
+    chunk = z.exchange_chunk_numel(plans)
+
+    def state(plan):
+        s = {k: plan.new_arena() for k in ("master", "m", "v", "grad")}
+        z.shard_gather(plan, master_full, s["master"])
+        s["w"], s["ws"], s["nout"] = plan.new_arena(torch.bfloat16), plan.new_workspace(), z.new_norm_out()
+        return s
+
+    ranks, ref = [state(p) for p in plans], state(ref_plan)
+    hp = z.Hparams(**w.hp)
+    for t in (1, 2):
+        grads = [(torch.randn(total, device="cuda", generator=gen) * 0.1).to(torch.bfloat16) for _ in range(dp)]
+        sends = []
+        for q in range(dp):
+            send = torch.empty((dp, chunk), dtype=torch.bfloat16, device="cuda")
+            z.pack_reduce_scatter(plans, grads[q], send)
+            sends.append(send)
+        for r, (pl, st) in enumerate(zip(plans, ranks)):
+            for q in range(dp - 1):
+                z.accumulate(pl, st["grad"], sends[q][r, :pl.arena_numel], overwrite_first=(q == 0))
+            z.accumulate_norm(pl, st["grad"], sends[dp - 1][r, :pl.arena_numel], st["ws"], st["nout"],
+                              overwrite_first=False, divisor=dp)
+        local = [z.read_norm(st["nout"])["sumsq"] for st in ranks]
+        for r, (pl, st) in enumerate(zip(plans, ranks)):
+            z.grad_norm(pl, st["grad"], st["ws"], st["nout"], extra_sumsq=sum(local) - local[r])
+            z.step(pl, st["master"], st["m"], st["v"], st["grad"], st["w"], hp, t, st["nout"])
+        for q in range(dp):
+            a = ref_plan.new_arena(torch.bfloat16)
+            z.shard_gather(ref_plan, grads[q], a)
+            if q < dp - 1:
+                z.accumulate(ref_plan, ref["grad"], a, overwrite_first=(q == 0))
+            else:
+                z.accumulate_norm(ref_plan, ref["grad"], a, ref["ws"], ref["nout"], overwrite_first=False,
+                                  divisor=dp)
+        z.step(ref_plan, ref["master"], ref["m"], ref["v"], ref["grad"], ref["w"], hp, t, ref["nout"])
+    for key in ("master", "m", "v"):
+        full, ref_full = torch.zeros(total, device="cuda"), torch.zeros(total, device="cuda")
+        for pl, st in zip(plans, ranks):
+            z.shard_scatter(pl, st[key], full)
+        z.shard_scatter(ref_plan, ref[key], ref_full)
+        assert torch.equal(full.view(torch.int32), ref_full.view(torch.int32)), key

@@ -49,6 +49,8 @@ MUTANTS = {
     "nan_not_quieted": ("return (uint16_t)((u >> 16) | 0x0040u);", "return (uint16_t)(u >> 16);"),
     "optimizer_bytes_not_sharded": ("out[2] = 12 * local_numel;", "out[2] = 12 * total_numel;"),
     "weights_bytes_fp32": ("out[0] = 2 * total_numel;", "out[0] = 4 * total_numel;"),
+    "divide_is_multiply": ("grad[j] = grad[j] / divisor;", "grad[j] = grad[j] * divisor;"),
+    "divide_by_reciprocal": ("grad[j] = grad[j] / divisor;", "grad[j] = grad[j] * (1.0f / divisor);"),
     "scaled_lr_ignored": ("const double lr_i = hp->lr * lr_scale[i];", "const double lr_i = hp->lr;"),
     "scaled_wd_ignored": ("const double wd_i = hp->weight_decay * wd_scale[i];",
                           "const double wd_i = hp->weight_decay;"),

@@ -543,3 +543,21 @@ def test_adamw_scaled_vs_torch_param_groups(oracle_mod):
     tp_all = np.concatenate([tp.detach().numpy() for tp in tparams])
     bound = 4 * np.spacing(np.abs(tp_all)) + 1e-5 * lr_el * 7
     assert np.all(np.abs(p - tp_all) <= bound)
+
+
+# --------------------------------------------------------------------------
+# Division of the reduced gradient by the world size.
+# --------------------------------------------------------------------------
+def test_divide_matches_numpy_float32_division(oracle_mod):
+    rng = np.random.default_rng(15)
+    g = (rng.standard_normal(100_003) * 10.0 ** rng.uniform(-30, 30, 100_003)).astype(np.float32)
+    for d in (1.0, 2.0, 3.0, 7.0, 8.0, 64.0, 1.5):
+        x = g.copy()
+        oracle_mod.divide(x, d)
+        assert np.array_equal(f32_bits(x), f32_bits(g / np.float32(d))), d
+    x = g.copy()
+    oracle_mod.divide(x, 1.0)
+    assert np.array_equal(f32_bits(x), f32_bits(g))
+    x = np.array([3.0, -9.0, 0.75], np.float32)
+    oracle_mod.divide(x, 3.0)
+    assert x.tolist() == [1.0, -3.0, 0.25]

@@ -85,8 +85,8 @@ def load_library(path=None):
         "zero1_plan_bytes": (ctypes.c_int, [vp, i32, i64p]),
         "zero1_workspace_bytes": (ctypes.c_size_t, [vp]),
         "zero1_accumulate": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, i32, vp]),
-        "zero1_accumulate_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, i32, ctypes.c_double, vp,
-                                                 ctypes.c_size_t, vp, vp]),
+        "zero1_accumulate_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, i32, ctypes.c_double,
+                                                 ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
         "zero1_grad_norm": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
         "zero1_grad_norm_static": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, vp]),
         "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
@@ -336,8 +336,10 @@ def _micro_array(plan, micro, dev):
                                                         host_ok=True).value for k, mb in enumerate(micro)])
 
 
-def accumulate_norm(plan, grad, micro, workspace, norm_out, overwrite_first=True, extra_sumsq=0.0, stream=None):
-    """zero1_accumulate_norm: accumulate the last micro-batch(es) and take the norm in one pass."""
+def accumulate_norm(plan, grad, micro, workspace, norm_out, overwrite_first=True, extra_sumsq=0.0, divisor=1.0,
+                    stream=None):
+    """zero1_accumulate_norm: accumulate the last micro-batch(es) and take the norm in one pass.
+    ``divisor`` (e.g. the data-parallel world size) divides the finished sum first."""
     lib = load_library()
     dev = grad.device
     gp = _ptr(grad, torch.float32, plan.arena_numel, "grad")
@@ -349,8 +351,8 @@ def accumulate_norm(plan, grad, micro, workspace, norm_out, overwrite_first=True
     if norm_out.numel() < NORM_OUT_BYTES:
         raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
     _check(lib.zero1_accumulate_norm(plan.handle, gp, arr, len(micro), 1 if overwrite_first else 0,
-                                     float(extra_sumsq), wp, workspace.numel(), op, _stream_ptr(stream, dev)),
-           "zero1_accumulate_norm")
+                                     float(divisor), float(extra_sumsq), wp, workspace.numel(), op,
+                                     _stream_ptr(stream, dev)), "zero1_accumulate_norm")
 
 
 def grad_norm(plan, grad, workspace, norm_out, extra_sumsq=0.0, stream=None):
@@ -542,14 +544,15 @@ class LocalShardAdamW:
         self.t = 0
         self._micro_seen = 0
 
-    def accumulate(self, micro, last=False, extra_sumsq=0.0, stream=None):
+    def accumulate(self, micro, last=False, extra_sumsq=0.0, divisor=1.0, stream=None):
         """Add one (or several) bf16 micro-batch gradient arenas; the first call of a step
         overwrites.  ``last=True`` marks the step's final micro-batch: the gradient norm
-        is taken in the same pass and step() will not read the gradient for it again."""
+        is taken in the same pass (after dividing the sum by ``divisor``, e.g. the world
+        size) and step() will not read the gradient for it again."""
         first = self._micro_seen == 0
         if last:
             accumulate_norm(self.plan, self.grad, micro, self.workspace, self.norm_out, overwrite_first=first,
-                            extra_sumsq=extra_sumsq, stream=stream)
+                            extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
         else:
             accumulate(self.plan, self.grad, micro, overwrite_first=first, stream=stream)
         self._micro_seen += 1 if isinstance(micro, torch.Tensor) else len(micro)

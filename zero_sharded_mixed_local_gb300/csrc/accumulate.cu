@@ -12,7 +12,9 @@
 // micro-batch, two 16-byte fp32 accesses.
 //
 // accumulate_norm_kernel fuses the last micro-batch's pass with the gradient
-// norm: each block owns one 16384-element norm tile, writes the accumulated
+// norm (and, when asked, with the division of the reduced gradient by the
+// world size that FSDP2 runs as its own kernel, "TorchTitan 生产级预训练方案",
+// appendix B.1: one IEEE division per element after the last addition): each block owns one 16384-element norm tile, writes the accumulated
 // gradient and adds its squares into float pairs with exactly the mapping and
 // order of sumsq_tiles_kernel, so the norm record is bit-identical to
 // zero1_grad_norm's while the gradient is never read back (4 bytes per element
@@ -114,6 +116,10 @@ __global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 5 : 1)
                 const int v = threadIdx.x + (half * (kVecsPerThread / 2) + q) * kTileThreads;
                 float acc[8];
                 widen8(raw[q], acc);
+                if (P.divide) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = __fdiv_rn(acc[j], P.divisor);
+                }
                 const float4 a = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 const float4 b = make_float4(acc[4], acc[5], acc[6], acc[7]);
                 if (v < nv) {
@@ -131,6 +137,10 @@ __global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 5 : 1)
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (v < nv) {
                 accumulate_vec(P, v0 + v, acc);
+                if (P.divide) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = __fdiv_rn(acc[j], P.divisor);
+                }
                 float4* g4 = reinterpret_cast<float4*>(P.grad) + 2 * (v0 + v);
                 g4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 g4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);

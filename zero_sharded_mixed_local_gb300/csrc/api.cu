@@ -5,9 +5,20 @@
 #include <cstdio>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "zero1_internal.h"
 
 namespace {
+
+// One NVTX range per compute call, so profiler timelines show each entry
+// point around its kernels (no cost unless a tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 thread_local char g_cuda_error[256] = "";
 
@@ -46,6 +57,7 @@ int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
 extern "C" int zero1_accumulate(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
                                 int32_t n_micro, int32_t overwrite_first, void* stream) {
+    NvtxRange range("zero1_accumulate");
     if (plan == nullptr || micro_bf16 == nullptr) return ZERO1_EINVAL;
     if (n_micro < 1 || n_micro > ZERO1_MAX_MICRO) return ZERO1_EINVAL;
     if (plan->arena_numel == 0) return ZERO1_OK;  // nothing to do; empty buffers may be NULL
@@ -70,10 +82,13 @@ extern "C" int zero1_accumulate(const zero1_plan* plan, float* grad, const uint1
 }
 
 extern "C" int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
-                                     int32_t n_micro, int32_t overwrite_first, double extra_sumsq, void* workspace,
-                                     size_t workspace_bytes, zero1_norm_out* d_out, void* stream) {
+                                     int32_t n_micro, int32_t overwrite_first, double grad_divisor,
+                                     double extra_sumsq, void* workspace, size_t workspace_bytes,
+                                     zero1_norm_out* d_out, void* stream) {
+    NvtxRange range("zero1_accumulate_norm");
     if (plan == nullptr || micro_bf16 == nullptr || d_out == nullptr) return ZERO1_EINVAL;
     if (n_micro < 1 || n_micro > ZERO1_MAX_MICRO) return ZERO1_EINVAL;
+    if (!std::isfinite(grad_divisor) || !(grad_divisor > 0.0)) return ZERO1_EINVAL;
     if (std::isnan(extra_sumsq) || extra_sumsq < 0.0) return ZERO1_EINVAL;
     if (!aligned16(d_out)) return ZERO1_EALIGN;
     const int64_t n_tiles = zero1::norm_tiles(plan->arena_numel);
@@ -96,6 +111,8 @@ extern "C" int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const 
     p.n_micro = n_micro;
     p.overwrite_first = overwrite_first ? 1 : 0;
     p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
+    p.divisor = static_cast<float>(grad_divisor);
+    p.divide = grad_divisor != 1.0 ? 1 : 0;
     const cudaError_t e = zero1::launch_accumulate_norm(p, static_cast<double*>(workspace), n_tiles, extra_sumsq,
                                                         d_out, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
@@ -103,6 +120,7 @@ extern "C" int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const 
 
 extern "C" int zero1_grad_norm(const zero1_plan* plan, const float* grad, double extra_sumsq, void* workspace,
                                size_t workspace_bytes, zero1_norm_out* d_out, void* stream) {
+    NvtxRange range("zero1_grad_norm");
     if (plan == nullptr || d_out == nullptr) return ZERO1_EINVAL;
     const int64_t n_tiles = zero1::norm_tiles(plan->arena_numel);
     if (n_tiles > 0) {
@@ -178,6 +196,7 @@ int launch_checked_step(const zero1_plan* plan, float* master, float* exp_avg, f
 extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
                           const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
                           const zero1_norm_out* d_norm, void* stream) {
+    NvtxRange range("zero1_step");
     zero1_step_scalars sc{};
     const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
     if (rc != ZERO1_OK) return rc;
@@ -192,6 +211,7 @@ extern "C" int zero1_step_scalars_fill(const zero1_plan* plan, const zero1_hpara
 extern "C" int zero1_step_dev(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
                               const float* grad, uint16_t* weight_bf16, const zero1_step_scalars* d_scalars,
                               const zero1_norm_out* d_norm, void* stream) {
+    NvtxRange range("zero1_step_dev");
     if (plan == nullptr || d_scalars == nullptr) return ZERO1_EINVAL;
     if (!aligned16(d_scalars)) return ZERO1_EALIGN;
     return launch_checked_step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, nullptr, d_scalars, d_norm,
@@ -233,11 +253,13 @@ int layout_copy(const zero1_plan* plan, const void* d_table, const void* src, vo
 
 extern "C" int zero1_shard_gather(const zero1_plan* plan, const void* d_table, const void* full, void* arena,
                                   int32_t elem_bytes, void* stream) {
+    NvtxRange range("zero1_shard_gather");
     return layout_copy(plan, d_table, full, arena, elem_bytes, true, stream);
 }
 
 extern "C" int zero1_shard_scatter(const zero1_plan* plan, const void* d_table, const void* arena, void* full,
                                    int32_t elem_bytes, void* stream) {
+    NvtxRange range("zero1_shard_scatter");
     return layout_copy(plan, d_table, arena, full, elem_bytes, false, stream);
 }
 

@@ -53,7 +53,9 @@ struct AccumulateParams {
     const uint16_t* micro[ZERO1_MAX_MICRO];
     int32_t n_micro;
     int32_t overwrite_first;
-    int64_t n_vec;  // arena_numel / 8
+    int64_t n_vec;      // arena_numel / 8
+    float divisor;      // accumulate_norm: divide the sum by this after the last addition
+    int32_t divide;     // 0: plain sum (divisor unused)
 };
 
 struct StepParams {
