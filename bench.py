@@ -212,11 +212,15 @@ def run_reference(args, w, world, rank):
     times = [oracle_sample_step(m_, mm, vv, mic, n, w.hp, args.warmup + t) for t in range(1, args.steps + 1)]
     sec = sum(times) / len(times)
     value = n / sec
+    import oracle
+    local = int(oracle.plan(w.params.numels, w.dp_size, w.dp_rank)[2])
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.description, "sample_elements": n, "micro_batches": w.micro_batches},
+        "config": {"workload": w.description, "local_params_per_gpu": local, "micro_batches": w.micro_batches,
+                   "dp_size": w.dp_size, "dp_rank": w.dp_rank, "parallelism": "zero1 dp%d shard" % w.dp_size,
+                   "sample_elements": n, "launch": "scalar C oracle on one host core"},
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
                          "sample": "%d elements drawn like the workload's decayed tensors, per step" % n},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
