@@ -47,14 +47,20 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def profile_traffic(kernel_src, workload):
-    """DRAM bytes per launch from the committed ncu summary, or None if it is
-    missing or was taken on a different version of the kernel source."""
-    path = os.path.join(ROOT, "profiles", "adamw_step_%s.md" % workload)
-    src = os.path.join(ROOT, "zero_sharded_mixed_local_gb300", "csrc", kernel_src)
+def profile_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` ("adamw_step" or "list_step") from its committed
+    ncu summary, or None if it is missing or was taken on a different version of the
+    kernel's sources (the kernel file and the per-element arithmetic it includes)."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+    csrc = os.path.join(ROOT, "zero_sharded_mixed_local_gb300", "csrc")
+    srcs = {"adamw_step": ["adamw_step.cu", "elementwise.cuh"],
+            "list_step": ["tensor_list.cu", "elementwise.cuh"]}[kernel]
     try:
         text = open(path, encoding="utf-8").read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for src in srcs:
+            h.update(open(os.path.join(csrc, src), "rb").read())
+        digest = h.hexdigest()[:16]
     except OSError:
         return None
     fields = {}
@@ -243,6 +249,9 @@ def main():
                          "micro-batch's accumulation")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step as a CUDA graph (StepGraph) instead of eager calls; one GPU only")
+    ap.add_argument("--tensor-list", action="store_true",
+                    help="run the tensor-list calls (one pointer per tensor shard, a run table walked by the "
+                         "kernels) on per-tensor views of the same buffers, instead of the arena calls")
     ap.add_argument("--micro-batches", type=int, default=None,
                     help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
     args = ap.parse_args()
@@ -282,13 +291,51 @@ def main():
     if world > 1:
         import torch.distributed as dist
         group = dist.group.WORLD
+    lists = None
+    if args.tensor_list:
+        if args.graph or args.unfused:
+            raise SystemExit("--tensor-list runs the fused eager calls")
+        args.no_e2e = True  # the end-to-end leg stages arenas
+        # one allocation per tensor shard, as a framework holds per-parameter state, filled
+        # from the generated arenas (which are then freed) and reached through pointer lists
+        def split(buf):
+            return [t.clone() for t in plan.shard_views(buf)]
+
+        lists = {name: z.PointerLists(plan, split(buf), torch.float32, dev)
+                 for name, buf in (("master", master), ("m", m), ("v", v), ("grad", grad))}
+        lists["w"] = z.PointerLists(plan, split(wbf), torch.bfloat16, dev)
+        lists["micro"] = [z.PointerLists(plan, split(mb), torch.bfloat16, dev) for mb in micros]
+        master = m = v = grad = wbf = micros = None
+        torch.cuda.empty_cache()
+        table, lws = plan.list_table(dev), plan.new_list_workspace(dev)
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     t_counter = [0]
 
+    def one_list_step(record=None):
+        t_counter[0] += 1
+        if record is not None:
+            record["a0"].record(stream)
+        for k in range(K - 1):
+            z.list_accumulate(plan, table, lists["grad"], lists["micro"][k], overwrite_first=(k == 0), stream=stream)
+        if record is not None:
+            record["n0"].record(stream)
+        z.list_accumulate_norm(plan, table, lists["grad"], lists["micro"][K - 1], lws, nout, overwrite_first=(K == 1),
+                               stream=stream)
+        if group is not None:
+            z.allreduce_sumsq_(nout, group)
+        if record is not None:
+            record["s0"].record(stream)
+        z.list_step(plan, table, lists["master"], lists["m"], lists["v"], lists["grad"], lists["w"], hp, t_counter[0],
+                    nout, stream=stream)
+        if record is not None:
+            record["s1"].record(stream)
+
     def one_step(record=None):
+        if lists is not None:
+            return one_list_step(record)
         t_counter[0] += 1
         if record is not None:
             record["a0"].record(stream)
@@ -363,7 +410,8 @@ def main():
     norm_bytes = 4 * P if args.unfused else 0
     path_bytes = (accumulate_bytes_per_elem(K) + STEP_BYTES_PER_ELEM) * P + norm_bytes
     last_bytes = (6 if K == 1 else 10) * P + norm_bytes
-    traffic = profile_traffic("adamw_step.cu", args.workload)
+    step_kernel = "list_step" if lists is not None else "adamw_step"
+    traffic = profile_traffic(step_kernel, args.workload)
 
     # ---- end to end through the public API: host gradients in, norm record out.  Every
     # step's micro-batch gradients start in pinned host memory and are copied to the device
@@ -478,6 +526,8 @@ def main():
                 "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
                 "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
                 "launch": "one CUDA graph per step (StepGraph)" if sgraph is not None else "eager calls",
+                "layout": ("tensor lists: one allocation per tensor shard, a 16384-element run table"
+                           if lists is not None else "arenas: one padded buffer per quantity"),
                 "l2": "no flush: each step streams %.1f GB, far above the 129 MB L2" % (path_bytes / 1e9),
             },
             "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
@@ -487,9 +537,9 @@ def main():
                 ("accumulate+grad_norm" if args.unfused else "accumulate_norm"): {
                     "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
                     "launches_per_step": 3 if args.unfused else 2},
-                "adamw_step": {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
+                step_kernel: {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
             }) if sgraph is None else None,
-            "roofline": ({"bound": "hbm", "kernel": "adamw_step_kernel", "achieved": step_gbs, "peak": peak,
+            "roofline": ({"bound": "hbm", "kernel": step_kernel + "_kernel", "achieved": step_gbs, "peak": peak,
                          "unit": "GB/s", "frac": step_gbs / peak, "traffic": traffic,
                          "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
                          "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P}) if sgraph is None else None,

@@ -367,6 +367,104 @@ int zero1_shard_gather(const zero1_plan* plan, const void* d_table, const void* 
 int zero1_shard_scatter(const zero1_plan* plan, const void* d_table, const void* arena, void* full,
                         int32_t elem_bytes, void* stream);
 
+/* ---- tensor lists: one buffer per tensor shard ---------------------------- */
+
+/* The same step over shards that live in separate buffers, one per tensor,
+ * as a framework holds them when each parameter keeps its own optimizer state
+ * ("ZeRO-1 风格的 Distributed Optimizer", section 6.3: every parameter is cut
+ * on its own, and each rank keeps the fp32 state of its slice of every
+ * parameter).  No arena and no copy into one: tensor i's buffers hold exactly
+ * shard_numel_i elements (zero1_plan_tensor), with no padding.
+ *
+ * A "pointer list" is a DEVICE array of n_tensors pointers (8 bytes each,
+ * model order), entry i pointing at tensor i's buffer of one quantity;
+ * entries of tensors whose shard is empty are never read and may be NULL.
+ * Build lists with zero1_list_ptrs_upload, which checks every entry.  The
+ * kernels walk a chunk table (zero1_list_table_upload) that cuts each shard
+ * into runs of at most 16384 elements; one thread block owns one run and
+ * stages the run's descriptor and buffer addresses in shared memory, so one
+ * launch serves any number and mix of tensor sizes.  A run moves 16-byte
+ * vectors when all its buffers start on 16-byte boundaries and falls back to
+ * element-wise accesses otherwise (same results, lower bandwidth).
+ *
+ * Results: the gradient, master, m, v and bf16 copy are bit-identical to the
+ * arena calls' on the same values (same per-element operations in the same
+ * order); the norm record is deterministic and within ~1e-13 relative of the
+ * exact sum of squares, but its partial sums follow the runs rather than
+ * arena tiles, so its last bits may differ from zero1_grad_norm's.  Error
+ * behaviour is as for the arena calls. */
+
+/* Device bytes of the plan's run table (16 per run: element offset in the
+ * tensor's buffer, tensor index, length, group); 0 for an empty shard. */
+size_t zero1_list_table_bytes(const zero1_plan* plan);
+
+/* Copy the run table into caller-owned device memory d_table (16-byte
+ * aligned, at least zero1_list_table_bytes bytes).  Asynchronous on `stream`;
+ * the plan may be destroyed once the call returns.  Valid only for this plan.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_table_upload(const zero1_plan* plan, void* d_table, size_t table_bytes, void* stream);
+
+/* Device workspace of the tensor-list norm passes (8 bytes per run). */
+size_t zero1_list_workspace_bytes(const zero1_plan* plan);
+
+/* Check n_lists pointer lists and copy them into device memory d_lists.
+ *   host_ptrs   HOST array of n_lists * n_tensors device addresses, list k
+ *               at [k*n_tensors, (k+1)*n_tensors); each entry of a tensor
+ *               with a non-empty shard must be non-NULL and a multiple of
+ *               elem_bytes (its natural alignment).  The array may be freed
+ *               once the call returns (the library stages it first).
+ *   n_lists     1 .. ZERO1_MAX_MICRO (several micro-batch lists at once)
+ *   elem_bytes  4 (fp32 buffers) or 2 (bf16 buffers)
+ *   d_lists     device destination, 16-byte aligned, at least
+ *               n_lists * n_tensors * 8 bytes (lists_bytes)
+ * Asynchronous on `stream` (not capturable into a CUDA graph: the source is
+ * pageable memory).  The library cannot check the buffers' lengths: buffer i
+ * must hold shard_numel_i elements.
+ * Errors: ZERO1_EINVAL (a NULL entry, a bad count or size), ZERO1_EALIGN (a
+ * misaligned entry or d_lists), ZERO1_ENOMEM, ZERO1_ECUDA. */
+int zero1_list_ptrs_upload(const zero1_plan* plan, const void* const* host_ptrs, int32_t n_lists,
+                           int32_t elem_bytes, void* d_lists, size_t lists_bytes, void* stream);
+
+/* zero1_accumulate over tensor lists.
+ *   d_table   this plan's uploaded run table
+ *   d_grad    pointer list of the fp32 gradient shards, read and written
+ *   d_micro   n_micro pointer lists of bf16 micro-batch gradient shards,
+ *             back to back in one device array (n_micro * n_tensors entries)
+ *   n_micro, overwrite_first   as for zero1_accumulate
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_accumulate(const zero1_plan* plan, const void* d_table, float* const* d_grad,
+                          const uint16_t* const* d_micro, int32_t n_micro, int32_t overwrite_first, void* stream);
+
+/* zero1_accumulate_norm over tensor lists: accumulate, optionally divide by
+ * grad_divisor, and the norm record, in one pass.  workspace holds
+ * zero1_list_workspace_bytes(plan) bytes; other arguments as above and as for
+ * zero1_accumulate_norm.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_accumulate_norm(const zero1_plan* plan, const void* d_table, float* const* d_grad,
+                               const uint16_t* const* d_micro, int32_t n_micro, int32_t overwrite_first,
+                               double grad_divisor, double extra_sumsq, void* workspace, size_t workspace_bytes,
+                               zero1_norm_out* d_out, void* stream);
+
+/* zero1_grad_norm over a gradient pointer list (read only).
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_grad_norm(const zero1_plan* plan, const void* d_table, const float* const* d_grad,
+                         double extra_sumsq, void* workspace, size_t workspace_bytes, zero1_norm_out* d_out,
+                         void* stream);
+
+/* zero1_step over tensor lists: clip + AdamW + bf16 copy, each tensor with
+ * its group's step size and decay factor.
+ *   d_master, d_exp_avg, d_exp_avg_sq   pointer lists of fp32 shards, read
+ *                                       and written
+ *   d_grad                              pointer list of fp32 shards, read
+ *   d_weight_bf16                       pointer list of bf16 shards, written;
+ *                                       NULL to skip the copy
+ *   hp, step_t, d_norm                  as for zero1_step
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_step(const zero1_plan* plan, const void* d_table, float* const* d_master,
+                    float* const* d_exp_avg, float* const* d_exp_avg_sq, const float* const* d_grad,
+                    uint16_t* const* d_weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                    const zero1_norm_out* d_norm, void* stream);
+
 /* ---- diagnostics --------------------------------------------------------- */
 
 /* Static description of a status code. */

@@ -266,3 +266,69 @@ def test_fused_pass_rejects_a_bad_divisor_before_any_launch(z):
     for d in (0.0, -2.0, float("nan"), float("inf")):
         rc = lib.zero1_accumulate_norm(plan.handle, fake, arr, 1, 1, d, 0.0, fake, 64, fake, None)
         assert rc == z.ZERO1_EINVAL, d
+
+
+@pytest.mark.parametrize("name", ["toy", "llama8b", "ragged"])
+def test_list_table_has_one_16_byte_entry_per_run(z, name):
+    w = get_workload(name)
+    plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank)
+    _, count, _ = oracle.plan(w.params.numels, w.dp_size, w.dp_rank)
+    runs = int(np.sum((count + 16383) // 16384))
+    lib = z.load_library()
+    assert lib.zero1_list_table_bytes(plan.handle) == 16 * runs
+    assert lib.zero1_list_workspace_bytes(plan.handle) == 8 * runs == plan.list_workspace_bytes
+
+
+def test_list_calls_reject_bad_arguments_before_any_launch(z):
+    lib = z.load_library()
+    plan = z.Plan([100, 8, 0], [0, 1, 0], 1, 0)
+    h = plan.handle
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    # pointer-list upload: entries of non-empty shards must be non-NULL and naturally aligned
+    ok = (ctypes.c_void_p * 3)(0x20000, 0x30000, None)        # the empty tensor's entry may be NULL
+    null = (ctypes.c_void_p * 3)(0x20000, None, None)
+    odd4 = (ctypes.c_void_p * 3)(0x20000, 0x30002, None)
+    assert lib.zero1_list_ptrs_upload(h, null, 1, 4, fake, 64, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_ptrs_upload(h, odd4, 1, 4, fake, 64, None) == z.ZERO1_EALIGN
+    assert lib.zero1_list_ptrs_upload(h, odd4, 1, 3, fake, 64, None) == z.ZERO1_EINVAL    # elem_bytes
+    assert lib.zero1_list_ptrs_upload(h, ok, 0, 4, fake, 64, None) == z.ZERO1_EINVAL       # n_lists
+    assert lib.zero1_list_ptrs_upload(h, ok, 17, 4, fake, 64, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_ptrs_upload(h, ok, 1, 4, fake, 16, None) == z.ZERO1_EINVAL       # too small
+    assert lib.zero1_list_ptrs_upload(h, ok, 1, 4, odd, 64, None) == z.ZERO1_EALIGN
+    assert lib.zero1_list_ptrs_upload(h, None, 1, 4, fake, 64, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_table_upload(h, fake, 8, None) == z.ZERO1_EINVAL                 # too small
+    assert lib.zero1_list_table_upload(h, odd, 64, None) == z.ZERO1_EALIGN
+    # compute calls
+    assert lib.zero1_list_accumulate(h, fake, fake, fake, 0, 1, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_accumulate(h, fake, fake, fake, 17, 1, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_accumulate(h, None, fake, fake, 1, 1, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_accumulate(h, fake, odd, fake, 1, 1, None) == z.ZERO1_EALIGN
+    assert lib.zero1_list_accumulate(h, fake, fake, None, 1, 1, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_workspace_bytes(h) == 16
+    for d in (0.0, -1.0, float("nan"), float("inf")):
+        assert lib.zero1_list_accumulate_norm(h, fake, fake, fake, 1, 1, d, 0.0, fake, 64, fake, None) == \
+            z.ZERO1_EINVAL
+    assert lib.zero1_list_accumulate_norm(h, fake, fake, fake, 1, 1, 1.0, 0.0, fake, 8, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_grad_norm(h, fake, fake, 0.0, fake, 8, fake, None) == z.ZERO1_EINVAL  # workspace
+    assert lib.zero1_list_grad_norm(h, fake, fake, -1.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_grad_norm(h, fake, fake, 0.0, odd, 64, fake, None) == z.ZERO1_EALIGN
+    assert lib.zero1_list_grad_norm(h, fake, fake, 0.0, fake, 64, None, None) == z.ZERO1_EINVAL
+    hp = z.binding._Hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    five = [fake] * 5
+    assert lib.zero1_list_step(h, fake, *five, ctypes.byref(hp), 0, None, None) == z.ZERO1_EINVAL  # t < 1
+    assert lib.zero1_list_step(h, fake, fake, fake, fake, odd, fake, ctypes.byref(hp), 1, None, None) == \
+        z.ZERO1_EALIGN
+    assert lib.zero1_list_step(h, fake, fake, fake, None, fake, fake, ctypes.byref(hp), 1, None, None) == \
+        z.ZERO1_EINVAL
+    bad = z.binding._Hparams(3e-4, 0.9, 1.0, 1e-8, 0.1, 1.0)
+    assert lib.zero1_list_step(h, fake, *five, ctypes.byref(bad), 1, None, None) == z.ZERO1_EINVAL
+    # an all-empty plan: nothing to do, NULL lists accepted
+    empty = z.Plan([0, 0], [0, 1], 1, 0)
+    assert lib.zero1_list_table_bytes(empty.handle) == 0
+    assert lib.zero1_list_table_upload(empty.handle, None, 0, None) == z.ZERO1_OK
+    assert lib.zero1_list_accumulate(empty.handle, None, None, None, 1, 1, None) == z.ZERO1_OK
+    assert lib.zero1_list_step(empty.handle, None, None, None, None, None, None, ctypes.byref(hp), 1, None,
+                               None) == z.ZERO1_OK
+    none = (ctypes.c_void_p * 2)(None, None)
+    assert lib.zero1_list_ptrs_upload(empty.handle, none, 1, 4, None, 0, None) == z.ZERO1_EINVAL  # no destination

@@ -1,0 +1,272 @@
+"""The tensor-list calls (one buffer per tensor shard, a run table walked by the
+kernels) against the CPU oracle and against the arena calls, on a GB300.
+
+The oracle sees the shards concatenated in model order with no padding, which
+is exactly what the list kernels walk; gradients and the moments must match it
+bit for bit, the norm within 1e-12 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_sharded_mixed_local_gb300 as z
+
+from parity import u16
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip_grad=1.0)
+# sizes around every boundary the kernels have: 8-element vectors, 2048-element block
+# passes, 16384-element runs; an empty tensor and one with fewer elements than ranks
+NUMELS = [1000, 7, 4096, 33, 16385, 40000, 1, 0, 65539, 2, 49152, 16384 * 3 + 8]
+NO_DECAY = [0, 1, 0, 1, 0, 0, 1, 0, 0, 1, 0, 0]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    z.load_library()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _buffers(counts, dtype, misaligned, dev):
+    """One buffer per shard; with `misaligned`, each starts one element past a 16-byte
+    boundary (a view into a larger allocation), which forces the element-wise path."""
+    out = []
+    for c in counts:
+        c = int(c)
+        if misaligned and c:
+            out.append(torch.zeros(c + 8, dtype=dtype, device=dev)[1:1 + c])
+        else:
+            out.append(torch.zeros(c, dtype=dtype, device=dev))
+    return out
+
+
+class ListProblem:
+    def __init__(self, numels, no_decay, dp=3, rank=1, misaligned=False, hp=None, seed=0, sigma=1e-3):
+        self.dev = torch.device("cuda")
+        self.hp = dict(hp or HP)
+        self.no_decay = np.asarray(no_decay, np.uint8)
+        self.plan = z.Plan(numels, self.no_decay, dp, rank)
+        self.counts = self.plan.layout().counts
+        self.gen = torch.Generator(device=self.dev).manual_seed(seed)
+        self.sigma = sigma
+        mk = lambda dt: _buffers(self.counts, dt, misaligned, self.dev)  # noqa: E731
+        self.master, self.m, self.v, self.grad = mk(torch.float32), mk(torch.float32), mk(torch.float32), mk(
+            torch.float32)
+        self.w = mk(torch.bfloat16)
+        for t, c, nd in zip(self.master, self.counts, self.no_decay):
+            if c:
+                t.copy_(torch.ones_like(t) if nd else torch.randn(int(c), generator=self.gen, device=self.dev) * 0.02)
+        self.opt = z.ShardListAdamW(numels, self.no_decay, dp, rank, hparams=self.hp, master=self.master,
+                                    exp_avg=self.m, exp_avg_sq=self.v, grad=self.grad, weight_bf16=self.w)
+        self.misaligned = misaligned
+
+    def micro(self):
+        return [(torch.randn(int(c), generator=self.gen, device=self.dev) * self.sigma).to(torch.bfloat16)
+                if c else torch.zeros(0, dtype=torch.bfloat16, device=self.dev) for c in self.counts]
+
+    def micro_like(self, lst):
+        """Same values in buffers with this problem's alignment."""
+        out = _buffers(self.counts, torch.bfloat16, self.misaligned, self.dev)
+        for a, b in zip(out, lst):
+            a.copy_(b)
+        return out
+
+    def flat(self, lst):
+        return torch.cat([t.reshape(-1) for t in lst]).cpu()
+
+
+def _oracle_state(pb):
+    return (pb.flat(pb.master).numpy().copy(), np.zeros(int(pb.counts.sum()), np.float32),
+            np.zeros(int(pb.counts.sum()), np.float32))
+
+
+def _eq(a, b):
+    a = np.asarray(a)
+    return a.shape == b.shape and np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("misaligned", [False, True])
+def test_list_step_matches_the_oracle_bit_for_bit(misaligned):
+    pb = ListProblem(NUMELS, NO_DECAY, misaligned=misaligned)
+    P, M, V = _oracle_state(pb)
+    n = P.size
+    for t in range(1, 4):
+        micros = [pb.micro_like(pb.micro()) for _ in range(2)]
+        pb.opt.accumulate(micros[0])
+        pb.opt.accumulate(micros[1], last=True)
+        pb.opt.step()
+        got = pb.opt.read_norm()
+        G = np.zeros(n, np.float32)
+        for k, mb in enumerate(micros):
+            oracle.accumulate(G, u16(pb.flat(mb)), overwrite=(k == 0))
+        assert _eq(pb.flat(pb.grad).numpy(), G), "gradient differs from the oracle at step %d" % t
+        ref = oracle.sumsq(G)
+        assert got["status"] == 0 and abs(got["sumsq"] - ref) <= 1e-12 * ref, (t, got["sumsq"], ref)
+        ok, _, coef = oracle.clip_coef(ref, HP["clip_grad"])
+        oracle.adamw(P, M, V, G, pb.counts, pb.no_decay, HP, t, coef)
+    for name, lst, ref in (("master", pb.master, P), ("m", pb.m, M), ("v", pb.v, V)):
+        assert _eq(pb.flat(lst).numpy(), ref), name
+    assert np.array_equal(u16(pb.flat(pb.w)), oracle.bf16_rne(P))
+
+
+def test_list_calls_equal_the_arena_calls():
+    """No clipping (so both sides use coef 1): every state element bit-identical to the
+    arena path's on the same values; the norms agree to 1e-12."""
+    hp = dict(HP, clip_grad=0.0)
+    pb = ListProblem(NUMELS, NO_DECAY, hp=hp, seed=3)
+    arena = z.LocalShardAdamW(NUMELS, NO_DECAY, 3, 1, hparams=hp)
+    for view, t in zip(arena.plan.shard_views(arena.master), pb.master):
+        view.copy_(t)
+    for step in range(2):
+        micros = [pb.micro() for _ in range(3)]
+        arenas = []
+        for mb in micros:
+            a = arena.plan.new_arena(torch.bfloat16)
+            for view, t in zip(arena.plan.shard_views(a), mb):
+                view.copy_(t)
+            arenas.append(a)
+        pb.opt.accumulate(micros[:2])
+        pb.opt.accumulate(micros[2], last=True)
+        arena.accumulate(arenas[:2])
+        arena.accumulate(arenas[2], last=True)
+        pb.opt.step()
+        arena.step()
+        a_norm, l_norm = arena.read_norm(), pb.opt.read_norm()
+        assert abs(a_norm["sumsq"] - l_norm["sumsq"]) <= 1e-12 * a_norm["sumsq"]
+    for name in ("grad", "master", "exp_avg", "exp_avg_sq", "weight_bf16"):
+        views = arena.plan.shard_views(getattr(arena, name))
+        for i, (a, b) in enumerate(zip(views, getattr(pb.opt, name))):
+            assert torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                               b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)), (name, i)
+
+
+def test_divisor_and_separate_norm_call():
+    """Fused pass with a world-size divisor equals the oracle's sum then divide; the
+    standalone norm call reproduces the fused record bit for bit, twice."""
+    pb = ListProblem(NUMELS, NO_DECAY, dp=2, rank=0, seed=5, sigma=1e-2)
+    micros = [pb.micro() for _ in range(2)]
+    pb.opt.accumulate(micros[0])
+    pb.opt.accumulate(micros[1], last=True, divisor=8.0)
+    fused = pb.opt.read_norm()
+    G = np.zeros(int(pb.counts.sum()), np.float32)
+    for k, mb in enumerate(micros):
+        oracle.accumulate(G, u16(pb.flat(mb)), overwrite=(k == 0))
+    oracle.divide(G, 8.0)
+    assert _eq(pb.flat(pb.grad).numpy(), G)
+    ref = oracle.sumsq(G)
+    assert abs(fused["sumsq"] - ref) <= 1e-12 * ref
+    nout = z.new_norm_out()
+    for _ in range(2):
+        z.list_grad_norm(pb.opt.plan, pb.opt.table, pb.opt._lists["grad"], pb.opt.workspace, nout)
+        again = z.read_norm(nout)
+        assert again["sumsq"] == fused["sumsq"] and again["n_partials"] == fused["n_partials"]
+    runs = int(np.sum((pb.counts + 16383) // 16384))
+    assert fused["n_partials"] == runs
+
+
+def test_nonfinite_gradient_skips_the_list_step():
+    pb = ListProblem(NUMELS, NO_DECAY, seed=7)
+    mb = pb.micro()
+    mb[4][100] = float("inf")
+    before = [t.clone() for t in pb.master]
+    pb.opt.accumulate(mb, last=True)
+    pb.opt.step()
+    got = pb.opt.read_norm()
+    assert got["status"] == z.ZERO1_ENONFINITE
+    for a, b in zip(before, pb.master):
+        assert torch.equal(a, b)
+    assert all(int(t.abs().sum()) == 0 for t in pb.m if t.numel())
+
+
+def test_list_step_without_bf16_copy():
+    pb = ListProblem(NUMELS, NO_DECAY, seed=9)
+    mb = pb.micro()
+    pb.opt.accumulate(mb, last=True)
+    L = pb.opt._lists
+    twin = [t.clone() for t in pb.master]
+    z.list_step(pb.opt.plan, pb.opt.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], None, z.Hparams(**HP), 1,
+                pb.opt.norm_out)
+    # the same step through the oracle on the cloned master
+    G = pb.flat(pb.grad).numpy()
+    P = torch.cat([t.reshape(-1) for t in twin]).cpu().numpy().copy()
+    M = np.zeros_like(P)
+    V = np.zeros_like(P)
+    ref = oracle.sumsq(G)
+    _, _, coef = oracle.clip_coef(ref, HP["clip_grad"])
+    oracle.adamw(P, M, V, G, pb.counts, pb.no_decay, HP, 1, coef)
+    assert _eq(pb.flat(pb.master).numpy(), P)
+    assert all(int(t.view(torch.int16).abs().sum()) == 0 for t in pb.w if t.numel())  # no copy written
+
+
+def test_parameter_groups_through_the_run_table():
+    """Four groups with their own lr and weight-decay multipliers, interleaved in model
+    order: each run steps with its tensor's group scalars."""
+    groups = [0, 1, 2, 3, 0, 2, 1, 3, 2, 1, 0, 3]
+    lr_scale = [1.0, 1.0, 0.25, 2.0, 1, 1, 1, 1]
+    wd_scale = [1.0, 0.0, 1.0, 0.5, 1, 1, 1, 1]
+    dev = torch.device("cuda")
+    plan = z.Plan(NUMELS, dp_size=3, dp_rank=1, groups=groups, lr_scale=lr_scale, wd_scale=wd_scale)
+    counts = plan.layout().counts
+    g = torch.Generator(device=dev).manual_seed(13)
+    master = [torch.randn(int(c), generator=g, device=dev) * 0.02 for c in counts]
+    grads = [torch.randn(int(c), generator=g, device=dev) * 1e-2 for c in counts]
+    m, v, w = plan.new_shards(), plan.new_shards(), plan.new_shards(torch.bfloat16)
+    P = torch.cat(master).cpu().numpy().copy()
+    G = torch.cat(grads).cpu().numpy().copy()
+    M, V = np.zeros_like(P), np.zeros_like(P)
+    lists = [z.PointerLists(plan, x, torch.float32) for x in (master, m, v, grads)]
+    wl = z.PointerLists(plan, w, torch.bfloat16)
+    table, ws, nout = plan.list_table(), plan.new_list_workspace(), z.new_norm_out()
+    for t in (1, 2):
+        z.list_grad_norm(plan, table, lists[3], ws, nout)
+        z.list_step(plan, table, *lists, wl, z.Hparams(**HP), t, nout)
+        ref = oracle.sumsq(G)
+        _, _, coef = oracle.clip_coef(ref, HP["clip_grad"])
+        oracle.adamw_scaled(P, M, V, G, counts, np.asarray(lr_scale)[groups], np.asarray(wd_scale)[groups], HP, t,
+                            coef)
+    assert _eq(torch.cat(master).cpu().numpy(), P) and _eq(torch.cat(m).cpu().numpy(), M)
+    assert np.array_equal(u16(torch.cat(w)), oracle.bf16_rne(P))
+
+
+def test_many_small_tensors_log_uniform():
+    """3000 tensors with sizes log-uniform in [1, 2^16] (the ragged mix, scaled down),
+    10% without decay, dp 2 rank 1, clipping active."""
+    rng = np.random.default_rng(11)
+    numels = np.floor(np.exp(rng.uniform(0, 16 * np.log(2), 3000))).astype(np.int64)
+    no_decay = (rng.random(3000) < 0.1).astype(np.uint8)
+    pb = ListProblem(numels, no_decay, dp=2, rank=1, seed=11, sigma=1e-2)
+    P, M, V = _oracle_state(pb)
+    for t in (1, 2):
+        mb = pb.micro()
+        pb.opt.accumulate(mb, last=True)
+        pb.opt.step()
+        got = pb.opt.read_norm()
+        G = np.zeros(P.size, np.float32)
+        oracle.accumulate(G, u16(pb.flat(mb)), overwrite=True)
+        ref = oracle.sumsq(G)
+        assert abs(got["sumsq"] - ref) <= 1e-12 * ref
+        ok, norm, coef = oracle.clip_coef(ref, HP["clip_grad"])
+        assert coef < 1.0  # clipping is active
+        oracle.adamw(P, M, V, G, pb.counts, pb.no_decay, HP, t, coef)
+    assert _eq(pb.flat(pb.master).numpy(), P) and _eq(pb.flat(pb.v).numpy(), V)
+    assert np.array_equal(u16(pb.flat(pb.w)), oracle.bf16_rne(P))
+
+
+def test_pointer_lists_are_checked():
+    plan = z.Plan([64, 8], [0, 1], 1, 0)
+    good = [torch.zeros(64, device="cuda"), torch.zeros(8, device="cuda")]
+    with pytest.raises(ValueError):
+        z.PointerLists(plan, [good[0], torch.zeros(9, device="cuda")], torch.float32)   # wrong length
+    with pytest.raises(TypeError):
+        z.PointerLists(plan, [good[0], good[1].to(torch.bfloat16)], torch.float32)     # wrong dtype
+    with pytest.raises(ValueError):
+        z.PointerLists(plan, [good[0]], torch.float32)                                   # wrong count
+    with pytest.raises(ValueError):
+        z.PointerLists(plan, [good[0], torch.zeros(16, device="cuda")[::2]], torch.float32)  # not contiguous
+    pl = z.PointerLists(plan, good, torch.float32)
+    assert pl.dev.cpu().tolist()[:2] == [good[0].data_ptr(), good[1].data_ptr()]

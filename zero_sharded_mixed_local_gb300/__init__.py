@@ -11,13 +11,15 @@ from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_
                       ZERO1_EINVAL, ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, LocalShardAdamW, Plan,
                       ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, exchange_chunk_numel, grad_norm, grad_norm_static, load_library,
                       pack_reduce_scatter, shard_gather, shard_scatter, unpack_all_gather, new_norm_out,
-                      read_norm, step, step_dev, step_scalars, StepGraph)
+                      read_norm, step, step_dev, step_scalars, StepGraph, PointerLists, ShardListAdamW,
+                      list_accumulate, list_accumulate_norm, list_grad_norm, list_step)
 
 __all__ = [
     "ARENA_ALIGN", "MAX_GROUPS", "MAX_MICRO", "NORM_OUT_BYTES", "ZERO1_EALIGN", "ZERO1_ECUDA", "ZERO1_EINVAL",
     "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_ETOOBIG", "ZERO1_OK", "Hparams", "LocalShardAdamW", "Plan", "ShardLayout",
     "Zero1Error", "accumulate", "accumulate_norm", "allreduce_sumsq_", "decode_norm", "exchange_chunk_numel", "grad_norm", "grad_norm_static", "load_library",
     "pack_reduce_scatter", "shard_gather", "shard_scatter", "unpack_all_gather", "new_norm_out", "read_norm", "step", "step_dev", "step_scalars", "StepGraph",
+    "PointerLists", "ShardListAdamW", "list_accumulate", "list_accumulate_norm", "list_grad_norm", "list_step",
 ]
 
 from . import checkpoint  # noqa: E402

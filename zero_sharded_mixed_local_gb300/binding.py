@@ -97,6 +97,15 @@ def load_library(path=None):
         "zero1_layout_table_upload": (ctypes.c_int, [vp, vp, ctypes.c_size_t, vp]),
         "zero1_shard_gather": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
         "zero1_shard_scatter": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
+        "zero1_list_table_bytes": (ctypes.c_size_t, [vp]),
+        "zero1_list_table_upload": (ctypes.c_int, [vp, vp, ctypes.c_size_t, vp]),
+        "zero1_list_workspace_bytes": (ctypes.c_size_t, [vp]),
+        "zero1_list_ptrs_upload": (ctypes.c_int, [vp, ctypes.POINTER(vp), i32, i32, vp, ctypes.c_size_t, vp]),
+        "zero1_list_accumulate": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, vp]),
+        "zero1_list_accumulate_norm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, ctypes.c_double, ctypes.c_double,
+                                                      vp, ctypes.c_size_t, vp, vp]),
+        "zero1_list_grad_norm": (ctypes.c_int, [vp, vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
+        "zero1_list_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
         "zero1_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "zero1_last_cuda_error": (ctypes.c_char_p, []),
     }
@@ -294,6 +303,31 @@ class Plan:
                                                        _stream_ptr(stream, device)), "zero1_layout_table_upload")
             cache[device] = t
         return cache[device]
+
+    @property
+    def list_workspace_bytes(self):
+        return self._lib.zero1_list_workspace_bytes(self._h)
+
+    def list_table(self, device="cuda", stream=None):
+        """Device copy of this plan's tensor-list run table (made once per device)."""
+        device = torch.device(device)
+        if device.index is None:
+            device = torch.device("cuda", torch.cuda.current_device())
+        cache = self.__dict__.setdefault("_list_tables", {})
+        if device not in cache:
+            nbytes = self._lib.zero1_list_table_bytes(self._h)
+            t = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+            _check(self._lib.zero1_list_table_upload(self._h, ctypes.c_void_p(t.data_ptr()), t.numel(),
+                                                     _stream_ptr(stream, device)), "zero1_list_table_upload")
+            cache[device] = t
+        return cache[device]
+
+    def new_list_workspace(self, device="cuda"):
+        return torch.empty(max(self.list_workspace_bytes, 16), dtype=torch.uint8, device=device)
+
+    def new_shards(self, dtype=torch.float32, device="cuda"):
+        """One zero-filled buffer per tensor shard (model order), for the tensor-list calls."""
+        return [torch.zeros(int(c), dtype=dtype, device=device) for c in self.layout().counts]
 
     # -- buffers (the caller owns them; these are conveniences) --
     def new_arena(self, dtype=torch.float32, device="cuda"):
@@ -645,3 +679,193 @@ class StepGraph:
         self.graphs[b].replay()
         self.done[b].record()
         o.t = t
+
+
+# ---- tensor lists: one buffer per tensor shard ----------------------------------------------
+
+class PointerLists:
+    """Device pointer lists for the tensor-list calls: ``n_lists`` lists of the plan's
+    per-tensor shard buffers of one dtype (model order), checked and uploaded by
+    zero1_list_ptrs_upload.  With ``keep`` (the default) it holds references to the
+    tensors so their memory stays valid while the lists exist.  ``lists`` is one list
+    of tensors or a list of them."""
+
+    def __init__(self, plan, lists, dtype, device=None, stream=None, keep=True):
+        lib = load_library()
+        if len(lists) and (isinstance(lists[0], torch.Tensor) or lists[0] is None):
+            lists = [lists]
+        lists = [list(x) for x in lists]
+        n = plan.num_tensors
+        if not 1 <= len(lists) <= MAX_MICRO:
+            raise ValueError("1..%d pointer lists per upload" % MAX_MICRO)
+        counts = plan.layout().counts
+        ptrs = []
+        for k, lst in enumerate(lists):
+            if len(lst) != n:
+                raise ValueError("list %d has %d tensors, the plan has %d" % (k, len(lst), n))
+            for i, t in enumerate(lst):
+                if int(counts[i]) == 0 and t is None:
+                    ptrs.append(None)
+                    continue
+                if not isinstance(t, torch.Tensor):
+                    raise TypeError("entry %d of list %d must be a torch.Tensor" % (i, k))
+                if t.device.type != "cuda":
+                    raise ValueError("entry %d of list %d must be on a CUDA device (got %s)" % (i, k, t.device))
+                if device is None:
+                    device = t.device
+                elif t.device != torch.device(device):
+                    raise ValueError("entry %d of list %d is on %s, expected %s" % (i, k, t.device, device))
+                if t.dtype != dtype:
+                    raise TypeError("entry %d of list %d must be %s (got %s)" % (i, k, dtype, t.dtype))
+                if not t.is_contiguous() or t.numel() != int(counts[i]):
+                    raise ValueError("entry %d of list %d must be contiguous with %d elements (got %d)"
+                                     % (i, k, int(counts[i]), t.numel()))
+                ptrs.append(t.data_ptr() if t.numel() else None)
+        if device is None:
+            device = torch.device("cuda", torch.cuda.current_device())
+        self.device = torch.device(device)
+        self.n_lists = len(lists)
+        count = self.n_lists * n
+        self.dev = torch.zeros(max(count, 2), dtype=torch.int64, device=self.device)
+        host = (ctypes.c_void_p * max(count, 1))(*ptrs)
+        _check(lib.zero1_list_ptrs_upload(plan.handle, host, self.n_lists, 2 if dtype == torch.bfloat16 else 4,
+                                          ctypes.c_void_p(self.dev.data_ptr()), self.dev.numel() * 8,
+                                          _stream_ptr(stream, self.device)), "zero1_list_ptrs_upload")
+        self.tensors = lists if keep else None
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.dev.data_ptr())
+
+
+def _list_args(plan, table, stream, device):
+    if not isinstance(table, torch.Tensor) or table.device.type != "cuda":
+        raise ValueError("table must be the plan's device run table (Plan.list_table)")
+    if table.numel() < plan._lib.zero1_list_table_bytes(plan.handle):
+        raise ValueError("table is smaller than this plan's run table")
+    return ctypes.c_void_p(table.data_ptr()), _stream_ptr(stream, device)
+
+
+def list_accumulate(plan, table, grads: PointerLists, micro: PointerLists, overwrite_first=True, stream=None):
+    """zero1_list_accumulate: every fp32 gradient shard = [itself +] the sum of its bf16
+    micro-batch shards (``micro`` holds one list per micro-batch)."""
+    lib = load_library()
+    tp, sp = _list_args(plan, table, stream, grads.device)
+    _check(lib.zero1_list_accumulate(plan.handle, tp, grads.ptr, micro.ptr, micro.n_lists,
+                                     1 if overwrite_first else 0, sp), "zero1_list_accumulate")
+
+
+def list_accumulate_norm(plan, table, grads: PointerLists, micro: PointerLists, workspace, norm_out,
+                         overwrite_first=True, extra_sumsq=0.0, divisor=1.0, stream=None):
+    """zero1_list_accumulate_norm: accumulate, divide by ``divisor`` and take the norm record."""
+    lib = load_library()
+    tp, sp = _list_args(plan, table, stream, grads.device)
+    ws = _ptr(workspace, torch.uint8, None, "workspace", grads.device)
+    no = _ptr(norm_out, torch.uint8, None, "norm_out", grads.device)
+    _check(lib.zero1_list_accumulate_norm(plan.handle, tp, grads.ptr, micro.ptr, micro.n_lists,
+                                          1 if overwrite_first else 0, float(divisor), float(extra_sumsq), ws,
+                                          workspace.numel(), no, sp), "zero1_list_accumulate_norm")
+
+
+def list_grad_norm(plan, table, grads: PointerLists, workspace, norm_out, extra_sumsq=0.0, stream=None):
+    """zero1_list_grad_norm: the norm record of the gradient shards."""
+    lib = load_library()
+    tp, sp = _list_args(plan, table, stream, grads.device)
+    ws = _ptr(workspace, torch.uint8, None, "workspace", grads.device)
+    no = _ptr(norm_out, torch.uint8, None, "norm_out", grads.device)
+    _check(lib.zero1_list_grad_norm(plan.handle, tp, grads.ptr, float(extra_sumsq), ws, workspace.numel(), no, sp),
+           "zero1_list_grad_norm")
+
+
+def list_step(plan, table, master: PointerLists, exp_avg: PointerLists, exp_avg_sq: PointerLists,
+              grads: PointerLists, weight_bf16, hparams, step_t, norm_out=None, stream=None):
+    """zero1_list_step: clip + AdamW + bf16 copy over the tensor lists (weight_bf16 may be None)."""
+    lib = load_library()
+    dev = master.device
+    tp, sp = _list_args(plan, table, stream, dev)
+    hp = hparams if isinstance(hparams, Hparams) else Hparams(**hparams)
+    no = None if norm_out is None else _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    _check(lib.zero1_list_step(plan.handle, tp, master.ptr, exp_avg.ptr, exp_avg_sq.ptr, grads.ptr,
+                               None if weight_bf16 is None else weight_bf16.ptr, ctypes.byref(hp._c()),
+                               int(step_t), no, sp), "zero1_list_step")
+
+
+class ShardListAdamW:
+    """LocalShardAdamW over per-tensor shard buffers instead of arenas.
+
+    ``master``, ``exp_avg``, ``exp_avg_sq``, ``grad`` and ``weight_bf16`` are lists of
+    tensors, one per parameter (model order, each exactly its shard's length); pass
+    your own (for instance the fp32 state a framework already keeps per parameter) or
+    let the constructor allocate zeroed ones.  Micro-batch gradients are lists of bf16
+    shard tensors; their device pointer lists are cached by (address, length) of every
+    tensor, so a loop that reuses the same gradient buffers uploads them once."""
+
+    def __init__(self, numels, no_decay, dp_size=1, dp_rank=0, hparams=None, device="cuda", master=None,
+                 exp_avg=None, exp_avg_sq=None, grad=None, weight_bf16=None):
+        self.device = torch.device(device)
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.plan = Plan(numels, no_decay, dp_size, dp_rank)
+        self.hp = hparams if isinstance(hparams, Hparams) else Hparams(**(hparams or {}))
+        mk = self.plan.new_shards
+        self.master = master if master is not None else mk(torch.float32, self.device)
+        self.exp_avg = exp_avg if exp_avg is not None else mk(torch.float32, self.device)
+        self.exp_avg_sq = exp_avg_sq if exp_avg_sq is not None else mk(torch.float32, self.device)
+        self.grad = grad if grad is not None else mk(torch.float32, self.device)
+        self.weight_bf16 = weight_bf16 if weight_bf16 is not None else mk(torch.bfloat16, self.device)
+        f32 = torch.float32
+        self._lists = {name: PointerLists(self.plan, getattr(self, name), f32, self.device)
+                       for name in ("master", "exp_avg", "exp_avg_sq", "grad")}
+        self._lists["weight_bf16"] = PointerLists(self.plan, self.weight_bf16, torch.bfloat16, self.device)
+        self.table = self.plan.list_table(self.device)
+        self.workspace = self.plan.new_list_workspace(self.device)
+        self.norm_out = new_norm_out(self.device)
+        self._micro_cache = {}
+        self.t = 0
+        self._micro_seen = 0
+        self._norm_ready = False
+
+    def _micro_lists(self, micro):
+        if len(micro) and isinstance(micro[0], torch.Tensor):
+            micro = [micro]
+        # A cached list stays valid for any tensors at the same addresses with the same
+        # lengths (what the upload checked); it keeps no reference to them.
+        key = tuple(tuple((t.data_ptr(), t.numel(), t.dtype, t.device, t.is_contiguous()) for t in lst)
+                    for lst in micro)
+        pl = self._micro_cache.get(key)
+        if pl is None:
+            if len(self._micro_cache) >= 8:
+                self._micro_cache.clear()
+            pl = self._micro_cache[key] = PointerLists(self.plan, micro, torch.bfloat16, self.device, keep=False)
+        return pl
+
+    def accumulate(self, micro, last=False, extra_sumsq=0.0, divisor=1.0, stream=None):
+        """Add one micro-batch (a list of bf16 shard tensors) or several (a list of such lists)."""
+        pl = self._micro_lists(micro)
+        first = self._micro_seen == 0
+        if last:
+            list_accumulate_norm(self.plan, self.table, self._lists["grad"], pl, self.workspace, self.norm_out,
+                                 overwrite_first=first, extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
+        else:
+            list_accumulate(self.plan, self.table, self._lists["grad"], pl, overwrite_first=first, stream=stream)
+        self._micro_seen += pl.n_lists
+        self._norm_ready = bool(last)
+
+    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None):
+        """Norm (unless the last accumulate took it) + optional all-reduce of sumsq + clip +
+        AdamW + bf16 copy."""
+        if not self._norm_ready:
+            list_grad_norm(self.plan, self.table, self._lists["grad"], self.workspace, self.norm_out, extra_sumsq,
+                           stream=stream)
+        self._norm_ready = False
+        if group is not None:
+            allreduce_sumsq_(self.norm_out, group)
+        self.t += 1
+        hp = self.hp if lr is None else Hparams(**{**self.hp.__dict__, "lr": lr})
+        L = self._lists
+        list_step(self.plan, self.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], L["weight_bf16"],
+                  hp, self.t, self.norm_out, stream=stream)
+        self._micro_seen = 0
+
+    def read_norm(self, stream=None):
+        return read_norm(self.norm_out, stream=stream)

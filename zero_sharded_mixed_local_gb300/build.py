@@ -17,7 +17,7 @@ BUILD = os.path.join(ROOT, "_build", "zero1")
 LIB = os.path.join(PKG, "libzero1.so")
 
 SOURCES = ["plan.cpp", "api.cu", "accumulate.cu", "grad_norm.cu", "adamw_step.cu", "grad_norm_static.cu",
-           "layout.cu"]
+           "layout.cu", "tensor_list.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-Wall",
                      "-I", INCLUDE, "-I", CSRC]

@@ -14,31 +14,19 @@
 // accumulate_norm_kernel fuses the last micro-batch's pass with the gradient
 // norm (and, when asked, with the division of the reduced gradient by the
 // world size that FSDP2 runs as its own kernel, "TorchTitan 生产级预训练方案",
-// appendix B.1: one IEEE division per element after the last addition): each block owns one 16384-element norm tile, writes the accumulated
-// gradient and adds its squares into float pairs with exactly the mapping and
+// appendix B.1: one IEEE division per element after the last addition): each
+// block owns one 16384-element norm tile, writes the accumulated gradient and
+// adds its squares into float pairs with exactly the mapping and
 // order of sumsq_tiles_kernel, so the norm record is bit-identical to
 // zero1_grad_norm's while the gradient is never read back (4 bytes per element
 // saved).
+#include "elementwise.cuh"
 #include "pair_sum.cuh"
 
 namespace zero1 {
 namespace {
 
 constexpr int kAccThreads = 256;
-
-__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
-
-__device__ __forceinline__ void widen8(const uint4& b, float (&f)[8]) {
-    f[0] = bf16_lo(b.x);
-    f[1] = bf16_hi(b.x);
-    f[2] = bf16_lo(b.y);
-    f[3] = bf16_hi(b.y);
-    f[4] = bf16_lo(b.z);
-    f[5] = bf16_hi(b.z);
-    f[6] = bf16_lo(b.w);
-    f[7] = bf16_hi(b.w);
-}
 
 __global__ void __launch_bounds__(kAccThreads)
     accumulate_kernel(const __grid_constant__ AccumulateParams P, int64_t first_vec) {

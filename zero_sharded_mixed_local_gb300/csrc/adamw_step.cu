@@ -19,34 +19,14 @@
 // index with the group boundaries (groups are contiguous in the arena), so no
 // per-tensor table is read.  The rounding-explicit intrinsics (__fmul_rn,
 // __fadd_rn, __fdiv_rn, __fsqrt_rn) are never contracted into FMAs, which
-// keeps the operation order exact.
-#include <cuda_bf16.h>
-
+// keeps the operation order exact (elementwise.cuh).
+#include "elementwise.cuh"
 #include "zero1_internal.h"
 
 namespace zero1 {
 namespace {
 
 constexpr int kStepThreads = 256;
-
-struct StepConsts {
-    float b1, b2, omb1, omb2, eps, sqrtbc2;
-};
-
-__device__ __forceinline__ void adamw_elem(float& p, float& m, float& v, float grad, float coef, float dfac,
-                                           float stepsize, const StepConsts& c) {
-    const float g = __fmul_rn(grad, coef);
-    p = __fmul_rn(p, dfac);
-    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
-    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
-    const float d = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.sqrtbc2), c.eps);
-    p = __fsub_rn(p, __fmul_rn(stepsize, __fdiv_rn(m, d)));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 // kDevScalars: the scalars come from P.dev_scalars (read by thread 0 into
 // shared memory after the loads are issued) rather than from P.sc.
@@ -80,12 +60,12 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
             s_sc = *P.dev_scalars;
             clip = s_sc.clip;
         }
-        // Clip coefficient from the device-resident norm: no host round trip.
+        // Clip coefficient from the device-resident norm: no host round trip
+        // (the rule of clip_from_norm, written out here because the call form
+        // costs the device-scalar variant four registers, 62 -> 66).
         float coef = 1.0f;
         int skip = 0;
         if (P.norm != nullptr) {
-            // The norm is re-derived from sumsq, so a caller may sum that one
-            // field across ranks in place between the norm and the step.
             const double sumsq = P.norm->sumsq;
             if (P.norm->status != ZERO1_OK || !isfinite(sumsq)) {
                 skip = 1;

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <new>
 
 #include <nvtx3/nvToolsExt.h>
 
@@ -285,3 +286,150 @@ extern "C" const char* zero1_strerror(int code) {
 }
 
 extern "C" const char* zero1_last_cuda_error(void) { return g_cuda_error; }
+
+/* ---- tensor lists --------------------------------------------------------- */
+
+extern "C" int zero1_list_table_upload(const zero1_plan* plan, void* d_table, size_t table_bytes, void* stream) {
+    if (plan == nullptr) return ZERO1_EINVAL;
+    const size_t need = plan->list_chunks.size() * sizeof(ListChunk);
+    if (need == 0) return ZERO1_OK;
+    if (d_table == nullptr || table_bytes < need) return ZERO1_EINVAL;
+    if (!aligned16(d_table)) return ZERO1_EALIGN;
+    const cudaError_t e = cudaMemcpyAsync(d_table, plan->list_chunks.data(), need, cudaMemcpyHostToDevice,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+extern "C" int zero1_list_ptrs_upload(const zero1_plan* plan, const void* const* host_ptrs, int32_t n_lists,
+                                      int32_t elem_bytes, void* d_lists, size_t lists_bytes, void* stream) {
+    if (plan == nullptr || n_lists < 1 || n_lists > ZERO1_MAX_MICRO) return ZERO1_EINVAL;
+    if (elem_bytes != 2 && elem_bytes != 4) return ZERO1_EINVAL;
+    const size_t count = static_cast<size_t>(n_lists) * static_cast<size_t>(plan->n_tensors);
+    if (count == 0) return ZERO1_OK;
+    if (host_ptrs == nullptr || d_lists == nullptr) return ZERO1_EINVAL;
+    if (lists_bytes < count * sizeof(void*)) return ZERO1_EINVAL;
+    if (!aligned16(d_lists)) return ZERO1_EALIGN;
+    for (int32_t k = 0; k < n_lists; ++k) {
+        for (int32_t i = 0; i < plan->n_tensors; ++i) {
+            const void* p = host_ptrs[static_cast<size_t>(k) * plan->n_tensors + i];
+            if (plan->shard_numel[i] == 0) continue;  // never dereferenced
+            if (p == nullptr) return ZERO1_EINVAL;
+            if (reinterpret_cast<uintptr_t>(p) % static_cast<uintptr_t>(elem_bytes)) return ZERO1_EALIGN;
+        }
+    }
+    // Copied from library-owned pageable memory: the call returns once the
+    // bytes are staged, whatever kind of memory the caller's array is.
+    std::vector<const void*> staged;
+    try {
+        staged.assign(host_ptrs, host_ptrs + count);
+    } catch (const std::bad_alloc&) {
+        return ZERO1_ENOMEM;
+    }
+    const cudaError_t e = cudaMemcpyAsync(d_lists, staged.data(), count * sizeof(void*), cudaMemcpyHostToDevice,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+namespace {
+
+// Checks shared by the tensor-list gradient passes.
+int list_grad_checked(const zero1_plan* plan, const void* d_table, float* const* d_grad,
+                      const uint16_t* const* d_micro, int32_t n_micro, int32_t overwrite_first, double grad_divisor,
+                      zero1::ListGradMode mode, double extra_sumsq, void* workspace, size_t workspace_bytes,
+                      zero1_norm_out* d_out, void* stream) {
+    if (plan == nullptr) return ZERO1_EINVAL;
+    const bool reads_micro = mode != zero1::ListGradMode::kNorm;
+    const bool norm = mode != zero1::ListGradMode::kAccumulate;
+    if (reads_micro && (n_micro < 1 || n_micro > ZERO1_MAX_MICRO)) return ZERO1_EINVAL;
+    if (norm) {
+        if (d_out == nullptr) return ZERO1_EINVAL;
+        if (!aligned16(d_out)) return ZERO1_EALIGN;
+        if (std::isnan(extra_sumsq) || extra_sumsq < 0.0) return ZERO1_EINVAL;
+    }
+    if (!std::isfinite(grad_divisor) || !(grad_divisor > 0.0)) return ZERO1_EINVAL;
+    const int64_t n_chunks = static_cast<int64_t>(plan->list_chunks.size());
+    if (n_chunks > 0) {
+        if (d_table == nullptr || d_grad == nullptr || (reads_micro && d_micro == nullptr)) return ZERO1_EINVAL;
+        if (!aligned16(d_table) || !aligned16(d_grad) || (reads_micro && !aligned16(d_micro))) return ZERO1_EALIGN;
+        if (norm) {
+            if (workspace == nullptr) return ZERO1_EINVAL;
+            if (workspace_bytes < static_cast<size_t>(n_chunks) * sizeof(double)) return ZERO1_EINVAL;
+            if (!aligned16(workspace)) return ZERO1_EALIGN;
+        }
+    } else if (!norm) {
+        return ZERO1_OK;  // nothing to do
+    }
+    zero1::ListParams p{};
+    p.table = static_cast<const ListChunk*>(d_table);
+    p.grad = d_grad;
+    p.micro = d_micro;
+    p.n_tensors = plan->n_tensors;
+    p.n_micro = reads_micro ? n_micro : 0;
+    p.overwrite_first = overwrite_first ? 1 : 0;
+    p.divisor = static_cast<float>(grad_divisor);
+    p.divide = grad_divisor != 1.0 ? 1 : 0;
+    const cudaError_t e = zero1::launch_list_grad(p, mode, n_chunks, static_cast<double*>(workspace), extra_sumsq,
+                                                  d_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int zero1_list_accumulate(const zero1_plan* plan, const void* d_table, float* const* d_grad,
+                                     const uint16_t* const* d_micro, int32_t n_micro, int32_t overwrite_first,
+                                     void* stream) {
+    NvtxRange range("zero1_list_accumulate");
+    return list_grad_checked(plan, d_table, d_grad, d_micro, n_micro, overwrite_first, 1.0,
+                             zero1::ListGradMode::kAccumulate, 0.0, nullptr, 0, nullptr, stream);
+}
+
+extern "C" int zero1_list_accumulate_norm(const zero1_plan* plan, const void* d_table, float* const* d_grad,
+                                          const uint16_t* const* d_micro, int32_t n_micro, int32_t overwrite_first,
+                                          double grad_divisor, double extra_sumsq, void* workspace,
+                                          size_t workspace_bytes, zero1_norm_out* d_out, void* stream) {
+    NvtxRange range("zero1_list_accumulate_norm");
+    return list_grad_checked(plan, d_table, d_grad, d_micro, n_micro, overwrite_first, grad_divisor,
+                             zero1::ListGradMode::kAccumulateNorm, extra_sumsq, workspace, workspace_bytes, d_out,
+                             stream);
+}
+
+extern "C" int zero1_list_grad_norm(const zero1_plan* plan, const void* d_table, const float* const* d_grad,
+                                    double extra_sumsq, void* workspace, size_t workspace_bytes,
+                                    zero1_norm_out* d_out, void* stream) {
+    NvtxRange range("zero1_list_grad_norm");
+    // The norm pass only reads through the gradient list.
+    return list_grad_checked(plan, d_table, const_cast<float* const*>(d_grad), nullptr, 0, 0, 1.0,
+                             zero1::ListGradMode::kNorm, extra_sumsq, workspace, workspace_bytes, d_out, stream);
+}
+
+extern "C" int zero1_list_step(const zero1_plan* plan, const void* d_table, float* const* d_master,
+                               float* const* d_exp_avg, float* const* d_exp_avg_sq, const float* const* d_grad,
+                               uint16_t* const* d_weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                               const zero1_norm_out* d_norm, void* stream) {
+    NvtxRange range("zero1_list_step");
+    zero1_step_scalars sc{};
+    const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
+    if (rc != ZERO1_OK) return rc;
+    const int64_t n_chunks = static_cast<int64_t>(plan->list_chunks.size());
+    if (n_chunks == 0) return ZERO1_OK;  // nothing to do; empty lists may be NULL
+    if (d_table == nullptr || d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr ||
+        d_grad == nullptr)
+        return ZERO1_EINVAL;
+    if (!aligned16(d_table) || !aligned16(d_master) || !aligned16(d_exp_avg) || !aligned16(d_exp_avg_sq) ||
+        !aligned16(d_grad))
+        return ZERO1_EALIGN;
+    if (d_weight_bf16 != nullptr && !aligned16(d_weight_bf16)) return ZERO1_EALIGN;
+    if (d_norm != nullptr && !aligned16(d_norm)) return ZERO1_EALIGN;
+    zero1::ListParams p{};
+    p.table = static_cast<const ListChunk*>(d_table);
+    p.grad = const_cast<float* const*>(d_grad);
+    p.master = d_master;
+    p.m = d_exp_avg;
+    p.v = d_exp_avg_sq;
+    p.w = d_weight_bf16;
+    p.norm = d_norm;
+    p.n_tensors = plan->n_tensors;
+    p.sc = sc;
+    const cudaError_t e = zero1::launch_list_step(p, n_chunks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}

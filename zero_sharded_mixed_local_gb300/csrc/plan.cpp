@@ -103,6 +103,13 @@ extern "C" int zero1_plan_create_grouped(const int64_t* numels, const uint8_t* g
             }
             model_offset += p->numel[i];
         }
+        // Runs of each tensor's own shard buffer, for the tensor-list calls.
+        for (int32_t i = 0; i < n_tensors; ++i) {
+            for (int64_t k = 0; k < p->shard_numel[i]; k += zero1::kNormTile) {
+                const int64_t len = std::min<int64_t>(zero1::kNormTile, p->shard_numel[i] - k);
+                p->list_chunks.push_back({k, i, static_cast<uint16_t>(len), p->group[i], 0});
+            }
+        }
     } catch (const std::bad_alloc&) {
         delete p;
         return ZERO1_ENOMEM;
@@ -164,4 +171,14 @@ extern "C" size_t zero1_workspace_bytes(const zero1_plan* plan) {
 extern "C" size_t zero1_layout_table_bytes(const zero1_plan* plan) {
     if (plan == nullptr) return 0;
     return plan->layout_chunks.size() * sizeof(LayoutChunk);
+}
+
+extern "C" size_t zero1_list_table_bytes(const zero1_plan* plan) {
+    if (plan == nullptr) return 0;
+    return plan->list_chunks.size() * sizeof(ListChunk);
+}
+
+extern "C" size_t zero1_list_workspace_bytes(const zero1_plan* plan) {
+    if (plan == nullptr) return 0;
+    return plan->list_chunks.size() * sizeof(double);
 }

@@ -17,6 +17,17 @@ struct LayoutChunk {
 };
 static_assert(sizeof(LayoutChunk) == 24, "LayoutChunk is 24 bytes");
 
+// One run of one tensor's shard, as the tensor-list kernels see it: block b
+// of a launch handles run b.
+struct ListChunk {
+    int64_t offset;   // first element inside the tensor's shard buffer (a multiple of kNormTile)
+    int32_t tensor;   // index into the pointer lists
+    uint16_t len;     // elements, 1 .. kNormTile
+    uint8_t group;    // the tensor's parameter group
+    uint8_t reserved;
+};
+static_assert(sizeof(ListChunk) == 16, "ListChunk is 16 bytes");
+
 struct zero1_plan {
     int32_t n_tensors = 0;
     int32_t dp_size = 1;
@@ -34,6 +45,7 @@ struct zero1_plan {
     double lr_scale[ZERO1_MAX_GROUPS] = {};
     double wd_scale[ZERO1_MAX_GROUPS] = {};
     std::vector<LayoutChunk> layout_chunks;  // the shard's runs, cut at kLayoutChunk elements
+    std::vector<ListChunk> list_chunks;      // the same runs per tensor, cut at kNormTile elements
 };
 
 namespace zero1 {
@@ -84,6 +96,32 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
 
 cudaError_t launch_layout_copy(const LayoutChunk* table, int64_t n_chunks, const void* src, void* dst,
                                int elem_bytes, bool to_arena, cudaStream_t stream);
+
+// Tensor-list launches: every quantity is a device array of n_tensors
+// pointers, one buffer per tensor shard.
+struct ListParams {
+    const ListChunk* table;
+    float* const* grad;
+    const uint16_t* const* micro;  // n_micro lists of n_tensors pointers, back to back
+    float* const* master;
+    float* const* m;
+    float* const* v;
+    uint16_t* const* w;            // may be null: no bf16 copy
+    const zero1_norm_out* norm;    // may be null: no clipping
+    int32_t n_tensors;
+    int32_t n_micro;
+    int32_t overwrite_first;
+    int32_t divide;                // 0: plain sum (divisor unused)
+    float divisor;
+    zero1_step_scalars sc;
+};
+
+// What list_grad passes do with the gradient runs.
+enum class ListGradMode { kAccumulate, kAccumulateNorm, kNorm };
+
+cudaError_t launch_list_grad(const ListParams& p, ListGradMode mode, int64_t n_chunks, double* partials,
+                             double extra_sumsq, zero1_norm_out* out, cudaStream_t stream);
+cudaError_t launch_list_step(const ListParams& p, int64_t n_chunks, cudaStream_t stream);
 
 // Record a CUDA error for zero1_last_cuda_error() and return ZERO1_ECUDA.
 int record_cuda_error(cudaError_t e);
