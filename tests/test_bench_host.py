@@ -1,0 +1,44 @@
+"""Host-side pieces of bench.py (no GPU): the CPU baseline legs run the oracle on
+contiguous element ranges in parallel and must give the single pass's results bit
+for bit, and the reference arm prints the contract's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from zero_sharded_mixed_local_gb300.workloads import get_workload  # noqa: E402
+
+
+def _sample(w, n, seed):
+    master, m, v, micros = bench.host_sample(w, n, seed=seed)
+    return master.copy(), m.copy(), v.copy(), micros
+
+
+def test_threaded_oracle_step_equals_the_single_pass():
+    w = get_workload("smollm1p7b")  # K = 8
+    n = 100_003 // 8 * 8 + 5   # ragged: not a multiple of the thread count or of 8
+    hp = dict(w.hp, clip_grad=1e-3)  # clipping active
+    a = _sample(w, n, 3)
+    b = _sample(w, n, 3)
+    split = n - 1234            # the last 1234 elements excluded from decay
+    for t in (1, 2):
+        bench.oracle_sample_step(a[0], a[1], a[2], a[3], split, hp, t, threads=1)
+        bench.oracle_sample_step(b[0], b[1], b[2], b[3], split, hp, t, threads=7)
+    for x, y in zip(a[:3], b[:3]):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "toy",
+                          "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    d = json.loads(out.stdout.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
