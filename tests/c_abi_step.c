@@ -7,6 +7,9 @@
  *                                        norm, then clip + AdamW + bf16 copy) on deterministic
  *                                        inputs; writes grad, master, m, v (fp32 arenas) and
  *                                        the bf16 copy (uint16) to out.bin, then the norm record
+ *   c_abi_step list <out.bin>            the same step through the tensor-list calls, one
+ *                                        cudaMalloc per tensor shard; out.bin has the same
+ *                                        format (each shard written at its arena offset)
  *
  * Inputs are a fixed function of the element index, so a test can rebuild them.
  * Test infrastructure: it checks that the C ABI is usable as declared.
@@ -46,9 +49,82 @@ static int check_cuda(cudaError_t e, const char* what) {
 static uint16_t grad_bits(int64_t j) { return (uint16_t)(0x3a00u + (uint16_t)((j * 37) % 512) - 256u + ((j & 1) ? 0x8000u : 0u)); }
 static float master_val(int64_t j) { return (float)((j * 13) % 200 - 100) * 1e-4f; }
 
+/* The step through the tensor-list calls: each quantity of each tensor is its own
+ * allocation; h_g / h_p hold the inputs in arena layout. */
+static int run_list(const zero1_plan* plan, const uint16_t* h_g, const float* h_p, int64_t n, const char* out) {
+    enum { GRAD, MASTER, EXP_AVG, EXP_AVG_SQ, WEIGHT, MICRO, NQ };
+    void* bufs[NQ][N_TENSORS];
+    const int elem[NQ] = {4, 4, 4, 4, 2, 2};
+    int64_t cnt[N_TENSORS], off[N_TENSORS];
+    for (int32_t i = 0; i < N_TENSORS; ++i) {
+        check(zero1_plan_tensor(plan, i, NULL, &cnt[i], &off[i]), "zero1_plan_tensor");
+        for (int q = 0; q < NQ; ++q) {
+            bufs[q][i] = NULL;
+            if (cnt[i] == 0) continue;
+            check_cuda(cudaMalloc(&bufs[q][i], (size_t)cnt[i] * elem[q]), "cudaMalloc");
+            check_cuda(cudaMemset(bufs[q][i], 0, (size_t)cnt[i] * elem[q]), "memset");
+        }
+        if (cnt[i]) {
+            check_cuda(cudaMemcpy(bufs[MICRO][i], h_g + off[i], cnt[i] * 2, cudaMemcpyHostToDevice), "H2D");
+            check_cuda(cudaMemcpy(bufs[MASTER][i], h_p + off[i], cnt[i] * 4, cudaMemcpyHostToDevice), "H2D");
+        }
+    }
+    cudaStream_t stream;
+    check_cuda(cudaStreamCreate(&stream), "stream");
+    void* d_lists[NQ];
+    for (int q = 0; q < NQ; ++q) {
+        check_cuda(cudaMalloc(&d_lists[q], N_TENSORS * sizeof(void*)), "cudaMalloc");
+        check(zero1_list_ptrs_upload(plan, (const void* const*)bufs[q], 1, elem[q], d_lists[q],
+                                     N_TENSORS * sizeof(void*), stream), "zero1_list_ptrs_upload");
+    }
+    const size_t tb = zero1_list_table_bytes(plan), wb = zero1_list_workspace_bytes(plan);
+    void *d_table, *d_ws;
+    zero1_norm_out* d_norm;
+    check_cuda(cudaMalloc(&d_table, tb ? tb : 16), "cudaMalloc");
+    check_cuda(cudaMalloc(&d_ws, wb ? wb : 16), "cudaMalloc");
+    check_cuda(cudaMalloc((void**)&d_norm, 32), "cudaMalloc");
+    check(zero1_list_table_upload(plan, d_table, tb, stream), "zero1_list_table_upload");
+    zero1_hparams hp = {3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0};
+    check(zero1_list_accumulate_norm(plan, d_table, (float* const*)d_lists[GRAD], (const uint16_t* const*)d_lists[MICRO],
+                                     1, 1, 1.0, 0.0, d_ws, wb, d_norm, stream), "zero1_list_accumulate_norm");
+    check(zero1_list_step(plan, d_table, (float* const*)d_lists[MASTER], (float* const*)d_lists[EXP_AVG],
+                          (float* const*)d_lists[EXP_AVG_SQ], (const float* const*)d_lists[GRAD],
+                          (uint16_t* const*)d_lists[WEIGHT], &hp, 1, d_norm, stream), "zero1_list_step");
+    zero1_norm_out rec;
+    check(zero1_read_norm(d_norm, stream, &rec), "zero1_read_norm");
+
+    /* back to arena layout (padding zero), in the format of the arena mode */
+    float* h_out = calloc((size_t)n, 4);
+    uint16_t* h_w = calloc((size_t)n, 2);
+    FILE* f = fopen(out, "wb");
+    if (!f) return 4;
+    const int order[4] = {GRAD, MASTER, EXP_AVG, EXP_AVG_SQ};
+    for (int a = 0; a < 4; ++a) {
+        memset(h_out, 0, (size_t)n * 4);
+        for (int32_t i = 0; i < N_TENSORS; ++i)
+            if (cnt[i])
+                check_cuda(cudaMemcpy(h_out + off[i], bufs[order[a]][i], cnt[i] * 4, cudaMemcpyDeviceToHost), "D2H");
+        fwrite(h_out, 4, (size_t)n, f);
+    }
+    for (int32_t i = 0; i < N_TENSORS; ++i)
+        if (cnt[i]) check_cuda(cudaMemcpy(h_w + off[i], bufs[WEIGHT][i], cnt[i] * 2, cudaMemcpyDeviceToHost), "D2H");
+    fwrite(h_w, 2, (size_t)n, f);
+    fwrite(&rec, sizeof rec, 1, f);
+    fclose(f);
+    printf("ok list sumsq %.17g norm %.17g status %d partials %d\n", rec.sumsq, rec.norm, rec.status, rec.n_partials);
+    for (int q = 0; q < NQ; ++q) {
+        for (int32_t i = 0; i < N_TENSORS; ++i) cudaFree(bufs[q][i]);
+        cudaFree(d_lists[q]);
+    }
+    cudaFree(d_table); cudaFree(d_ws); cudaFree(d_norm);
+    cudaStreamDestroy(stream);
+    free(h_out); free(h_w);
+    return 0;
+}
+
 int main(int argc, char** argv) {
     if (argc < 2) {
-        fprintf(stderr, "usage: %s plan | step <out.bin>\n", argv[0]);
+        fprintf(stderr, "usage: %s plan | step <out.bin> | list <out.bin>\n", argv[0]);
         return 1;
     }
     zero1_plan* plan = NULL;
@@ -65,7 +141,8 @@ int main(int argc, char** argv) {
         zero1_plan_destroy(plan);
         return 0;
     }
-    if (strcmp(argv[1], "step") != 0 || argc < 3) return 1;
+    const int list_mode = strcmp(argv[1], "list") == 0;
+    if ((strcmp(argv[1], "step") != 0 && !list_mode) || argc < 3) return 1;
 
     /* host inputs: the shard elements get values, padding stays zero */
     uint16_t* h_g = calloc((size_t)n, sizeof(uint16_t));
@@ -77,6 +154,13 @@ int main(int argc, char** argv) {
             h_g[o + k] = grad_bits(o + k);
             h_p[o + k] = master_val(o + k);
         }
+    }
+    if (list_mode) {
+        int rc = run_list(plan, h_g, h_p, n, argv[2]);
+        free(h_g);
+        free(h_p);
+        zero1_plan_destroy(plan);
+        return rc;
     }
     float *d_grad, *d_p, *d_m, *d_v;
     uint16_t *d_w, *d_g;

@@ -51,9 +51,11 @@ def _inputs(n, offsets, counts):
 
 
 @pytest.mark.gpu
-def test_step_from_c_matches_the_oracle(program, tmp_path):
+@pytest.mark.parametrize("mode", ["step", "list"])
+def test_step_from_c_matches_the_oracle(program, tmp_path, mode):
+    """The arena calls, and the tensor-list calls on one cudaMalloc per tensor shard."""
     outp = str(tmp_path / "out.bin")
-    r = subprocess.run([program, "step", outp], capture_output=True, text=True)
+    r = subprocess.run([program, mode, outp], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     lines = subprocess.run([program, "plan"], check=True, capture_output=True, text=True).stdout.splitlines()
     n = int(lines[0].split()[5])
