@@ -1,0 +1,42 @@
+"""bench.py's JSON line on a GPU: one small run, checked against the keys and units the
+measurement contract asks for (the driver runs the full-size default itself)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                         timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, lines
+    return json.loads(lines[0])
+
+
+@pytest.mark.parametrize("extra", [[], ["--tensor-list"]])
+def test_bench_line_has_the_contract_keys(extra):
+    d = _run("--workload", "toy", "--steps", "3", "--warmup", "3", "--cpu-baseline-seconds", "1", *extra)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "clocks", "gpu_launches", "e2e"):
+        assert k in d, k
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
+    assert d["unit"] == "params/s" and d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert "workload" in d["config"]
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    c = d["cpu_baseline"]
+    assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["sample"]
+    assert d["gpu_launches"] == 3 * (2 + 2)  # K=2: one accumulate, the fused pass (2 kernels), the step
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    if not extra:
+        e = d["e2e"]
+        assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 24

@@ -303,3 +303,59 @@ def test_llama8b_full_size_list_equals_arena():
     for arena, shards in ((grad, lg), (master, lm), (m, lmm), (v, lv), (wbf, lw)):
         for i, (a, b) in enumerate(zip(plan.shard_views(arena), shards)):
             assert torch.equal(a, b), i
+
+
+@pytest.mark.parametrize("guard", [64, 65])
+def test_list_calls_write_nothing_outside_the_shards(guard):
+    """Every shard buffer sits between guard zones filled with a pattern (64 elements keeps the
+    shards 16-byte aligned, 65 forces the element-wise path); after every list call has run,
+    the guards are unchanged.  Sizes cover partial last vectors and runs."""
+    numels = [1000, 7, 16384 + 9, 33, 2, 16384 * 2 + 24]
+    nd = [0, 1, 0, 1, 1, 0]
+    plan = z.Plan(numels, nd, 3, 1)
+    counts = [int(c) for c in plan.layout().counts]
+    G = guard
+    g = torch.Generator(device="cuda").manual_seed(17)
+    bufs = {}
+
+    def guarded(name, dtype, fill=None):
+        out = []
+        for i, c in enumerate(counts):
+            buf = torch.empty(c + 2 * G, dtype=dtype, device="cuda")
+            buf.view(torch.uint8).fill_(0xA5)
+            mid = buf[G:G + c]
+            if fill is None:
+                mid.zero_()
+            else:
+                mid.copy_(fill(c))
+            out.append((buf, mid))
+        bufs[name] = out
+        return [mid for _, mid in out]
+
+    rnd = lambda s: (lambda c: torch.randn(c, device="cuda", generator=g) * s)  # noqa: E731
+    grad = guarded("grad", torch.float32)
+    master = guarded("master", torch.float32, rnd(0.02))
+    m, v = guarded("m", torch.float32), guarded("v", torch.float32)
+    w = guarded("w", torch.bfloat16)
+    mb = guarded("mb", torch.bfloat16, rnd(0.1))
+    mb2 = guarded("mb2", torch.bfloat16, rnd(0.1))
+    L = {k: z.PointerLists(plan, x, torch.float32) for k, x in (("grad", grad), ("master", master), ("m", m), ("v", v))}
+    wl = z.PointerLists(plan, w, torch.bfloat16)
+    one, two = z.PointerLists(plan, mb, torch.bfloat16), z.PointerLists(plan, [mb, mb2], torch.bfloat16)
+    table, ws, nout = plan.list_table(), plan.new_list_workspace(), z.new_norm_out()
+    z.list_accumulate(plan, table, L["grad"], one)
+    z.list_accumulate(plan, table, L["grad"], two, overwrite_first=False)
+    z.list_accumulate(plan, table, L["grad"], two, overwrite_first=True)
+    z.list_accumulate_norm(plan, table, L["grad"], one, ws, nout, overwrite_first=False, divisor=3.0)
+    z.list_accumulate_norm(plan, table, L["grad"], one, ws, nout, overwrite_first=True)
+    z.list_grad_norm(plan, table, L["grad"], ws, nout)
+    z.list_step(plan, table, L["master"], L["m"], L["v"], L["grad"], wl, z.Hparams(), 1, nout)
+    z.list_step(plan, table, L["master"], L["m"], L["v"], L["grad"], None, z.Hparams(), 2, nout)
+    torch.cuda.synchronize()
+    assert z.read_norm(nout)["status"] == 0
+    for name, lst in bufs.items():
+        for i, (buf, mid) in enumerate(lst):
+            raw = buf.view(torch.uint8)
+            eb = buf.element_size()
+            head, tail = raw[:G * eb], raw[(G + mid.numel()) * eb:]
+            assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), (name, i)
