@@ -130,3 +130,37 @@ def test_ranks_save_concurrently_with_gloo(z, tmp_path):
     assert z.checkpoint.load(path, plan, *arenas) == 3
     for k, a in zip(("master", "exp_avg", "exp_avg_sq"), arenas):
         assert torch.equal(a, _arena_from_full(plan, full[k], 1, 0))
+
+
+def test_checkpoint_from_and_into_shard_lists(z, tmp_path):
+    """Per-tensor shard lists (the tensor-list form) save the same files as arenas and load
+    back at another dp size, in either form."""
+    full = _full_state(42)
+    path = str(tmp_path / "ckpt")
+    model_off = np.concatenate([[0], np.cumsum(NUMELS)[:-1]])
+
+    def shards(plan, dp, r, q):
+        start, count, _ = oracle.plan(NUMELS, dp, r)
+        return [torch.from_numpy(full[q][model_off[i] + start[i]:model_off[i] + start[i] + count[i]].copy())
+                for i in range(len(NUMELS))]
+
+    for r in range(3):
+        plan = z.Plan(NUMELS, ND, 3, r)
+        z.checkpoint.save(path, plan, *[shards(plan, 3, r, q) for q in ("master", "exp_avg", "exp_avg_sq")], step_t=9)
+    for q in ("master", "exp_avg", "exp_avg_sq"):
+        assert np.array_equal(np.fromfile(os.path.join(path, q + ".bin"), dtype="<f4"), full[q])
+    for r in range(5):
+        plan = z.Plan(NUMELS, ND, 5, r)
+        lists = [[torch.full((int(c),), 5.0) for c in plan.layout().counts] for _ in range(3)]
+        assert z.checkpoint.load(path, plan, *lists) == 9
+        for q, lst in zip(("master", "exp_avg", "exp_avg_sq"), lists):
+            for a, b in zip(lst, shards(plan, 5, r, q)):
+                assert torch.equal(a, b)
+        arenas = [torch.full((plan.arena_numel,), 5.0) for _ in range(3)]
+        z.checkpoint.load(path, plan, *arenas)
+        for q, a in zip(("master", "exp_avg", "exp_avg_sq"), arenas):
+            assert torch.equal(a, _arena_from_full(plan, full[q], 5, r))
+    plan = z.Plan(NUMELS, ND, 5, 0)
+    bad = [torch.zeros(int(c) + 1) for c in plan.layout().counts]
+    with pytest.raises(ValueError):
+        z.checkpoint.load(path, plan, bad, bad, bad)

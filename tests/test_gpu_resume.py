@@ -1,0 +1,83 @@
+"""Checkpoint and resume through the optimizer classes on a GB300: stepping twice, saving,
+loading into a fresh optimizer and stepping once more equals three uninterrupted steps,
+bit for bit, for both layouts and with parameter groups."""
+import pytest
+import torch
+
+import zero_sharded_mixed_local_gb300 as z
+
+pytestmark = pytest.mark.gpu
+
+NUMELS = [1000, 7, 4096, 33, 16385, 40000]
+GROUPS = [0, 1, 2, 1, 0, 2]
+LR_SCALE = [1.0, 1.0, 0.25, 1, 1, 1, 1, 1]
+WD_SCALE = [1.0, 0.0, 0.5, 1, 1, 1, 1, 1]
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip_grad=1.0)
+
+
+def _make(kind):
+    kw = dict(dp_size=2, dp_rank=0, hparams=HP, groups=GROUPS, lr_scale=LR_SCALE, wd_scale=WD_SCALE)
+    return z.LocalShardAdamW(NUMELS, **kw) if kind == "arena" else z.ShardListAdamW(NUMELS, **kw)
+
+
+def _micro(opt, step):
+    g = torch.Generator(device="cuda").manual_seed(100 + step)
+    if isinstance(opt, z.LocalShardAdamW):
+        a = opt.plan.new_arena(torch.bfloat16)
+        for v in opt.plan.shard_views(a):
+            v.copy_(torch.randn(v.numel(), device="cuda", generator=g) * 1e-2)
+        return a
+    return [(torch.randn(int(c), device="cuda", generator=g) * 1e-2).to(torch.bfloat16)
+            for c in opt.plan.layout().counts]
+
+
+def _init(opt):
+    g = torch.Generator(device="cuda").manual_seed(7)
+    views = opt.plan.shard_views(opt.master) if isinstance(opt, z.LocalShardAdamW) else opt.master
+    for v in views:
+        v.copy_(torch.randn(v.numel(), device="cuda", generator=g) * 0.02)
+
+
+def _state(opt):
+    if isinstance(opt, z.LocalShardAdamW):
+        return [torch.cat([v.clone() for v in opt.plan.shard_views(a)]) for a in (opt.master, opt.exp_avg,
+                                                                                 opt.exp_avg_sq)]
+    return [torch.cat([t.clone() for t in lst]) for lst in (opt.master, opt.exp_avg, opt.exp_avg_sq)]
+
+
+@pytest.mark.parametrize("kind", ["arena", "list"])
+@pytest.mark.parametrize("use_async", [False, True])
+def test_resume_equals_uninterrupted(kind, use_async, tmp_path):
+    a = _make(kind)
+    _init(a)
+    for s in range(3):
+        a.accumulate(_micro(a, s), last=True)
+        a.step()
+    b = _make(kind)
+    _init(b)
+    for s in range(2):
+        b.accumulate(_micro(b, s), last=True)
+        b.step()
+    fut = b.save_checkpoint(str(tmp_path / "ck"), meta={"kind": kind}, async_=use_async)
+    if use_async:
+        fut.result()
+    c = _make(kind)  # a fresh process's optimizer
+    assert c.load_checkpoint(str(tmp_path / "ck")) == 2
+    c.accumulate(_micro(c, 2), last=True)
+    c.step()
+    for x, y in zip(_state(a), _state(c)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_list_checkpoint_loads_into_arenas_at_another_dp(tmp_path):
+    lst = _make("list")
+    _init(lst)
+    lst.accumulate(_micro(lst, 0), last=True)
+    lst.step()
+    lst.save_checkpoint(str(tmp_path / "ck"))
+    # rank 0 of dp 2 saved its own runs (and meta.json); the same rank reads them back as arenas
+    arena = z.LocalShardAdamW(NUMELS, dp_size=2, dp_rank=0, hparams=HP, groups=GROUPS, lr_scale=LR_SCALE,
+                              wd_scale=WD_SCALE)
+    assert arena.load_checkpoint(str(tmp_path / "ck")) == 1
+    for x, y in zip(_state(lst), _state(arena)):
+        assert torch.equal(x, y)

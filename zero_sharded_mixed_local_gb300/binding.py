@@ -563,9 +563,10 @@ class LocalShardAdamW:
     global batch; both only launch kernels on the current stream.
     """
 
-    def __init__(self, numels, no_decay, dp_size=1, dp_rank=0, hparams=None, device="cuda"):
+    def __init__(self, numels, no_decay=None, dp_size=1, dp_rank=0, hparams=None, device="cuda", groups=None,
+                 lr_scale=None, wd_scale=None):
         self.device = torch.device(device)
-        self.plan = Plan(numels, no_decay, dp_size, dp_rank)
+        self.plan = Plan(numels, no_decay, dp_size, dp_rank, groups=groups, lr_scale=lr_scale, wd_scale=wd_scale)
         self.hp = hparams if isinstance(hparams, Hparams) else Hparams(**(hparams or {}))
         mk = self.plan.new_arena
         self.grad = mk(torch.float32, self.device)
@@ -611,6 +612,20 @@ class LocalShardAdamW:
 
     def read_norm(self, stream=None):
         return read_norm(self.norm_out, stream=stream)
+
+    def save_checkpoint(self, path, meta=None, async_=False):
+        """Write this rank's master / m / v shard and the step count (see ``checkpoint``)."""
+        from . import checkpoint
+        fn = checkpoint.save_async if async_ else checkpoint.save
+        return fn(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.t, meta)
+
+    def load_checkpoint(self, path):
+        """Fill master / m / v from a checkpoint written at any dp size; restores the step count."""
+        from . import checkpoint
+        self.t = checkpoint.load(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq)
+        self._micro_seen = 0
+        self._norm_ready = False
+        return self.t
 
 
 class StepGraph:
@@ -800,12 +815,13 @@ class ShardListAdamW:
     shard tensors; their device pointer lists are cached by (address, length) of every
     tensor, so a loop that reuses the same gradient buffers uploads them once."""
 
-    def __init__(self, numels, no_decay, dp_size=1, dp_rank=0, hparams=None, device="cuda", master=None,
-                 exp_avg=None, exp_avg_sq=None, grad=None, weight_bf16=None):
+    def __init__(self, numels, no_decay=None, dp_size=1, dp_rank=0, hparams=None, device="cuda", master=None,
+                 exp_avg=None, exp_avg_sq=None, grad=None, weight_bf16=None, groups=None, lr_scale=None,
+                 wd_scale=None):
         self.device = torch.device(device)
         if self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
-        self.plan = Plan(numels, no_decay, dp_size, dp_rank)
+        self.plan = Plan(numels, no_decay, dp_size, dp_rank, groups=groups, lr_scale=lr_scale, wd_scale=wd_scale)
         self.hp = hparams if isinstance(hparams, Hparams) else Hparams(**(hparams or {}))
         mk = self.plan.new_shards
         self.master = master if master is not None else mk(torch.float32, self.device)
@@ -869,3 +885,18 @@ class ShardListAdamW:
 
     def read_norm(self, stream=None):
         return read_norm(self.norm_out, stream=stream)
+
+    def save_checkpoint(self, path, meta=None, async_=False):
+        """Write this rank's master / m / v shards and the step count (see ``checkpoint``)."""
+        from . import checkpoint
+        fn = checkpoint.save_async if async_ else checkpoint.save
+        return fn(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.t, meta)
+
+    def load_checkpoint(self, path):
+        """Fill the master / m / v shards from a checkpoint written at any dp size (in either
+        layout); restores the step count."""
+        from . import checkpoint
+        self.t = checkpoint.load(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq)
+        self._micro_seen = 0
+        self._norm_ready = False
+        return self.t

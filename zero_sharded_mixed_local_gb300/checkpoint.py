@@ -15,6 +15,10 @@ plan.
 ``save_async`` copies the arenas to host memory before returning (training
 may go on changing them) and writes the files in a background thread, the
 asynchronous checkpointing the same section describes.
+
+Each quantity is given either as an arena (one padded fp32 tensor laid out by
+the plan) or as a list of per-tensor shard tensors in model order (the form
+the tensor-list calls step); the files are the same either way.
 """
 import concurrent.futures
 import json
@@ -43,11 +47,26 @@ def _runs(plan):
             for i in range(len(numels)) if L.counts[i]]
 
 
-def _host_copy(arena):
-    if arena.dtype != torch.float32:
-        raise TypeError("optimizer state arenas are fp32")
-    t = arena.detach()
-    return t.cpu().numpy() if t.device.type != "cpu" else t.numpy().copy()
+def _host_copy(plan, x):
+    """Host fp32 array in arena layout from an arena tensor or a list of shard tensors."""
+    if isinstance(x, torch.Tensor):
+        if x.dtype != torch.float32:
+            raise TypeError("optimizer state arenas are fp32")
+        t = x.detach()
+        return t.cpu().numpy() if t.device.type != "cpu" else t.numpy().copy()
+    L = plan.layout()
+    shards = list(x)
+    if len(shards) != len(L.counts):
+        raise ValueError("%d shard tensors for a plan of %d tensors" % (len(shards), len(L.counts)))
+    host = np.zeros(plan.arena_numel, np.float32)
+    for i, (t, o, c) in enumerate(zip(shards, L.offsets, L.counts)):
+        o, c = int(o), int(c)
+        if c == 0:
+            continue
+        if t.dtype != torch.float32 or t.numel() != c:
+            raise ValueError("shard %d must be fp32 with %d elements" % (i, c))
+        host[o:o + c] = t.detach().reshape(-1).cpu().numpy()
+    return host
 
 
 def _write(path, plan, snap, step_t, meta):
@@ -85,7 +104,7 @@ def save(path, plan, master, exp_avg, exp_avg_sq, step_t, meta=None):
     if sys.byteorder != "little":  # pragma: no cover - every supported host is little-endian
         raise RuntimeError("little-endian host expected")
     os.makedirs(path, exist_ok=True)
-    snap = {q: _host_copy(a) for q, a in zip(QUANTITIES, (master, exp_avg, exp_avg_sq))}
+    snap = {q: _host_copy(plan, a) for q, a in zip(QUANTITIES, (master, exp_avg, exp_avg_sq))}
     _write(path, plan, snap, step_t, meta)
 
 
@@ -93,7 +112,7 @@ def save_async(path, plan, master, exp_avg, exp_avg_sq, step_t, meta=None):
     """As save(), but only the device-to-host snapshot happens before returning; the
     files are written in a background thread.  Returns a concurrent.futures.Future."""
     os.makedirs(path, exist_ok=True)
-    snap = {q: _host_copy(a) for q, a in zip(QUANTITIES, (master, exp_avg, exp_avg_sq))}
+    snap = {q: _host_copy(plan, a) for q, a in zip(QUANTITIES, (master, exp_avg, exp_avg_sq))}
     return _executor.submit(_write, path, plan, snap, step_t, meta)
 
 
@@ -106,15 +125,22 @@ def read_meta(path):
 
 
 def load(path, plan, master, exp_avg, exp_avg_sq):
-    """Fill this rank's arenas (any dp_size) from the checkpoint; returns its step count.
-    Padding elements are set to zero."""
+    """Fill this rank's arenas or shard lists (any dp_size) from the checkpoint; returns its
+    step count.  Arena padding elements are set to zero."""
     info = read_meta(path)
     if [int(n) for n in info["numels"]] != [int(n) for n in _numels(plan)]:
         raise ValueError("checkpoint tensor sizes do not match the plan")
     runs = _runs(plan)
+    L = plan.layout()
     for q, arena in zip(QUANTITIES, (master, exp_avg, exp_avg_sq)):
-        if arena.dtype != torch.float32 or arena.numel() != plan.arena_numel:
-            raise ValueError("%s arena must be fp32 with %d elements" % (q, plan.arena_numel))
+        if isinstance(arena, torch.Tensor):
+            if arena.dtype != torch.float32 or arena.numel() != plan.arena_numel:
+                raise ValueError("%s arena must be fp32 with %d elements" % (q, plan.arena_numel))
+        else:
+            arena = list(arena)
+            if len(arena) != len(L.counts) or any(
+                    int(c) and (t.dtype != torch.float32 or t.numel() != int(c)) for t, c in zip(arena, L.counts)):
+                raise ValueError("%s shards must be fp32 tensors of the plan's shard sizes" % q)
         host = np.zeros(plan.arena_numel, np.float32)
         fd = os.open(os.path.join(path, q + ".bin"), os.O_RDONLY)
         try:
@@ -128,6 +154,11 @@ def load(path, plan, master, exp_avg, exp_avg_sq):
                     got += k
         finally:
             os.close(fd)
-        arena.copy_(torch.from_numpy(host))
+        if isinstance(arena, torch.Tensor):
+            arena.copy_(torch.from_numpy(host))
+        else:
+            for t, o, c in zip(arena, L.offsets, L.counts):
+                if int(c):
+                    t.copy_(torch.from_numpy(host[int(o):int(o) + int(c)]).view_as(t))
     return int(info["step"])
 
