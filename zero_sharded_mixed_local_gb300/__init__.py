@@ -23,6 +23,7 @@ __all__ = [
 ]
 
 from . import checkpoint  # noqa: E402
+from .optim import Zero1AdamW, default_no_decay  # noqa: E402
 from .schedules import lr_at, mup_groups  # noqa: E402
 
-__all__ += ["checkpoint", "lr_at", "mup_groups"]
+__all__ += ["checkpoint", "lr_at", "mup_groups", "Zero1AdamW", "default_no_decay"]
