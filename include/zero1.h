@@ -400,7 +400,11 @@ size_t zero1_list_table_bytes(const zero1_plan* plan);
 
 /* Copy the run table into caller-owned device memory d_table (16-byte
  * aligned, at least zero1_list_table_bytes bytes).  Asynchronous on `stream`;
- * the plan may be destroyed once the call returns.  Valid only for this plan.
+ * the plan may be destroyed once the call returns.  Valid only for this plan:
+ * like buffer lengths, which plan a device table came from cannot be checked
+ * (the kernels only skip a run whose tensor index, length or group is out of
+ * range for the plan they are called with, so a stray table cannot send them
+ * past the pointer lists).
  * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
 int zero1_list_table_upload(const zero1_plan* plan, void* d_table, size_t table_bytes, void* stream);
 

@@ -85,6 +85,13 @@ __device__ __forceinline__ void store8_bf16(uint16_t* x, int n, bool vec, const 
 
 __device__ __forceinline__ bool misaligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
+// A run descriptor this launch can use: a table built for another plan (more
+// tensors, or corrupted) is skipped rather than read through.
+__device__ __forceinline__ bool run_in_range(const ListChunk& ch, int32_t n_tensors) {
+    return ch.tensor >= 0 && ch.tensor < n_tensors && ch.len >= 1 && ch.len <= kNormTile &&
+           ch.group < ZERO1_MAX_GROUPS && ch.offset >= 0;
+}
+
 // Gradient passes over the runs: accumulate (as zero1_accumulate), accumulate
 // and take the norm partials (as zero1_accumulate_norm), or the partials alone
 // (as zero1_grad_norm).  One block per run, thread t owning vectors t + 256r
@@ -108,6 +115,10 @@ __global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 6 : 4)
     __shared__ float2 s_warp[kTileThreads / 32];
     const int64_t c = first_chunk + blockIdx.x;
     const ListChunk ch = P.table[c];
+    if (!run_in_range(ch, P.n_tensors)) {  // the same for every thread of the block
+        if (kSumsSquares && threadIdx.x == 0) partials[c] = make_float2(0.f, 0.f);
+        return;
+    }
     float* grad = P.grad[ch.tensor];
     bool missing = grad == nullptr, unaligned = false;
     const uint16_t* micro0 = nullptr;
@@ -234,6 +245,7 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
     __shared__ int s_skip;
     const int64_t b = first_block + blockIdx.x;
     const ListChunk ch = P.table[b / kStepSubBlocks];
+    if (!run_in_range(ch, P.n_tensors)) return;  // the same for every thread of the block
     const int sub = static_cast<int>(b % kStepSubBlocks);
     float* master = P.master[ch.tensor];
     float* m = P.m[ch.tensor];
