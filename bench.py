@@ -153,6 +153,16 @@ def barrier(world):
         dist.barrier()
 
 
+def sum_over_ranks(x, world):
+    """Whole-job total of a per-rank count (the ranks' shards differ by the remainder rule)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.int64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return int(t.item())
+
+
 def max_over_ranks(x, world):
     if world == 1:
         return x
@@ -455,6 +465,7 @@ def main():
 
     total_ms = start.elapsed_time(end)
     total_ms = max_over_ranks(total_ms, world)
+    P_job = sum_over_ranks(P, world)  # parameters all ranks step per step
     ms_step = total_ms / args.steps
     if sgraph is None:
         acc_ms = statistics.mean(r["a0"].elapsed_time(r["n0"]) for r in recs)      # the first K-1 micro-batches
@@ -546,7 +557,7 @@ def main():
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
         copy_ms = statistics.mean(a.elapsed_time(b) for a, b in copy_ev)
         assert all(r["status"] == 0 for r in seen)
-        e2e = {"value": world * P / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
+        e2e = {"value": P_job / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(mb.numel() * mb.element_size() for mb in host_micros),
                "d2h_bytes_per_step": z.NORM_OUT_BYTES, "h2d_copy_gbs_before": h2d_gbs,
                "h2d_copy_ms_in_loop": copy_ms,
@@ -565,7 +576,7 @@ def main():
     if rank == 0:
         out = {
             "metric": METRIC,
-            "value": world * P / (ms_step * 1e-3),
+            "value": P_job / (ms_step * 1e-3),
             "unit": "params/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -579,6 +590,7 @@ def main():
             "config": {
                 "workload": w.description,
                 "local_params_per_gpu": P,
+                "params_per_step_all_ranks": P_job,
                 "arena_elems": plan.arena_numel,
                 "micro_batches": K,
                 "dp_size": w.dp_size,
