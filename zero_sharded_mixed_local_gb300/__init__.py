@@ -5,25 +5,33 @@ described for nanotron's distributed optimizer: accumulate bf16 micro-batch
 gradients in fp32, take the global gradient L2 norm for clipping, run AdamW
 on the fp32 master / m / v shard and write the bf16 weights the all-gather
 ships.  The work runs in hand-written CUDA kernels behind the C ABI of
-``libzero1.so`` (``include/zero1.h``); this package is its thin binding.
+``libzero1.so`` (``include/zero1.h``).  ``binding`` is its thin ctypes binding;
+``optim`` holds the optimizer objects built on it (arena and tensor-list
+shards, CUDA-graph replay, a torch-module wrapper); ``checkpoint`` and
+``schedules`` are host-side helpers.
 """
-from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_EALIGN, ZERO1_ECUDA,
-                      ZERO1_EINVAL, ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, LocalShardAdamW, Plan,
-                      ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, exchange_chunk_numel, grad_norm, grad_norm_static, load_library,
-                      pack_reduce_scatter, shard_gather, shard_scatter, unpack_all_gather, new_norm_out,
-                      read_norm, step, step_dev, step_scalars, StepGraph, PointerLists, ShardListAdamW,
-                      list_accumulate, list_accumulate_norm, list_grad_norm, list_step)
+from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_EALIGN, ZERO1_ECUDA, ZERO1_EINVAL,
+                      ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, Plan, PointerLists,
+                      ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm,
+                      exchange_chunk_numel, grad_norm, grad_norm_static, list_accumulate, list_accumulate_norm,
+                      list_grad_norm, list_step, load_library, new_norm_out, pack_reduce_scatter, read_norm,
+                      shard_gather, shard_scatter, step, step_dev, step_scalars, unpack_all_gather)
+from . import checkpoint
+from .optim import LocalShardAdamW, ShardListAdamW, StepGraph, Zero1AdamW, default_no_decay
+from .schedules import lr_at, mup_groups
 
 __all__ = [
+    # status codes and limits
     "ARENA_ALIGN", "MAX_GROUPS", "MAX_MICRO", "NORM_OUT_BYTES", "ZERO1_EALIGN", "ZERO1_ECUDA", "ZERO1_EINVAL",
-    "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_ETOOBIG", "ZERO1_OK", "Hparams", "LocalShardAdamW", "Plan", "ShardLayout",
-    "Zero1Error", "accumulate", "accumulate_norm", "allreduce_sumsq_", "decode_norm", "exchange_chunk_numel", "grad_norm", "grad_norm_static", "load_library",
-    "pack_reduce_scatter", "shard_gather", "shard_scatter", "unpack_all_gather", "new_norm_out", "read_norm", "step", "step_dev", "step_scalars", "StepGraph",
-    "PointerLists", "ShardListAdamW", "list_accumulate", "list_accumulate_norm", "list_grad_norm", "list_step",
+    "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_ETOOBIG", "ZERO1_OK", "Zero1Error", "load_library",
+    # plan and arena calls
+    "Hparams", "Plan", "ShardLayout", "accumulate", "accumulate_norm", "grad_norm", "grad_norm_static", "step",
+    "step_dev", "step_scalars", "new_norm_out", "read_norm", "decode_norm", "allreduce_sumsq_",
+    # exchanges
+    "exchange_chunk_numel", "pack_reduce_scatter", "shard_gather", "shard_scatter", "unpack_all_gather",
+    # tensor lists
+    "PointerLists", "list_accumulate", "list_accumulate_norm", "list_grad_norm", "list_step",
+    # optimizer objects and helpers
+    "LocalShardAdamW", "ShardListAdamW", "StepGraph", "Zero1AdamW", "default_no_decay", "checkpoint", "lr_at",
+    "mup_groups",
 ]
-
-from . import checkpoint  # noqa: E402
-from .optim import Zero1AdamW, default_no_decay  # noqa: E402
-from .schedules import lr_at, mup_groups  # noqa: E402
-
-__all__ += ["checkpoint", "lr_at", "mup_groups", "Zero1AdamW", "default_no_decay"]

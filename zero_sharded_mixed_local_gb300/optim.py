@@ -1,4 +1,11 @@
-"""A ZeRO-1 AdamW over a torch module's parameters, on top of the tensor-list calls.
+"""Optimizer objects built on the binding: one rank's ZeRO-1 AdamW state and step.
+
+``LocalShardAdamW`` owns one rank's shard as flat arenas; ``StepGraph`` replays
+its step as one CUDA graph; ``ShardListAdamW`` owns the same state as one buffer
+per tensor shard (the tensor-list calls); ``Zero1AdamW`` wraps a torch module.
+
+Zero1AdamW: a ZeRO-1 AdamW over a torch module's parameters, on top of the
+tensor-list calls.
 
 The pages' distributed optimizer ("ZeRO-1 风格的 Distributed Optimizer", sections
 6.2-6.3) wraps a model's named parameters: each rank keeps the fp32 master
@@ -20,7 +27,248 @@ norm weights and biases).
 """
 import torch
 
-from .binding import Hparams, Plan, ShardListAdamW
+from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, Hparams, list_accumulate,
+                      list_accumulate_norm, list_grad_norm, list_step, new_norm_out, Plan, PointerLists, read_norm,
+                      step, step_dev, step_scalars, STEP_SCALARS_BYTES)
+
+
+class LocalShardAdamW:
+    """One data-parallel rank's ZeRO-1 optimizer shard, resident on one GPU.
+
+    Owns the arenas of the local shard (fp32 grad, master, m, v and the bf16
+    copy), the norm workspace and record, and the step counter.  A training
+    loop calls ``accumulate`` once per micro-batch and ``step`` once per
+    global batch; both only launch kernels on the current stream.
+    """
+
+    def __init__(self, numels, no_decay=None, dp_size=1, dp_rank=0, hparams=None, device="cuda", groups=None,
+                 lr_scale=None, wd_scale=None):
+        self.device = torch.device(device)
+        self.plan = Plan(numels, no_decay, dp_size, dp_rank, groups=groups, lr_scale=lr_scale, wd_scale=wd_scale)
+        self.hp = hparams if isinstance(hparams, Hparams) else Hparams(**(hparams or {}))
+        mk = self.plan.new_arena
+        self.grad = mk(torch.float32, self.device)
+        self.master = mk(torch.float32, self.device)
+        self.exp_avg = mk(torch.float32, self.device)
+        self.exp_avg_sq = mk(torch.float32, self.device)
+        self.weight_bf16 = mk(torch.bfloat16, self.device)
+        self.workspace = self.plan.new_workspace(self.device)
+        self.norm_out = new_norm_out(self.device)
+        self.t = 0
+        self._micro_seen = 0
+
+    def accumulate(self, micro, last=False, extra_sumsq=0.0, divisor=1.0, stream=None):
+        """Add one (or several) bf16 micro-batch gradient arenas; the first call of a step
+        overwrites.  ``last=True`` marks the step's final micro-batch: the gradient norm
+        is taken in the same pass (after dividing the sum by ``divisor``, e.g. the world
+        size) and step() will not read the gradient for it again."""
+        first = self._micro_seen == 0
+        if last:
+            accumulate_norm(self.plan, self.grad, micro, self.workspace, self.norm_out, overwrite_first=first,
+                            extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
+        else:
+            accumulate(self.plan, self.grad, micro, overwrite_first=first, stream=stream)
+        self._micro_seen += 1 if isinstance(micro, torch.Tensor) else len(micro)
+        self._norm_ready = bool(last)
+
+    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None):
+        """Norm + clip + AdamW + bf16 copy; returns nothing (read_norm() syncs).
+
+        The norm is taken here unless the last accumulate() already did.  With
+        ``group`` (a torch.distributed process group of the data-parallel ranks)
+        the local sum of squares is all-reduced before the update."""
+        if not getattr(self, "_norm_ready", False):
+            grad_norm(self.plan, self.grad, self.workspace, self.norm_out, extra_sumsq, stream=stream)
+        self._norm_ready = False
+        if group is not None:
+            allreduce_sumsq_(self.norm_out, group)
+        self.t += 1
+        hp = self.hp if lr is None else Hparams(**{**self.hp.__dict__, "lr": lr})
+        step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
+             self.norm_out, stream=stream)
+        self._micro_seen = 0
+
+    def read_norm(self, stream=None):
+        return read_norm(self.norm_out, stream=stream)
+
+    def save_checkpoint(self, path, meta=None, async_=False):
+        """Write this rank's master / m / v shard and the step count (see ``checkpoint``)."""
+        from . import checkpoint
+        fn = checkpoint.save_async if async_ else checkpoint.save
+        return fn(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.t, meta)
+
+    def load_checkpoint(self, path):
+        """Fill master / m / v from a checkpoint written at any dp size; restores the step count."""
+        from . import checkpoint
+        self.t = checkpoint.load(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq)
+        self._micro_seen = 0
+        self._norm_ready = False
+        return self.t
+
+
+class StepGraph:
+    """The whole local step of a LocalShardAdamW captured as CUDA graphs.
+
+    One replay runs what accumulate(..., last=True) + step() launch: the
+    accumulation of the micro-batch buffers given here (their contents at
+    replay time), the fused norm, and the AdamW pass.  The step's scalars
+    (which change with t and lr) are not baked into the graph: before each
+    replay the host writes them into a pinned buffer that a captured copy
+    moves to the device.  Two graphs over two pinned buffers alternate, so
+    the host may write step t+1's scalars while step t still runs; it waits
+    only for step t-1.  No collective is captured: use it where the sum of
+    squares needs no all-reduce (one rank, or a caller that all-reduces the
+    norm record in its own graph).
+    """
+
+    def __init__(self, opt, micro_buffers):
+        self.opt = opt
+        self.micro = list(micro_buffers)
+        if not self.micro:
+            raise ValueError("at least one micro-batch buffer")
+        dev = opt.device
+        self.h = [torch.zeros(128, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.d = [torch.zeros(128, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self._warm_kernels(dev)
+        self.graphs = [self._capture(b) for b in range(2)]
+
+    def _warm_kernels(self, dev):
+        # Load every kernel the graph uses (lazy module loading) on a throwaway one-tensor plan,
+        # so the capture itself launches nothing for the first time.
+        tiny = Plan([16], [0])
+        a = [tiny.new_arena(torch.float32, dev) for _ in range(4)]
+        w = tiny.new_arena(torch.bfloat16, dev)
+        mbs = [tiny.new_arena(torch.bfloat16, dev) for _ in self.micro]
+        ws, nout = tiny.new_workspace(dev), new_norm_out(dev)
+        for k, mb in enumerate(mbs[:-1]):
+            accumulate(tiny, a[0], mb, overwrite_first=(k == 0))
+        accumulate_norm(tiny, a[0], mbs[-1], ws, nout, overwrite_first=(len(mbs) == 1))
+        sc = torch.frombuffer(bytearray(step_scalars(tiny, self.opt.hp, 1)), dtype=torch.uint8).to(dev)
+        step_dev(tiny, a[1], a[2], a[3], a[0], w, sc, nout)
+        torch.cuda.synchronize(dev)
+
+    def _capture(self, b):
+        o = self.opt
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.d[b].copy_(self.h[b], non_blocking=True)
+            for k, mb in enumerate(self.micro[:-1]):
+                accumulate(o.plan, o.grad, mb, overwrite_first=(k == 0))
+            accumulate_norm(o.plan, o.grad, self.micro[-1], o.workspace, o.norm_out,
+                            overwrite_first=(len(self.micro) == 1))
+            step_dev(o.plan, o.master, o.exp_avg, o.exp_avg_sq, o.grad, o.weight_bf16, self.d[b], o.norm_out)
+        return g
+
+    def replay(self, lr=None):
+        """One local step at t = opt.t + 1 (lr overrides the optimizer's lr for this step)."""
+        o = self.opt
+        t = o.t + 1
+        b = t % 2
+        self.done[b].synchronize()  # the replay that last read pinned buffer b (step t-2) is done
+        hp = o.hp if lr is None else Hparams(**{**o.hp.__dict__, "lr": lr})
+        self.h[b][:STEP_SCALARS_BYTES].copy_(torch.frombuffer(bytearray(step_scalars(o.plan, hp, t)),
+                                                              dtype=torch.uint8))
+        self.graphs[b].replay()
+        self.done[b].record()
+        o.t = t
+
+
+class ShardListAdamW:
+    """LocalShardAdamW over per-tensor shard buffers instead of arenas.
+
+    ``master``, ``exp_avg``, ``exp_avg_sq``, ``grad`` and ``weight_bf16`` are lists of
+    tensors, one per parameter (model order, each exactly its shard's length); pass
+    your own (for instance the fp32 state a framework already keeps per parameter) or
+    let the constructor allocate zeroed ones.  Micro-batch gradients are lists of bf16
+    shard tensors; their device pointer lists are cached by (address, length) of every
+    tensor, so a loop that reuses the same gradient buffers uploads them once."""
+
+    def __init__(self, numels, no_decay=None, dp_size=1, dp_rank=0, hparams=None, device="cuda", master=None,
+                 exp_avg=None, exp_avg_sq=None, grad=None, weight_bf16=None, groups=None, lr_scale=None,
+                 wd_scale=None):
+        self.device = torch.device(device)
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.plan = Plan(numels, no_decay, dp_size, dp_rank, groups=groups, lr_scale=lr_scale, wd_scale=wd_scale)
+        self.hp = hparams if isinstance(hparams, Hparams) else Hparams(**(hparams or {}))
+        mk = self.plan.new_shards
+        self.master = master if master is not None else mk(torch.float32, self.device)
+        self.exp_avg = exp_avg if exp_avg is not None else mk(torch.float32, self.device)
+        self.exp_avg_sq = exp_avg_sq if exp_avg_sq is not None else mk(torch.float32, self.device)
+        self.grad = grad if grad is not None else mk(torch.float32, self.device)
+        self.weight_bf16 = weight_bf16 if weight_bf16 is not None else mk(torch.bfloat16, self.device)
+        f32 = torch.float32
+        self._lists = {name: PointerLists(self.plan, getattr(self, name), f32, self.device)
+                       for name in ("master", "exp_avg", "exp_avg_sq", "grad")}
+        self._lists["weight_bf16"] = PointerLists(self.plan, self.weight_bf16, torch.bfloat16, self.device)
+        self.table = self.plan.list_table(self.device)
+        self.workspace = self.plan.new_list_workspace(self.device)
+        self.norm_out = new_norm_out(self.device)
+        self._micro_cache = {}
+        self.t = 0
+        self._micro_seen = 0
+        self._norm_ready = False
+
+    def _micro_lists(self, micro):
+        if len(micro) and isinstance(micro[0], torch.Tensor):
+            micro = [micro]
+        # A cached list stays valid for any tensors at the same addresses with the same
+        # lengths (what the upload checked); it keeps no reference to them.
+        key = tuple(tuple((t.data_ptr(), t.numel(), t.dtype, t.device, t.is_contiguous()) for t in lst)
+                    for lst in micro)
+        pl = self._micro_cache.get(key)
+        if pl is None:
+            if len(self._micro_cache) >= 8:
+                self._micro_cache.clear()
+            pl = self._micro_cache[key] = PointerLists(self.plan, micro, torch.bfloat16, self.device, keep=False)
+        return pl
+
+    def accumulate(self, micro, last=False, extra_sumsq=0.0, divisor=1.0, stream=None):
+        """Add one micro-batch (a list of bf16 shard tensors) or several (a list of such lists)."""
+        pl = self._micro_lists(micro)
+        first = self._micro_seen == 0
+        if last:
+            list_accumulate_norm(self.plan, self.table, self._lists["grad"], pl, self.workspace, self.norm_out,
+                                 overwrite_first=first, extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
+        else:
+            list_accumulate(self.plan, self.table, self._lists["grad"], pl, overwrite_first=first, stream=stream)
+        self._micro_seen += pl.n_lists
+        self._norm_ready = bool(last)
+
+    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None):
+        """Norm (unless the last accumulate took it) + optional all-reduce of sumsq + clip +
+        AdamW + bf16 copy."""
+        if not self._norm_ready:
+            list_grad_norm(self.plan, self.table, self._lists["grad"], self.workspace, self.norm_out, extra_sumsq,
+                           stream=stream)
+        self._norm_ready = False
+        if group is not None:
+            allreduce_sumsq_(self.norm_out, group)
+        self.t += 1
+        hp = self.hp if lr is None else Hparams(**{**self.hp.__dict__, "lr": lr})
+        L = self._lists
+        list_step(self.plan, self.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], L["weight_bf16"],
+                  hp, self.t, self.norm_out, stream=stream)
+        self._micro_seen = 0
+
+    def read_norm(self, stream=None):
+        return read_norm(self.norm_out, stream=stream)
+
+    def save_checkpoint(self, path, meta=None, async_=False):
+        """Write this rank's master / m / v shards and the step count (see ``checkpoint``)."""
+        from . import checkpoint
+        fn = checkpoint.save_async if async_ else checkpoint.save
+        return fn(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.t, meta)
+
+    def load_checkpoint(self, path):
+        """Fill the master / m / v shards from a checkpoint written at any dp size (in either
+        layout); restores the step count."""
+        from . import checkpoint
+        self.t = checkpoint.load(path, self.plan, self.master, self.exp_avg, self.exp_avg_sq)
+        self._micro_seen = 0
+        self._norm_ready = False
+        return self.t
 
 
 def default_no_decay(name, p):
