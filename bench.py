@@ -33,7 +33,9 @@ METRIC = "AdamW shard-step params/sec and HBM GB/s (fraction of GB300 peak), 1 G
 STEP_BYTES_PER_ELEM = 30          # adamw_step: grad 4 R, master/m/v 12 R + 12 W, bf16 2 W
 
 
-def accumulate_bytes_per_elem(k):
+def accumulate_bytes_per_elem(k, k_way=False):
+    if k_way:  # all K micro-batches in one pass: 2K R + 4 W
+        return 2 * k + 4
     # first micro-batch overwrites (2 R + 4 W); each further one is 2 + 4 R + 4 W
     return 6 + 10 * (k - 1)
 
@@ -322,6 +324,9 @@ def main():
     ap.add_argument("--tensor-list", action="store_true",
                     help="run the tensor-list calls (one pointer per tensor shard, a run table walked by the "
                          "kernels) on per-tensor views of the same buffers, instead of the arena calls")
+    ap.add_argument("--k-way", action="store_true",
+                    help="accumulate all K micro-batch gradients (already resident) in one fused pass with the "
+                         "norm, instead of one call per micro-batch as they arrive")
     ap.add_argument("--micro-batches", type=int, default=None,
                     help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
     args = ap.parse_args()
@@ -374,7 +379,10 @@ def main():
         lists = {name: z.PointerLists(plan, split(buf), torch.float32, dev)
                  for name, buf in (("master", master), ("m", m), ("v", v), ("grad", grad))}
         lists["w"] = z.PointerLists(plan, split(wbf), torch.bfloat16, dev)
-        lists["micro"] = [z.PointerLists(plan, split(mb), torch.bfloat16, dev) for mb in micros]
+        micro_shards = [split(mb) for mb in micros]
+        lists["micro"] = [z.PointerLists(plan, ms, torch.bfloat16, dev) for ms in micro_shards]
+        lists["micro_all"] = z.PointerLists(plan, micro_shards, torch.bfloat16, dev)  # K lists back to back
+        del micro_shards
         master = m = v = grad = wbf = micros = None
         torch.cuda.empty_cache()
         table, lws = plan.list_table(dev), plan.new_list_workspace(dev)
@@ -388,12 +396,16 @@ def main():
         t_counter[0] += 1
         if record is not None:
             record["a0"].record(stream)
-        for k in range(K - 1):
+        for k in range(0 if args.k_way else K - 1):
             z.list_accumulate(plan, table, lists["grad"], lists["micro"][k], overwrite_first=(k == 0), stream=stream)
         if record is not None:
             record["n0"].record(stream)
-        z.list_accumulate_norm(plan, table, lists["grad"], lists["micro"][K - 1], lws, nout, overwrite_first=(K == 1),
-                               stream=stream)
+        if args.k_way:
+            z.list_accumulate_norm(plan, table, lists["grad"], lists["micro_all"], lws, nout, overwrite_first=True,
+                                   stream=stream)
+        else:
+            z.list_accumulate_norm(plan, table, lists["grad"], lists["micro"][K - 1], lws, nout,
+                                   overwrite_first=(K == 1), stream=stream)
         if group is not None:
             z.allreduce_sumsq_(nout, group)
         if record is not None:
@@ -409,11 +421,13 @@ def main():
         t_counter[0] += 1
         if record is not None:
             record["a0"].record(stream)
-        for k in range(K - 1):
+        for k in range(0 if args.k_way else K - 1):
             z.accumulate(plan, grad, micros[k], overwrite_first=(k == 0), stream=stream)
         if record is not None:
             record["n0"].record(stream)
-        if args.unfused:
+        if args.k_way:
+            z.accumulate_norm(plan, grad, micros, ws, nout, overwrite_first=True, stream=stream)
+        elif args.unfused:
             z.accumulate(plan, grad, micros[K - 1], overwrite_first=(K == 1), stream=stream)
             z.grad_norm(plan, grad, ws, nout, 0.0, stream=stream)
         else:
@@ -427,6 +441,8 @@ def main():
         if record is not None:
             record["s1"].record(stream)
 
+    if args.k_way and (args.unfused or args.graph):
+        raise SystemExit("--k-way runs the fused eager calls")
     sgraph = None
     if args.graph:
         if world > 1:
@@ -479,8 +495,8 @@ def main():
     step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9 if sgraph is None else None
     # fused: the norm rides on the last micro-batch's pass (no separate 4-byte read)
     norm_bytes = 4 * P if args.unfused else 0
-    path_bytes = (accumulate_bytes_per_elem(K) + STEP_BYTES_PER_ELEM) * P + norm_bytes
-    last_bytes = (6 if K == 1 else 10) * P + norm_bytes
+    path_bytes = (accumulate_bytes_per_elem(K, args.k_way) + STEP_BYTES_PER_ELEM) * P + norm_bytes
+    last_bytes = accumulate_bytes_per_elem(K, True) * P if args.k_way else (6 if K == 1 else 10) * P + norm_bytes
     step_kernel = "list_step" if lists is not None else "adamw_step"
     traffic = profile_traffic(step_kernel, args.workload)
 
@@ -522,10 +538,13 @@ def main():
                         copy_ev[-1][1].record(side)
                     copied[b].record(side)
                 stream.wait_event(copied[b])
-                for k in range(K - 1):
-                    z.accumulate(plan, grads[b], stage[b][k], overwrite_first=(k == 0), stream=stream)
-                z.accumulate_norm(plan, grads[b], stage[b][K - 1], wss[b], nouts[b], overwrite_first=(K == 1),
-                                  stream=stream)
+                if args.k_way:
+                    z.accumulate_norm(plan, grads[b], stage[b], wss[b], nouts[b], overwrite_first=True, stream=stream)
+                else:
+                    for k in range(K - 1):
+                        z.accumulate(plan, grads[b], stage[b][k], overwrite_first=(k == 0), stream=stream)
+                    z.accumulate_norm(plan, grads[b], stage[b][K - 1], wss[b], nouts[b], overwrite_first=(K == 1),
+                                      stream=stream)
                 if group is not None:
                     z.allreduce_sumsq_(nouts[b], group)
                 opt_t[0] += 1
@@ -597,6 +616,8 @@ def main():
                 "dp_rank": dp_rank,
                 "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
                 "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
+                "accumulate": ("all K micro-batches in one pass (K-way)" if args.k_way
+                               else "one call per micro-batch, as they arrive"),
                 "launch": "one CUDA graph per step (StepGraph)" if sgraph is not None else "eager calls",
                 "layout": ("tensor lists: one allocation per tensor shard, a 16384-element run table"
                            if lists is not None else "arenas: one padded buffer per quantity"),
@@ -605,7 +626,8 @@ def main():
             "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
             "kernels": ({
                 "accumulate": {"ms": acc_ms, "gbs": (accumulate_bytes_per_elem(K) * P - last_bytes) /
-                               (acc_ms * 1e-3) / 1e9 if K > 1 else None, "launches_per_step": K - 1},
+                               (acc_ms * 1e-3) / 1e9 if K > 1 and not args.k_way else None,
+                               "launches_per_step": 0 if args.k_way else K - 1},
                 ("accumulate+grad_norm" if args.unfused else "accumulate_norm"): {
                     "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
                     "launches_per_step": 3 if args.unfused else 2},
@@ -618,7 +640,7 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "gpu_launches": args.steps * (K + 2 + (1 if args.unfused else 0)),  # also inside each graph
+            "gpu_launches": args.steps * ((3 if args.k_way else K + 2) + (1 if args.unfused else 0)),  # also in graphs
         }
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -226,6 +226,29 @@ def test_accumulate_many_micro_batches_in_one_call():
     assert np.array_equal(pb.grad.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("K", [2, 3, 4, 5, 6, 7, 8, 9])
+def test_k_way_fused_pass_matches_the_oracle(K):
+    """All K micro-batches in one fused accumulate-and-norm call (the K-specialised kernels for
+    K <= 8, the general one above): the gradient bit for bit, the norm record equal to the
+    separate calls', with and without the world-size divisor; several tiles and a ragged tail."""
+    pb = Problem(_custom([40000, 17, 3 * 16384 + 40], [0, 1, 0], K=K, steps=1, sigma=0.5))
+    micros = pb.gen.micro_grads()
+    ref = oracle_grad(pb.n, [u16(m) for m in micros])
+    for divisor in (1.0, 3.0):
+        z.accumulate_norm(pb.plan, pb.grad, micros, pb.ws, pb.nout, overwrite_first=True, divisor=divisor)
+        got = z.read_norm(pb.nout)
+        exp = ref.copy()
+        if divisor != 1.0:
+            oracle.divide(exp, divisor)
+        assert np.array_equal(pb.grad.cpu().numpy().view(np.uint32), exp.view(np.uint32)), divisor
+        # the same gradient through the separate norm call: identical record
+        nout2 = z.new_norm_out()
+        z.grad_norm(pb.plan, pb.grad, pb.ws, nout2)
+        assert z.read_norm(nout2)["sumsq"] == got["sumsq"]
+        s = oracle.sumsq(exp)
+        assert abs(got["sumsq"] - s) <= 1e-12 * s
+
+
 def test_norm_is_deterministic_and_extra_sumsq_adds():
     pb = Problem(_custom([16384 * 7 + 40, 9], [0, 1], K=1, steps=1, sigma=0.3))
     z.accumulate(pb.plan, pb.grad, pb.gen.micro_grads())

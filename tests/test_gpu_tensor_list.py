@@ -359,3 +359,26 @@ def test_list_calls_write_nothing_outside_the_shards(guard):
             eb = buf.element_size()
             head, tail = raw[:G * eb], raw[(G + mid.numel()) * eb:]
             assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), (name, i)
+
+
+@pytest.mark.parametrize("K", [2, 3, 5, 8, 9])
+@pytest.mark.parametrize("misaligned", [False, True])
+def test_k_way_list_pass_matches_the_oracle(K, misaligned):
+    """All K micro-batch lists in one list_accumulate_norm call (the K-specialised kernels for
+    K <= 8, the general one above), and in one list_accumulate call, aligned and misaligned."""
+    pb = ListProblem(NUMELS, NO_DECAY, misaligned=misaligned, seed=20 + K, sigma=0.3)
+    micros = [pb.micro_like(pb.micro()) for _ in range(K)]
+    G = np.zeros(int(pb.counts.sum()), np.float32)
+    for k, mb in enumerate(micros):
+        oracle.accumulate(G, u16(pb.flat(mb)), overwrite=(k == 0))
+    pl = z.PointerLists(pb.opt.plan, micros, torch.bfloat16)
+    z.list_accumulate_norm(pb.opt.plan, pb.opt.table, pb.opt._lists["grad"], pl, pb.opt.workspace, pb.opt.norm_out,
+                           overwrite_first=True, divisor=2.0)
+    got = pb.opt.read_norm()
+    Gd = G.copy()
+    oracle.divide(Gd, 2.0)
+    assert _eq(pb.flat(pb.grad).numpy(), Gd)
+    ref = oracle.sumsq(Gd)
+    assert abs(got["sumsq"] - ref) <= 1e-12 * ref
+    z.list_accumulate(pb.opt.plan, pb.opt.table, pb.opt._lists["grad"], pl, overwrite_first=True)
+    assert _eq(pb.flat(pb.grad).numpy(), G)

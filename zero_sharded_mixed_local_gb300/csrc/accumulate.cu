@@ -141,6 +141,66 @@ __global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 5 : 1)
     if (threadIdx.x == 0) partials[tile] = make_float2(sq.s[0], sq.c[0]);
 }
 
+// K micro-batches already resident (2 <= K <= 8), grad overwritten: one pass
+// reads the K bf16 arenas and writes the fp32 sum, grad = ((m0 + m1) + m2) +
+// ..., the additions of K separate calls in the same order, and adds the
+// squares with the tile mapping above.  All K 16-byte loads of a vector go out
+// before its additions (K is a template parameter, so nothing waits on a
+// runtime-bounded loop); two vectors at a time for K <= 4.  The minimum of one
+// block per SM in the launch bounds matters: without it ptxas held the kernel
+// to 40 registers, too few to keep K loads in flight (K = 8 on the 213.9M-
+// element shard: 0.70 ms at 40 registers, 0.594 ms = 7.2 TB/s at 76).  The
+// division by the world size is a template parameter, so the plain sum
+// carries no division code.
+template <int K, bool kDivide>
+__global__ void __launch_bounds__(kTileThreads, 1)
+    accumulate_norm_kway_kernel(const __grid_constant__ AccumulateParams P, float2* __restrict__ partials,
+                                int64_t first_tile) {
+    constexpr int kUnroll = K <= 4 ? 2 : 1;
+    __shared__ float2 s_warp[kTileThreads / 32];
+    const int64_t tile = first_tile + blockIdx.x;
+    const int64_t v0 = tile * kVecsPerTile;
+    const int64_t nv = P.n_vec - v0 < kVecsPerTile ? P.n_vec - v0 : kVecsPerTile;
+    SquarePairs sq;
+#pragma unroll kUnroll
+    for (int r = 0; r < kVecsPerThread; ++r) {
+        const int v = threadIdx.x + r * kTileThreads;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (v < nv) {
+            uint4 raw[K];
+#pragma unroll
+            for (int k = 0; k < K; ++k) raw[k] = reinterpret_cast<const uint4*>(P.micro[k])[v0 + v];
+            widen8(raw[0], acc);
+#pragma unroll
+            for (int k = 1; k < K; ++k) {
+                float f[8];
+                widen8(raw[k], f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], f[j]);
+            }
+            if (kDivide) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = __fdiv_rn(acc[j], P.divisor);
+            }
+            float4* g4 = reinterpret_cast<float4*>(P.grad) + 2 * (v0 + v);
+            g4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            g4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        sq.add_vec(make_float4(acc[0], acc[1], acc[2], acc[3]), make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+    sq.fold();
+    block_pair_sum<kTileThreads>(sq.s[0], sq.c[0], s_warp);
+    if (threadIdx.x == 0) partials[tile] = make_float2(sq.s[0], sq.c[0]);
+}
+
+template <int K>
+void launch_kway(const AccumulateParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
+    if (p.divide)
+        accumulate_norm_kway_kernel<K, true><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
+    else
+        accumulate_norm_kway_kernel<K, false><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
+}
+
 }  // namespace
 
 cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, int64_t n_tiles, double extra_sumsq,
@@ -148,10 +208,19 @@ cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, 
     float2* pairs = reinterpret_cast<float2*>(partials);
     for (int64_t first = 0; first < n_tiles; first += 0x7fffffff) {
         const int64_t nb = n_tiles - first < 0x7fffffff ? n_tiles - first : 0x7fffffff;
-        if (p.overwrite_first && p.n_micro == 1)
-            accumulate_norm_kernel<true><<<static_cast<unsigned>(nb), kTileThreads, 0, stream>>>(p, pairs, first);
-        else
-            accumulate_norm_kernel<false><<<static_cast<unsigned>(nb), kTileThreads, 0, stream>>>(p, pairs, first);
+        const unsigned g = static_cast<unsigned>(nb);
+        const int kway = p.overwrite_first ? p.n_micro : 0;
+        switch (kway) {
+            case 1: accumulate_norm_kernel<true><<<g, kTileThreads, 0, stream>>>(p, pairs, first); break;
+            case 2: launch_kway<2>(p, g, pairs, first, stream); break;
+            case 3: launch_kway<3>(p, g, pairs, first, stream); break;
+            case 4: launch_kway<4>(p, g, pairs, first, stream); break;
+            case 5: launch_kway<5>(p, g, pairs, first, stream); break;
+            case 6: launch_kway<6>(p, g, pairs, first, stream); break;
+            case 7: launch_kway<7>(p, g, pairs, first, stream); break;
+            case 8: launch_kway<8>(p, g, pairs, first, stream); break;
+            default: accumulate_norm_kernel<false><<<g, kTileThreads, 0, stream>>>(p, pairs, first);
+        }
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

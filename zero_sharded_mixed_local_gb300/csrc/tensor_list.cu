@@ -97,21 +97,27 @@ __device__ __forceinline__ bool run_in_range(const ListChunk& ch, int32_t n_tens
 // (as zero1_grad_norm).  One block per run, thread t owning vectors t + 256r
 // (r = 0..7, the norm's fixed order).  Every thread reads the run descriptor
 // and its buffers' addresses itself (broadcast loads through L1), so nothing
-// waits on a barrier before the data loads go out.  A full aligned run with one
-// micro-batch issues its loads two vectors at a time ahead of the arithmetic;
-// other runs take the element-wise-capable loop.  A run whose list entry is
+// waits on a barrier before the data loads go out.  A run whose list entry is
 // NULL is skipped (the upload call rejects such lists).
 //
-// kOneOverwrite (grad = the one micro-batch): 6 blocks per SM (registers capped
-// at 40, a few spilled).  Measured on the 1.0B-element shard, fused pass: 0.933
-// ms, against 0.978 ms for batches of four at 5 blocks, 1.001 ms uncapped and
+// kK = 0 handles any micro-batch count and either overwrite mode, through the
+// element-wise-capable loop (or, for one micro-batch or the norm alone, a full
+// aligned run's loads two vectors ahead).  kK = 1..8 is the overwriting pass
+// over exactly kK micro-batches: their addresses stay in registers and a full
+// aligned run issues all kK loads of a vector (of two vectors, for kK <= 4)
+// before the additions, which run in micro-batch order as in kK separate calls.
+//
+// kK = 1 (grad = the one micro-batch): 6 blocks per SM (registers capped at 40,
+// a few spilled).  Measured on the 1.0B-element shard, fused pass: 0.911 ms,
+// against 0.978 ms for batches of four at 5 blocks, 1.001 ms uncapped and
 // 0.985 ms for a shared-memory prologue behind a barrier.
-template <ListGradMode kMode, bool kOneOverwrite>
-__global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 6 : 4)
+template <ListGradMode kMode, int kK>
+__global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
     list_grad_kernel(const __grid_constant__ ListParams P, float2* __restrict__ partials, int64_t first_chunk) {
     constexpr bool kReadsMicro = kMode != ListGradMode::kNorm;
     constexpr bool kSumsSquares = kMode != ListGradMode::kAccumulate;
     constexpr int kBatch = 2;
+    constexpr int kSlots = kK > 0 ? kK : 1;
     __shared__ float2 s_warp[kTileThreads / 32];
     const int64_t c = first_chunk + blockIdx.x;
     const ListChunk ch = P.table[c];
@@ -122,12 +128,24 @@ __global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 6 : 4)
     float* grad = P.grad[ch.tensor];
     bool missing = grad == nullptr, unaligned = false;
     const uint16_t* micro0 = nullptr;
+    const uint16_t* mp[kSlots];
     if (kReadsMicro) {
-        for (int k = 0; k < P.n_micro; ++k) {
-            const uint16_t* mk = P.micro[static_cast<int64_t>(k) * P.n_tensors + ch.tensor];
-            missing |= mk == nullptr;
-            if (mk != nullptr) unaligned |= misaligned16(mk + ch.offset);
-            if (k == 0 && mk != nullptr) micro0 = mk + ch.offset;
+        if (kK > 0) {
+#pragma unroll
+            for (int k = 0; k < kSlots; ++k) {
+                const uint16_t* mk = P.micro[static_cast<int64_t>(k) * P.n_tensors + ch.tensor];
+                missing |= mk == nullptr;
+                mp[k] = mk != nullptr ? mk + ch.offset : nullptr;
+                unaligned |= misaligned16(mp[k]);
+            }
+            micro0 = mp[0];
+        } else {
+            for (int k = 0; k < P.n_micro; ++k) {
+                const uint16_t* mk = P.micro[static_cast<int64_t>(k) * P.n_tensors + ch.tensor];
+                missing |= mk == nullptr;
+                if (mk != nullptr) unaligned |= misaligned16(mk + ch.offset);
+                if (k == 0 && mk != nullptr) micro0 = mk + ch.offset;
+            }
         }
     }
     if (missing) {  // the same for every thread of the block
@@ -137,11 +155,38 @@ __global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 6 : 4)
     grad += ch.offset;
     unaligned |= misaligned16(grad);
     const int len = ch.len;
-    const bool overwrite = kOneOverwrite || (kReadsMicro && P.overwrite_first);
+    const bool overwrite = kK > 0 || (kReadsMicro && P.overwrite_first);
     const bool divide = kMode == ListGradMode::kAccumulateNorm && P.divide;
+    const bool full = !unaligned && len == kNormTile;
 
     SquarePairs sq;
-    if (!unaligned && len == kNormTile && (kMode == ListGradMode::kNorm || P.n_micro == 1)) {
+    if (kK >= 2 && full) {
+        constexpr int kUnroll = kK <= 4 ? 2 : 1;
+#pragma unroll kUnroll
+        for (int r = 0; r < kVecsPerThread; ++r) {
+            const int v = threadIdx.x + r * kTileThreads;
+            uint4 raw[kSlots];
+#pragma unroll
+            for (int k = 0; k < kSlots; ++k) raw[k] = reinterpret_cast<const uint4*>(mp[k])[v];
+            float acc[8];
+            widen8(raw[0], acc);
+#pragma unroll
+            for (int k = 1; k < kSlots; ++k) {
+                float f[8];
+                widen8(raw[k], f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], f[j]);
+            }
+            if (divide) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = __fdiv_rn(acc[j], P.divisor);
+            }
+            reinterpret_cast<float4*>(grad)[2 * v] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            reinterpret_cast<float4*>(grad)[2 * v + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (kSumsSquares)
+                sq.add_vec(make_float4(acc[0], acc[1], acc[2], acc[3]), make_float4(acc[4], acc[5], acc[6], acc[7]));
+        }
+    } else if (kK <= 1 && full && (kMode == ListGradMode::kNorm || P.n_micro == 1)) {
 #pragma unroll
         for (int h = 0; h < kVecsPerThread / kBatch; ++h) {
             uint4 raw[kBatch];
@@ -314,13 +359,29 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
 
 namespace {
 
+template <ListGradMode kMode, int kK>
+void launch_k(const ListParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
+    list_grad_kernel<kMode, kK><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
+}
+
 template <ListGradMode kMode>
 cudaError_t launch_grad_mode(const ListParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
-    const bool one_overwrite = kMode != ListGradMode::kNorm && p.overwrite_first && p.n_micro == 1;
-    if (one_overwrite)
-        list_grad_kernel<kMode, true><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
-    else
-        list_grad_kernel<kMode, false><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
+    if constexpr (kMode == ListGradMode::kNorm) {
+        launch_k<kMode, 0>(p, nb, pairs, first, stream);
+    } else {
+        // the micro-batch count, when the pass overwrites the gradient with their sum
+        switch (p.overwrite_first ? p.n_micro : 0) {
+            case 1: launch_k<kMode, 1>(p, nb, pairs, first, stream); break;
+            case 2: launch_k<kMode, 2>(p, nb, pairs, first, stream); break;
+            case 3: launch_k<kMode, 3>(p, nb, pairs, first, stream); break;
+            case 4: launch_k<kMode, 4>(p, nb, pairs, first, stream); break;
+            case 5: launch_k<kMode, 5>(p, nb, pairs, first, stream); break;
+            case 6: launch_k<kMode, 6>(p, nb, pairs, first, stream); break;
+            case 7: launch_k<kMode, 7>(p, nb, pairs, first, stream); break;
+            case 8: launch_k<kMode, 8>(p, nb, pairs, first, stream); break;
+            default: launch_k<kMode, 0>(p, nb, pairs, first, stream);
+        }
+    }
     return cudaGetLastError();
 }
 
