@@ -327,6 +327,10 @@ def main():
     ap.add_argument("--k-way", action="store_true",
                     help="accumulate all K micro-batch gradients (already resident) in one fused pass with the "
                          "norm, instead of one call per micro-batch as they arrive")
+    ap.add_argument("--exchange", action="store_true",
+                    help="add the copies around the local step: pack the last micro-batch's reduce-scatter input "
+                         "from a model-layout bf16 gradient (zero1_shard_gather) and unpack the bf16 weights into "
+                         "the model layout (zero1_shard_scatter)")
     ap.add_argument("--micro-batches", type=int, default=None,
                     help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
     args = ap.parse_args()
@@ -420,6 +424,10 @@ def main():
             return one_list_step(record)
         t_counter[0] += 1
         if record is not None:
+            record["x0"].record(stream)
+        if full_g is not None:  # pack: this rank's chunk of the reduce-scatter input
+            z.shard_gather(plan, full_g, micros[K - 1], stream=stream)
+        if record is not None:
             record["a0"].record(stream)
         for k in range(0 if args.k_way else K - 1):
             z.accumulate(plan, grad, micros[k], overwrite_first=(k == 0), stream=stream)
@@ -440,9 +448,22 @@ def main():
         z.step(plan, master, m, v, grad, wbf, hp, t_counter[0], nout, stream=stream)
         if record is not None:
             record["s1"].record(stream)
+        if full_w is not None:  # unpack: the bf16 weights into the model layout
+            z.shard_scatter(plan, wbf, full_w, stream=stream)
+        if record is not None:
+            record["x1"].record(stream)
 
     if args.k_way and (args.unfused or args.graph):
         raise SystemExit("--k-way runs the fused eager calls")
+    full_g = full_w = None
+    if args.exchange:
+        if lists is not None or args.graph:
+            raise SystemExit("--exchange runs the arena calls eagerly")
+        args.no_e2e = True
+        # the model-layout gradient holds this rank's shard values where the plan puts them
+        full_g = torch.zeros(plan.total_numel, dtype=torch.bfloat16, device=dev)
+        full_w = torch.zeros(plan.total_numel, dtype=torch.bfloat16, device=dev)
+        z.shard_scatter(plan, micros[K - 1], full_g)
     sgraph = None
     if args.graph:
         if world > 1:
@@ -467,7 +488,7 @@ def main():
     visible = [d for d in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if d.strip()]
     clocks = ClockSampler(visible[local].strip() if local < len(visible) else local)  # index or UUID
     clocks.start()
-    recs = [{k: ev() for k in ("a0", "n0", "s0", "s1")} for _ in range(args.steps)]
+    recs = [{k: ev() for k in ("x0", "a0", "n0", "s0", "s1", "x1")} for _ in range(args.steps)]
     start, end = ev(), ev()
     torch.cuda.synchronize()
     barrier(world)
@@ -489,13 +510,21 @@ def main():
         step_ms = statistics.mean(r["s0"].elapsed_time(r["s1"]) for r in recs)
     else:  # one graph launch per step: no per-kernel events inside it
         acc_ms = accnorm_ms = step_ms = float("nan")
+    exchange = None
+    if full_g is not None:  # the layout copies move 2 + 2 bytes per local element each
+        pack_ms = statistics.mean(r["x0"].elapsed_time(r["a0"]) for r in recs)
+        unpack_ms = statistics.mean(r["s1"].elapsed_time(r["x1"]) for r in recs)
+        exchange = {"shard_gather": {"ms": pack_ms, "gbs": 4 * P / (pack_ms * 1e-3) / 1e9, "launches_per_step": 1},
+                    "shard_scatter": {"ms": unpack_ms, "gbs": 4 * P / (unpack_ms * 1e-3) / 1e9,
+                                      "launches_per_step": 1}}
     z.read_norm(nout, stream)
 
     peak, peak_kind = measured_peaks()
     step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9 if sgraph is None else None
     # fused: the norm rides on the last micro-batch's pass (no separate 4-byte read)
     norm_bytes = 4 * P if args.unfused else 0
-    path_bytes = (accumulate_bytes_per_elem(K, args.k_way) + STEP_BYTES_PER_ELEM) * P + norm_bytes
+    path_bytes = (accumulate_bytes_per_elem(K, args.k_way) + STEP_BYTES_PER_ELEM) * P + norm_bytes + \
+        (8 * P if full_g is not None else 0)
     last_bytes = accumulate_bytes_per_elem(K, True) * P if args.k_way else (6 if K == 1 else 10) * P + norm_bytes
     step_kernel = "list_step" if lists is not None else "adamw_step"
     traffic = profile_traffic(step_kernel, args.workload)
@@ -618,6 +647,8 @@ def main():
                 "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
                 "accumulate": ("all K micro-batches in one pass (K-way)" if args.k_way
                                else "one call per micro-batch, as they arrive"),
+                "exchange": ("pack the reduce-scatter input and unpack the bf16 weights, model layout <-> arena"
+                             if full_g is not None else "none (the local step only)"),
                 "launch": "one CUDA graph per step (StepGraph)" if sgraph is not None else "eager calls",
                 "layout": ("tensor lists: one allocation per tensor shard, a 16384-element run table"
                            if lists is not None else "arenas: one padded buffer per quantity"),
@@ -632,6 +663,7 @@ def main():
                     "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
                     "launches_per_step": 3 if args.unfused else 2},
                 step_kernel: {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
+                **(exchange or {}),
             }) if sgraph is None else None,
             "roofline": ({"bound": "hbm", "kernel": step_kernel + "_kernel", "achieved": step_gbs, "peak": peak,
                          "unit": "GB/s", "frac": step_gbs / peak, "traffic": traffic,
@@ -640,7 +672,8 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "gpu_launches": args.steps * ((3 if args.k_way else K + 2) + (1 if args.unfused else 0)),  # also in graphs
+            "gpu_launches": args.steps * ((3 if args.k_way else K + 2) + (1 if args.unfused else 0) +
+                                          (2 if full_g is not None else 0)),  # also inside each graph
         }
         print(json.dumps(out), flush=True)
     if world > 1:
