@@ -180,3 +180,23 @@ def test_module_optimizer_steps_only_its_slice():
         rest = torch.cat([p.detach().view(-1)[:s], p.detach().view(-1)[s + c:]])
         rest_b = torch.cat([b.view(-1)[:s], b.view(-1)[s + c:]])
         assert torch.equal(rest, rest_b)
+
+
+def test_module_optimizer_follows_reallocated_gradients():
+    """zero_grad(set_to_none=True) makes autograd allocate new gradient tensors every step;
+    the optimizer must read the new ones (its cached pointer lists are keyed on them), and
+    give the same parameters as a run that keeps the gradient buffers."""
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip_grad=1.0)
+    runs = []
+    for set_to_none in (False, True):
+        model = _model(4).to(torch.bfloat16)
+        opt = z.Zero1AdamW(model.named_parameters(), hparams=hp)
+        g = torch.Generator(device="cuda").manual_seed(9)
+        for step in range(4):
+            model.zero_grad(set_to_none=set_to_none)
+            x = torch.randn(32, 64, device="cuda", generator=g)
+            model(x.bfloat16()).float().pow(2).mean().backward()
+            opt.step()
+        runs.append([p.detach().clone() for p in model.parameters()])
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)

@@ -181,8 +181,9 @@ class ShardListAdamW:
     tensors, one per parameter (model order, each exactly its shard's length); pass
     your own (for instance the fp32 state a framework already keeps per parameter) or
     let the constructor allocate zeroed ones.  Micro-batch gradients are lists of bf16
-    shard tensors; their device pointer lists are cached by (address, length) of every
-    tensor, so a loop that reuses the same gradient buffers uploads them once."""
+    shard tensors, whose device pointer lists are cached by (address, length) of every
+    tensor, so a loop that reuses the same gradient buffers uploads them once; or a
+    PointerLists the caller built once."""
 
     def __init__(self, numels, no_decay=None, dp_size=1, dp_rank=0, hparams=None, device="cuda", master=None,
                  exp_avg=None, exp_avg_sq=None, grad=None, weight_bf16=None, groups=None, lr_scale=None,
@@ -211,12 +212,13 @@ class ShardListAdamW:
         self._norm_ready = False
 
     def _micro_lists(self, micro):
+        if isinstance(micro, PointerLists):
+            return micro
         if len(micro) and isinstance(micro[0], torch.Tensor):
             micro = [micro]
-        # A cached list stays valid for any tensors at the same addresses with the same
-        # lengths (what the upload checked); it keeps no reference to them.
-        key = tuple(tuple((t.data_ptr(), t.numel(), t.dtype, t.device, t.is_contiguous()) for t in lst)
-                    for lst in micro)
+        # A cached upload stays valid for tensors at the same addresses with the same lengths
+        # (what the upload checked); it keeps no reference to them.
+        key = tuple(tuple((t.data_ptr(), t.numel()) for t in lst) for lst in micro)
         pl = self._micro_cache.get(key)
         if pl is None:
             if len(self._micro_cache) >= 8:
@@ -225,7 +227,8 @@ class ShardListAdamW:
         return pl
 
     def accumulate(self, micro, last=False, extra_sumsq=0.0, divisor=1.0, stream=None):
-        """Add one micro-batch (a list of bf16 shard tensors) or several (a list of such lists)."""
+        """Add one micro-batch (a list of bf16 shard tensors), several (a list of such lists), or
+        a PointerLists built for them once (no per-call host work)."""
         pl = self._micro_lists(micro)
         first = self._micro_seen == 0
         if last:
@@ -305,6 +308,8 @@ class Zero1AdamW:
                                   master=master, weight_bf16=weights)
         self.no_decay = flags
         self._pending = 0
+        self._grad_ident = None
+        self._grad_pl = None
 
     @property
     def hparams(self) -> Hparams:
@@ -314,27 +319,36 @@ class Zero1AdamW:
     def t(self):
         return self.opt.t
 
-    def _grad_views(self):
+    def _grad_lists(self):
+        """Device pointer lists of every parameter's gradient slice.  Slicing thousands of
+        gradients costs the host milliseconds per call, so the lists are reused while every
+        p.grad is the same tensor at the same address."""
+        grads = [p.grad for _, p in self.named]
+        ident = [(id(g), g.data_ptr() if g is not None else 0) for g in grads]
+        if ident == self._grad_ident and self._grad_pl is not None:
+            return self._grad_pl
         views = []
-        for (n, p), (s, c) in zip(self.named, self._slices):
-            g = p.grad
+        for (n, p), g, (s, c) in zip(self.named, grads, self._slices):
             if g is None:
                 raise ValueError("parameter %s has no gradient" % n)
             if g.dtype != torch.bfloat16 or not g.is_contiguous():
                 raise ValueError("gradient of %s must be contiguous bf16" % n)
             views.append(g.view(-1)[s:s + c])
-        return views
+        # no reference kept: the identity check above decides whether the addresses still hold
+        self._grad_pl = PointerLists(self.opt.plan, views, torch.bfloat16, self.device, keep=False)
+        self._grad_ident = ident
+        return self._grad_pl
 
     def accumulate(self, last=False, stream=None):
         """Add every parameter's current bf16 gradient slice into the fp32 accumulator."""
-        self.opt.accumulate(self._grad_views(), last=last, stream=stream)
+        self.opt.accumulate(self._grad_lists(), last=last, stream=stream)
         self._pending += 1
 
     def step(self, lr=None, group=None, stream=None):
         """Clip + AdamW on this rank's slices; the bf16 weights land in the model's parameters.
         ``group``: a torch.distributed group whose ranks' sums of squares make the global norm."""
         if self._pending == 0:
-            self.opt.accumulate(self._grad_views(), last=True, stream=stream)
+            self.opt.accumulate(self._grad_lists(), last=True, stream=stream)
         self.opt.step(lr=lr, group=group, stream=stream)
         self._pending = 0
 
