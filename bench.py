@@ -370,26 +370,28 @@ def main():
     if world > 1:
         import torch.distributed as dist
         group = dist.group.WORLD
-    lists = None
+    lists = lopt = None
     if args.tensor_list:
-        if args.graph or args.unfused:
-            raise SystemExit("--tensor-list runs the fused eager calls")
+        if args.unfused:
+            raise SystemExit("--tensor-list runs the fused calls")
         args.no_e2e = True  # the end-to-end leg stages arenas
         # one allocation per tensor shard, as a framework holds per-parameter state, filled
         # from the generated arenas (which are then freed) and reached through pointer lists
         def split(buf):
             return [t.clone() for t in plan.shard_views(buf)]
 
-        lists = {name: z.PointerLists(plan, split(buf), torch.float32, dev)
-                 for name, buf in (("master", master), ("m", m), ("v", v), ("grad", grad))}
-        lists["w"] = z.PointerLists(plan, split(wbf), torch.bfloat16, dev)
+        lopt = z.ShardListAdamW(w.params.numels, w.params.no_decay, w.dp_size, dp_rank, hparams=hp, device=dev,
+                                master=split(master), exp_avg=split(m), exp_avg_sq=split(v), grad=split(grad),
+                                weight_bf16=split(wbf))
+        lists = {"master": lopt._lists["master"], "m": lopt._lists["exp_avg"], "v": lopt._lists["exp_avg_sq"],
+                 "grad": lopt._lists["grad"], "w": lopt._lists["weight_bf16"]}
         micro_shards = [split(mb) for mb in micros]
         lists["micro"] = [z.PointerLists(plan, ms, torch.bfloat16, dev) for ms in micro_shards]
         lists["micro_all"] = z.PointerLists(plan, micro_shards, torch.bfloat16, dev)  # K lists back to back
-        del micro_shards
         master = m = v = grad = wbf = micros = None
         torch.cuda.empty_cache()
-        table, lws = plan.list_table(dev), plan.new_list_workspace(dev)
+        table, lws = lopt.table, lopt.workspace
+        lopt.norm_out = nout
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream(dev)
@@ -468,10 +470,13 @@ def main():
     if args.graph:
         if world > 1:
             raise SystemExit("--graph runs one rank (the captured step holds no all-reduce)")
-        from types import SimpleNamespace
-        state = SimpleNamespace(plan=plan, grad=grad, workspace=ws, norm_out=nout, master=master, exp_avg=m,
-                                exp_avg_sq=v, weight_bf16=wbf, hp=hp, t=0, device=dev)
-        sgraph = z.StepGraph(state, micros)
+        if lopt is not None:
+            sgraph = z.StepGraph(lopt, lists["micro"])
+        else:
+            from types import SimpleNamespace
+            state = SimpleNamespace(plan=plan, grad=grad, workspace=ws, norm_out=nout, master=master, exp_avg=m,
+                                    exp_avg_sq=v, weight_bf16=wbf, hp=hp, t=0, device=dev)
+            sgraph = z.StepGraph(state, micros)
 
         def one_step(record=None):  # noqa: F811  (the graph replaces the eager calls)
             if record is not None:

@@ -469,6 +469,17 @@ int zero1_list_step(const zero1_plan* plan, const void* d_table, float* const* d
                     uint16_t* const* d_weight_bf16, const zero1_hparams* hp, int64_t step_t,
                     const zero1_norm_out* d_norm, void* stream);
 
+/* zero1_list_step with the step's scalars read from DEVICE memory (d_scalars,
+ * 16-byte aligned, filled by zero1_step_scalars_fill) when the kernel runs, so
+ * a CUDA graph that captured the call can replay every step; the tensor-list
+ * counterpart of zero1_step_dev, with the same arithmetic and results as
+ * zero1_list_step.  The pages have no counterpart of this call.
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_step_dev(const zero1_plan* plan, const void* d_table, float* const* d_master,
+                        float* const* d_exp_avg, float* const* d_exp_avg_sq, const float* const* d_grad,
+                        uint16_t* const* d_weight_bf16, const zero1_step_scalars* d_scalars,
+                        const zero1_norm_out* d_norm, void* stream);
+
 /* ---- diagnostics --------------------------------------------------------- */
 
 /* Static description of a status code. */

@@ -1,6 +1,7 @@
-"""The local step captured as CUDA graphs (StepGraph over zero1_step_dev): the same
-results, bit for bit, as the eager calls, while the step count and the learning
-rate change between replays."""
+"""The local step captured as CUDA graphs (StepGraph over zero1_step_dev, and over
+zero1_list_step_dev for the tensor-list path): the same results, bit for bit, as
+the eager calls, while the step count and the learning rate change between
+replays."""
 import pytest
 import torch
 
@@ -82,3 +83,39 @@ def test_step_graph_replays_equal_eager_steps(K):
                  (graphed.grad, eager.grad)):
         assert torch.equal(_bits(a), _bits(b))
     assert graphed.read_norm() == eager.read_norm()
+
+
+@pytest.mark.parametrize("K", [1, 3])
+def test_step_graph_replays_the_tensor_list_path(K):
+    """StepGraph over a ShardListAdamW (zero1_list_step_dev): replays equal the eager list
+    calls bit for bit, with the learning rate changing every step."""
+    numels = [1000, 7, 4096, 33, 16385, 40000]
+    nd = [0, 1, 0, 1, 0, 0]
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip_grad=1.0)
+
+    def make():
+        opt = z.ShardListAdamW(numels, nd, dp_size=3, dp_rank=1, hparams=hp)
+        g = torch.Generator(device="cuda").manual_seed(11)
+        for t in opt.master:
+            t.normal_(0.0, 0.02, generator=g)
+        return opt
+
+    eager, graphed = make(), make()
+    counts = eager.plan.layout().counts
+    micro = [[torch.zeros(int(c), dtype=torch.bfloat16, device="cuda") for c in counts] for _ in range(K)]
+    sg = z.StepGraph(graphed, micro)
+    g = torch.Generator(device="cuda").manual_seed(12)
+    for step in range(4):
+        for mb in micro:
+            for t in mb:
+                t.copy_(torch.randn(t.numel(), device="cuda", generator=g) * 0.05)
+        lr = 1e-3 * (step + 1)
+        for k, mb in enumerate(micro):
+            eager.accumulate(mb, last=(k == K - 1))
+        eager.step(lr=lr)
+        sg.replay(lr=lr)
+    torch.cuda.synchronize()
+    assert graphed.t == eager.t == 4
+    for name in ("master", "exp_avg", "exp_avg_sq", "weight_bf16", "grad"):
+        for a, b in zip(getattr(eager, name), getattr(graphed, name)):
+            assert torch.equal(_bits(a), _bits(b)), name

@@ -106,6 +106,7 @@ def load_library(path=None):
                                                       vp, ctypes.c_size_t, vp, vp]),
         "zero1_list_grad_norm": (ctypes.c_int, [vp, vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
         "zero1_list_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
+        "zero1_list_step_dev": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "zero1_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "zero1_last_cuda_error": (ctypes.c_char_p, []),
     }
@@ -661,3 +662,19 @@ def list_step(plan, table, master: PointerLists, exp_avg: PointerLists, exp_avg_
     _check(lib.zero1_list_step(plan.handle, tp, master.ptr, exp_avg.ptr, exp_avg_sq.ptr, grads.ptr,
                                None if weight_bf16 is None else weight_bf16.ptr, ctypes.byref(hp._c()),
                                int(step_t), no, sp), "zero1_list_step")
+
+
+def list_step_dev(plan, table, master: PointerLists, exp_avg: PointerLists, exp_avg_sq: PointerLists,
+                  grads: PointerLists, weight_bf16, d_scalars, norm_out=None, stream=None):
+    """zero1_list_step_dev: list_step with the step scalars in device memory (``d_scalars``, a
+    CUDA uint8 tensor holding step_scalars() bytes), for CUDA-graph replay."""
+    lib = load_library()
+    dev = master.device
+    tp, sp = _list_args(plan, table, stream, dev)
+    sc = _ptr(d_scalars, torch.uint8, None, "d_scalars", dev)
+    if d_scalars.numel() < STEP_SCALARS_BYTES:
+        raise ValueError("d_scalars holds %d bytes, the step scalars need %d" % (d_scalars.numel(), STEP_SCALARS_BYTES))
+    no = None if norm_out is None else _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    _check(lib.zero1_list_step_dev(plan.handle, tp, master.ptr, exp_avg.ptr, exp_avg_sq.ptr, grads.ptr,
+                                   None if weight_bf16 is None else weight_bf16.ptr, sc, no, sp),
+           "zero1_list_step_dev")

@@ -402,14 +402,13 @@ extern "C" int zero1_list_grad_norm(const zero1_plan* plan, const void* d_table,
                              zero1::ListGradMode::kNorm, extra_sumsq, workspace, workspace_bytes, d_out, stream);
 }
 
-extern "C" int zero1_list_step(const zero1_plan* plan, const void* d_table, float* const* d_master,
-                               float* const* d_exp_avg, float* const* d_exp_avg_sq, const float* const* d_grad,
-                               uint16_t* const* d_weight_bf16, const zero1_hparams* hp, int64_t step_t,
-                               const zero1_norm_out* d_norm, void* stream) {
-    NvtxRange range("zero1_list_step");
-    zero1_step_scalars sc{};
-    const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
-    if (rc != ZERO1_OK) return rc;
+namespace {
+
+// Checks shared by zero1_list_step and zero1_list_step_dev, and the launch.
+int list_step_checked(const zero1_plan* plan, const void* d_table, float* const* d_master, float* const* d_exp_avg,
+                      float* const* d_exp_avg_sq, const float* const* d_grad, uint16_t* const* d_weight_bf16,
+                      const zero1_step_scalars* sc, const zero1_step_scalars* d_scalars,
+                      const zero1_norm_out* d_norm, void* stream) {
     const int64_t n_chunks = static_cast<int64_t>(plan->list_chunks.size());
     if (n_chunks == 0) return ZERO1_OK;  // nothing to do; empty lists may be NULL
     if (d_table == nullptr || d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr ||
@@ -429,7 +428,33 @@ extern "C" int zero1_list_step(const zero1_plan* plan, const void* d_table, floa
     p.w = d_weight_bf16;
     p.norm = d_norm;
     p.n_tensors = plan->n_tensors;
-    p.sc = sc;
+    if (sc != nullptr) p.sc = *sc;
+    p.dev_scalars = d_scalars;
     const cudaError_t e = zero1::launch_list_step(p, n_chunks, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int zero1_list_step(const zero1_plan* plan, const void* d_table, float* const* d_master,
+                               float* const* d_exp_avg, float* const* d_exp_avg_sq, const float* const* d_grad,
+                               uint16_t* const* d_weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                               const zero1_norm_out* d_norm, void* stream) {
+    NvtxRange range("zero1_list_step");
+    zero1_step_scalars sc{};
+    const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
+    if (rc != ZERO1_OK) return rc;
+    return list_step_checked(plan, d_table, d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_weight_bf16, &sc, nullptr,
+                             d_norm, stream);
+}
+
+extern "C" int zero1_list_step_dev(const zero1_plan* plan, const void* d_table, float* const* d_master,
+                                   float* const* d_exp_avg, float* const* d_exp_avg_sq, const float* const* d_grad,
+                                   uint16_t* const* d_weight_bf16, const zero1_step_scalars* d_scalars,
+                                   const zero1_norm_out* d_norm, void* stream) {
+    NvtxRange range("zero1_list_step_dev");
+    if (plan == nullptr || d_scalars == nullptr) return ZERO1_EINVAL;
+    if (!aligned16(d_scalars)) return ZERO1_EALIGN;
+    return list_step_checked(plan, d_table, d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_weight_bf16, nullptr,
+                             d_scalars, d_norm, stream);
 }

@@ -271,7 +271,9 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
     }
 }
 
-// Fused clip + AdamW + bf16 copy over the runs.  Each run is split into
+// Fused clip + AdamW + bf16 copy over the runs (kDevScalars: the step's
+// scalars are read from device memory by thread 0, next to the clip, as the
+// arena kernel does for CUDA-graph replay).  Each run is split into
 // kStepSubBlocks blocks of 4096 elements (no reduction here, so any mapping
 // works): thread t of sub-block s owns vectors 512s + t and 512s + t + 256.
 // Every thread reads the run descriptor and the five addresses itself and
@@ -284,10 +286,11 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
 constexpr int kStepSubBlocks = 4;
 constexpr int kStepVecsPerThread = kVecsPerThread / kStepSubBlocks;  // 2
 
-template <bool kWriteBf16>
+template <bool kWriteBf16, bool kDevScalars>
 __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid_constant__ ListParams P, int64_t first_block) {
     __shared__ float s_coef;
     __shared__ int s_skip;
+    __shared__ zero1_step_scalars s_sc;
     const int64_t b = first_block + blockIdx.x;
     const ListChunk ch = P.table[b / kStepSubBlocks];
     if (!run_in_range(ch, P.n_tensors)) return;  // the same for every thread of the block
@@ -321,9 +324,14 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
         load8(v + e0, n0, vec, vv);
     }
     if (threadIdx.x == 0) {
+        double clip = P.sc.clip;
+        if (kDevScalars) {
+            s_sc = *P.dev_scalars;
+            clip = s_sc.clip;
+        }
         float coef;
         int skip;
-        clip_from_norm(P.norm, P.sc.clip, coef, skip);
+        clip_from_norm(P.norm, clip, coef, skip);
         s_coef = coef;
         s_skip = skip;
     }
@@ -331,9 +339,10 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
     if (s_skip || e0 >= len) return;  // a non-finite gradient norm leaves every buffer as it is
 
     const float coef = s_coef;
-    const StepConsts sc{P.sc.b1, P.sc.b2, P.sc.omb1, P.sc.omb2, P.sc.eps, P.sc.sqrtbc2};
-    const float dfac = P.sc.dfac[ch.group];
-    const float stepsize = P.sc.stepsize[ch.group];
+    const zero1_step_scalars& S = kDevScalars ? s_sc : P.sc;
+    const StepConsts sc{S.b1, S.b2, S.omb1, S.omb2, S.eps, S.sqrtbc2};
+    const float dfac = S.dfac[ch.group];
+    const float stepsize = S.stepsize[ch.group];
 #pragma unroll 1
     for (int r = 0; r < kStepVecsPerThread; ++r) {
         const int e = 8 * (v0 + r * kTileThreads);
@@ -415,10 +424,16 @@ cudaError_t launch_list_step(const ListParams& p, int64_t n_chunks, cudaStream_t
     const int64_t n_blocks = n_chunks * kStepSubBlocks;
     for (int64_t first = 0; first < n_blocks; first += 0x7fffffff) {
         const unsigned nb = static_cast<unsigned>(n_blocks - first < 0x7fffffff ? n_blocks - first : 0x7fffffff);
-        if (p.w != nullptr)
-            list_step_kernel<true><<<nb, kTileThreads, 0, stream>>>(p, first);
-        else
-            list_step_kernel<false><<<nb, kTileThreads, 0, stream>>>(p, first);
+        if (p.dev_scalars != nullptr) {
+            if (p.w != nullptr)
+                list_step_kernel<true, true><<<nb, kTileThreads, 0, stream>>>(p, first);
+            else
+                list_step_kernel<false, true><<<nb, kTileThreads, 0, stream>>>(p, first);
+        } else if (p.w != nullptr) {
+            list_step_kernel<true, false><<<nb, kTileThreads, 0, stream>>>(p, first);
+        } else {
+            list_step_kernel<false, false><<<nb, kTileThreads, 0, stream>>>(p, first);
+        }
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

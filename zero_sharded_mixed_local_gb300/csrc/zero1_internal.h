@@ -113,7 +113,8 @@ struct ListParams {
     int32_t overwrite_first;
     int32_t divide;                // 0: plain sum (divisor unused)
     float divisor;
-    zero1_step_scalars sc;
+    zero1_step_scalars sc;                   // the step's scalars, at launch
+    const zero1_step_scalars* dev_scalars;   // or read from device memory when the kernel runs
 };
 
 // What list_grad passes do with the gradient runs.

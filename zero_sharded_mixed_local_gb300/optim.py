@@ -28,8 +28,8 @@ norm weights and biases).
 import torch
 
 from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, Hparams, list_accumulate,
-                      list_accumulate_norm, list_grad_norm, list_step, new_norm_out, Plan, PointerLists, read_norm,
-                      step, step_dev, step_scalars, STEP_SCALARS_BYTES)
+                      list_accumulate_norm, list_grad_norm, list_step, list_step_dev, new_norm_out, Plan,
+                      PointerLists, read_norm, step, step_dev, step_scalars, STEP_SCALARS_BYTES)
 
 
 class LocalShardAdamW:
@@ -107,25 +107,32 @@ class LocalShardAdamW:
 
 
 class StepGraph:
-    """The whole local step of a LocalShardAdamW captured as CUDA graphs.
+    """The whole local step of a LocalShardAdamW or a ShardListAdamW captured as CUDA graphs.
 
     One replay runs what accumulate(..., last=True) + step() launch: the
     accumulation of the micro-batch buffers given here (their contents at
-    replay time), the fused norm, and the AdamW pass.  The step's scalars
-    (which change with t and lr) are not baked into the graph: before each
-    replay the host writes them into a pinned buffer that a captured copy
-    moves to the device.  Two graphs over two pinned buffers alternate, so
-    the host may write step t+1's scalars while step t still runs; it waits
-    only for step t-1.  No collective is captured: use it where the sum of
-    squares needs no all-reduce (one rank, or a caller that all-reduces the
-    norm record in its own graph).
+    replay time), the fused norm, and the AdamW pass.  For a ShardListAdamW
+    each micro-batch is a list of per-tensor bf16 shard tensors or a
+    PointerLists; their pointer lists are uploaded here, before capture.  The
+    step's scalars (which change with t and lr) are not baked into the graph:
+    before each replay the host writes them into a pinned buffer that a
+    captured copy moves to the device.  Two graphs over two pinned buffers
+    alternate, so the host may write step t+1's scalars while step t still
+    runs; it waits only for step t-1.  No collective is captured: use it where
+    the sum of squares needs no all-reduce (one rank, or a caller that
+    all-reduces the norm record in its own graph).
     """
 
     def __init__(self, opt, micro_buffers):
         self.opt = opt
-        self.micro = list(micro_buffers)
-        if not self.micro:
+        self.lists = isinstance(opt, ShardListAdamW)
+        micro = list(micro_buffers)
+        if not micro:
             raise ValueError("at least one micro-batch buffer")
+        if self.lists:  # uploads cannot run inside a capture
+            micro = [m if isinstance(m, PointerLists) else PointerLists(opt.plan, m, torch.bfloat16, opt.device)
+                     for m in micro]
+        self.micro = micro
         dev = opt.device
         self.h = [torch.zeros(128, dtype=torch.uint8).pin_memory() for _ in range(2)]
         self.d = [torch.zeros(128, dtype=torch.uint8, device=dev) for _ in range(2)]
@@ -135,17 +142,31 @@ class StepGraph:
 
     def _warm_kernels(self, dev):
         # Load every kernel the graph uses (lazy module loading) on a throwaway one-tensor plan,
-        # so the capture itself launches nothing for the first time.
+        # with the same sequence of calls, so the capture itself launches nothing for the first time.
         tiny = Plan([16], [0])
-        a = [tiny.new_arena(torch.float32, dev) for _ in range(4)]
-        w = tiny.new_arena(torch.bfloat16, dev)
-        mbs = [tiny.new_arena(torch.bfloat16, dev) for _ in self.micro]
-        ws, nout = tiny.new_workspace(dev), new_norm_out(dev)
-        for k, mb in enumerate(mbs[:-1]):
-            accumulate(tiny, a[0], mb, overwrite_first=(k == 0))
-        accumulate_norm(tiny, a[0], mbs[-1], ws, nout, overwrite_first=(len(mbs) == 1))
         sc = torch.frombuffer(bytearray(step_scalars(tiny, self.opt.hp, 1)), dtype=torch.uint8).to(dev)
-        step_dev(tiny, a[1], a[2], a[3], a[0], w, sc, nout)
+        ws, nout = None, new_norm_out(dev)
+        if self.lists:
+            def one(dtype):
+                return [torch.zeros(16, dtype=dtype, device=dev)]
+            f32 = [PointerLists(tiny, one(torch.float32), torch.float32, dev) for _ in range(4)]
+            wl = PointerLists(tiny, one(torch.bfloat16), torch.bfloat16, dev)
+            mbs = [PointerLists(tiny, [one(torch.bfloat16) for _ in range(m.n_lists)], torch.bfloat16, dev)
+                   for m in self.micro]
+            table, ws = tiny.list_table(dev), tiny.new_list_workspace(dev)
+            for k, mb in enumerate(mbs[:-1]):
+                list_accumulate(tiny, table, f32[0], mb, overwrite_first=(k == 0))
+            list_accumulate_norm(tiny, table, f32[0], mbs[-1], ws, nout, overwrite_first=(len(mbs) == 1))
+            list_step_dev(tiny, table, f32[1], f32[2], f32[3], f32[0], wl, sc, nout)
+        else:
+            a = [tiny.new_arena(torch.float32, dev) for _ in range(4)]
+            w = tiny.new_arena(torch.bfloat16, dev)
+            mbs = [tiny.new_arena(torch.bfloat16, dev) for _ in self.micro]
+            ws = tiny.new_workspace(dev)
+            for k, mb in enumerate(mbs[:-1]):
+                accumulate(tiny, a[0], mb, overwrite_first=(k == 0))
+            accumulate_norm(tiny, a[0], mbs[-1], ws, nout, overwrite_first=(len(mbs) == 1))
+            step_dev(tiny, a[1], a[2], a[3], a[0], w, sc, nout)
         torch.cuda.synchronize(dev)
 
     def _capture(self, b):
@@ -153,11 +174,20 @@ class StepGraph:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.d[b].copy_(self.h[b], non_blocking=True)
-            for k, mb in enumerate(self.micro[:-1]):
-                accumulate(o.plan, o.grad, mb, overwrite_first=(k == 0))
-            accumulate_norm(o.plan, o.grad, self.micro[-1], o.workspace, o.norm_out,
-                            overwrite_first=(len(self.micro) == 1))
-            step_dev(o.plan, o.master, o.exp_avg, o.exp_avg_sq, o.grad, o.weight_bf16, self.d[b], o.norm_out)
+            if self.lists:
+                L = o._lists
+                for k, mb in enumerate(self.micro[:-1]):
+                    list_accumulate(o.plan, o.table, L["grad"], mb, overwrite_first=(k == 0))
+                list_accumulate_norm(o.plan, o.table, L["grad"], self.micro[-1], o.workspace, o.norm_out,
+                                     overwrite_first=(len(self.micro) == 1))
+                list_step_dev(o.plan, o.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"],
+                              L["weight_bf16"], self.d[b], o.norm_out)
+            else:
+                for k, mb in enumerate(self.micro[:-1]):
+                    accumulate(o.plan, o.grad, mb, overwrite_first=(k == 0))
+                accumulate_norm(o.plan, o.grad, self.micro[-1], o.workspace, o.norm_out,
+                                overwrite_first=(len(self.micro) == 1))
+                step_dev(o.plan, o.master, o.exp_avg, o.exp_avg_sq, o.grad, o.weight_bf16, self.d[b], o.norm_out)
         return g
 
     def replay(self, lr=None):
