@@ -280,8 +280,8 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
 // issues its first vector's loads before the block's one barrier, behind which
 // thread 0 derives the clip coefficient.  Registers are capped at 64 (4 blocks
 // per SM).  Measured per step on the 1.0B-element shard (separately allocated
-// tensors): 4.32 ms, against 4.38 ms for one block per run with the addresses
-// staged in shared memory behind a barrier; on the 20,000-tensor list 11.90 ms
+// tensors): 4.28 ms, against 4.38 ms for one block per run with the addresses
+// staged in shared memory behind a barrier; on the 20,000-tensor list 11.70 ms
 // against 11.99 ms.
 constexpr int kStepSubBlocks = 4;
 constexpr int kStepVecsPerThread = kVecsPerThread / kStepSubBlocks;  // 2
