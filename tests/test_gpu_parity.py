@@ -494,3 +494,48 @@ def test_data_parallel_average_emulated_on_one_gpu():
             z.shard_scatter(pl, st[key], full)
         z.shard_scatter(ref_plan, ref[key], ref_full)
         assert torch.equal(full.view(torch.int32), ref_full.view(torch.int32)), key
+
+
+def test_arena_beyond_2_to_32_elements():
+    """Maximum size: one tensor of 2^32 + 2^20 + 5 elements (dp 1; 86 GB resident) and a tiny
+    excluded one.  Every gradient element is 2^-8 (exact in bf16), so the sum of squares is
+    N * 2^-16 exactly; elements around 2^31, 2^32 and the tail are stepped by the oracle."""
+    n0 = (1 << 32) + (1 << 20) + 5
+    plan = z.Plan([n0, 3], [0, 1], 1, 0)
+    n, N = plan.arena_numel, plan.local_numel
+    dev = torch.device("cuda")
+    mb = torch.full((n,), 2.0 ** -8, dtype=torch.bfloat16, device=dev)
+    mb[n0:plan.group_range(1)[0]] = 0  # padding after tensor 0
+    mb[plan.group_range(1)[0] + 3:] = 0
+    g = torch.Generator(device=dev).manual_seed(3)
+    master = torch.zeros(n, dtype=torch.float32, device=dev)
+    master[:n0].normal_(0.0, 0.02, generator=g)
+    b1 = plan.group_range(1)[0]
+    master[b1:b1 + 3] = 1.0
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    grad = torch.empty_like(master)
+    wbf = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    ws, nout = plan.new_workspace(dev), z.new_norm_out(dev)
+    edges = [(1 << 31) - 12, (1 << 32) - 12, n0 - 12, b1]
+    idx = np.unique(np.concatenate([np.arange(e, e + 24) for e in edges] +
+                                   [np.random.default_rng(0).integers(0, n0, 100000)]))
+    idx = idx[(idx < n0) | ((idx >= b1) & (idx < b1 + 3))]
+    it = torch.from_numpy(idx).to(dev)
+    P0 = master[it].cpu().numpy().copy()
+    z.accumulate_norm(plan, grad, mb, ws, nout)
+    hp = dict(HP)
+    z.step(plan, master, m, v, grad, wbf, z.Hparams(**hp), 1, nout)
+    got = z.read_norm(nout)
+    assert got["status"] == 0
+    assert got["sumsq"] == N * 2.0 ** -16, (got["sumsq"], N * 2.0 ** -16)
+    G = grad[it].cpu().numpy()
+    assert np.all(G == np.float32(2.0 ** -8))
+    ok, norm, coef = oracle.clip_coef(N * 2.0 ** -16, hp["clip_grad"])
+    P, M, V = P0.copy(), np.zeros_like(P0), np.zeros_like(P0)
+    dec = int(np.sum(idx < n0))
+    oracle.adamw(P, M, V, G, [dec, idx.size - dec], [0, 1], hp, 1, coef)
+    for name, t, ref in (("master", master, P), ("m", m, M), ("v", v, V)):
+        assert np.array_equal(t[it].cpu().numpy().view(np.uint32), ref.view(np.uint32)), name
+    assert np.array_equal(u16(wbf[it]), oracle.bf16_rne(P))
+    del mb, master, m, v, grad, wbf
+    torch.cuda.empty_cache()

@@ -382,3 +382,44 @@ def test_k_way_list_pass_matches_the_oracle(K, misaligned):
     assert abs(got["sumsq"] - ref) <= 1e-12 * ref
     z.list_accumulate(pb.opt.plan, pb.opt.table, pb.opt._lists["grad"], pl, overwrite_first=True)
     assert _eq(pb.flat(pb.grad).numpy(), G)
+
+
+def test_list_tensor_beyond_2_to_32_elements():
+    """Maximum size through the list calls: one shard of 2^32 + 2^20 + 5 elements (run offsets
+    past 2^32) plus a 3-element excluded one, gradients all 2^-8, so the sum of squares is
+    N * 2^-16 exactly; elements around 2^31, 2^32 and the tail are stepped by the oracle."""
+    n0 = (1 << 32) + (1 << 20) + 5
+    plan = z.Plan([n0, 3], [0, 1], 1, 0)
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(4)
+    master = [torch.empty(n0, device=dev).normal_(0.0, 0.02, generator=g), torch.ones(3, device=dev)]
+    m = [torch.zeros(n0, device=dev), torch.zeros(3, device=dev)]
+    v = [torch.zeros(n0, device=dev), torch.zeros(3, device=dev)]
+    grad = [torch.empty(n0, device=dev), torch.empty(3, device=dev)]
+    w = [torch.zeros(n0, dtype=torch.bfloat16, device=dev), torch.zeros(3, dtype=torch.bfloat16, device=dev)]
+    mb = [torch.full((n0,), 2.0 ** -8, dtype=torch.bfloat16, device=dev),
+          torch.full((3,), 2.0 ** -8, dtype=torch.bfloat16, device=dev)]
+    idx = np.unique(np.concatenate([np.arange(e, e + 24) for e in ((1 << 31) - 12, (1 << 32) - 12, n0 - 24)] +
+                                   [np.random.default_rng(1).integers(0, n0, 100000)]))
+    it = torch.from_numpy(idx).to(dev)
+    P0 = np.concatenate([master[0][it].cpu().numpy(), master[1].cpu().numpy()])
+    L = [z.PointerLists(plan, x, torch.float32) for x in (master, m, v, grad)]
+    wl, ml = z.PointerLists(plan, w, torch.bfloat16), z.PointerLists(plan, mb, torch.bfloat16)
+    table, ws, nout = plan.list_table(), plan.new_list_workspace(), z.new_norm_out()
+    z.list_accumulate_norm(plan, table, L[3], ml, ws, nout)
+    z.list_step(plan, table, *L, wl, z.Hparams(**HP), 1, nout)
+    got = z.read_norm(nout)
+    N = n0 + 3
+    assert got["status"] == 0 and got["sumsq"] == N * 2.0 ** -16, got
+    G = np.concatenate([grad[0][it].cpu().numpy(), grad[1].cpu().numpy()])
+    assert np.all(G == np.float32(2.0 ** -8))
+    _, _, coef = oracle.clip_coef(N * 2.0 ** -16, HP["clip_grad"])
+    P, M, V = P0.copy(), np.zeros_like(P0), np.zeros_like(P0)
+    oracle.adamw(P, M, V, G, [idx.size, 3], [0, 1], HP, 1, coef)
+    for name, lst, ref in (("master", master, P), ("m", m, M), ("v", v, V)):
+        gotv = np.concatenate([lst[0][it].cpu().numpy(), lst[1].cpu().numpy()])
+        assert np.array_equal(gotv.view(np.uint32), ref.view(np.uint32)), name
+    wv = torch.cat([w[0][it], w[1]])
+    assert np.array_equal(u16(wv), oracle.bf16_rne(P))
+    del master, m, v, grad, w, mb, L, wl, ml
+    torch.cuda.empty_cache()
