@@ -332,3 +332,37 @@ def test_list_calls_reject_bad_arguments_before_any_launch(z):
                                None) == z.ZERO1_OK
     none = (ctypes.c_void_p * 2)(None, None)
     assert lib.zero1_list_ptrs_upload(empty.handle, none, 1, 4, None, 0, None) == z.ZERO1_EINVAL  # no destination
+
+
+def test_binding_signatures_match_the_header(z):
+    """Every declared entry point has ctypes argument types of the header's kinds and count
+    (pointer, int32, int64, size_t, double), so no argument is passed at the wrong width."""
+    src = ""
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src += open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+
+    def c_kind(a):
+        if "*" in a or "[" in a:
+            return "ptr"
+        for key, k in (("size_t", "size"), ("int64_t", "i64"), ("double", "f64"), ("int32_t", "i32")):
+            if key in a:
+                return k
+        return "i32" if re.match(r"(const\s+)?int\b", a) else a
+
+    def py_kind(t):
+        if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+            return "ptr"
+        return {ctypes.c_int32: "i32", ctypes.c_int64: "i64", ctypes.c_size_t: "size", ctypes.c_double: "f64"}.get(t, t)
+
+    lib = z.load_library()
+    checked = 0
+    for m in re.finditer(r"\b(zero1_\w+)\s*\(([^;]*?)\)\s*;", src, re.S):
+        name, args = m.group(1), m.group(2).strip()
+        args = [] if args in ("", "void") else [a.strip() for a in args.split(",")]
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None, name
+        assert [c_kind(a) for a in args] == [py_kind(t) for t in argtypes], name
+        checked += 1
+    assert checked == len(declared_functions())
