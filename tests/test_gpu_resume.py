@@ -81,3 +81,25 @@ def test_list_checkpoint_loads_into_arenas_at_another_dp(tmp_path):
     assert arena.load_checkpoint(str(tmp_path / "ck")) == 1
     for x, y in zip(_state(lst), _state(arena)):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("kind", ["arena", "list"])
+def test_skipped_step_keeps_the_step_count_with_check_finite(kind):
+    """A non-finite gradient skips the step on the device; with check_finite the step count
+    stays, so the next finite step is step 1 and equals a fresh optimizer's first step."""
+    a, b = _make(kind), _make(kind)
+    _init(a)
+    _init(b)
+    bad = _micro(a, 0)
+    if kind == "arena":
+        bad[0] = float("inf")
+    else:
+        bad[0][0] = float("inf")
+    a.accumulate(bad, last=True)
+    assert a.step(check_finite=True) is False and a.t == 0
+    a.accumulate(_micro(a, 1), last=True)
+    assert a.step(check_finite=True) is True and a.t == 1
+    b.accumulate(_micro(b, 1), last=True)
+    b.step()
+    for x, y in zip(_state(a), _state(b)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))

@@ -32,6 +32,15 @@ from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, 
                       PointerLists, read_norm, step, step_dev, step_scalars, STEP_SCALARS_BYTES)
 
 
+def _applied(opt, stream):
+    """Whether the step just launched applied (a finite global norm); a skipped step gives its
+    number back, so bias correction stays matched to the updates m and v received."""
+    if read_norm(opt.norm_out, stream=stream)["status"] == 0:
+        return True
+    opt.t -= 1
+    return False
+
+
 class LocalShardAdamW:
     """One data-parallel rank's ZeRO-1 optimizer shard, resident on one GPU.
 
@@ -71,12 +80,16 @@ class LocalShardAdamW:
         self._micro_seen += 1 if isinstance(micro, torch.Tensor) else len(micro)
         self._norm_ready = bool(last)
 
-    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None):
-        """Norm + clip + AdamW + bf16 copy; returns nothing (read_norm() syncs).
+    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None, check_finite=False):
+        """Norm + clip + AdamW + bf16 copy.
 
         The norm is taken here unless the last accumulate() already did.  With
         ``group`` (a torch.distributed process group of the data-parallel ranks)
-        the local sum of squares is all-reduced before the update."""
+        the local sum of squares is all-reduced before the update.  A non-finite
+        norm makes the kernel skip the update on the device; the step count ``t``
+        still advances unless ``check_finite`` is set, which synchronises, leaves
+        ``t`` unchanged for a skipped step and returns whether the step applied
+        (otherwise the call returns None without waiting)."""
         if not getattr(self, "_norm_ready", False):
             grad_norm(self.plan, self.grad, self.workspace, self.norm_out, extra_sumsq, stream=stream)
         self._norm_ready = False
@@ -87,6 +100,7 @@ class LocalShardAdamW:
         step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
              self.norm_out, stream=stream)
         self._micro_seen = 0
+        return _applied(self, stream) if check_finite else None
 
     def read_norm(self, stream=None):
         return read_norm(self.norm_out, stream=stream)
@@ -269,9 +283,9 @@ class ShardListAdamW:
         self._micro_seen += pl.n_lists
         self._norm_ready = bool(last)
 
-    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None):
+    def step(self, extra_sumsq=0.0, lr=None, group=None, stream=None, check_finite=False):
         """Norm (unless the last accumulate took it) + optional all-reduce of sumsq + clip +
-        AdamW + bf16 copy."""
+        AdamW + bf16 copy; ``check_finite`` as for LocalShardAdamW.step."""
         if not self._norm_ready:
             list_grad_norm(self.plan, self.table, self._lists["grad"], self.workspace, self.norm_out, extra_sumsq,
                            stream=stream)
@@ -284,6 +298,7 @@ class ShardListAdamW:
         list_step(self.plan, self.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], L["weight_bf16"],
                   hp, self.t, self.norm_out, stream=stream)
         self._micro_seen = 0
+        return _applied(self, stream) if check_finite else None
 
     def read_norm(self, stream=None):
         return read_norm(self.norm_out, stream=stream)
@@ -374,13 +389,15 @@ class Zero1AdamW:
         self.opt.accumulate(self._grad_lists(), last=last, stream=stream)
         self._pending += 1
 
-    def step(self, lr=None, group=None, stream=None):
+    def step(self, lr=None, group=None, stream=None, check_finite=False):
         """Clip + AdamW on this rank's slices; the bf16 weights land in the model's parameters.
-        ``group``: a torch.distributed group whose ranks' sums of squares make the global norm."""
+        ``group``: a torch.distributed group whose ranks' sums of squares make the global norm;
+        ``check_finite`` as for LocalShardAdamW.step."""
         if self._pending == 0:
             self.opt.accumulate(self._grad_lists(), last=True, stream=stream)
-        self.opt.step(lr=lr, group=group, stream=stream)
+        applied = self.opt.step(lr=lr, group=group, stream=stream, check_finite=check_finite)
         self._pending = 0
+        return applied
 
     def read_norm(self, stream=None):
         """The last step's gradient norm record (synchronises)."""
