@@ -61,6 +61,14 @@ def test_toy_full_parity():
     assert res["master"] <= MAX_ULP
 
 
+def test_toy_200_steps_every_element():
+    """A long run: 200 steps of the toy shard with fresh gradients every step (K = 2, clipping
+    decided anew each step); every arena element still equal to the oracle's at the end."""
+    res = run_parity("toy", steps=200, fresh_grads=True)
+    assert res["master"] == 0 and res["m"] == 0 and res["v"] == 0
+    assert res["compared"] == Problem("toy").n
+
+
 def test_toy_full_parity_unfused_calls():
     run_parity("toy", fused=False)
 
