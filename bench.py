@@ -306,7 +306,7 @@ def run_reference(args, w, world, rank):
 
 
 # ------------------------------------------------------------------ GPU
-def main():
+def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -322,8 +322,8 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="replay the step as a CUDA graph (StepGraph) instead of eager calls; one GPU only")
     ap.add_argument("--tensor-list", action="store_true",
-                    help="run the tensor-list calls (one pointer per tensor shard, a run table walked by the "
-                         "kernels) on per-tensor views of the same buffers, instead of the arena calls")
+                    help="run the tensor-list calls (one allocation per tensor shard, a run table walked by "
+                         "the kernels) instead of the arena calls")
     ap.add_argument("--k-way", action="store_true",
                     help="accumulate all K micro-batch gradients (already resident) in one fused pass with the "
                          "norm, instead of one call per micro-batch as they arrive")
@@ -334,291 +334,339 @@ def main():
     ap.add_argument("--micro-batches", type=int, default=None,
                     help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
     args = ap.parse_args()
+    if args.tensor_list and args.unfused:
+        raise SystemExit("--tensor-list runs the fused calls")
+    if args.k_way and (args.unfused or args.graph):
+        raise SystemExit("--k-way runs the fused eager calls")
+    if args.exchange and (args.tensor_list or args.graph):
+        raise SystemExit("--exchange runs the arena calls eagerly")
+    if args.tensor_list or args.exchange:
+        args.no_e2e = True  # the end-to-end leg stages arenas for the plain step
+    return args
 
-    from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout, get_workload
+
+EVENTS = ("x0", "a0", "n0", "s0", "s1", "x1")  # exchange in, accumulate, last pass, step, exchange out
+
+
+class StepBench:
+    """One rank's bench state: the plan, the buffers of the chosen layout and the step.
+
+    With N ranks each rank steps a different data-parallel shard of the same model
+    (weak scaling); the one exchange on the path is the all-reduce of the sum of
+    squares."""
+
+    def __init__(self, args, w, z, world, rank, local):
+        from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout
+        self.args, self.w, self.z, self.world = args, w, z, world
+        self.dev = dev = torch.device("cuda", local)
+        self.dp_rank = (w.dp_rank + rank) % w.dp_size if world > 1 else w.dp_rank
+        self.plan = plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, self.dp_rank)
+        L = plan.layout()
+        gen = InputGenerator(w, Layout(L.counts, L.offsets, L.no_decay, L.arena_numel), dev, seed=w.seed + rank)
+        self.P, self.K = plan.local_numel, w.micro_batches
+        self.master = gen.master()
+        self.m, self.v, self.grad = gen.zeros(), gen.zeros(), gen.zeros()
+        self.wbf = gen.zeros(torch.bfloat16)
+        self.micros = gen.micro_grads()
+        self.ws, self.nout = plan.new_workspace(dev), z.new_norm_out(dev)
+        self.hp = z.Hparams(**w.hp)
+        self.group = None
+        if world > 1:
+            import torch.distributed as dist
+            self.group = dist.group.WORLD
+        self.stream = torch.cuda.current_stream(dev)
+        self.t = 0
+        self.lists = self.lopt = None
+        if args.tensor_list:
+            self._to_tensor_lists()
+        self.full_g = self.full_w = None
+        if args.exchange:
+            # the model-layout gradient holds this rank's shard values where the plan puts them
+            self.full_g = torch.zeros(plan.total_numel, dtype=torch.bfloat16, device=dev)
+            self.full_w = torch.zeros(plan.total_numel, dtype=torch.bfloat16, device=dev)
+            z.shard_scatter(plan, self.micros[self.K - 1], self.full_g)
+        self.graph = None
+        if args.graph:
+            self._capture_graph()
+        torch.cuda.synchronize()
+
+    def _to_tensor_lists(self):
+        """One allocation per tensor shard, as a framework holds per-parameter state, filled from
+        the generated arenas (which are then freed) and reached through pointer lists."""
+        z, plan, dev = self.z, self.plan, self.dev
+
+        def split(buf):
+            return [t.clone() for t in plan.shard_views(buf)]
+
+        w = self.w
+        lopt = z.ShardListAdamW(w.params.numels, w.params.no_decay, w.dp_size, self.dp_rank, hparams=self.hp,
+                                device=dev, master=split(self.master), exp_avg=split(self.m),
+                                exp_avg_sq=split(self.v), grad=split(self.grad), weight_bf16=split(self.wbf))
+        L = lopt._lists
+        micro_shards = [split(mb) for mb in self.micros]
+        self.lists = {"master": L["master"], "m": L["exp_avg"], "v": L["exp_avg_sq"], "grad": L["grad"],
+                      "w": L["weight_bf16"],
+                      "micro": [z.PointerLists(plan, ms, torch.bfloat16, dev) for ms in micro_shards],
+                      "micro_all": z.PointerLists(plan, micro_shards, torch.bfloat16, dev)}  # K lists back to back
+        self.master = self.m = self.v = self.grad = self.wbf = self.micros = None
+        torch.cuda.empty_cache()
+        self.table, self.lws = lopt.table, lopt.workspace
+        lopt.norm_out = self.nout
+        self.lopt = lopt
+
+    def _capture_graph(self):
+        if self.world > 1:
+            raise SystemExit("--graph runs one rank (the captured step holds no all-reduce)")
+        if self.lopt is not None:
+            self.graph = self.z.StepGraph(self.lopt, self.lists["micro"])
+        else:
+            from types import SimpleNamespace
+            state = SimpleNamespace(plan=self.plan, grad=self.grad, workspace=self.ws, norm_out=self.nout,
+                                    master=self.master, exp_avg=self.m, exp_avg_sq=self.v, weight_bf16=self.wbf,
+                                    hp=self.hp, t=0, device=self.dev)
+            self.graph = self.z.StepGraph(state, self.micros)
+
+    @property
+    def step_kernel(self):
+        return "list_step" if self.lists is not None else "adamw_step"
+
+    def step(self, rec=None):
+        """One pass of the hot path; `rec` (a dict of CUDA events, EVENTS) brackets its parts."""
+        mark = (lambda k: rec[k].record(self.stream)) if rec is not None else (lambda k: None)
+        if self.graph is not None:  # one graph launch: no events inside it
+            mark("a0")
+            self.graph.replay()
+            mark("s1")
+        elif self.lists is not None:
+            self._list_step(mark)
+        else:
+            self._arena_step(mark)
+
+    def _list_step(self, mark):
+        z, a, K, L, s = self.z, self.args, self.K, self.lists, self.stream
+        self.t += 1
+        mark("a0")
+        for k in range(0 if a.k_way else K - 1):
+            z.list_accumulate(self.plan, self.table, L["grad"], L["micro"][k], overwrite_first=(k == 0), stream=s)
+        mark("n0")
+        if a.k_way:
+            z.list_accumulate_norm(self.plan, self.table, L["grad"], L["micro_all"], self.lws, self.nout,
+                                   overwrite_first=True, stream=s)
+        else:
+            z.list_accumulate_norm(self.plan, self.table, L["grad"], L["micro"][K - 1], self.lws, self.nout,
+                                   overwrite_first=(K == 1), stream=s)
+        if self.group is not None:
+            z.allreduce_sumsq_(self.nout, self.group)
+        mark("s0")
+        z.list_step(self.plan, self.table, L["master"], L["m"], L["v"], L["grad"], L["w"], self.hp, self.t,
+                    self.nout, stream=s)
+        mark("s1")
+
+    def _arena_step(self, mark):
+        z, a, K, s, plan = self.z, self.args, self.K, self.stream, self.plan
+        self.t += 1
+        mark("x0")
+        if self.full_g is not None:  # pack: this rank's chunk of the reduce-scatter input
+            z.shard_gather(plan, self.full_g, self.micros[K - 1], stream=s)
+        mark("a0")
+        for k in range(0 if a.k_way else K - 1):
+            z.accumulate(plan, self.grad, self.micros[k], overwrite_first=(k == 0), stream=s)
+        mark("n0")
+        if a.k_way:
+            z.accumulate_norm(plan, self.grad, self.micros, self.ws, self.nout, overwrite_first=True, stream=s)
+        elif a.unfused:
+            z.accumulate(plan, self.grad, self.micros[K - 1], overwrite_first=(K == 1), stream=s)
+            z.grad_norm(plan, self.grad, self.ws, self.nout, 0.0, stream=s)
+        else:  # the last micro-batch's accumulation also takes the gradient norm
+            z.accumulate_norm(plan, self.grad, self.micros[K - 1], self.ws, self.nout, overwrite_first=(K == 1),
+                              stream=s)
+        if self.group is not None:
+            z.allreduce_sumsq_(self.nout, self.group)
+        mark("s0")
+        z.step(plan, self.master, self.m, self.v, self.grad, self.wbf, self.hp, self.t, self.nout, stream=s)
+        mark("s1")
+        if self.full_w is not None:  # unpack: the bf16 weights into the model layout
+            z.shard_scatter(plan, self.wbf, self.full_w, stream=s)
+        mark("x1")
+
+    def launches_per_step(self):
+        a = self.args
+        return (3 if a.k_way else self.K + 2) + (1 if a.unfused else 0) + (2 if self.full_g is not None else 0)
+
+    def path_bytes(self):
+        """Algorithmic bytes of one step (padding excluded)."""
+        a, P = self.args, self.P
+        return ((accumulate_bytes_per_elem(self.K, a.k_way) + STEP_BYTES_PER_ELEM) * P + (4 * P if a.unfused else 0) +
+                (8 * P if self.full_g is not None else 0))
+
+
+def time_steps(b, args, world, local):
+    """W untimed steps, then K timed ones between barriers and synchronises, with the clocks
+    sampled meanwhile; returns (per-step event records, max-over-ranks ms, clock summary)."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    barrier(world)
+    visible = [d for d in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if d.strip()]
+    clocks = ClockSampler(visible[local].strip() if local < len(visible) else local)  # index or UUID
+    clocks.start()
+    recs = [{k: ev() for k in EVENTS} for _ in range(args.steps)]
+    start, end = ev(), ev()
+    torch.cuda.synchronize()
+    barrier(world)
+    start.record(b.stream)
+    for i in range(args.steps):
+        b.step(recs[i])
+    end.record(b.stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    return recs, max_over_ranks(start.elapsed_time(end), world), clk
+
+
+def kernel_report(b, recs, args):
+    """Per-kernel times (CUDA events around each part of the step) and their GB/s."""
+    if b.graph is not None:  # one graph launch per step: no per-kernel events inside it
+        return None, None
+    P, K = b.P, b.K
+    mean = lambda a, c: statistics.mean(r[a].elapsed_time(r[c]) for r in recs)  # noqa: E731
+    acc_ms, accnorm_ms, step_ms = mean("a0", "n0"), mean("n0", "s0"), mean("s0", "s1")
+    norm_bytes = 4 * P if args.unfused else 0
+    last_bytes = accumulate_bytes_per_elem(K, True) * P if args.k_way else (6 if K == 1 else 10) * P + norm_bytes
+    kernels = {
+        "accumulate": {"ms": acc_ms, "gbs": (accumulate_bytes_per_elem(K) * P - last_bytes) / (acc_ms * 1e-3) / 1e9
+                       if K > 1 and not args.k_way else None, "launches_per_step": 0 if args.k_way else K - 1},
+        ("accumulate+grad_norm" if args.unfused else "accumulate_norm"): {
+            "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
+            "launches_per_step": 3 if args.unfused else 2},
+        b.step_kernel: {"ms": step_ms, "gbs": STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9,
+                        "launches_per_step": 1},
+    }
+    if b.full_g is not None:  # the layout copies move 2 + 2 bytes per local element each
+        for name, (x, y) in (("shard_gather", ("x0", "a0")), ("shard_scatter", ("s1", "x1"))):
+            ms = mean(x, y)
+            kernels[name] = {"ms": ms, "gbs": 4 * P / (ms * 1e-3) / 1e9, "launches_per_step": 1}
+    peak, peak_kind = measured_peaks()
+    achieved = kernels[b.step_kernel]["gbs"]
+    roofline = {"bound": "hbm", "kernel": b.step_kernel + "_kernel", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": profile_traffic(b.step_kernel, args.workload),
+                "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
+                "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P}
+    return kernels, roofline
+
+
+def run_e2e(b, args, world, P_job):
+    """The same step end to end through the public API: host gradients in, norm record out.
+
+    Every step's micro-batch gradients start in pinned host memory and are copied to the
+    device by the copy engines on a side stream (cudaMemcpyAsync via Tensor.copy_); every
+    step's 24-byte norm record is copied back and read on the host, one step behind, as a
+    training loop logs it.  Two staging buffers and two gradient arenas let step t+1's
+    transfer (link-bound, on DMA engines) overlap step t's kernels (HBM-bound, on the SMs)."""
+    z, plan, K, stream, dev = b.z, b.plan, b.K, b.stream, b.dev
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    host_micros = [mb.cpu().pin_memory() for mb in b.micros]
+    stage = [b.micros, [torch.empty_like(mb) for mb in b.micros]]
+    grads = [b.grad, plan.new_arena(torch.float32, dev)]
+    wss = [b.ws, plan.new_workspace(dev)]
+    nouts = [b.nout, z.new_norm_out(dev)]
+    host_rec = [torch.empty(32, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    side = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    step_done = [torch.cuda.Event(), torch.cuda.Event()]
+    seen, copy_ev = [], []
+
+    def e2e_steps(n_steps, first_event=None, time_copies=False):
+        for t in range(n_steps):
+            i = t % 2
+            with torch.cuda.stream(side):
+                if t >= 2:
+                    side.wait_event(step_done[i])  # staging buffer i is free once step t-2 is done
+                elif first_event is not None:
+                    side.wait_event(first_event)
+                if time_copies:
+                    copy_ev.append((ev(), ev()))
+                    copy_ev[-1][0].record(side)
+                for k in range(K):
+                    stage[i][k].copy_(host_micros[k], non_blocking=True)
+                if time_copies:
+                    copy_ev[-1][1].record(side)
+                copied[i].record(side)
+            stream.wait_event(copied[i])
+            if args.k_way:
+                z.accumulate_norm(plan, grads[i], stage[i], wss[i], nouts[i], overwrite_first=True, stream=stream)
+            else:
+                for k in range(K - 1):
+                    z.accumulate(plan, grads[i], stage[i][k], overwrite_first=(k == 0), stream=stream)
+                z.accumulate_norm(plan, grads[i], stage[i][K - 1], wss[i], nouts[i], overwrite_first=(K == 1),
+                                  stream=stream)
+            if b.group is not None:
+                z.allreduce_sumsq_(nouts[i], b.group)
+            b.t += 1
+            z.step(plan, b.master, b.m, b.v, grads[i], b.wbf, b.hp, b.t, nouts[i], stream=stream)
+            host_rec[i].copy_(nouts[i], non_blocking=True)  # device -> host, on the step's stream
+            step_done[i].record(stream)
+            if t >= 1:  # read the previous step's result
+                step_done[1 - i].synchronize()
+                seen.append(z.decode_norm(host_rec[1 - i]))
+        step_done[(n_steps - 1) % 2].synchronize()
+        seen.append(z.decode_norm(host_rec[(n_steps - 1) % 2]))
+
+    e2e_steps(2)
+    torch.cuda.synchronize()
+    h2d_bytes = sum(mb.numel() * mb.element_size() for mb in host_micros)
+    # the host link's own speed on this box, for reading the e2e number: one plain copy
+    c0, c1 = ev(), ev()
+    c0.record(stream)
+    for k in range(K):
+        stage[0][k].copy_(host_micros[k], non_blocking=True)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    h2d_gbs = h2d_bytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    barrier(world)
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    e2e_steps(args.steps, first_event=e0, time_copies=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    copy_ms = statistics.mean(x.elapsed_time(y) for x, y in copy_ev)
+    assert all(r["status"] == 0 for r in seen)
+    return {"value": P_job / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": z.NORM_OUT_BYTES, "h2d_copy_gbs_before": h2d_gbs,
+            "h2d_copy_ms_in_loop": copy_ms, "h2d_copy_gbs_in_loop": h2d_bytes / (copy_ms * 1e-3) / 1e9,
+            "how": "pinned host gradients copied by the DMA engines on a side stream into two staging "
+                   "buffers, overlapping the previous step's kernels; norm record read back every step"}
+
+
+def main():
+    args = parse_args()
+    from zero_sharded_mixed_local_gb300.workloads import get_workload
     w = get_workload(args.workload)
     if args.micro_batches is not None:
         w.micro_batches = args.micro_batches
         w.description += " (K overridden to %d)" % args.micro_batches
 
     if args.impl == "reference":
-        rank = int(os.environ.get("RANK", "0"))
-        run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
 
     import zero_sharded_mixed_local_gb300 as z
 
     world, rank, local = dist_setup()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+    torch.cuda.set_device(torch.device("cuda", local))
     z.load_library()
+    b = StepBench(args, w, z, world, rank, local)
 
-    # With N ranks each simulates a different data-parallel shard of the same model.
-    dp_rank = (w.dp_rank + rank) % w.dp_size if world > 1 else w.dp_rank
-    plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, dp_rank)
-    L = plan.layout()
-    gen = InputGenerator(w, Layout(L.counts, L.offsets, L.no_decay, L.arena_numel), dev, seed=w.seed + rank)
-    P = plan.local_numel
-    K = w.micro_batches
-    master = gen.master()
-    m, v, grad = gen.zeros(), gen.zeros(), gen.zeros()
-    wbf = gen.zeros(torch.bfloat16)
-    micros = gen.micro_grads()
-    ws, nout = plan.new_workspace(dev), z.new_norm_out(dev)
-    hp = z.Hparams(**w.hp)
-    group = None
-    if world > 1:
-        import torch.distributed as dist
-        group = dist.group.WORLD
-    lists = lopt = None
-    if args.tensor_list:
-        if args.unfused:
-            raise SystemExit("--tensor-list runs the fused calls")
-        args.no_e2e = True  # the end-to-end leg stages arenas
-        # one allocation per tensor shard, as a framework holds per-parameter state, filled
-        # from the generated arenas (which are then freed) and reached through pointer lists
-        def split(buf):
-            return [t.clone() for t in plan.shard_views(buf)]
-
-        lopt = z.ShardListAdamW(w.params.numels, w.params.no_decay, w.dp_size, dp_rank, hparams=hp, device=dev,
-                                master=split(master), exp_avg=split(m), exp_avg_sq=split(v), grad=split(grad),
-                                weight_bf16=split(wbf))
-        lists = {"master": lopt._lists["master"], "m": lopt._lists["exp_avg"], "v": lopt._lists["exp_avg_sq"],
-                 "grad": lopt._lists["grad"], "w": lopt._lists["weight_bf16"]}
-        micro_shards = [split(mb) for mb in micros]
-        lists["micro"] = [z.PointerLists(plan, ms, torch.bfloat16, dev) for ms in micro_shards]
-        lists["micro_all"] = z.PointerLists(plan, micro_shards, torch.bfloat16, dev)  # K lists back to back
-        master = m = v = grad = wbf = micros = None
-        torch.cuda.empty_cache()
-        table, lws = lopt.table, lopt.workspace
-        lopt.norm_out = nout
-    torch.cuda.synchronize()
-
-    stream = torch.cuda.current_stream(dev)
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    t_counter = [0]
-
-    def one_list_step(record=None):
-        t_counter[0] += 1
-        if record is not None:
-            record["a0"].record(stream)
-        for k in range(0 if args.k_way else K - 1):
-            z.list_accumulate(plan, table, lists["grad"], lists["micro"][k], overwrite_first=(k == 0), stream=stream)
-        if record is not None:
-            record["n0"].record(stream)
-        if args.k_way:
-            z.list_accumulate_norm(plan, table, lists["grad"], lists["micro_all"], lws, nout, overwrite_first=True,
-                                   stream=stream)
-        else:
-            z.list_accumulate_norm(plan, table, lists["grad"], lists["micro"][K - 1], lws, nout,
-                                   overwrite_first=(K == 1), stream=stream)
-        if group is not None:
-            z.allreduce_sumsq_(nout, group)
-        if record is not None:
-            record["s0"].record(stream)
-        z.list_step(plan, table, lists["master"], lists["m"], lists["v"], lists["grad"], lists["w"], hp, t_counter[0],
-                    nout, stream=stream)
-        if record is not None:
-            record["s1"].record(stream)
-
-    def one_step(record=None):
-        if lists is not None:
-            return one_list_step(record)
-        t_counter[0] += 1
-        if record is not None:
-            record["x0"].record(stream)
-        if full_g is not None:  # pack: this rank's chunk of the reduce-scatter input
-            z.shard_gather(plan, full_g, micros[K - 1], stream=stream)
-        if record is not None:
-            record["a0"].record(stream)
-        for k in range(0 if args.k_way else K - 1):
-            z.accumulate(plan, grad, micros[k], overwrite_first=(k == 0), stream=stream)
-        if record is not None:
-            record["n0"].record(stream)
-        if args.k_way:
-            z.accumulate_norm(plan, grad, micros, ws, nout, overwrite_first=True, stream=stream)
-        elif args.unfused:
-            z.accumulate(plan, grad, micros[K - 1], overwrite_first=(K == 1), stream=stream)
-            z.grad_norm(plan, grad, ws, nout, 0.0, stream=stream)
-        else:
-            # the last micro-batch's accumulation also takes the gradient norm
-            z.accumulate_norm(plan, grad, micros[K - 1], ws, nout, overwrite_first=(K == 1), stream=stream)
-        if group is not None:
-            z.allreduce_sumsq_(nout, group)
-        if record is not None:
-            record["s0"].record(stream)
-        z.step(plan, master, m, v, grad, wbf, hp, t_counter[0], nout, stream=stream)
-        if record is not None:
-            record["s1"].record(stream)
-        if full_w is not None:  # unpack: the bf16 weights into the model layout
-            z.shard_scatter(plan, wbf, full_w, stream=stream)
-        if record is not None:
-            record["x1"].record(stream)
-
-    if args.k_way and (args.unfused or args.graph):
-        raise SystemExit("--k-way runs the fused eager calls")
-    full_g = full_w = None
-    if args.exchange:
-        if lists is not None or args.graph:
-            raise SystemExit("--exchange runs the arena calls eagerly")
-        args.no_e2e = True
-        # the model-layout gradient holds this rank's shard values where the plan puts them
-        full_g = torch.zeros(plan.total_numel, dtype=torch.bfloat16, device=dev)
-        full_w = torch.zeros(plan.total_numel, dtype=torch.bfloat16, device=dev)
-        z.shard_scatter(plan, micros[K - 1], full_g)
-    sgraph = None
-    if args.graph:
-        if world > 1:
-            raise SystemExit("--graph runs one rank (the captured step holds no all-reduce)")
-        if lopt is not None:
-            sgraph = z.StepGraph(lopt, lists["micro"])
-        else:
-            from types import SimpleNamespace
-            state = SimpleNamespace(plan=plan, grad=grad, workspace=ws, norm_out=nout, master=master, exp_avg=m,
-                                    exp_avg_sq=v, weight_bf16=wbf, hp=hp, t=0, device=dev)
-            sgraph = z.StepGraph(state, micros)
-
-        def one_step(record=None):  # noqa: F811  (the graph replaces the eager calls)
-            if record is not None:
-                record["a0"].record(stream)
-            sgraph.replay()
-            if record is not None:
-                record["s1"].record(stream)
-
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    barrier(world)
-
-    visible = [d for d in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if d.strip()]
-    clocks = ClockSampler(visible[local].strip() if local < len(visible) else local)  # index or UUID
-    clocks.start()
-    recs = [{k: ev() for k in ("x0", "a0", "n0", "s0", "s1", "x1")} for _ in range(args.steps)]
-    start, end = ev(), ev()
-    torch.cuda.synchronize()
-    barrier(world)
-    start.record(stream)
-    for i in range(args.steps):
-        one_step(recs[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-
-    total_ms = start.elapsed_time(end)
-    total_ms = max_over_ranks(total_ms, world)
-    P_job = sum_over_ranks(P, world)  # parameters all ranks step per step
+    recs, total_ms, clk = time_steps(b, args, world, local)
+    P_job = sum_over_ranks(b.P, world)  # parameters all ranks step per step
     ms_step = total_ms / args.steps
-    if sgraph is None:
-        acc_ms = statistics.mean(r["a0"].elapsed_time(r["n0"]) for r in recs)      # the first K-1 micro-batches
-        accnorm_ms = statistics.mean(r["n0"].elapsed_time(r["s0"]) for r in recs)  # last micro-batch + norm
-        step_ms = statistics.mean(r["s0"].elapsed_time(r["s1"]) for r in recs)
-    else:  # one graph launch per step: no per-kernel events inside it
-        acc_ms = accnorm_ms = step_ms = float("nan")
-    exchange = None
-    if full_g is not None:  # the layout copies move 2 + 2 bytes per local element each
-        pack_ms = statistics.mean(r["x0"].elapsed_time(r["a0"]) for r in recs)
-        unpack_ms = statistics.mean(r["s1"].elapsed_time(r["x1"]) for r in recs)
-        exchange = {"shard_gather": {"ms": pack_ms, "gbs": 4 * P / (pack_ms * 1e-3) / 1e9, "launches_per_step": 1},
-                    "shard_scatter": {"ms": unpack_ms, "gbs": 4 * P / (unpack_ms * 1e-3) / 1e9,
-                                      "launches_per_step": 1}}
-    z.read_norm(nout, stream)
+    kernels, roofline = kernel_report(b, recs, args)
+    z.read_norm(b.nout, b.stream)
+    path_bytes = b.path_bytes()
 
-    peak, peak_kind = measured_peaks()
-    step_gbs = STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9 if sgraph is None else None
-    # fused: the norm rides on the last micro-batch's pass (no separate 4-byte read)
-    norm_bytes = 4 * P if args.unfused else 0
-    path_bytes = (accumulate_bytes_per_elem(K, args.k_way) + STEP_BYTES_PER_ELEM) * P + norm_bytes + \
-        (8 * P if full_g is not None else 0)
-    last_bytes = accumulate_bytes_per_elem(K, True) * P if args.k_way else (6 if K == 1 else 10) * P + norm_bytes
-    step_kernel = "list_step" if lists is not None else "adamw_step"
-    traffic = profile_traffic(step_kernel, args.workload)
-
-    # ---- end to end through the public API: host gradients in, norm record out.  Every
-    # step's micro-batch gradients start in pinned host memory and are copied to the device
-    # by the copy engines on a side stream (cudaMemcpyAsync via Tensor.copy_); every step's
-    # 24-byte norm record is copied back and read on the host, one step behind, as a training
-    # loop logs it.  Two staging buffers and two gradient arenas let step t+1's transfer
-    # (link-bound, on DMA engines) overlap step t's kernels (HBM-bound, on the SMs).
-    e2e = None
-    if not args.no_e2e and sgraph is None:
-        host_micros = [mb.cpu().pin_memory() for mb in micros]
-        stage = [micros, [torch.empty_like(mb) for mb in micros]]
-        grads = [grad, plan.new_arena(torch.float32, dev)]
-        wss = [ws, plan.new_workspace(dev)]
-        nouts = [nout, z.new_norm_out(dev)]
-        host_rec = [torch.empty(32, dtype=torch.uint8).pin_memory() for _ in range(2)]
-        side = torch.cuda.Stream(dev)
-        copied = [torch.cuda.Event(), torch.cuda.Event()]
-        step_done = [torch.cuda.Event(), torch.cuda.Event()]
-        opt_t = [t_counter[0]]
-        seen = []
-        copy_ev = []
-
-        def e2e_steps(n_steps, first_event=None, time_copies=False):
-            for t in range(n_steps):
-                b = t % 2
-                with torch.cuda.stream(side):
-                    if t >= 2:
-                        side.wait_event(step_done[b])  # staging buffer b is free once step t-2 is done
-                    elif first_event is not None:
-                        side.wait_event(first_event)
-                    if time_copies:
-                        copy_ev.append((ev(), ev()))
-                        copy_ev[-1][0].record(side)
-                    for k in range(K):
-                        stage[b][k].copy_(host_micros[k], non_blocking=True)
-                    if time_copies:
-                        copy_ev[-1][1].record(side)
-                    copied[b].record(side)
-                stream.wait_event(copied[b])
-                if args.k_way:
-                    z.accumulate_norm(plan, grads[b], stage[b], wss[b], nouts[b], overwrite_first=True, stream=stream)
-                else:
-                    for k in range(K - 1):
-                        z.accumulate(plan, grads[b], stage[b][k], overwrite_first=(k == 0), stream=stream)
-                    z.accumulate_norm(plan, grads[b], stage[b][K - 1], wss[b], nouts[b], overwrite_first=(K == 1),
-                                      stream=stream)
-                if group is not None:
-                    z.allreduce_sumsq_(nouts[b], group)
-                opt_t[0] += 1
-                z.step(plan, master, m, v, grads[b], wbf, hp, opt_t[0], nouts[b], stream=stream)
-                host_rec[b].copy_(nouts[b], non_blocking=True)  # device -> host, on the step's stream
-                step_done[b].record(stream)
-                if t >= 1:  # read the previous step's result
-                    step_done[1 - b].synchronize()
-                    seen.append(z.decode_norm(host_rec[1 - b]))
-            step_done[(n_steps - 1) % 2].synchronize()
-            seen.append(z.decode_norm(host_rec[(n_steps - 1) % 2]))
-
-        e2e_steps(2)
-        torch.cuda.synchronize()
-        # the host link's own speed on this machine, for reading the e2e number: one plain copy
-        c0, c1 = ev(), ev()
-        c0.record(stream)
-        for k in range(K):
-            stage[0][k].copy_(host_micros[k], non_blocking=True)
-        c1.record(stream)
-        torch.cuda.synchronize()
-        h2d_gbs = sum(mb.numel() * mb.element_size() for mb in host_micros) / (c0.elapsed_time(c1) * 1e-3) / 1e9
-        barrier(world)
-        e0, e1 = ev(), ev()
-        e0.record(stream)
-        e2e_steps(args.steps, first_event=e0, time_copies=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-        copy_ms = statistics.mean(a.elapsed_time(b) for a, b in copy_ev)
-        assert all(r["status"] == 0 for r in seen)
-        e2e = {"value": P_job / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": sum(mb.numel() * mb.element_size() for mb in host_micros),
-               "d2h_bytes_per_step": z.NORM_OUT_BYTES, "h2d_copy_gbs_before": h2d_gbs,
-               "h2d_copy_ms_in_loop": copy_ms,
-               "h2d_copy_gbs_in_loop": sum(mb.numel() * mb.element_size() for mb in host_micros) /
-                                        (copy_ms * 1e-3) / 1e9,
-               "how": "pinned host gradients copied by the DMA engines on a side stream into two staging "
-                      "buffers, overlapping the previous step's kernels; norm record read back every step"}
-        del host_micros, stage
+    e2e = run_e2e(b, args, world, P_job) if not args.no_e2e and b.graph is None else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -642,43 +690,30 @@ def main():
             "data": "synthetic",
             "config": {
                 "workload": w.description,
-                "local_params_per_gpu": P,
+                "local_params_per_gpu": b.P,
                 "params_per_step_all_ranks": P_job,
-                "arena_elems": plan.arena_numel,
-                "micro_batches": K,
+                "arena_elems": b.plan.arena_numel,
+                "micro_batches": b.K,
                 "dp_size": w.dp_size,
-                "dp_rank": dp_rank,
+                "dp_rank": b.dp_rank,
                 "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
                 "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
                 "accumulate": ("all K micro-batches in one pass (K-way)" if args.k_way
                                else "one call per micro-batch, as they arrive"),
                 "exchange": ("pack the reduce-scatter input and unpack the bf16 weights, model layout <-> arena"
-                             if full_g is not None else "none (the local step only)"),
-                "launch": "one CUDA graph per step (StepGraph)" if sgraph is not None else "eager calls",
+                             if b.full_g is not None else "none (the local step only)"),
+                "launch": "one CUDA graph per step (StepGraph)" if b.graph is not None else "eager calls",
                 "layout": ("tensor lists: one allocation per tensor shard, a 16384-element run table"
-                           if lists is not None else "arenas: one padded buffer per quantity"),
+                           if b.lists is not None else "arenas: one padded buffer per quantity"),
                 "l2": "no flush: each step streams %.1f GB, far above the 129 MB L2" % (path_bytes / 1e9),
             },
             "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
-            "kernels": ({
-                "accumulate": {"ms": acc_ms, "gbs": (accumulate_bytes_per_elem(K) * P - last_bytes) /
-                               (acc_ms * 1e-3) / 1e9 if K > 1 and not args.k_way else None,
-                               "launches_per_step": 0 if args.k_way else K - 1},
-                ("accumulate+grad_norm" if args.unfused else "accumulate_norm"): {
-                    "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
-                    "launches_per_step": 3 if args.unfused else 2},
-                step_kernel: {"ms": step_ms, "gbs": step_gbs, "launches_per_step": 1},
-                **(exchange or {}),
-            }) if sgraph is None else None,
-            "roofline": ({"bound": "hbm", "kernel": step_kernel + "_kernel", "achieved": step_gbs, "peak": peak,
-                         "unit": "GB/s", "frac": step_gbs / peak, "traffic": traffic,
-                         "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
-                         "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P}) if sgraph is None else None,
+            "kernels": kernels,
+            "roofline": roofline,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "gpu_launches": args.steps * ((3 if args.k_way else K + 2) + (1 if args.unfused else 0) +
-                                          (2 if full_g is not None else 0)),  # also inside each graph
+            "gpu_launches": args.steps * b.launches_per_step(),  # also inside each graph
         }
         print(json.dumps(out), flush=True)
     if world > 1:
