@@ -402,7 +402,7 @@ class StepBench:
         lopt = z.ShardListAdamW(w.params.numels, w.params.no_decay, w.dp_size, self.dp_rank, hparams=self.hp,
                                 device=dev, master=split(self.master), exp_avg=split(self.m),
                                 exp_avg_sq=split(self.v), grad=split(self.grad), weight_bf16=split(self.wbf))
-        L = lopt._lists
+        L = lopt.pointer_lists
         micro_shards = [split(mb) for mb in self.micros]
         self.lists = {"master": L["master"], "m": L["exp_avg"], "v": L["exp_avg_sq"], "grad": L["grad"],
                       "w": L["weight_bf16"],

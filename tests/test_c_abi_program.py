@@ -24,7 +24,8 @@ def program(tmp_path_factory):
     exe = str(tmp_path_factory.mktemp("cabi") / "c_abi_step")
     cmd = ["gcc", "-std=c11", "-O1", "-Wall", "-I", os.path.join(ROOT, "include"), "-I", os.path.join(CUDA, "include"),
            os.path.join(ROOT, "tests", "c_abi_step.c"), "-o", exe, "-L", libdir, "-lzero1",
-           "-Wl,-rpath," + libdir, "-L", os.path.join(CUDA, "lib64"), "-lcudart", "-Wl,-rpath," + os.path.join(CUDA, "lib64")]
+           "-Wl,-rpath," + libdir, "-L", os.path.join(CUDA, "lib64"), "-lcudart",
+           "-Wl,-rpath," + os.path.join(CUDA, "lib64")]
     subprocess.run(cmd, check=True, capture_output=True, text=True)
     return exe
 

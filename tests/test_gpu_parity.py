@@ -383,7 +383,8 @@ def test_no_call_writes_outside_its_buffers():
     g = torch.Generator(device="cuda").manual_seed(9)
     L = plan.layout()
     for o, c in zip(L.offsets, L.counts):
-        bufs["mb"][1][int(o):int(o) + int(c)] = (torch.randn(int(c), device="cuda", generator=g) * 0.1).to(torch.bfloat16)
+        bufs["mb"][1][int(o):int(o) + int(c)] = (torch.randn(int(c), device="cuda", generator=g) * 0.1).to(
+            torch.bfloat16)
         bufs["master"][1][int(o):int(o) + int(c)] = torch.randn(int(c), device="cuda", generator=g) * 0.02
     bufs["full32"][1].normal_(generator=g)
     bufs["full16"][1].normal_(generator=g)

@@ -162,7 +162,7 @@ def test_divisor_and_separate_norm_call():
     assert abs(fused["sumsq"] - ref) <= 1e-12 * ref
     nout = z.new_norm_out()
     for _ in range(2):
-        z.list_grad_norm(pb.opt.plan, pb.opt.table, pb.opt._lists["grad"], pb.opt.workspace, nout)
+        z.list_grad_norm(pb.opt.plan, pb.opt.table, pb.opt.pointer_lists["grad"], pb.opt.workspace, nout)
         again = z.read_norm(nout)
         assert again["sumsq"] == fused["sumsq"] and again["n_partials"] == fused["n_partials"]
     runs = int(np.sum((pb.counts + 16383) // 16384))
@@ -187,10 +187,10 @@ def test_list_step_without_bf16_copy():
     pb = ListProblem(NUMELS, NO_DECAY, seed=9)
     mb = pb.micro()
     pb.opt.accumulate(mb, last=True)
-    L = pb.opt._lists
+    L = pb.opt.pointer_lists
     twin = [t.clone() for t in pb.master]
-    z.list_step(pb.opt.plan, pb.opt.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], None, z.Hparams(**HP), 1,
-                pb.opt.norm_out)
+    z.list_step(pb.opt.plan, pb.opt.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], None,
+                z.Hparams(**HP), 1, pb.opt.norm_out)
     # the same step through the oracle on the cloned master
     G = pb.flat(pb.grad).numpy()
     P = torch.cat([t.reshape(-1) for t in twin]).cpu().numpy().copy()
@@ -372,15 +372,16 @@ def test_k_way_list_pass_matches_the_oracle(K, misaligned):
     for k, mb in enumerate(micros):
         oracle.accumulate(G, u16(pb.flat(mb)), overwrite=(k == 0))
     pl = z.PointerLists(pb.opt.plan, micros, torch.bfloat16)
-    z.list_accumulate_norm(pb.opt.plan, pb.opt.table, pb.opt._lists["grad"], pl, pb.opt.workspace, pb.opt.norm_out,
-                           overwrite_first=True, divisor=2.0)
+    gl = pb.opt.pointer_lists["grad"]
+    z.list_accumulate_norm(pb.opt.plan, pb.opt.table, gl, pl, pb.opt.workspace, pb.opt.norm_out, overwrite_first=True,
+                           divisor=2.0)
     got = pb.opt.read_norm()
     Gd = G.copy()
     oracle.divide(Gd, 2.0)
     assert _eq(pb.flat(pb.grad).numpy(), Gd)
     ref = oracle.sumsq(Gd)
     assert abs(got["sumsq"] - ref) <= 1e-12 * ref
-    z.list_accumulate(pb.opt.plan, pb.opt.table, pb.opt._lists["grad"], pl, overwrite_first=True)
+    z.list_accumulate(pb.opt.plan, pb.opt.table, gl, pl, overwrite_first=True)
     assert _eq(pb.flat(pb.grad).numpy(), G)
 
 

@@ -1,11 +1,10 @@
 """Optimizer objects built on the binding: one rank's ZeRO-1 AdamW state and step.
 
-``LocalShardAdamW`` owns one rank's shard as flat arenas; ``StepGraph`` replays
-its step as one CUDA graph; ``ShardListAdamW`` owns the same state as one buffer
-per tensor shard (the tensor-list calls); ``Zero1AdamW`` wraps a torch module.
-
-Zero1AdamW: a ZeRO-1 AdamW over a torch module's parameters, on top of the
-tensor-list calls.
+- ``LocalShardAdamW`` owns one rank's shard as flat arenas.
+- ``ShardListAdamW`` owns the same state as one buffer per tensor shard (the
+  tensor-list calls).
+- ``StepGraph`` replays either one's step as CUDA graphs.
+- ``Zero1AdamW`` wraps a torch module's parameters.
 
 The pages' distributed optimizer ("ZeRO-1 风格的 Distributed Optimizer", sections
 6.2-6.3) wraps a model's named parameters: each rank keeps the fp32 master
@@ -302,6 +301,12 @@ class ShardListAdamW:
 
     def read_norm(self, stream=None):
         return read_norm(self.norm_out, stream=stream)
+
+    @property
+    def pointer_lists(self):
+        """The device pointer lists of the state buffers: "master", "exp_avg", "exp_avg_sq",
+        "grad" and "weight_bf16" (PointerLists), for calling the list functions directly."""
+        return dict(self._lists)
 
     def save_checkpoint(self, path, meta=None, async_=False):
         """Write this rank's master / m / v shards and the step count (see ``checkpoint``)."""
