@@ -548,3 +548,30 @@ def test_arena_beyond_2_to_32_elements():
     assert np.array_equal(u16(wbf[it]), oracle.bf16_rne(P))
     del mb, master, m, v, grad, wbf
     torch.cuda.empty_cache()
+
+
+def test_four_element_worked_example_on_the_gpu():
+    """The hand-worked four-element case of the oracle pins (two tensors, clipping at norm 1.625,
+    a repeated and a sign-flipped gradient), through the C ABI: the same numbers."""
+    from test_oracle_pins import FOUR_G, FOUR_HP, FOUR_P, FOUR_P0
+    plan = z.Plan([2, 2], [0, 1], 1, 0)
+    offs = plan.layout().offsets
+    n = plan.arena_numel
+    dev = torch.device("cuda")
+    master = torch.zeros(n, device=dev)
+    for i, o in enumerate(offs):
+        master[int(o):int(o) + 2] = torch.tensor(FOUR_P0[2 * i:2 * i + 2])
+    m, v, grad = torch.zeros_like(master), torch.zeros_like(master), torch.zeros_like(master)
+    wbf = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    ws, nout = plan.new_workspace(dev), z.new_norm_out(dev)
+    hp = z.Hparams(**FOUR_HP, clip_grad=1.0)
+    for t, (g, expect) in enumerate(zip(FOUR_G, FOUR_P), start=1):
+        mb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        for i, o in enumerate(offs):
+            mb[int(o):int(o) + 2] = torch.tensor(g[2 * i:2 * i + 2]).to(torch.bfloat16)
+        z.accumulate_norm(plan, grad, mb, ws, nout)
+        z.step(plan, master, m, v, grad, wbf, hp, t, nout)
+        got = z.read_norm(nout)
+        assert got["sumsq"] == 2.640625 and got["norm"] == 1.625
+        vals = torch.cat([master[int(o):int(o) + 2] for o in offs]).cpu().numpy()
+        np.testing.assert_allclose(vals, expect, rtol=0, atol=2.5e-7)

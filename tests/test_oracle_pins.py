@@ -561,3 +561,36 @@ def test_divide_matches_numpy_float32_division(oracle_mod):
     x = np.array([3.0, -9.0, 0.75], np.float32)
     oracle_mod.divide(x, 3.0)
     assert x.tolist() == [1.0, -3.0, 0.25]
+
+
+# A four-element case worked by hand ("ZeRO-1 风格的 Distributed Optimizer", section 6.6 hyper-parameters
+# beta1 0.9, beta2 0.95, eps 1e-8, weight decay 0.1, clip_grad 1.0; lr 0.1 for round numbers).  Tensor A
+# (decayed) holds elements 0-1, tensor B (a norm weight, no decay) elements 2-3; bf16-exact gradients.
+#   step 1: g = [0.375, -0.5, 0, 1.5]; sum of squares 0.140625 + 0.25 + 2.25 = 2.640625, norm 1.625,
+#           clipped by c = 1/(1.625 + 1e-6).  From m = v = 0 the bias-corrected update is g/|g| (eps is
+#           ~1e-8 of |cg| and vanishes in fp32): +1, -1, 0, +1; A decays by 1 - 0.1*0.1 = 0.99, B does not:
+#           p = [0.5*0.99 - 0.1, -0.25*0.99 + 0.1, 1.0, 1.0 - 0.1] = [0.395, -0.1475, 1.0, 0.9].
+#   step 2: g = [0.375, 0.5, 0, -1.5] (norm 1.625 again, same c).  Element 0 repeats its gradient, so
+#           m^ = c*0.375 and sqrt(v^) = c*0.375: update 1, p = 0.395*0.99 - 0.1 = 0.29105.  Elements 1 and 3
+#           flip sign: m2 = c*(0.09*g1 + 0.1*g2) = 0.01*c*g2, m^ = m2/0.19; v2 = 0.05*c^2*(0.95 + 1)*g^2,
+#           v^ = v2/0.0975 = c^2*g^2: update = (0.01/0.19)*sign(g2) = 0.0526315789*sign(g2), so
+#           p1 = -0.1475*0.99 - 0.1*0.0526315789 = -0.1512881579 and p3 = 0.9 + 0.00526315789 = 0.9052631579.
+#           Element 2 (g = 0 twice) stays 1.0.
+FOUR_HP = dict(lr=0.1, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+FOUR_P0 = [0.5, -0.25, 1.0, 1.0]
+FOUR_G = ([0.375, -0.5, 0.0, 1.5], [0.375, 0.5, 0.0, -1.5])
+FOUR_P = ([0.395, -0.1475, 1.0, 0.9], [0.29105, -0.1512881579, 1.0, 0.9052631579])
+
+
+def test_four_element_two_step_worked_example(oracle_mod):
+    p = np.array(FOUR_P0, np.float32)
+    m, v = np.zeros(4, np.float32), np.zeros(4, np.float32)
+    for t, (g, expect) in enumerate(zip(FOUR_G, FOUR_P), start=1):
+        micro = oracle_mod.bf16_rne(np.array(g, np.float32))
+        info = oracle_mod.full_step(p, m, v, [micro], [2, 2], [0, 1], FOUR_HP, t, 1.0)
+        assert info["sumsq"] == 2.640625 and info["norm"] == 1.625
+        assert info["coef"] == np.float32(1.0 / (1.625 + 1e-6))
+        np.testing.assert_allclose(p, expect, rtol=0, atol=2.5e-7)
+    # m2 = c*(0.09*g1 + 0.1*g2): 0.375*0.19 = 0.07125, 0.09*(-0.5) + 0.05 = 0.005, 0.135 - 0.15 = -0.015
+    c = 1.0 / 1.625
+    np.testing.assert_allclose(m[[0, 1, 3]], [c * 0.07125, c * 0.005, -c * 0.015], rtol=1e-5)
