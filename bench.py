@@ -155,21 +155,27 @@ def barrier(world):
         dist.barrier()
 
 
+def _collective_device():
+    import torch.distributed as dist
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+
 def sum_over_ranks(x, world):
     """Whole-job total of a per-rank count (the ranks' shards differ by the remainder rule)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.int64, device="cuda")
+    t = torch.tensor([x], dtype=torch.int64, device=_collective_device())
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return int(t.item())
 
 
 def max_over_ranks(x, world):
+    """The slowest rank's time: the whole job waits for it."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_collective_device())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

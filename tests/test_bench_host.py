@@ -42,3 +42,41 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def _rank_worker(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench as b
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        b.barrier(world)
+        total = b.sum_over_ranks(1_000_000_007 + rank, world)   # shard sizes differ by rank
+        slowest = b.max_over_ranks(5.0 + rank * 0.25, world)     # per-rank step times
+        q.put((rank, total, slowest))
+    finally:
+        dist.destroy_process_group()
+        q.close()
+        q.join_thread()
+
+
+def test_bench_rank_helpers_with_gloo():
+    """The whole-job bookkeeping of a multi-rank bench run, as two gloo processes: the job's
+    parameter count is the sum of every rank's shard, the step time the slowest rank's."""
+    import socket
+    import torch.multiprocessing as mp
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, 2_000_000_015, 5.25), (1, 2_000_000_015, 5.25)]
