@@ -339,6 +339,8 @@ def parse_args():
                          "the model layout (zero1_shard_scatter)")
     ap.add_argument("--micro-batches", type=int, default=None,
                     help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="seed of the synthetic inputs (default: the workload's own, 0); rank r adds r")
     args = ap.parse_args()
     if args.tensor_list and args.unfused:
         raise SystemExit("--tensor-list runs the fused calls")
@@ -653,6 +655,8 @@ def main():
     if args.micro_batches is not None:
         w.micro_batches = args.micro_batches
         w.description += " (K overridden to %d)" % args.micro_batches
+    if args.seed is not None:
+        w.seed = args.seed
 
     if args.impl == "reference":
         run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
@@ -703,6 +707,7 @@ def main():
                 "dp_size": w.dp_size,
                 "dp_rank": b.dp_rank,
                 "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
+                "seed": w.seed,
                 "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
                 "accumulate": ("all K micro-batches in one pass (K-way)" if args.k_way
                                else "one call per micro-batch, as they arrive"),
