@@ -31,6 +31,7 @@ if ROOT not in sys.path:
 
 METRIC = "AdamW shard-step params/sec and HBM GB/s (fraction of GB300 peak), 1 GPU"
 STEP_BYTES_PER_ELEM = 30          # adamw_step: grad 4 R, master/m/v 12 R + 12 W, bf16 2 W
+NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e, nominal
 
 
 def accumulate_bytes_per_elem(k, k_way=False):
@@ -560,6 +561,7 @@ def kernel_report(b, recs, args):
     roofline = {"bound": "hbm", "kernel": b.step_kernel + "_kernel", "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": profile_traffic(b.step_kernel, args.workload),
                 "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
+                "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P}
     return kernels, roofline
 
