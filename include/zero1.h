@@ -54,6 +54,8 @@ extern "C" {
 /* Each shard starts on a multiple of this many elements inside an arena, so
  * that 16-byte vector loads of bf16 (8 elements) never straddle tensors. */
 #define ZERO1_ARENA_ALIGN 8
+/* The numels of one plan add up to at most this many elements (2^56). */
+#define ZERO1_MAX_TOTAL_NUMEL (((int64_t)1) << 56)
 /* Tensors are grouped (at most ZERO1_MAX_GROUPS groups); each group has its
  * own learning-rate and weight-decay multipliers.  zero1_plan_create's
  * no_decay flags make group 0 (decayed) and group 1 (excluded). */
@@ -109,8 +111,9 @@ typedef struct zero1_norm_out {
  * elements; the padding elements between shards must be zero when the
  * buffers are created and the library keeps them zero.
  * Errors: ZERO1_EINVAL (n_tensors < 0, dp_size < 1, dp_rank outside
- * [0, dp_size), a negative numel, a no_decay value other than 0/1, a null
- * pointer with n_tensors > 0, out == NULL), ZERO1_ENOMEM. */
+ * [0, dp_size), a negative numel, numels adding up to more than
+ * ZERO1_MAX_TOTAL_NUMEL, a no_decay value other than 0/1, a null pointer
+ * with n_tensors > 0, out == NULL), ZERO1_ENOMEM. */
 int zero1_plan_create(const int64_t* numels, const uint8_t* no_decay, int32_t n_tensors,
                       int32_t dp_size, int32_t dp_rank, zero1_plan** out);
 
@@ -224,7 +227,8 @@ int zero1_grad_norm(const zero1_plan* plan, const float* grad, double extra_sums
  *                 taken: the average over data-parallel ranks that FSDP2
  *                 runs as a single divide kernel after the fp32
  *                 reduce-scatter ("TorchTitan 生产级预训练方案", appendix B.1).
- *                 1 keeps the plain sum (no division); must be finite > 0
+ *                 1 keeps the plain sum (no division); must be finite > 0,
+ *                 and stay so once rounded to fp32 (else ZERO1_EINVAL)
  *   extra_sumsq, workspace, workspace_bytes, d_out  as for zero1_grad_norm
  * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
 int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,

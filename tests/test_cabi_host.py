@@ -100,6 +100,7 @@ def test_plan_rejects_bad_arguments(z):
     nd = np.array([0, 1], np.uint8)
     bad_nd = np.array([0, 2], np.uint8)
     neg = np.array([4, -1], np.int64)
+    huge = np.array([1 << 55, (1 << 55) + 1], np.int64)   # adds up to 2^56 + 1 elements
     cases = [                  # (numels, no_decay, n_tensors, dp_size, dp_rank)
         (n, nd, 2, 2, 2),      # rank == dp
         (n, nd, 2, 2, -1),     # negative rank
@@ -108,6 +109,7 @@ def test_plan_rejects_bad_arguments(z):
         (n, nd, 2, 0, 0),      # dp == 0
         (n, bad_nd, 2, 1, 0),  # no_decay not 0/1
         (neg, nd, 2, 1, 0),    # negative numel
+        (huge, nd, 2, 1, 0),   # more than ZERO1_MAX_TOTAL_NUMEL in all
     ]
     for numels, flags, count, dp, rank in cases:
         rc = lib.zero1_plan_create(numels.ctypes.data, flags.ctypes.data, count, dp, rank, ctypes.byref(h))
@@ -263,7 +265,7 @@ def test_fused_pass_rejects_a_bad_divisor_before_any_launch(z):
     plan = z.Plan([100, 8], [0, 1], 1, 0)
     fake = ctypes.c_void_p(0x10000)
     arr = (ctypes.c_void_p * 1)(0x20000)
-    for d in (0.0, -2.0, float("nan"), float("inf")):
+    for d in (0.0, -2.0, float("nan"), float("inf"), 1e300, 1e-300):  # the last two leave fp32
         rc = lib.zero1_accumulate_norm(plan.handle, fake, arr, 1, 1, d, 0.0, fake, 64, fake, None)
         assert rc == z.ZERO1_EINVAL, d
 
@@ -306,7 +308,7 @@ def test_list_calls_reject_bad_arguments_before_any_launch(z):
     assert lib.zero1_list_accumulate(h, fake, odd, fake, 1, 1, None) == z.ZERO1_EALIGN
     assert lib.zero1_list_accumulate(h, fake, fake, None, 1, 1, None) == z.ZERO1_EINVAL
     assert lib.zero1_list_workspace_bytes(h) == 16
-    for d in (0.0, -1.0, float("nan"), float("inf")):
+    for d in (0.0, -1.0, float("nan"), float("inf"), 1e300, 1e-300):
         assert lib.zero1_list_accumulate_norm(h, fake, fake, fake, 1, 1, d, 0.0, fake, 64, fake, None) == \
             z.ZERO1_EINVAL
     assert lib.zero1_list_accumulate_norm(h, fake, fake, fake, 1, 1, 1.0, 0.0, fake, 8, fake, None) == z.ZERO1_EINVAL

@@ -30,6 +30,13 @@ int cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A gradient divisor is used as fp32: it must be finite and positive after
+// that rounding too (1e300 would become inf, 1e-300 zero).
+bool divisor_ok(double d) {
+    const float f = static_cast<float>(d);
+    return std::isfinite(d) && d > 0.0 && std::isfinite(f) && f > 0.0f;
+}
+
 // Can kernels on the current device read `p`?  Device and managed memory,
 // and pinned or registered host memory (unified addressing), always; plain
 // pageable host memory only where the device reads host page tables (ATS on
@@ -89,7 +96,7 @@ extern "C" int zero1_accumulate_norm(const zero1_plan* plan, float* grad, const 
     NvtxRange range("zero1_accumulate_norm");
     if (plan == nullptr || micro_bf16 == nullptr || d_out == nullptr) return ZERO1_EINVAL;
     if (n_micro < 1 || n_micro > ZERO1_MAX_MICRO) return ZERO1_EINVAL;
-    if (!std::isfinite(grad_divisor) || !(grad_divisor > 0.0)) return ZERO1_EINVAL;
+    if (!divisor_ok(grad_divisor)) return ZERO1_EINVAL;
     if (std::isnan(extra_sumsq) || extra_sumsq < 0.0) return ZERO1_EINVAL;
     if (!aligned16(d_out)) return ZERO1_EALIGN;
     const int64_t n_tiles = zero1::norm_tiles(plan->arena_numel);
@@ -346,7 +353,7 @@ int list_grad_checked(const zero1_plan* plan, const void* d_table, float* const*
         if (!aligned16(d_out)) return ZERO1_EALIGN;
         if (std::isnan(extra_sumsq) || extra_sumsq < 0.0) return ZERO1_EINVAL;
     }
-    if (!std::isfinite(grad_divisor) || !(grad_divisor > 0.0)) return ZERO1_EINVAL;
+    if (!divisor_ok(grad_divisor)) return ZERO1_EINVAL;
     const int64_t n_chunks = static_cast<int64_t>(plan->list_chunks.size());
     if (n_chunks > 0) {
         if (d_table == nullptr || d_grad == nullptr || (reads_micro && d_micro == nullptr)) return ZERO1_EINVAL;

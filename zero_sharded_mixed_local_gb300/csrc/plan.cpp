@@ -37,8 +37,11 @@ extern "C" int zero1_plan_create_grouped(const int64_t* numels, const uint8_t* g
     *out = nullptr;
     if (n_tensors < 0 || dp_size < 1 || dp_rank < 0 || dp_rank >= dp_size) return ZERO1_EINVAL;
     if (n_tensors > 0 && (numels == nullptr || group == nullptr)) return ZERO1_EINVAL;
+    int64_t total = 0;  // bounded so that no offset, padded or not, can overflow
     for (int32_t i = 0; i < n_tensors; ++i) {
-        if (numels[i] < 0 || group[i] >= ZERO1_MAX_GROUPS) return ZERO1_EINVAL;
+        if (numels[i] < 0 || numels[i] > ZERO1_MAX_TOTAL_NUMEL - total || group[i] >= ZERO1_MAX_GROUPS)
+            return ZERO1_EINVAL;
+        total += numels[i];
     }
     for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) {
         if (lr_scale && !(std::isfinite(lr_scale[g]) && lr_scale[g] >= 0.0)) return ZERO1_EINVAL;
