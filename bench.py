@@ -412,6 +412,7 @@ class StepBench:
                                 device=dev, master=split(self.master), exp_avg=split(self.m),
                                 exp_avg_sq=split(self.v), grad=split(self.grad), weight_bf16=split(self.wbf))
         L = lopt.pointer_lists
+        plan = self.plan = lopt.plan  # the list calls take the plan whose run table they use
         micro_shards = [split(mb) for mb in self.micros]
         self.lists = {"master": L["master"], "m": L["exp_avg"], "v": L["exp_avg_sq"], "grad": L["grad"],
                       "w": L["weight_bf16"],

@@ -103,3 +103,24 @@ def test_skipped_step_keeps_the_step_count_with_check_finite(kind):
     b.step()
     for x, y in zip(_state(a), _state(b)):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+@pytest.mark.parametrize("kind", ["arena", "list"])
+def test_another_ranks_nonfinite_sum_skips_the_step(kind, monkeypatch):
+    """After the all-reduce of the sums of squares the local record's status is still OK, but
+    the sum is inf because another rank's gradient overflowed: the kernel skips the update,
+    and check_finite reports the skip and keeps the step count."""
+    import zero_sharded_mixed_local_gb300.optim as optim
+
+    def allreduce_with_an_inf_rank(norm_out, group):  # what the sum over the ranks gives
+        norm_out[:8].view(torch.float64).fill_(float("inf"))
+
+    monkeypatch.setattr(optim, "allreduce_sumsq_", allreduce_with_an_inf_rank)
+    a = _make(kind)
+    _init(a)
+    before = _state(a)
+    a.accumulate(_micro(a, 0), last=True)
+    assert a.step(group=object(), check_finite=True) is False and a.t == 0
+    assert z.read_norm(a.norm_out)["status"] == 0  # the local norm itself was finite
+    for x, y in zip(_state(a), before):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))

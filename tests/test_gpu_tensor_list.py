@@ -270,6 +270,27 @@ def test_pointer_lists_are_checked():
         z.PointerLists(plan, [good[0], torch.zeros(16, device="cuda")[::2]], torch.float32)  # not contiguous
     pl = z.PointerLists(plan, good, torch.float32)
     assert pl.dev.cpu().tolist()[:2] == [good[0].data_ptr(), good[1].data_ptr()]
+    # each call checks its lists against the plan's shard sizes, their dtype and list count, and
+    # that the run table is the plan's own, before anything is launched
+    other = z.Plan([64, 16], [0, 1], 1, 0)
+    table, ws, nout = plan.list_table(), plan.new_list_workspace(), z.new_norm_out()
+    foreign = z.PointerLists(other, [torch.zeros(64, device="cuda"), torch.zeros(16, device="cuda")], torch.float32)
+    bf = z.PointerLists(plan, [t.to(torch.bfloat16) for t in good], torch.bfloat16)
+    two = z.PointerLists(plan, [good, good], torch.float32)
+    with pytest.raises(ValueError):
+        z.list_grad_norm(plan, table, foreign, ws, nout)            # another plan's shard sizes
+    with pytest.raises(TypeError):
+        z.list_grad_norm(plan, table, bf, ws, nout)                 # bf16 shards as gradients
+    with pytest.raises(ValueError):
+        z.list_grad_norm(plan, other.list_table(), pl, ws, nout)    # another plan's run table
+    with pytest.raises(ValueError):
+        z.list_grad_norm(plan, table, pl, ws, nout[:16])            # short norm record
+    with pytest.raises(ValueError):
+        z.list_step(plan, table, two, pl, pl, pl, None, z.Hparams(), 1)   # two lists as the master
+    with pytest.raises(TypeError):
+        z.list_accumulate(plan, table, pl, pl)                      # fp32 shards as micro-batches
+    z.list_grad_norm(plan, table, pl, ws, nout)                     # the right arguments pass
+    assert z.read_norm(nout)["sumsq"] == 0.0
 
 
 def test_llama8b_full_size_list_equals_arena():

@@ -344,6 +344,15 @@ class Plan:
         return [arena[int(o):int(o) + int(c)] for o, c in zip(L.offsets, L.counts)]
 
 
+def _norm_ptr(norm_out, name="norm_out", device=None):
+    """Raw pointer of a norm-record buffer: a 16-byte aligned CUDA uint8 tensor of at least
+    NORM_OUT_BYTES bytes."""
+    p = _ptr(norm_out, torch.uint8, None, name, device)
+    if norm_out.numel() < NORM_OUT_BYTES:
+        raise ValueError("%s needs %d bytes (got %d)" % (name, NORM_OUT_BYTES, norm_out.numel()))
+    return p
+
+
 def new_norm_out(device="cuda"):
     """Device buffer for a zero1_norm_out (24 bytes, 16-byte aligned)."""
     return torch.zeros(32, dtype=torch.uint8, device=device)
@@ -382,9 +391,7 @@ def accumulate_norm(plan, grad, micro, workspace, norm_out, overwrite_first=True
     wp = _ptr(workspace, torch.uint8, None, "workspace", dev)
     if workspace.numel() < plan.workspace_bytes:
         raise ValueError("workspace has %d bytes, the plan needs %d" % (workspace.numel(), plan.workspace_bytes))
-    op = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
-    if norm_out.numel() < NORM_OUT_BYTES:
-        raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
+    op = _norm_ptr(norm_out, device=dev)
     _check(lib.zero1_accumulate_norm(plan.handle, gp, arr, len(micro), 1 if overwrite_first else 0,
                                      float(divisor), float(extra_sumsq), wp, workspace.numel(), op,
                                      _stream_ptr(stream, dev)), "zero1_accumulate_norm")
@@ -398,9 +405,7 @@ def grad_norm(plan, grad, workspace, norm_out, extra_sumsq=0.0, stream=None):
     wp = _ptr(workspace, torch.uint8, None, "workspace", dev)
     if workspace.numel() < plan.workspace_bytes:
         raise ValueError("workspace has %d bytes, the plan needs %d" % (workspace.numel(), plan.workspace_bytes))
-    op = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
-    if norm_out.numel() < NORM_OUT_BYTES:
-        raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
+    op = _norm_ptr(norm_out, device=dev)
     _check(lib.zero1_grad_norm(plan.handle, gp, float(extra_sumsq), wp, workspace.numel(), op,
                                _stream_ptr(stream, dev)), "zero1_grad_norm")
 
@@ -419,9 +424,7 @@ def grad_norm_static(plan, grad, norm_out, extra_sumsq=0.0, stream=None):
                          % (plan.arena_numel, STATIC_NORM_MAX_NUMEL))
     dev = norm_out.device
     gp = _ptr(grad, torch.float32, plan.arena_numel, "grad", dev)
-    op = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
-    if norm_out.numel() < NORM_OUT_BYTES:
-        raise ValueError("norm_out needs %d bytes" % NORM_OUT_BYTES)
+    op = _norm_ptr(norm_out, device=dev)
     _check(lib.zero1_grad_norm_static(plan.handle, gp, float(extra_sumsq), op, _stream_ptr(stream, dev)),
            "zero1_grad_norm_static")
 
@@ -434,9 +437,7 @@ def step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, hparams, step_t, 
     ptrs = [_ptr(master, torch.float32, n, "master", dev), _ptr(exp_avg, torch.float32, n, "exp_avg", dev),
             _ptr(exp_avg_sq, torch.float32, n, "exp_avg_sq", dev), _ptr(grad, torch.float32, n, "grad", dev)]
     wp = None if weight_bf16 is None else _ptr(weight_bf16, torch.bfloat16, n, "weight_bf16", dev)
-    npp = None
-    if norm_out is not None:
-        npp = _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    npp = None if norm_out is None else _norm_ptr(norm_out, device=dev)
     hp = hparams._c() if isinstance(hparams, Hparams) else Hparams(**hparams)._c()
     _check(lib.zero1_step(plan.handle, *ptrs, wp, ctypes.byref(hp), int(step_t), npp, _stream_ptr(stream, dev)),
            "zero1_step")
@@ -463,7 +464,7 @@ def step_dev(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, d_scalars, no
     sp = _ptr(d_scalars, torch.uint8, None, "d_scalars", dev)
     if d_scalars.numel() < STEP_SCALARS_BYTES:
         raise ValueError("d_scalars needs %d bytes" % STEP_SCALARS_BYTES)
-    npp = None if norm_out is None else _ptr(norm_out, torch.uint8, None, "norm_out", dev)
+    npp = None if norm_out is None else _norm_ptr(norm_out, device=dev)
     _check(lib.zero1_step_dev(plan.handle, *ptrs, wp, sp, npp, _stream_ptr(stream, dev)), "zero1_step_dev")
 
 
@@ -471,7 +472,7 @@ def read_norm(norm_out, stream=None):
     """zero1_read_norm: synchronise the stream and return the norm record as a dict."""
     lib = load_library()
     out = _NormOut()
-    _check(lib.zero1_read_norm(_ptr(norm_out, torch.uint8, None, "norm_out"),
+    _check(lib.zero1_read_norm(_norm_ptr(norm_out),
                                _stream_ptr(stream, norm_out.device), ctypes.byref(out)), "zero1_read_norm")
     return {"sumsq": out.sumsq, "norm": out.norm, "status": out.status, "n_partials": out.n_partials}
 
@@ -566,6 +567,10 @@ class PointerLists:
 
     def __init__(self, plan, lists, dtype, device=None, stream=None, keep=True):
         lib = load_library()
+        if device is not None:
+            device = torch.device(device)
+            if device.type == "cuda" and device.index is None:
+                device = torch.device("cuda", torch.cuda.current_device())
         if len(lists) and (isinstance(lists[0], torch.Tensor) or lists[0] is None):
             lists = [lists]
         lists = [list(x) for x in lists]
@@ -587,7 +592,7 @@ class PointerLists:
                     raise ValueError("entry %d of list %d must be on a CUDA device (got %s)" % (i, k, t.device))
                 if device is None:
                     device = t.device
-                elif t.device != torch.device(device):
+                elif t.device != device:
                     raise ValueError("entry %d of list %d is on %s, expected %s" % (i, k, t.device, device))
                 if t.dtype != dtype:
                     raise TypeError("entry %d of list %d must be %s (got %s)" % (i, k, dtype, t.dtype))
@@ -606,6 +611,8 @@ class PointerLists:
                                           ctypes.c_void_p(self.dev.data_ptr()), self.dev.numel() * 8,
                                           _stream_ptr(stream, self.device)), "zero1_list_ptrs_upload")
         self.tensors = lists if keep else None
+        self.dtype = dtype
+        self.counts = counts  # the plan's shard sizes: the calls check the lists against their plan
 
     @property
     def ptr(self):
@@ -613,30 +620,55 @@ class PointerLists:
 
 
 def _list_args(plan, table, stream, device):
-    if not isinstance(table, torch.Tensor) or table.device.type != "cuda":
-        raise ValueError("table must be the plan's device run table (Plan.list_table)")
-    if table.numel() < plan._lib.zero1_list_table_bytes(plan.handle):
-        raise ValueError("table is smaller than this plan's run table")
+    # The library cannot see inside device memory: a run table of another plan would
+    # index past the pointer lists, so only the table this plan uploaded is accepted.
+    if not isinstance(table, torch.Tensor) or plan.__dict__.get("_list_tables", {}).get(table.device) is not table:
+        raise ValueError("table must be this plan's device run table (Plan.list_table)")
+    if table.device != device:
+        raise ValueError("table is on %s, the lists on %s" % (table.device, device))
     return ctypes.c_void_p(table.data_ptr()), _stream_ptr(stream, device)
+
+
+def _lists(plan, pl, name, dtype, device, one_list=True):
+    """Device pointer of checked PointerLists: built for this plan's shard sizes, of
+    ``dtype``, on ``device``, holding one list (or 1..MAX_MICRO micro-batch lists)."""
+    if not isinstance(pl, PointerLists):
+        raise TypeError("%s must be PointerLists" % name)
+    counts = plan.layout().counts
+    if pl.counts is not counts and not np.array_equal(pl.counts, counts):
+        raise ValueError("%s was built for a plan with other shard sizes" % name)
+    if pl.dtype != dtype:
+        raise TypeError("%s must hold %s shards (got %s)" % (name, dtype, pl.dtype))
+    if pl.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, pl.device, device))
+    if one_list and pl.n_lists != 1:
+        raise ValueError("%s must be a single list (got %d)" % (name, pl.n_lists))
+    return pl.ptr
 
 
 def list_accumulate(plan, table, grads: PointerLists, micro: PointerLists, overwrite_first=True, stream=None):
     """zero1_list_accumulate: every fp32 gradient shard = [itself +] the sum of its bf16
     micro-batch shards (``micro`` holds one list per micro-batch)."""
     lib = load_library()
-    tp, sp = _list_args(plan, table, stream, grads.device)
-    _check(lib.zero1_list_accumulate(plan.handle, tp, grads.ptr, micro.ptr, micro.n_lists,
-                                     1 if overwrite_first else 0, sp), "zero1_list_accumulate")
+    dev = grads.device
+    tp, sp = _list_args(plan, table, stream, dev)
+    gp = _lists(plan, grads, "grads", torch.float32, dev)
+    mp = _lists(plan, micro, "micro", torch.bfloat16, dev, one_list=False)
+    _check(lib.zero1_list_accumulate(plan.handle, tp, gp, mp, micro.n_lists, 1 if overwrite_first else 0, sp),
+           "zero1_list_accumulate")
 
 
 def list_accumulate_norm(plan, table, grads: PointerLists, micro: PointerLists, workspace, norm_out,
                          overwrite_first=True, extra_sumsq=0.0, divisor=1.0, stream=None):
     """zero1_list_accumulate_norm: accumulate, divide by ``divisor`` and take the norm record."""
     lib = load_library()
-    tp, sp = _list_args(plan, table, stream, grads.device)
-    ws = _ptr(workspace, torch.uint8, None, "workspace", grads.device)
-    no = _ptr(norm_out, torch.uint8, None, "norm_out", grads.device)
-    _check(lib.zero1_list_accumulate_norm(plan.handle, tp, grads.ptr, micro.ptr, micro.n_lists,
+    dev = grads.device
+    tp, sp = _list_args(plan, table, stream, dev)
+    gp = _lists(plan, grads, "grads", torch.float32, dev)
+    mp = _lists(plan, micro, "micro", torch.bfloat16, dev, one_list=False)
+    ws = _ptr(workspace, torch.uint8, None, "workspace", dev)
+    no = _norm_ptr(norm_out, device=dev)
+    _check(lib.zero1_list_accumulate_norm(plan.handle, tp, gp, mp, micro.n_lists,
                                           1 if overwrite_first else 0, float(divisor), float(extra_sumsq), ws,
                                           workspace.numel(), no, sp), "zero1_list_accumulate_norm")
 
@@ -644,11 +676,20 @@ def list_accumulate_norm(plan, table, grads: PointerLists, micro: PointerLists, 
 def list_grad_norm(plan, table, grads: PointerLists, workspace, norm_out, extra_sumsq=0.0, stream=None):
     """zero1_list_grad_norm: the norm record of the gradient shards."""
     lib = load_library()
-    tp, sp = _list_args(plan, table, stream, grads.device)
-    ws = _ptr(workspace, torch.uint8, None, "workspace", grads.device)
-    no = _ptr(norm_out, torch.uint8, None, "norm_out", grads.device)
-    _check(lib.zero1_list_grad_norm(plan.handle, tp, grads.ptr, float(extra_sumsq), ws, workspace.numel(), no, sp),
+    dev = grads.device
+    tp, sp = _list_args(plan, table, stream, dev)
+    gp = _lists(plan, grads, "grads", torch.float32, dev)
+    ws = _ptr(workspace, torch.uint8, None, "workspace", dev)
+    no = _norm_ptr(norm_out, device=dev)
+    _check(lib.zero1_list_grad_norm(plan.handle, tp, gp, float(extra_sumsq), ws, workspace.numel(), no, sp),
            "zero1_list_grad_norm")
+
+
+def _step_lists(plan, master, exp_avg, exp_avg_sq, grads, weight_bf16, dev):
+    f32 = [_lists(plan, pl, name, torch.float32, dev) for pl, name in
+           ((master, "master"), (exp_avg, "exp_avg"), (exp_avg_sq, "exp_avg_sq"), (grads, "grads"))]
+    w = None if weight_bf16 is None else _lists(plan, weight_bf16, "weight_bf16", torch.bfloat16, dev)
+    return f32 + [w]
 
 
 def list_step(plan, table, master: PointerLists, exp_avg: PointerLists, exp_avg_sq: PointerLists,
@@ -657,11 +698,11 @@ def list_step(plan, table, master: PointerLists, exp_avg: PointerLists, exp_avg_
     lib = load_library()
     dev = master.device
     tp, sp = _list_args(plan, table, stream, dev)
+    ptrs = _step_lists(plan, master, exp_avg, exp_avg_sq, grads, weight_bf16, dev)
     hp = hparams if isinstance(hparams, Hparams) else Hparams(**hparams)
-    no = None if norm_out is None else _ptr(norm_out, torch.uint8, None, "norm_out", dev)
-    _check(lib.zero1_list_step(plan.handle, tp, master.ptr, exp_avg.ptr, exp_avg_sq.ptr, grads.ptr,
-                               None if weight_bf16 is None else weight_bf16.ptr, ctypes.byref(hp._c()),
-                               int(step_t), no, sp), "zero1_list_step")
+    no = None if norm_out is None else _norm_ptr(norm_out, device=dev)
+    _check(lib.zero1_list_step(plan.handle, tp, *ptrs, ctypes.byref(hp._c()), int(step_t), no, sp),
+           "zero1_list_step")
 
 
 def list_step_dev(plan, table, master: PointerLists, exp_avg: PointerLists, exp_avg_sq: PointerLists,
@@ -671,10 +712,9 @@ def list_step_dev(plan, table, master: PointerLists, exp_avg: PointerLists, exp_
     lib = load_library()
     dev = master.device
     tp, sp = _list_args(plan, table, stream, dev)
+    ptrs = _step_lists(plan, master, exp_avg, exp_avg_sq, grads, weight_bf16, dev)
     sc = _ptr(d_scalars, torch.uint8, None, "d_scalars", dev)
     if d_scalars.numel() < STEP_SCALARS_BYTES:
         raise ValueError("d_scalars holds %d bytes, the step scalars need %d" % (d_scalars.numel(), STEP_SCALARS_BYTES))
-    no = None if norm_out is None else _ptr(norm_out, torch.uint8, None, "norm_out", dev)
-    _check(lib.zero1_list_step_dev(plan.handle, tp, master.ptr, exp_avg.ptr, exp_avg_sq.ptr, grads.ptr,
-                                   None if weight_bf16 is None else weight_bf16.ptr, sc, no, sp),
-           "zero1_list_step_dev")
+    no = None if norm_out is None else _norm_ptr(norm_out, device=dev)
+    _check(lib.zero1_list_step_dev(plan.handle, tp, *ptrs, sc, no, sp), "zero1_list_step_dev")

@@ -24,6 +24,8 @@ gradients before) sit outside this rank's step.  Weight decay is skipped for
 parameters the ``no_decay`` predicate selects (by default 1-D parameters:
 norm weights and biases).
 """
+import math
+
 import torch
 
 from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, Hparams, list_accumulate,
@@ -32,9 +34,12 @@ from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, 
 
 
 def _applied(opt, stream):
-    """Whether the step just launched applied (a finite global norm); a skipped step gives its
-    number back, so bias correction stays matched to the updates m and v received."""
-    if read_norm(opt.norm_out, stream=stream)["status"] == 0:
+    """Whether the step just launched applied; a skipped step gives its number back, so bias
+    correction stays matched to the updates m and v received.  The kernel skips on the same
+    two conditions: a non-finite local norm (the record's status) or a non-finite sum of
+    squares after the all-reduce (another rank's inf or NaN)."""
+    rec = read_norm(opt.norm_out, stream=stream)
+    if rec["status"] == 0 and math.isfinite(rec["sumsq"]):
         return True
     opt.t -= 1
     return False
@@ -133,7 +138,9 @@ class StepGraph:
     alternate, so the host may write step t+1's scalars while step t still
     runs; it waits only for step t-1.  No collective is captured: use it where
     the sum of squares needs no all-reduce (one rank, or a caller that
-    all-reduces the norm record in its own graph).
+    all-reduces the norm record in its own graph).  A replay whose norm is not
+    finite leaves the state untouched (the kernel skips) while ``t`` still advances,
+    as with ``step()`` without ``check_finite``.
     """
 
     def __init__(self, opt, micro_buffers):
@@ -224,7 +231,7 @@ class ShardListAdamW:
     tensors, one per parameter (model order, each exactly its shard's length); pass
     your own (for instance the fp32 state a framework already keeps per parameter) or
     let the constructor allocate zeroed ones.  Micro-batch gradients are lists of bf16
-    shard tensors, whose device pointer lists are cached by (address, length) of every
+    shard tensors, whose device pointer lists are cached by (address, length, dtype) of every
     tensor, so a loop that reuses the same gradient buffers uploads them once; or a
     PointerLists the caller built once."""
 
@@ -260,8 +267,8 @@ class ShardListAdamW:
         if len(micro) and isinstance(micro[0], torch.Tensor):
             micro = [micro]
         # A cached upload stays valid for tensors at the same addresses with the same lengths
-        # (what the upload checked); it keeps no reference to them.
-        key = tuple(tuple((t.data_ptr(), t.numel()) for t in lst) for lst in micro)
+        # and dtype (what the upload checked); it keeps no reference to them.
+        key = tuple(tuple((t.data_ptr(), t.numel(), t.dtype) for t in lst) for lst in micro)
         pl = self._micro_cache.get(key)
         if pl is None:
             if len(self._micro_cache) >= 8:
