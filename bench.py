@@ -258,7 +258,7 @@ def timed_oracle_steps(w, n, threads, budget_s, max_steps=50):
     return steps * n / total, steps, total
 
 
-def cpu_baseline(w, target_s=12.0, max_elems=1 << 27):
+def cpu_baseline(w, target_s=10.0, max_elems=1 << 27):
     """Time the oracle as it stands on a bounded sample for about target_s seconds: two thirds on
     every host core (contiguous ranges, the headline value), the rest on one core."""
     threads = host_threads()
@@ -322,6 +322,9 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--checkpoint-io", action="store_true",
+                    help="also time an optimizer-shard checkpoint of the state (save_async, save, load) on "
+                         "the host's disk, outside the timed step")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--unfused", action="store_true",
                     help="take the norm in its own pass (zero1_grad_norm) instead of fusing it into the last "
@@ -675,6 +678,56 @@ def run_e2e(b, args, world, P_job):
                    "buffers, overlapping the previous step's kernels; norm record read back every step"}
 
 
+def checkpoint_io(b):
+    """This rank's optimizer-shard checkpoint (master, m, v) on the host disk, after the timed
+    steps: how long save_async holds the caller (the device-to-host snapshot) with new and with
+    reused page-locked staging, the whole save (fsync'd files), and a load into scrambled state
+    that must restore it bit for bit."""
+    import shutil
+    import tempfile
+    z = b.z
+    states = ((b.lopt.master, b.lopt.exp_avg, b.lopt.exp_avg_sq) if b.lopt is not None
+              else (b.master, b.m, b.v))
+    if any(x is None for x in states):
+        return None  # an arena graph run keeps its state in the graph's own object
+    flat = lambda x: list(x) if isinstance(x, (list, tuple)) else [x]  # noqa: E731
+    before = [t.clone() for x in states for t in flat(x)]
+    nbytes = 12 * b.P
+    d = tempfile.mkdtemp(prefix="zero1-ckpt-")
+    out = {"bytes": nbytes, "where": "the host's local disk, fsync'd; %s" % (
+        "per-tensor shard lists" if b.lopt is not None else "arenas")}
+    try:
+        for label in ("new_staging", "reused_staging"):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fut = z.checkpoint.save_async(d, b.plan, *states, step_t=max(b.t, 1))
+            t1 = time.perf_counter()
+            fut.result()
+            t2 = time.perf_counter()
+            out["snapshot_ms_" + label] = (t1 - t0) * 1e3
+            out["save_s_" + label] = t2 - t0
+        out["snapshot_gbs"] = nbytes / (out["snapshot_ms_reused_staging"] * 1e-3) / 1e9
+        out["save_gbs"] = nbytes / out["save_s_reused_staging"] / 1e9
+        for x in states:
+            for t in flat(x):
+                t.fill_(-1.0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        z.checkpoint.load(d, b.plan, *states)
+        torch.cuda.synchronize()
+        out["load_s"] = time.perf_counter() - t0
+        out["load_gbs"] = nbytes / out["load_s"] / 1e9
+        after = [t for x in states for t in flat(x)]
+        out["restored_bit_exact"] = all(torch.equal(u.view(torch.int32), v.view(torch.int32))
+                                        for u, v in zip(before, after))
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+        z.checkpoint.release_staging()
+    if not out["restored_bit_exact"]:
+        raise SystemExit("checkpoint load did not restore the state")
+    return out
+
+
 def main():
     args = parse_args()
     from zero_sharded_mixed_local_gb300.workloads import get_workload
@@ -703,6 +756,8 @@ def main():
     path_bytes = b.path_bytes()
 
     e2e = run_e2e(b, args, world, P_job) if not args.no_e2e and b.graph is None else None
+
+    ckpt = checkpoint_io(b) if args.checkpoint_io and world == 1 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -752,6 +807,8 @@ def main():
             "clocks": clk,
             "gpu_launches": args.steps * b.launches_per_step(),  # also inside each graph
         }
+        if ckpt is not None:
+            out["checkpoint"] = ckpt
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist

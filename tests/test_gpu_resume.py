@@ -124,3 +124,27 @@ def test_another_ranks_nonfinite_sum_skips_the_step(kind, monkeypatch):
     assert z.read_norm(a.norm_out)["status"] == 0  # the local norm itself was finite
     for x, y in zip(_state(a), before):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+@pytest.mark.parametrize("kind", ["arena", "list"])
+def test_overlapping_checkpoints_keep_their_own_snapshots(kind, tmp_path):
+    """Two asynchronous saves in flight at once, the state stepped in between: each takes its
+    own page-locked staging, so each checkpoint holds the state of the moment it was taken."""
+    a = _make(kind)
+    _init(a)
+    s0 = _state(a)
+    f0 = a.save_checkpoint(str(tmp_path / "c0"), async_=True)
+    a.accumulate(_micro(a, 0), last=True)
+    a.step()
+    s1 = _state(a)
+    f1 = a.save_checkpoint(str(tmp_path / "c1"), async_=True)
+    a.accumulate(_micro(a, 1), last=True)
+    a.step()  # changes the state while the second save may still be writing
+    f0.result()
+    f1.result()
+    for path, want, t in (("c0", s0, 0), ("c1", s1, 1)):
+        b = _make(kind)
+        assert b.load_checkpoint(str(tmp_path / path)) == t
+        for x, y in zip(_state(b), want):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    z.checkpoint.release_staging()
