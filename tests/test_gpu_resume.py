@@ -132,6 +132,7 @@ def test_overlapping_checkpoints_keep_their_own_snapshots(kind, tmp_path):
     own page-locked staging, so each checkpoint holds the state of the moment it was taken."""
     a = _make(kind)
     _init(a)
+    z.checkpoint.prepare_staging(a.plan)
     s0 = _state(a)
     f0 = a.save_checkpoint(str(tmp_path / "c0"), async_=True)
     a.accumulate(_micro(a, 0), last=True)

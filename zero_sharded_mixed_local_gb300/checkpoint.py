@@ -20,8 +20,8 @@ State on the GPU is copied through page-locked host buffers: one copy per
 arena (or per shard) on the current stream and one synchronisation, at the
 speed of the CPU-GPU link rather than of pageable staging.  The buffers are
 kept for the next checkpoint (pinning many GB costs more than the copy), at
-most one set per arena size while no save is in flight; ``release_staging()``
-frees them.
+most one set per arena size while no save is in flight; ``prepare_staging()``
+pins them ahead of the first checkpoint and ``release_staging()`` frees them.
 
 Each quantity is given either as an arena (one padded fp32 tensor laid out by
 the plan) or as a list of per-tensor shard tensors in model order (the form
@@ -67,6 +67,14 @@ class _StagingPool:
 
 
 _staging = _StagingPool()
+
+
+def prepare_staging(plan):
+    """Pin one checkpoint's worth of staging buffers for ``plan`` now (at start-up, say), so the
+    first snapshot does not pay for pinning.  Needs CUDA."""
+    bufs = [_staging.take(plan.arena_numel) for _ in QUANTITIES]
+    for b in bufs:
+        _staging.give(b)
 
 
 def release_staging():
