@@ -584,6 +584,11 @@ def kernel_report(b, recs, args):
         for name, (x, y) in (("shard_gather", ("x0", "a0")), ("shard_scatter", ("s1", "x1"))):
             ms = mean(x, y)
             kernels[name] = {"ms": ms, "gbs": 4 * P / (ms * 1e-3) / 1e9, "launches_per_step": 1}
+    pairs = {"accumulate": ("a0", "n0"), "accumulate_norm": ("n0", "s0"), "accumulate+grad_norm": ("n0", "s0"),
+             b.step_kernel: ("s0", "s1"), "shard_gather": ("x0", "a0"), "shard_scatter": ("s1", "x1")}
+    for name, k in kernels.items():  # "ms" is the mean over the timed steps; the spread beside it
+        times = [r[pairs[name][0]].elapsed_time(r[pairs[name][1]]) for r in recs]
+        k["ms_median"], k["ms_min"], k["ms_max"] = statistics.median(times), min(times), max(times)
     peak, peak_kind = measured_peaks()
     achieved = kernels[b.step_kernel]["gbs"]
     roofline = {"bound": "hbm", "kernel": b.step_kernel + "_kernel", "achieved": achieved, "peak": peak,

@@ -40,3 +40,14 @@ def test_bench_line_has_the_contract_keys(extra):
     if not extra:
         e = d["e2e"]
         assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 24
+    for k in d["kernels"].values():
+        assert k["ms_min"] <= k["ms_median"] <= k["ms_max"]
+
+
+@pytest.mark.parametrize("extra", [[], ["--tensor-list"]])
+def test_bench_checkpoint_io_restores_the_state(extra):
+    d = _run("--workload", "toy", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-e2e",
+             "--checkpoint-io", *extra)
+    c = d["checkpoint"]
+    assert c["restored_bit_exact"] is True and c["bytes"] == 12 * d["config"]["local_params_per_gpu"]
+    assert c["save_gbs"] > 0 and c["load_gbs"] > 0 and c["snapshot_gbs"] > 0
