@@ -322,6 +322,8 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-torch-baseline", action="store_true",
+                    help="skip the stock-PyTorch version of the step on the same GPU")
     ap.add_argument("--checkpoint-io", action="store_true",
                     help="also time an optimizer-shard checkpoint of the state (save_async, save, load) on "
                          "the host's disk, outside the timed step")
@@ -683,6 +685,74 @@ def run_e2e(b, args, world, P_job):
                    "buffers, overlapping the previous step's kernels; norm record read back every step"}
 
 
+def torch_baseline(b, args):
+    """The same step in stock PyTorch, on the same GPU and the same arenas, the way the pages'
+    nanotron configuration runs it (accumulate_grad_in_fp32, clip_grad 1.0, torch_adam_is_fused):
+    the bf16 micro-batch gradients copied / added into the fp32 gradient, clip_grad_norm_
+    (foreach), torch.optim.AdamW(fused=True) with a decay and a no-decay group, then the bf16 copy
+    of the master.  A GPU comparison for the fused kernels; run last, since it changes the state.
+    Its own arithmetic differs in order (lerp, addcdiv) and it writes the clipped gradient back."""
+    if b.master is None or b.world > 1:
+        return None
+    P, K, hp = b.P, b.K, b.hp
+    master, grad, wbf, micros = b.master, b.grad, b.wbf, b.micros
+    groups = []
+    for g, wd in ((0, hp.weight_decay), (1, 0.0)):
+        lo, hi = b.plan.group_range(g)
+        if hi > lo:
+            pv = master[lo:hi]
+            pv.grad = grad[lo:hi]
+            groups.append({"params": [pv], "weight_decay": wd})
+    params = [g["params"][0] for g in groups]
+    opt = torch.optim.AdamW(groups, lr=hp.lr, betas=(hp.beta1, hp.beta2), eps=hp.eps, fused=True)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    parts = ("accumulate", "clip_grad_norm_", "adamw_fused", "bf16_copy")
+
+    def step(rec=None):
+        def mark(j):
+            if rec is not None:
+                rec[j].record()
+        mark(0)
+        grad.copy_(micros[0])
+        for k in range(1, K):
+            grad.add_(micros[k])
+        mark(1)
+        torch.nn.utils.clip_grad_norm_(params, hp.clip_grad, foreach=True)
+        mark(2)
+        opt.step()
+        mark(3)
+        wbf.copy_(master)
+        mark(4)
+
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=b.dev) if b.path_bytes() < 4 * L2_BYTES else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    recs = []
+    for _ in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        recs.append([ev() for _ in range(5)])
+        step(recs[-1])
+    torch.cuda.synchronize()
+    ms = statistics.mean(r[0].elapsed_time(r[4]) for r in recs)
+    op_bytes = (accumulate_bytes_per_elem(K), 4 + 8, 28, 6)  # clip: norm read, then the scale R+W
+    ops = {}
+    for j, (name, nb) in enumerate(zip(parts, op_bytes)):
+        t = statistics.mean(r[j].elapsed_time(r[j + 1]) for r in recs)
+        ops[name] = {"ms": t, "bytes_per_param": nb, "gbs": nb * P / (t * 1e-3) / 1e9}
+    per_param = accumulate_bytes_per_elem(K) + 4 + 8 + 28 + 6  # norm read, clip scale R+W, AdamW, bf16 copy
+    del opt
+    return {"value": P / (ms * 1e-3), "unit": "params/s", "ms_per_step": ms, "bytes_per_param": per_param,
+            "hbm_gbs": per_param * P / (ms * 1e-3) / 1e9, "ops": ops,
+            "timing": "CUDA events around each op of every step, mean over the timed steps%s" % (
+                " (L2 flushed before each step)" if flush is not None else ""),
+            "how": "stock PyTorch %s on the same arenas: copy_/add_ of the K bf16 micro-batches into the fp32 "
+                   "gradient, clip_grad_norm_(foreach=True), torch.optim.AdamW(fused=True) with decay and no-decay "
+                   "groups, bf16 copy_ of the master" % torch.__version__}
+
+
 def checkpoint_io(b):
     """This rank's optimizer-shard checkpoint (master, m, v) on the host disk, after the timed
     steps: how long save_async holds the caller (the device-to-host snapshot) with new and with
@@ -767,6 +837,7 @@ def main():
     e2e = run_e2e(b, args, world, P_job) if not args.no_e2e and b.graph is None else None
 
     ckpt = checkpoint_io(b) if args.checkpoint_io and world == 1 else None
+    tb = None if args.no_torch_baseline else torch_baseline(b, args)  # last: it changes the state
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -818,6 +889,9 @@ def main():
         }
         if ckpt is not None:
             out["checkpoint"] = ckpt
+        if tb is not None:
+            tb["ours_over_torch"] = out["value"] / tb["value"]
+            out["torch_baseline"] = tb
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist

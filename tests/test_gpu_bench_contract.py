@@ -40,6 +40,8 @@ def test_bench_line_has_the_contract_keys(extra):
     if not extra:
         e = d["e2e"]
         assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 24
+        tb = d["torch_baseline"]  # the stock PyTorch step on the same GPU
+        assert tb["value"] > 0 and tb["bytes_per_param"] == 6 + 10 + 4 + 8 + 28 + 6  # K = 2
     for k in d["kernels"].values():
         assert k["ms_min"] <= k["ms_median"] <= k["ms_max"]
 
