@@ -374,7 +374,9 @@ class StepBench:
         self.args, self.w, self.z, self.world = args, w, z, world
         self.dev = dev = torch.device("cuda", local)
         self.dp_rank = (w.dp_rank + rank) % w.dp_size if world > 1 else w.dp_rank
+        t0 = time.perf_counter()
         self.plan = plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, self.dp_rank)
+        self.plan_ms = (time.perf_counter() - t0) * 1e3  # a1, on the host, once per job
         L = plan.layout()
         gen = InputGenerator(w, Layout(L.counts, L.offsets, L.no_decay, L.arena_numel), dev, seed=w.seed + rank)
         self.P, self.K = plan.local_numel, w.micro_batches
@@ -887,6 +889,9 @@ def main():
             "clocks": clk,
             "gpu_launches": args.steps * b.launches_per_step(),  # also inside each graph
         }
+        out["plan"] = {"build_ms": b.plan_ms, "tensors": len(w.params.numels),
+                       "list_table_bytes": int(b.z.load_library().zero1_list_table_bytes(b.plan.handle)),
+                       "layout_table_bytes": int(b.z.load_library().zero1_layout_table_bytes(b.plan.handle))}
         if ckpt is not None:
             out["checkpoint"] = ckpt
         if tb is not None:
