@@ -80,22 +80,27 @@ def profile_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms around the timed region.
+    Each sample carries nvidia-smi's own timestamp, so the median SM clock is taken over the
+    samples that fall inside the region (all samples if none do); the throttle reasons are
+    collected over every sample, a superset of the region's."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
         self.thread = None
+        self.region = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -108,6 +113,18 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def mark(self, t_begin, t_end):
+        """The timed region in host wall-clock seconds (time.time())."""
+        self.region = (t_begin, t_end)
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def stop(self):
         if self.proc is None:
             return None
@@ -119,24 +136,27 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, mx, reasons = [], None, set()
+        samples, mx, reasons = [], None, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                samples.append((self._when(parts[0]), float(parts[2])))
+                mx = float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
-        if not sm:
+        if not samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [mhz for when, mhz in samples
+                  if self.region is not None and when is not None and self.region[0] <= when <= self.region[1]]
+        return {"sm_mhz": statistics.median(inside or [mhz for _, mhz in samples]), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(samples), "samples_in_timed_region": len(inside),
+                "interval_ms": self.INTERVAL_MS}
 
 
 def dist_setup():
@@ -543,6 +563,7 @@ def time_steps(b, args, world, local):
     start, end = ev(), ev()
     torch.cuda.synchronize()
     barrier(world)
+    t_begin = time.time()
     start.record(b.stream)
     for i in range(args.steps):
         if flush is not None:
@@ -552,6 +573,7 @@ def time_steps(b, args, world, local):
         recs[i]["t1"].record(b.stream)
     end.record(b.stream)
     torch.cuda.synchronize()
+    clocks.mark(t_begin, time.time())
     barrier(world)
     clk = clocks.stop()
     if flush is not None:

@@ -80,3 +80,30 @@ def test_bench_rank_helpers_with_gloo():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert got == [(0, 2_000_000_015, 5.25), (1, 2_000_000_015, 5.25)]
+
+
+def test_clock_samples_inside_the_timed_region():
+    """The median SM clock comes from the nvidia-smi samples stamped inside the timed region;
+    throttle reasons are gathered from every sample (a superset of the region's)."""
+    c = bench.ClockSampler(0)
+    c.lines = [
+        "2026/12/02 10:18:33.100, 0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:18:33.150, 0, 1980, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:18:33.200, 0, 1990, 2070, 1310.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:18:34.150, 0, 1500, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "not a sample line",
+    ]
+    c.mark(c._when("2026/12/02 10:18:33.120"), c._when("2026/12/02 10:18:33.500"))
+
+    class _Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            pass
+
+    c.proc = _Done()
+    got = c.stop()
+    assert got["samples"] == 4 and got["samples_in_timed_region"] == 2
+    assert got["sm_mhz"] == 1985.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"]
