@@ -489,6 +489,13 @@ int zero1_list_step_dev(const zero1_plan* plan, const void* d_table, float* cons
 /* Static description of a status code. */
 const char* zero1_strerror(int code);
 
+/* Kernel launches the library has issued since it was loaded, over all
+ * threads: a diagnostic, so a caller can count the kernels its calls cost
+ * and see that they reach the GPU.  A launch made while a stream is being
+ * captured into a CUDA graph counts once, at capture; graph replays do not
+ * count.  Never fails. */
+uint64_t zero1_launch_count(void);
+
 /* Text of the CUDA error behind the calling thread's last ZERO1_ECUDA
  * ("" if none). */
 const char* zero1_last_cuda_error(void);

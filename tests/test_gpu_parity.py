@@ -575,3 +575,23 @@ def test_four_element_worked_example_on_the_gpu():
         assert got["sumsq"] == 2.640625 and got["norm"] == 1.625
         vals = torch.cat([master[int(o):int(o) + 2] for o in offs]).cpu().numpy()
         np.testing.assert_allclose(vals, expect, rtol=0, atol=2.5e-7)
+
+
+def test_launch_count_counts_each_kernel():
+    """zero1_launch_count grows by the kernels each call launches: a plain accumulate one, the
+    fused last pass two (the tile pass and the final reduction), the step one, a separate norm
+    two; a call rejected before any launch none."""
+    pb = Problem(_custom([16384 * 2 + 13, 77], [0, 1], K=2, steps=1, sigma=0.1))
+    micros = pb.gen.micro_grads()
+    c0 = z.launch_count()
+    z.accumulate(pb.plan, pb.grad, micros[0])
+    assert z.launch_count() - c0 == 1
+    z.accumulate_norm(pb.plan, pb.grad, micros[1], pb.ws, pb.nout, overwrite_first=False)
+    assert z.launch_count() - c0 == 3
+    z.step(pb.plan, pb.master, pb.m, pb.v, pb.grad, pb.wbf, pb.hp, 1, pb.nout)
+    assert z.launch_count() - c0 == 4
+    z.grad_norm(pb.plan, pb.grad, pb.ws, pb.nout)
+    assert z.launch_count() - c0 == 6
+    with pytest.raises(z.Zero1Error):
+        z.step(pb.plan, pb.master, pb.m, pb.v, pb.grad, pb.wbf, pb.hp, 0, pb.nout)  # t < 1
+    assert z.launch_count() - c0 == 6

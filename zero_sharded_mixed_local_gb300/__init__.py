@@ -13,9 +13,10 @@ shards, CUDA-graph replay, a torch-module wrapper); ``checkpoint`` and
 from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_EALIGN, ZERO1_ECUDA, ZERO1_EINVAL,
                       ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, Plan, PointerLists,
                       ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm,
-                      exchange_chunk_numel, grad_norm, grad_norm_static, list_accumulate, list_accumulate_norm,
-                      list_grad_norm, list_step, list_step_dev, load_library, new_norm_out, pack_reduce_scatter,
-                      read_norm, shard_gather, shard_scatter, step, step_dev, step_scalars, unpack_all_gather)
+                      exchange_chunk_numel, grad_norm, grad_norm_static, launch_count, list_accumulate,
+                      list_accumulate_norm, list_grad_norm, list_step, list_step_dev, load_library, new_norm_out,
+                      pack_reduce_scatter, read_norm, shard_gather, shard_scatter, step, step_dev, step_scalars,
+                      unpack_all_gather)
 from . import checkpoint
 from .optim import LocalShardAdamW, ShardListAdamW, StepGraph, Zero1AdamW, default_no_decay
 from .schedules import lr_at, mup_groups

@@ -109,6 +109,7 @@ def load_library(path=None):
         "zero1_list_step_dev": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "zero1_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "zero1_last_cuda_error": (ctypes.c_char_p, []),
+        "zero1_launch_count": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -116,6 +117,11 @@ def load_library(path=None):
         fn.argtypes = args
     _lib = lib
     return lib
+
+
+def launch_count():
+    """zero1_launch_count: kernel launches the library has issued since it was loaded."""
+    return int(load_library().zero1_launch_count())
 
 
 def _check(code, where):

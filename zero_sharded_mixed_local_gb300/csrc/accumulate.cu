@@ -285,7 +285,7 @@ cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, 
             case 8: launch_kway<8>(p, g, pairs, first, stream); break;
             default: accumulate_norm_kernel<false><<<g, kTileThreads, 0, stream>>>(p, pairs, first);
         }
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = after_launch();
         if (e != cudaSuccess) return e;
     }
     return launch_norm_final(pairs, n_tiles, extra_sumsq, out, stream);
@@ -295,7 +295,7 @@ cudaError_t launch_accumulate(const AccumulateParams& p, cudaStream_t stream) {
     for (int64_t first = 0; first < p.n_vec; first += kMaxGridVectors(kAccThreads)) {
         const int64_t n = p.n_vec - first < kMaxGridVectors(kAccThreads) ? p.n_vec - first : kMaxGridVectors(kAccThreads);
         accumulate_kernel<<<static_cast<unsigned>((n + kAccThreads - 1) / kAccThreads), kAccThreads, 0, stream>>>(p, first);
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = after_launch();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -137,7 +137,7 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t stream) {
         } else {
             adamw_step_kernel<false, false><<<grid, kStepThreads, 0, stream>>>(p, first);
         }
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = after_launch();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -1,6 +1,7 @@
 // C entry points of the compute calls: argument checks, derivation of the
 // fp32 step scalars, and the kernel launches.  Nothing here allocates device
 // memory or synchronises, except zero1_read_norm.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -61,7 +62,18 @@ namespace zero1 {
 
 int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+cudaError_t after_launch() {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError();
+}
+
 }  // namespace zero1
+
+extern "C" uint64_t zero1_launch_count(void) { return zero1::g_launches.load(std::memory_order_relaxed); }
 
 extern "C" int zero1_accumulate(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
                                 int32_t n_micro, int32_t overwrite_first, void* stream) {

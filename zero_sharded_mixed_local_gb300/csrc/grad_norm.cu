@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kFinalThreads)
 cudaError_t launch_norm_final(const float2* partials, int64_t n_tiles, double extra_sumsq, zero1_norm_out* out,
                               cudaStream_t stream) {
     sumsq_final_kernel<<<1, kFinalThreads, 0, stream>>>(partials, n_tiles, extra_sumsq, out);
-    return cudaGetLastError();
+    return after_launch();
 }
 
 cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int64_t n_tiles, double extra_sumsq,
@@ -88,7 +88,7 @@ cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int
     for (int64_t first = 0; first < n_tiles; first += 0x7fffffff) {
         const int64_t nb = n_tiles - first < 0x7fffffff ? n_tiles - first : 0x7fffffff;
         sumsq_tiles_kernel<<<static_cast<unsigned>(nb), kTileThreads, 0, stream>>>(grad, n / 8, pairs, first);
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = after_launch();
         if (e != cudaSuccess) return e;
     }
     return launch_norm_final(pairs, n_tiles, extra_sumsq, out, stream);

@@ -51,7 +51,7 @@ cudaError_t launch_typed(const LayoutChunk* table, int64_t n_chunks, const void*
         const int64_t nb = n_chunks - first < 0x7fffffff ? n_chunks - first : 0x7fffffff;
         layout_copy_kernel<T, kToArena><<<static_cast<unsigned>(nb), kLayoutThreads, 0, stream>>>(
             table, static_cast<const T*>(src), static_cast<T*>(dst), first);
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = after_launch();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -391,7 +391,7 @@ cudaError_t launch_grad_mode(const ListParams& p, unsigned nb, float2* pairs, in
             default: launch_k<kMode, 0>(p, nb, pairs, first, stream);
         }
     }
-    return cudaGetLastError();
+    return after_launch();
 }
 
 }  // namespace
@@ -434,7 +434,7 @@ cudaError_t launch_list_step(const ListParams& p, int64_t n_chunks, cudaStream_t
         } else {
             list_step_kernel<false, false><<<nb, kTileThreads, 0, stream>>>(p, first);
         }
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = after_launch();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
