@@ -44,6 +44,8 @@ def test_bench_line_has_the_contract_keys(extra):
         assert tb["value"] > 0 and tb["bytes_per_param"] == 6 + 10 + 4 + 8 + 28 + 6  # K = 2
     for k in d["kernels"].values():
         assert k["ms_min"] <= k["ms_median"] <= k["ms_max"]
+    assert d["plan"]["tensors"] == 20 and d["plan"]["build_ms"] >= 0 and d["plan"]["list_table_bytes"] > 0
+    assert d["clocks"]["interval_ms"] == 50 and d["clocks"]["samples"] >= d["clocks"]["samples_in_timed_region"]
 
 
 @pytest.mark.parametrize("extra", [[], ["--tensor-list"]])
