@@ -595,3 +595,29 @@ def test_launch_count_counts_each_kernel():
     with pytest.raises(z.Zero1Error):
         z.step(pb.plan, pb.master, pb.m, pb.v, pb.grad, pb.wbf, pb.hp, 0, pb.nout)  # t < 1
     assert z.launch_count() - c0 == 6
+
+
+def test_random_configurations_match_the_oracle():
+    """Forty seeded random configurations, every element compared over two steps: 1-12 tensors of 0 to
+    70,000 elements (a fifth of them under 20, so below the rank count or inside one vector), dp 1-8 at
+    a random rank, 1-6 micro-batches, four groups with random lr and weight-decay multipliers, and the
+    hyper-parameters drawn too (lr, both betas, eps, weight decay, clip off or on), with gradient scales
+    from far below to far above the clip threshold."""
+    rng = np.random.default_rng(2024)
+    for case in range(40):
+        nt = int(rng.integers(1, 13))
+        small = rng.random(nt) < 0.2
+        numels = [int(x) for x in np.where(small, rng.integers(0, 20, nt), rng.integers(0, 70000, nt))]
+        dp = int(rng.integers(1, 9))
+        numels[0] += 1000 * dp  # at least one shard on every rank
+        rank = int(rng.integers(0, dp))
+        hp = dict(lr=float(10 ** rng.uniform(-5, -2)), beta1=float(rng.uniform(0.8, 0.99)),
+                  beta2=float(rng.uniform(0.9, 0.9999)), eps=float(10 ** rng.uniform(-10, -6)),
+                  weight_decay=float(rng.uniform(0.0, 0.2)), clip_grad=float(rng.choice([0.0, 0.5, 1.0, 5.0])))
+        w = _custom(numels, [0] * nt, dp, rank, K=int(rng.integers(1, 7)), steps=2,
+                    sigma=float(10 ** rng.uniform(-4, -1)), name="random%d" % case, hp=hp,
+                    groups=[int(g) for g in rng.integers(0, 4, nt)],
+                    lr_scale=[float(x) for x in rng.uniform(0.1, 2.0, 8)],
+                    wd_scale=[float(x) for x in rng.choice([0.0, 0.5, 1.0, 2.0], 8)])
+        res = run_parity(w, seed=case)
+        assert res["master"] == 0 and res["m"] == 0 and res["v"] == 0, (case, res)
