@@ -206,6 +206,8 @@ def test_lr_schedule_closed_forms(z):
     assert all(a >= b for a, b in zip(vals, vals[1:]))
     with pytest.raises(ValueError):
         z.lr_at(0, lr, wu, dec, mn)
+    with pytest.raises(ValueError):  # an unknown curve is refused even where it would not be used
+        z.lr_at(1, lr, wu, 0, mn, "exponential")
 
 
 def test_mup_groups_follow_the_hidden_width_rule(z):

@@ -25,6 +25,8 @@ def lr_at(step, lr, warmup_steps, decay_steps, min_lr, decay_style="cosine"):
     """
     if step < 1:
         raise ValueError("steps count from 1")
+    if decay_style not in ("cosine", "linear", "constant"):
+        raise ValueError("unknown decay_style %r" % decay_style)
     if warmup_steps > 0 and step <= warmup_steps:
         return lr * step / warmup_steps
     k = step - warmup_steps
@@ -35,9 +37,7 @@ def lr_at(step, lr, warmup_steps, decay_steps, min_lr, decay_style="cosine"):
     frac = k / decay_steps
     if decay_style == "linear":
         return min_lr + (lr - min_lr) * (1.0 - frac)
-    if decay_style == "cosine":
-        return min_lr + (lr - min_lr) * 0.5 * (1.0 + math.cos(math.pi * frac))
-    raise ValueError("unknown decay_style %r" % decay_style)
+    return min_lr + (lr - min_lr) * 0.5 * (1.0 + math.cos(math.pi * frac))  # cosine
 
 
 def param_kind(name):
