@@ -130,8 +130,17 @@ def _check(code, where):
 
 
 def _stream_ptr(stream, device):
+    """The stream a call launches on.  The library launches on the current CUDA device, so the
+    tensors' device must be the current one (a kernel given another device's memory or stream
+    would fail); say so here rather than through a CUDA error."""
+    device = torch.device(device)
+    if device.type == "cuda" and device.index is not None and device.index != torch.cuda.current_device():
+        raise ValueError("the buffers are on %s but the current CUDA device is cuda:%d; call inside "
+                         "torch.cuda.device(%d)" % (device, torch.cuda.current_device(), device.index))
     if stream is None:
         stream = torch.cuda.current_stream(device)
+    elif stream.device != device and device.index is not None:
+        raise ValueError("stream is on %s, the buffers on %s" % (stream.device, device))
     return ctypes.c_void_p(stream.cuda_stream)
 
 
