@@ -53,11 +53,11 @@ def measured_peaks():
 def profile_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` ("adamw_step" or "list_step") from its committed
     ncu summary, or None if it is missing or was taken on a different version of the
-    kernel's sources (the kernel file and the per-element arithmetic it includes)."""
+    kernel's sources (the kernel file, the per-element arithmetic and the launch helper it includes)."""
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
     csrc = os.path.join(ROOT, "zero_sharded_mixed_local_gb300", "csrc")
-    srcs = {"adamw_step": ["adamw_step.cu", "elementwise.cuh"],
-            "list_step": ["tensor_list.cu", "elementwise.cuh"]}[kernel]
+    srcs = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "launch.cuh"],
+            "list_step": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"]}[kernel]
     try:
         text = open(path, encoding="utf-8").read()
         h = hashlib.sha256()

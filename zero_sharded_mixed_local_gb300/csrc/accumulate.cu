@@ -21,6 +21,7 @@
 // zero1_grad_norm's while the gradient is never read back (4 bytes per element
 // saved).
 #include "elementwise.cuh"
+#include "launch.cuh"
 #include "pair_sum.cuh"
 
 namespace zero1 {
@@ -30,6 +31,7 @@ constexpr int kAccThreads = 256;
 
 __global__ void __launch_bounds__(kAccThreads)
     accumulate_kernel(const __grid_constant__ AccumulateParams P, int64_t first_vec) {
+    pdl_enter();
     const int64_t i = first_vec + static_cast<int64_t>(blockIdx.x) * kAccThreads + threadIdx.x;
     if (i >= P.n_vec) return;
     float4* g4 = reinterpret_cast<float4*>(P.grad) + 2 * i;
@@ -84,6 +86,7 @@ __device__ __forceinline__ void accumulate_vec(const AccumulateParams& P, int64_
 template <bool kOneOverwrite>
 __global__ void __launch_bounds__(kTileThreads, kOneOverwrite ? 5 : 1)
     accumulate_norm_kernel(const __grid_constant__ AccumulateParams P, float2* __restrict__ partials, int64_t first_tile) {
+    pdl_enter();
     __shared__ float2 s_warp[kTileThreads / 32];
     const int64_t tile = first_tile + blockIdx.x;
     const int64_t v0 = tile * kVecsPerTile;
@@ -153,6 +156,7 @@ template <bool kDivide>
 __global__ void __launch_bounds__(kTileThreads, 2)
     accumulate_norm_add1_kernel(const __grid_constant__ AccumulateParams P, float2* __restrict__ partials,
                                 int64_t first_tile) {
+    pdl_enter();
     __shared__ float2 s_warp[kTileThreads / 32];
     const uint4* __restrict__ micro = reinterpret_cast<const uint4*>(P.micro[0]);
     float4* __restrict__ grad = reinterpret_cast<float4*>(P.grad);
@@ -214,6 +218,7 @@ template <int K, bool kDivide>
 __global__ void __launch_bounds__(kTileThreads, 1)
     accumulate_norm_kway_kernel(const __grid_constant__ AccumulateParams P, float2* __restrict__ partials,
                                 int64_t first_tile) {
+    pdl_enter();
     constexpr int kUnroll = K <= 4 ? 2 : 1;
     __shared__ float2 s_warp[kTileThreads / 32];
     const int64_t tile = first_tile + blockIdx.x;
@@ -252,11 +257,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 }
 
 template <int K>
-void launch_kway(const AccumulateParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
-    if (p.divide)
-        accumulate_norm_kway_kernel<K, true><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
-    else
-        accumulate_norm_kway_kernel<K, false><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
+cudaError_t launch_kway(const AccumulateParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
+    if (p.divide) return launch(accumulate_norm_kway_kernel<K, true>, nb, kTileThreads, stream, p, pairs, first);
+    return launch(accumulate_norm_kway_kernel<K, false>, nb, kTileThreads, stream, p, pairs, first);
 }
 
 }  // namespace
@@ -268,24 +271,22 @@ cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, 
         const int64_t nb = n_tiles - first < 0x7fffffff ? n_tiles - first : 0x7fffffff;
         const unsigned g = static_cast<unsigned>(nb);
         const int kway = p.overwrite_first ? p.n_micro : (p.n_micro == 1 ? -1 : 0);
+        cudaError_t e;
         switch (kway) {
             case -1:
-                if (p.divide)
-                    accumulate_norm_add1_kernel<true><<<g, kTileThreads, 0, stream>>>(p, pairs, first);
-                else
-                    accumulate_norm_add1_kernel<false><<<g, kTileThreads, 0, stream>>>(p, pairs, first);
+                e = p.divide ? launch(accumulate_norm_add1_kernel<true>, g, kTileThreads, stream, p, pairs, first)
+                             : launch(accumulate_norm_add1_kernel<false>, g, kTileThreads, stream, p, pairs, first);
                 break;
-            case 1: accumulate_norm_kernel<true><<<g, kTileThreads, 0, stream>>>(p, pairs, first); break;
-            case 2: launch_kway<2>(p, g, pairs, first, stream); break;
-            case 3: launch_kway<3>(p, g, pairs, first, stream); break;
-            case 4: launch_kway<4>(p, g, pairs, first, stream); break;
-            case 5: launch_kway<5>(p, g, pairs, first, stream); break;
-            case 6: launch_kway<6>(p, g, pairs, first, stream); break;
-            case 7: launch_kway<7>(p, g, pairs, first, stream); break;
-            case 8: launch_kway<8>(p, g, pairs, first, stream); break;
-            default: accumulate_norm_kernel<false><<<g, kTileThreads, 0, stream>>>(p, pairs, first);
+            case 1: e = launch(accumulate_norm_kernel<true>, g, kTileThreads, stream, p, pairs, first); break;
+            case 2: e = launch_kway<2>(p, g, pairs, first, stream); break;
+            case 3: e = launch_kway<3>(p, g, pairs, first, stream); break;
+            case 4: e = launch_kway<4>(p, g, pairs, first, stream); break;
+            case 5: e = launch_kway<5>(p, g, pairs, first, stream); break;
+            case 6: e = launch_kway<6>(p, g, pairs, first, stream); break;
+            case 7: e = launch_kway<7>(p, g, pairs, first, stream); break;
+            case 8: e = launch_kway<8>(p, g, pairs, first, stream); break;
+            default: e = launch(accumulate_norm_kernel<false>, g, kTileThreads, stream, p, pairs, first);
         }
-        const cudaError_t e = after_launch();
         if (e != cudaSuccess) return e;
     }
     return launch_norm_final(pairs, n_tiles, extra_sumsq, out, stream);
@@ -294,8 +295,8 @@ cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, 
 cudaError_t launch_accumulate(const AccumulateParams& p, cudaStream_t stream) {
     for (int64_t first = 0; first < p.n_vec; first += kMaxGridVectors(kAccThreads)) {
         const int64_t n = p.n_vec - first < kMaxGridVectors(kAccThreads) ? p.n_vec - first : kMaxGridVectors(kAccThreads);
-        accumulate_kernel<<<static_cast<unsigned>((n + kAccThreads - 1) / kAccThreads), kAccThreads, 0, stream>>>(p, first);
-        const cudaError_t e = after_launch();
+        const cudaError_t e = launch(accumulate_kernel, static_cast<unsigned>((n + kAccThreads - 1) / kAccThreads),
+                                     kAccThreads, stream, p, first);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

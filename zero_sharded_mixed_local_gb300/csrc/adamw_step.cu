@@ -21,6 +21,7 @@
 // __fadd_rn, __fdiv_rn, __fsqrt_rn) are never contracted into FMAs, which
 // keeps the operation order exact (elementwise.cuh).
 #include "elementwise.cuh"
+#include "launch.cuh"
 #include "zero1_internal.h"
 
 namespace zero1 {
@@ -32,6 +33,7 @@ constexpr int kStepThreads = 256;
 // shared memory after the loads are issued) rather than from P.sc.
 template <bool kWriteBf16, bool kDevScalars>
 __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_constant__ StepParams P, int64_t first_vec) {
+    pdl_enter();
     __shared__ float s_coef;
     __shared__ int s_skip;
     __shared__ zero1_step_scalars s_sc;
@@ -127,17 +129,13 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t stream) {
     for (int64_t first = 0; first < p.n_vec; first += kMaxGridVectors(kStepThreads)) {
         const int64_t n = p.n_vec - first < kMaxGridVectors(kStepThreads) ? p.n_vec - first : kMaxGridVectors(kStepThreads);
         const unsigned grid = static_cast<unsigned>((n + kStepThreads - 1) / kStepThreads);
-        if (p.dev_scalars != nullptr) {
-            if (p.w != nullptr)
-                adamw_step_kernel<true, true><<<grid, kStepThreads, 0, stream>>>(p, first);
-            else
-                adamw_step_kernel<false, true><<<grid, kStepThreads, 0, stream>>>(p, first);
-        } else if (p.w != nullptr) {
-            adamw_step_kernel<true, false><<<grid, kStepThreads, 0, stream>>>(p, first);
-        } else {
-            adamw_step_kernel<false, false><<<grid, kStepThreads, 0, stream>>>(p, first);
-        }
-        const cudaError_t e = after_launch();
+        cudaError_t e;
+        if (p.dev_scalars != nullptr)
+            e = p.w != nullptr ? launch(adamw_step_kernel<true, true>, grid, kStepThreads, stream, p, first)
+                               : launch(adamw_step_kernel<false, true>, grid, kStepThreads, stream, p, first);
+        else
+            e = p.w != nullptr ? launch(adamw_step_kernel<true, false>, grid, kStepThreads, stream, p, first)
+                               : launch(adamw_step_kernel<false, false>, grid, kStepThreads, stream, p, first);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

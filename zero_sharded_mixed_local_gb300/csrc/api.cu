@@ -66,9 +66,10 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 }  // namespace
 
-cudaError_t after_launch() {
+cudaError_t after_launch(cudaError_t launched) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError();
+    const cudaError_t last = cudaGetLastError();  // also clears it
+    return launched != cudaSuccess ? launched : last;
 }
 
 }  // namespace zero1

@@ -22,6 +22,7 @@
 //                 double, adds the other ranks' share and writes
 //                 {sumsq, norm, status}.
 // Memory-bound: 4 bytes read per element.
+#include "launch.cuh"
 #include "pair_sum.cuh"
 
 namespace zero1 {
@@ -31,6 +32,7 @@ constexpr int kFinalThreads = 1024;
 
 __global__ void __launch_bounds__(kTileThreads)
     sumsq_tiles_kernel(const float* __restrict__ grad, int64_t n_vec, float2* __restrict__ partials, int64_t first_tile) {
+    pdl_enter();
     __shared__ float2 s_warp[kTileThreads / 32];
     const int64_t tile = first_tile + blockIdx.x;
     const int64_t v0 = tile * kVecsPerTile;
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(kTileThreads)
 
 __global__ void __launch_bounds__(kFinalThreads)
     sumsq_final_kernel(const float2* __restrict__ partials, int64_t n_tiles, double extra, zero1_norm_out* out) {
+    pdl_enter();
     __shared__ float2 s_warp[kFinalThreads / 32];
     float s = 0.f, c = 0.f;
     for (int64_t i = threadIdx.x; i < n_tiles; i += kFinalThreads) {
@@ -77,8 +80,7 @@ __global__ void __launch_bounds__(kFinalThreads)
 
 cudaError_t launch_norm_final(const float2* partials, int64_t n_tiles, double extra_sumsq, zero1_norm_out* out,
                               cudaStream_t stream) {
-    sumsq_final_kernel<<<1, kFinalThreads, 0, stream>>>(partials, n_tiles, extra_sumsq, out);
-    return after_launch();
+    return launch(sumsq_final_kernel, 1, kFinalThreads, stream, partials, n_tiles, extra_sumsq, out);
 }
 
 cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int64_t n_tiles, double extra_sumsq,
@@ -87,8 +89,8 @@ cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int
     float2* pairs = reinterpret_cast<float2*>(partials);
     for (int64_t first = 0; first < n_tiles; first += 0x7fffffff) {
         const int64_t nb = n_tiles - first < 0x7fffffff ? n_tiles - first : 0x7fffffff;
-        sumsq_tiles_kernel<<<static_cast<unsigned>(nb), kTileThreads, 0, stream>>>(grad, n / 8, pairs, first);
-        const cudaError_t e = after_launch();
+        const cudaError_t e = launch(sumsq_tiles_kernel, static_cast<unsigned>(nb), kTileThreads, stream, grad,
+                                     n / 8, pairs, first);
         if (e != cudaSuccess) return e;
     }
     return launch_norm_final(pairs, n_tiles, extra_sumsq, out, stream);

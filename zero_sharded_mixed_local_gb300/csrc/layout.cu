@@ -18,6 +18,7 @@
 // vectors plus an element-wise tail; any other chunk moves element by
 // element (coalesced across the warp).  Element-wise bf16 copies measured
 // 5.8 TB/s on a 1.0B-element shard: two bytes per instruction bound them.
+#include "launch.cuh"
 #include "zero1_internal.h"
 
 namespace zero1 {
@@ -29,6 +30,7 @@ template <typename T, bool kToArena>
 __global__ void __launch_bounds__(kLayoutThreads)
     layout_copy_kernel(const LayoutChunk* __restrict__ table, const T* __restrict__ src, T* __restrict__ dst,
                        int64_t first_chunk) {
+    pdl_enter();
     const LayoutChunk ch = table[first_chunk + blockIdx.x];
     const T* s = src + (kToArena ? ch.model_offset : ch.arena_offset);
     T* d = dst + (kToArena ? ch.arena_offset : ch.model_offset);
@@ -49,9 +51,8 @@ template <typename T, bool kToArena>
 cudaError_t launch_typed(const LayoutChunk* table, int64_t n_chunks, const void* src, void* dst, cudaStream_t stream) {
     for (int64_t first = 0; first < n_chunks; first += 0x7fffffff) {
         const int64_t nb = n_chunks - first < 0x7fffffff ? n_chunks - first : 0x7fffffff;
-        layout_copy_kernel<T, kToArena><<<static_cast<unsigned>(nb), kLayoutThreads, 0, stream>>>(
-            table, static_cast<const T*>(src), static_cast<T*>(dst), first);
-        const cudaError_t e = after_launch();
+        const cudaError_t e = launch(layout_copy_kernel<T, kToArena>, static_cast<unsigned>(nb), kLayoutThreads, stream,
+                                     table, static_cast<const T*>(src), static_cast<T*>(dst), first);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -30,6 +30,7 @@
 // shards packed at 32-byte offsets stepped 6% slower than the same shards in
 // separate 512-byte-aligned allocations).
 #include "elementwise.cuh"
+#include "launch.cuh"
 #include "pair_sum.cuh"
 
 namespace zero1 {
@@ -114,6 +115,7 @@ __device__ __forceinline__ bool run_in_range(const ListChunk& ch, int32_t n_tens
 template <ListGradMode kMode, int kK>
 __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
     list_grad_kernel(const __grid_constant__ ListParams P, float2* __restrict__ partials, int64_t first_chunk) {
+    pdl_enter();
     constexpr bool kReadsMicro = kMode != ListGradMode::kNorm;
     constexpr bool kSumsSquares = kMode != ListGradMode::kAccumulate;
     constexpr int kBatch = 2;
@@ -288,6 +290,7 @@ constexpr int kStepVecsPerThread = kVecsPerThread / kStepSubBlocks;  // 2
 
 template <bool kWriteBf16, bool kDevScalars>
 __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid_constant__ ListParams P, int64_t first_block) {
+    pdl_enter();
     __shared__ float s_coef;
     __shared__ int s_skip;
     __shared__ zero1_step_scalars s_sc;
@@ -369,29 +372,28 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
 namespace {
 
 template <ListGradMode kMode, int kK>
-void launch_k(const ListParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
-    list_grad_kernel<kMode, kK><<<nb, kTileThreads, 0, stream>>>(p, pairs, first);
+cudaError_t launch_k(const ListParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
+    return launch(list_grad_kernel<kMode, kK>, nb, kTileThreads, stream, p, pairs, first);
 }
 
 template <ListGradMode kMode>
 cudaError_t launch_grad_mode(const ListParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
     if constexpr (kMode == ListGradMode::kNorm) {
-        launch_k<kMode, 0>(p, nb, pairs, first, stream);
+        return launch_k<kMode, 0>(p, nb, pairs, first, stream);
     } else {
         // the micro-batch count, when the pass overwrites the gradient with their sum
         switch (p.overwrite_first ? p.n_micro : 0) {
-            case 1: launch_k<kMode, 1>(p, nb, pairs, first, stream); break;
-            case 2: launch_k<kMode, 2>(p, nb, pairs, first, stream); break;
-            case 3: launch_k<kMode, 3>(p, nb, pairs, first, stream); break;
-            case 4: launch_k<kMode, 4>(p, nb, pairs, first, stream); break;
-            case 5: launch_k<kMode, 5>(p, nb, pairs, first, stream); break;
-            case 6: launch_k<kMode, 6>(p, nb, pairs, first, stream); break;
-            case 7: launch_k<kMode, 7>(p, nb, pairs, first, stream); break;
-            case 8: launch_k<kMode, 8>(p, nb, pairs, first, stream); break;
-            default: launch_k<kMode, 0>(p, nb, pairs, first, stream);
+            case 1: return launch_k<kMode, 1>(p, nb, pairs, first, stream);
+            case 2: return launch_k<kMode, 2>(p, nb, pairs, first, stream);
+            case 3: return launch_k<kMode, 3>(p, nb, pairs, first, stream);
+            case 4: return launch_k<kMode, 4>(p, nb, pairs, first, stream);
+            case 5: return launch_k<kMode, 5>(p, nb, pairs, first, stream);
+            case 6: return launch_k<kMode, 6>(p, nb, pairs, first, stream);
+            case 7: return launch_k<kMode, 7>(p, nb, pairs, first, stream);
+            case 8: return launch_k<kMode, 8>(p, nb, pairs, first, stream);
+            default: return launch_k<kMode, 0>(p, nb, pairs, first, stream);
         }
     }
-    return after_launch();
 }
 
 }  // namespace
@@ -424,17 +426,13 @@ cudaError_t launch_list_step(const ListParams& p, int64_t n_chunks, cudaStream_t
     const int64_t n_blocks = n_chunks * kStepSubBlocks;
     for (int64_t first = 0; first < n_blocks; first += 0x7fffffff) {
         const unsigned nb = static_cast<unsigned>(n_blocks - first < 0x7fffffff ? n_blocks - first : 0x7fffffff);
-        if (p.dev_scalars != nullptr) {
-            if (p.w != nullptr)
-                list_step_kernel<true, true><<<nb, kTileThreads, 0, stream>>>(p, first);
-            else
-                list_step_kernel<false, true><<<nb, kTileThreads, 0, stream>>>(p, first);
-        } else if (p.w != nullptr) {
-            list_step_kernel<true, false><<<nb, kTileThreads, 0, stream>>>(p, first);
-        } else {
-            list_step_kernel<false, false><<<nb, kTileThreads, 0, stream>>>(p, first);
-        }
-        const cudaError_t e = after_launch();
+        cudaError_t e;
+        if (p.dev_scalars != nullptr)
+            e = p.w != nullptr ? launch(list_step_kernel<true, true>, nb, kTileThreads, stream, p, first)
+                               : launch(list_step_kernel<false, true>, nb, kTileThreads, stream, p, first);
+        else
+            e = p.w != nullptr ? launch(list_step_kernel<true, false>, nb, kTileThreads, stream, p, first)
+                               : launch(list_step_kernel<false, false>, nb, kTileThreads, stream, p, first);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -127,9 +127,10 @@ cudaError_t launch_list_step(const ListParams& p, int64_t n_chunks, cudaStream_t
 // Record a CUDA error for zero1_last_cuda_error() and return ZERO1_ECUDA.
 int record_cuda_error(cudaError_t e);
 
-// Called once right after every kernel launch: counts it for
-// zero1_launch_count() and returns the launch's error (cudaGetLastError).
-cudaError_t after_launch();
+// Called once for every kernel launch with the launch call's own result:
+// counts it for zero1_launch_count() and returns the launch's error (that
+// result, else cudaGetLastError()).
+cudaError_t after_launch(cudaError_t launched = cudaSuccess);
 
 // Work items one full-grid launch may cover (2^31 - 1 blocks of `threads`).
 constexpr int64_t kMaxGridVectors(int threads) { return static_cast<int64_t>(0x7fffffff) * threads; }
