@@ -6,6 +6,7 @@ raw pointers and forwards the current CUDA stream.  It has no fallback: when
 the library is missing or a call fails it raises.
 """
 import ctypes
+import functools
 import os
 from dataclasses import dataclass
 
@@ -133,13 +134,17 @@ def _stream_ptr(stream, device):
     """The stream a call launches on.  The library launches on the current CUDA device, so the
     tensors' device must be the current one (a kernel given another device's memory or stream
     would fail); say so here rather than through a CUDA error."""
-    device = torch.device(device)
-    if device.type == "cuda" and device.index is not None and device.index != torch.cuda.current_device():
-        raise ValueError("the buffers are on %s but the current CUDA device is cuda:%d; call inside "
-                         "torch.cuda.device(%d)" % (device, torch.cuda.current_device(), device.index))
+    if not isinstance(device, torch.device):
+        device = torch.device(device)
+    index = device.index
+    if index is not None and device.type == "cuda":
+        current = torch.cuda.current_device()
+        if index != current:
+            raise ValueError("the buffers are on %s but the current CUDA device is cuda:%d; call inside "
+                             "torch.cuda.device(%d)" % (device, current, index))
     if stream is None:
-        stream = torch.cuda.current_stream(device)
-    elif stream.device != device and device.index is not None:
+        stream = torch.cuda.current_stream()  # the current device's, checked above
+    elif index is not None and stream.device_index != index:
         raise ValueError("stream is on %s, the buffers on %s" % (stream.device, device))
     return ctypes.c_void_p(stream.cuda_stream)
 
@@ -149,11 +154,11 @@ def _ptr(t, dtype, numel, name, device=None, host_ok=False):
     kernels read it directly over the CPU-GPU link."""
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
-    pinned_host = host_ok and t.device.type == "cpu" and t.is_pinned()
-    if t.device.type != "cuda" and not pinned_host:
-        raise ValueError("%s must be on a CUDA device%s (got %s)" % (name, " or pinned host memory" if host_ok else "",
-                                                                   t.device))
-    if device is not None and t.device.type == "cuda" and t.device != device:
+    if not t.is_cuda:
+        if not (host_ok and t.device.type == "cpu" and t.is_pinned()):
+            raise ValueError("%s must be on a CUDA device%s (got %s)" % (
+                name, " or pinned host memory" if host_ok else "", t.device))
+    elif device is not None and device.index is not None and t.get_device() != device.index:
         raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
     if t.dtype != dtype:
         raise TypeError("%s must be %s (got %s)" % (name, dtype, t.dtype))
@@ -161,9 +166,17 @@ def _ptr(t, dtype, numel, name, device=None, host_ok=False):
         raise ValueError("%s must be contiguous" % name)
     if numel is not None and t.numel() != numel:
         raise ValueError("%s has %d elements, the plan's arena has %d" % (name, t.numel(), numel))
-    if t.data_ptr() % 16:
+    ptr = t.data_ptr()
+    if ptr % 16:
         raise ValueError("%s must start on a 16-byte boundary" % name)
-    return ctypes.c_void_p(t.data_ptr())
+    return ctypes.c_void_p(ptr)
+
+
+@functools.lru_cache(maxsize=256)
+def _hparams_struct(values):
+    """The ctypes zero1_hparams for a tuple of settings (the library only reads it); building
+    one costs more per call than looking it up."""
+    return _Hparams(*values)
 
 
 @dataclass
@@ -178,7 +191,7 @@ class Hparams:
     clip_grad: float = 1.0
 
     def _c(self):
-        return _Hparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.clip_grad)
+        return _hparams_struct((self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.clip_grad))
 
 
 @dataclass
@@ -233,6 +246,9 @@ class Plan:
         self._h = h
         self._lib = lib
         self.dp_size, self.dp_rank = int(dp_size), int(dp_rank)
+        # a plan never changes after creation: its sizes are read once, not on every call
+        self._sizes = (lib.zero1_plan_num_tensors(h), lib.zero1_plan_total_numel(h), lib.zero1_plan_local_numel(h),
+                       lib.zero1_plan_arena_numel(h), lib.zero1_workspace_bytes(h), lib.zero1_list_workspace_bytes(h))
         self._groups = grp.copy()
         self.numels = numels.copy()
         self._layout = None
@@ -254,23 +270,23 @@ class Plan:
 
     @property
     def num_tensors(self):
-        return self._lib.zero1_plan_num_tensors(self._h)
+        return self._sizes[0]
 
     @property
     def total_numel(self):
-        return self._lib.zero1_plan_total_numel(self._h)
+        return self._sizes[1]
 
     @property
     def local_numel(self):
-        return self._lib.zero1_plan_local_numel(self._h)
+        return self._sizes[2]
 
     @property
     def arena_numel(self):
-        return self._lib.zero1_plan_arena_numel(self._h)
+        return self._sizes[3]
 
     @property
     def workspace_bytes(self):
-        return self._lib.zero1_workspace_bytes(self._h)
+        return self._sizes[4]
 
     def tensor(self, i):
         s, c, o = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
@@ -322,7 +338,7 @@ class Plan:
 
     @property
     def list_workspace_bytes(self):
-        return self._lib.zero1_list_workspace_bytes(self._h)
+        return self._sizes[5]
 
     def list_table(self, device="cuda", stream=None):
         """Device copy of this plan's tensor-list run table (made once per device)."""

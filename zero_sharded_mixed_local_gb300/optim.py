@@ -24,6 +24,7 @@ gradients before) sit outside this rank's step.  Weight decay is skipped for
 parameters the ``no_decay`` predicate selects (by default 1-D parameters:
 norm weights and biases).
 """
+import dataclasses
 import math
 
 import torch
@@ -100,7 +101,7 @@ class LocalShardAdamW:
         if group is not None:
             allreduce_sumsq_(self.norm_out, group)
         self.t += 1
-        hp = self.hp if lr is None else Hparams(**{**self.hp.__dict__, "lr": lr})
+        hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
         step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
              self.norm_out, stream=stream)
         self._micro_seen = 0
@@ -216,7 +217,7 @@ class StepGraph:
         t = o.t + 1
         b = t % 2
         self.done[b].synchronize()  # the replay that last read pinned buffer b (step t-2) is done
-        hp = o.hp if lr is None else Hparams(**{**o.hp.__dict__, "lr": lr})
+        hp = o.hp if lr is None else dataclasses.replace(o.hp, lr=lr)
         self.h[b][:STEP_SCALARS_BYTES].copy_(torch.frombuffer(bytearray(step_scalars(o.plan, hp, t)),
                                                               dtype=torch.uint8))
         self.graphs[b].replay()
@@ -299,7 +300,7 @@ class ShardListAdamW:
         if group is not None:
             allreduce_sumsq_(self.norm_out, group)
         self.t += 1
-        hp = self.hp if lr is None else Hparams(**{**self.hp.__dict__, "lr": lr})
+        hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
         L = self._lists
         list_step(self.plan, self.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], L["weight_bf16"],
                   hp, self.t, self.norm_out, stream=stream)
