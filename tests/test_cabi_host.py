@@ -370,3 +370,17 @@ def test_binding_signatures_match_the_header(z):
         assert [c_kind(a) for a in args] == [py_kind(t) for t in argtypes], name
         checked += 1
     assert checked == len(declared_functions())
+
+
+def test_plan_sizes_are_the_librarys(z):
+    """The Python Plan reads its sizes once at creation; they must be the library's own answers."""
+    lib = z.load_library()
+    w = get_workload("ragged")
+    plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank)
+    h = plan.handle
+    assert plan.num_tensors == lib.zero1_plan_num_tensors(h) == len(w.params.numels)
+    assert plan.total_numel == lib.zero1_plan_total_numel(h)
+    assert plan.local_numel == lib.zero1_plan_local_numel(h)
+    assert plan.arena_numel == lib.zero1_plan_arena_numel(h)
+    assert plan.workspace_bytes == lib.zero1_workspace_bytes(h)
+    assert plan.list_workspace_bytes == lib.zero1_list_workspace_bytes(h)
