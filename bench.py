@@ -41,6 +41,77 @@ def accumulate_bytes_per_elem(k, k_way=False):
     return 6 + 10 * (k - 1)
 
 
+L2_BYTES = 129e6  # GB300 L2
+
+
+def path_bytes_for(args, P, K, total=None, world=1):
+    """Algorithmic bytes of one step over P local parameters (padding excluded).  A
+    --data-parallel rank also moves, per micro-batch, its model-layout gradient through the
+    pack (2 R + 2 W per model parameter) and the all-to-all (2 R + 2 W), and adds the world's
+    chunks (2 B each per local parameter); after the step the all-gather (2 R per local, 2 W
+    per model parameter) and the unpack (2 R + 2 W per model parameter)."""
+    if getattr(args, "data_parallel", False):
+        total = P if total is None else total
+        acc = sum(2 * world + (4 if k == 0 else 8) for k in range(K)) * P
+        return K * 8 * total + acc + STEP_BYTES_PER_ELEM * P + 2 * P + 6 * total
+    return ((accumulate_bytes_per_elem(K, args.k_way) + STEP_BYTES_PER_ELEM) * P + (4 * P if args.unfused else 0) +
+            (8 * P if args.exchange else 0))
+
+
+def flushes_l2(path_bytes):
+    """A step whose bytes would mostly stay in L2 from one step to the next is timed with L2 flushed."""
+    return path_bytes < 4 * L2_BYTES
+
+
+def l2_note(path_bytes):
+    if flushes_l2(path_bytes):
+        return ("L2 flushed before every step (256 MB write outside the step's events): a step moves %.1f MB "
+                "against the 129 MB L2" % (path_bytes / 1e6))
+    return "no flush: each step streams %.1f GB, far above the 129 MB L2" % (path_bytes / 1e9)
+
+
+def data_parallel_workload(w, world):
+    """--data-parallel: the workload's whole model over a ZeRO-1 job of `world` ranks."""
+    w.dp_size, w.dp_rank = world, 0
+    w.description = "%s-shaped list, whole model (%d params), ZeRO-1 data-parallel job of %d rank%s, K=%d" % (
+        w.name, sum(w.params.numels), world, "s" if world > 1 else "", w.micro_batches)
+    return w
+
+
+def rank_dp_rank(w, world, rank):
+    """The data-parallel shard rank `rank` of a `world`-GPU job steps (weak scaling: one shard per GPU)."""
+    return (w.dp_rank + rank) % w.dp_size if world > 1 else w.dp_rank
+
+
+def step_config(args, w, local, job, arena, dp_rank):
+    """The `config` record of a bench line: the same keys and values for the GPU arm and the
+    reference (oracle) arm of one workload and one set of options."""
+    return {
+        "workload": w.description,
+        "local_params_per_gpu": int(local),
+        "params_per_step_all_ranks": int(job),
+        "arena_elems": int(arena),
+        "micro_batches": w.micro_batches,
+        "dp_size": w.dp_size,
+        "dp_rank": int(dp_rank),
+        "parallelism": ("zero1 data-parallel job, dp%d (one shard per GPU, real collectives)" % w.dp_size
+                        if getattr(args, "data_parallel", False) else "zero1 dp%d shard per GPU" % w.dp_size),
+        "seed": w.seed,
+        "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
+        "accumulate": ("all K micro-batches in one pass (K-way)" if args.k_way
+                       else "one call per micro-batch, as they arrive"),
+        "exchange": ("reduce-scatter (pack, all-to-all of bf16 chunks, owner's fp32 sum in (micro-batch, rank) "
+                     "order, divide by the world size), sum-of-squares all-reduce, all-gather + unpack of the bf16 "
+                     "weights" if getattr(args, "data_parallel", False) else
+                     "pack the reduce-scatter input and unpack the bf16 weights, model layout <-> arena"
+                     if args.exchange else "none (the local step only)"),
+        "launch": "one CUDA graph per step (StepGraph)" if args.graph else "eager calls",
+        "layout": ("tensor lists: one allocation per tensor shard, a 16384-element run table"
+                   if args.tensor_list else "arenas: one padded buffer per quantity"),
+        "l2": l2_note(path_bytes_for(args, local, w.micro_batches, int(sum(w.params.numels)), w.dp_size)),
+    }
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -50,33 +121,99 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def profile_traffic(kernel, workload):
-    """DRAM bytes per launch of `kernel` ("adamw_step" or "list_step") from its committed
-    ncu summary, or None if it is missing or was taken on a different version of the
-    kernel's sources (the kernel file, the per-element arithmetic and the launch helper it includes)."""
-    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+TRAFFIC_SOURCES = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "launch.cuh"],
+                   "list_step": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"]}
+
+
+def kernel_source_hash(kernel):
+    """First 16 hex digits of the SHA-256 of the kernel's sources (the kernel file, the
+    per-element arithmetic and the launch helper it includes)."""
     csrc = os.path.join(ROOT, "zero_sharded_mixed_local_gb300", "csrc")
-    srcs = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "launch.cuh"],
-            "list_step": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"]}[kernel]
+    h = hashlib.sha256()
+    for src in TRAFFIC_SOURCES[kernel]:
+        with open(os.path.join(csrc, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record_path(kernel, workload=None):
+    """profiles/traffic_<kernel>_<workload>.json; without `workload`, the one record of `kernel`
+    (None if there is none)."""
+    if workload is not None:
+        return os.path.join(ROOT, "profiles", "traffic_%s_%s.json" % (kernel, workload))
+    import glob
+    found = sorted(glob.glob(os.path.join(ROOT, "profiles", "traffic_%s_*.json" % kernel)))
+    return found[0] if len(found) == 1 else None
+
+
+def profile_traffic(kernel, params):
+    """DRAM bytes per launch of `kernel` ("adamw_step" or "list_step") over `params` parameters:
+    the machine-written record profiles/traffic_<kernel>.json holds the ncu DRAM read + write
+    bytes of launches on a small workload, per parameter; scaled here to `params`.  None if the
+    record is missing or was taken on other kernel sources."""
+    path = traffic_record_path(kernel)
+    if path is None:
+        return None, None
     try:
-        text = open(path, encoding="utf-8").read()
-        h = hashlib.sha256()
-        for src in srcs:
-            h.update(open(os.path.join(csrc, src), "rb").read())
-        digest = h.hexdigest()[:16]
-    except OSError:
-        return None
-    fields = {}
-    for line in text.splitlines():
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_source_sha256_16") != digest:
-        return None
-    try:
-        return int(float(fields["traffic_bytes_per_launch"]))
-    except (KeyError, ValueError):
-        return None
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_sha256_16") != kernel_source_hash(kernel):
+            return None, None
+        return int(round(float(rec["traffic_bytes_per_param"]) * params)), (
+            "%s: ncu DRAM read + write on %s (%d params per launch, %d launches), %.4f B/param, scaled to %d params"
+            % (os.path.relpath(path, ROOT), rec["capture"]["workload"],
+               rec["capture"]["params_per_launch"], rec["capture"]["launches"], rec["traffic_bytes_per_param"],
+               params))
+    except (OSError, KeyError, ValueError, TypeError):
+        return None, None
+
+
+def parse_ncu_csv(path, kernel):
+    """Per-launch (dram read, dram write, duration ns) of the launches of `kernel` in an ncu
+    `--csv --log-file` metrics list."""
+    import csv
+    rows = {}
+    with open(path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for r in csv.DictReader(lines):
+        if kernel not in r["Kernel Name"]:
+            continue
+        d = rows.setdefault(r["ID"], {})
+        unit, value = r["Metric Unit"], float(r["Metric Value"].replace(",", ""))
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9,
+                 "ns": 1, "nsecond": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}[unit]
+        d[r["Metric Name"]] = value * scale
+    return [(d["dram__bytes_read.sum"], d["dram__bytes_write.sum"], d.get("gpu__time_duration.sum"))
+            for _, d in sorted(rows.items(), key=lambda kv: int(kv[0]))]
+
+
+def write_traffic_record(csv_path, kernel, workload, command, params, out=None):
+    """Summarise an ncu capture of `kernel` on `workload` (`params` parameters per launch) into
+    the machine-written record profile_traffic() reads."""
+    launches = parse_ncu_csv(csv_path, kernel + "_kernel")
+    if not launches:
+        raise SystemExit("no %s_kernel launches in %s" % (kernel, csv_path))
+    rd = statistics.mean(x[0] for x in launches)
+    wr = statistics.mean(x[1] for x in launches)
+    durs = [x[2] for x in launches if x[2] is not None]
+    rec = {
+        "kernel": kernel + "_kernel",
+        "kernel_source_sha256_16": kernel_source_hash(kernel),
+        "capture": {"workload": workload, "params_per_launch": int(params), "launches": len(launches),
+                    "command": command, "csv": os.path.basename(csv_path)},
+        "dram_read_bytes_per_launch": int(round(rd)),
+        "dram_write_bytes_per_launch": int(round(wr)),
+        "traffic_bytes_per_launch": int(round(rd + wr)),
+        "traffic_bytes_per_param": (rd + wr) / params,
+        "algorithmic_bytes_per_param": STEP_BYTES_PER_ELEM,
+        "ncu_duration_us_per_launch": statistics.mean(durs) / 1e3 if durs else None,
+        "note": "cold-cache, serialised ncu launches: use the bytes, not the duration",
+    }
+    out = out or traffic_record_path(kernel, workload)
+    with open(out, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 class ClockSampler:
@@ -159,14 +296,25 @@ class ClockSampler:
                 "interval_ms": self.INTERVAL_MS}
 
 
-def dist_setup():
+def dist_setup(one_rank_group=False):
+    """(world, rank, local rank) from the launcher's environment; an NCCL process group when
+    there are several ranks, or with `one_rank_group` a one-rank NCCL group on this GPU."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
+    if world > 1 or one_rank_group:
         import torch.distributed as dist
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if world > 1:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            import socket
+            sock = socket.socket()
+            sock.bind(("127.0.0.1", 0))
+            port = sock.getsockname()[1]
+            sock.close()
+            dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0, world_size=1,
+                                    device_id=torch.device("cuda", local))
     return world, rank, local
 
 
@@ -298,6 +446,14 @@ def cpu_baseline(w, target_s=10.0, max_elems=1 << 27):
             "single_core": {"value": value1, "elements": n1, "steps": steps1, "seconds": total1}}
 
 
+def oracle_shard_sizes(w, dp_rank):
+    """(local elements, padded arena elements) of one dp rank's shard: the oracle's shard split,
+    each shard padded to a multiple of 8 elements as the arenas are."""
+    import oracle
+    _, count, local = oracle.plan(w.params.numels, w.dp_size, dp_rank)
+    return int(local), int(sum((int(c) + 7) // 8 * 8 for c in count))
+
+
 def run_reference(args, w, world, rank):
     if rank != 0:
         return
@@ -315,16 +471,21 @@ def run_reference(args, w, world, rank):
              for t in range(1, args.steps + 1)]
     sec = sum(times) / len(times)
     value = n / sec
-    import oracle
-    local = int(oracle.plan(w.params.numels, w.dp_size, w.dp_rank)[2])
+    # the same workload record as the GPU arm: rank 0's shard, and every rank's shard in the job total
+    dp0 = rank_dp_rank(w, world, 0)
+    local, arena = oracle_shard_sizes(w, dp0)
+    job = sum(oracle_shard_sizes(w, rank_dp_rank(w, world, r))[0] for r in range(world))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.description, "local_params_per_gpu": local, "micro_batches": w.micro_batches,
-                   "dp_size": w.dp_size, "dp_rank": w.dp_rank, "parallelism": "zero1 dp%d shard" % w.dp_size,
-                   "sample_elements": n,
-                   "launch": "scalar C oracle on %d host threads over contiguous element ranges" % threads},
+        "scaling": "strong" if args.data_parallel else "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": step_config(args, w, local, job, arena, dp0),
+        "oracle_sample": {"sample_elements": n,
+                          "launch": "scalar C oracle on %d host threads over contiguous element ranges" % threads,
+                          "note": "each step runs the whole path (K-micro-batch accumulate, norm, AdamW + bf16 "
+                                  "copy) over this many elements drawn like the workload's decayed tensors; "
+                                  "params/s = elements / step time"},
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": threads, "kind": "oracle",
                          "sample": "%d elements drawn like the workload's decayed tensors, per step" % n,
                          "single_core": {"value": value1, "elements": 1 << 22}},
@@ -363,10 +524,21 @@ def parse_args():
                     help="add the copies around the local step: pack the last micro-batch's reduce-scatter input "
                          "from a model-layout bf16 gradient (zero1_shard_gather) and unpack the bf16 weights into "
                          "the model layout (zero1_shard_scatter)")
+    ap.add_argument("--data-parallel", action="store_true",
+                    help="the workload's whole model stepped by a ZeRO-1 job of this run's ranks (dp size = the "
+                         "number of GPUs, rank r owns shard r): per micro-batch the pack, the all-to-all and the "
+                         "owner's fp32 accumulation, the sum-of-squares all-reduce, the local step, the all-gather "
+                         "and unpack of the bf16 weights (DataParallelStep, NCCL; one GPU runs a one-rank group)")
     ap.add_argument("--micro-batches", type=int, default=None,
                     help="override the workload's K (used to profile the one-micro-batch path on a small shard)")
     ap.add_argument("--seed", type=int, default=None,
                     help="seed of the synthetic inputs (default: the workload's own, 0); rank r adds r")
+    ap.add_argument("--write-traffic-record", metavar="NCU_CSV", default=None,
+                    help="no GPU work: summarise an ncu --csv metrics list (dram__bytes_read.sum, "
+                         "dram__bytes_write.sum, gpu__time_duration.sum) of the step kernel on --workload into "
+                         "profiles/traffic_<kernel>.json, the record roofline.traffic is scaled from")
+    ap.add_argument("--traffic-command", default="",
+                    help="with --write-traffic-record: the ncu command that made the CSV, stored in the record")
     args = ap.parse_args()
     if args.tensor_list and args.unfused:
         raise SystemExit("--tensor-list runs the fused calls")
@@ -374,8 +546,12 @@ def parse_args():
         raise SystemExit("--k-way runs the fused eager calls")
     if args.exchange and (args.tensor_list or args.graph):
         raise SystemExit("--exchange runs the arena calls eagerly")
-    if args.tensor_list or args.exchange:
+    if args.data_parallel and (args.tensor_list or args.graph or args.exchange or args.k_way or args.unfused):
+        raise SystemExit("--data-parallel runs the arena calls eagerly, one call per micro-batch")
+    if args.tensor_list or args.exchange or args.data_parallel:
         args.no_e2e = True  # the end-to-end leg stages arenas for the plain step
+    if args.data_parallel:
+        args.no_torch_baseline = True
     return args
 
 
@@ -393,7 +569,7 @@ class StepBench:
         from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout
         self.args, self.w, self.z, self.world = args, w, z, world
         self.dev = dev = torch.device("cuda", local)
-        self.dp_rank = (w.dp_rank + rank) % w.dp_size if world > 1 else w.dp_rank
+        self.dp_rank = rank_dp_rank(w, world, rank)
         t0 = time.perf_counter()
         self.plan = plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, self.dp_rank)
         self.plan_ms = (time.perf_counter() - t0) * 1e3  # a1, on the host, once per job
@@ -532,12 +708,88 @@ class StepBench:
 
     def path_bytes(self):
         """Algorithmic bytes of one step (padding excluded)."""
-        a, P = self.args, self.P
-        return ((accumulate_bytes_per_elem(self.K, a.k_way) + STEP_BYTES_PER_ELEM) * P + (4 * P if a.unfused else 0) +
-                (8 * P if self.full_g is not None else 0))
+        return path_bytes_for(self.args, self.P, self.K)
 
 
-L2_BYTES = 129e6  # GB300 L2
+class DataParallelBench:
+    """--data-parallel: the workload's whole model stepped by a ZeRO-1 job of the run's ranks,
+    rank r owning shard r of dp = ranks.  One step is this rank's part of the job
+    (DataParallelStep): per micro-batch the pack of its model-layout bf16 gradient, the
+    all-to-all and the owner's ordered fp32 accumulation (the last one divided by the world
+    size, with the norm), the sum-of-squares all-reduce, the local step, and the all-gather and
+    unpack of the bf16 weights.  Rank r's gradients are its own draw (seed + r)."""
+
+    def __init__(self, args, w, z, world, rank, local):
+        import torch.distributed as dist
+        from zero_sharded_mixed_local_gb300.exchange import DataParallelStep
+        from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout
+        self.args, self.w, self.z, self.world = args, w, z, world
+        self.dev = dev = torch.device("cuda", local)
+        self.dp_rank = rank
+        t0 = time.perf_counter()
+        self.opt = opt = z.LocalShardAdamW(w.params.numels, w.params.no_decay, world, rank,
+                                           hparams=z.Hparams(**w.hp), device=dev)
+        self.plan = plan = opt.plan
+        self.plan_ms = (time.perf_counter() - t0) * 1e3
+        L = plan.layout()
+        opt.master.copy_(InputGenerator(w, Layout(L.counts, L.offsets, L.no_decay, L.arena_numel), dev,
+                                        seed=w.seed).master())
+        opt.weight_bf16.copy_(opt.master.to(torch.bfloat16))
+        model = Layout.packed(w.params.numels, w.params.no_decay)
+        self.micros = InputGenerator(w, model, dev, seed=w.seed + rank).micro_grads()
+        self.dps = DataParallelStep(opt, group=dist.group.WORLD)
+        self.weights = torch.zeros(plan.total_numel, dtype=torch.bfloat16, device=dev)
+        self.P, self.K, self.total = plan.local_numel, w.micro_batches, plan.total_numel
+        self.stream = torch.cuda.current_stream(dev)
+        self.nout = opt.norm_out
+        self.graph = self.lists = self.master = self.full_g = self.lopt = None
+        self.t = 0
+        torch.cuda.synchronize()
+
+    step_kernel = "adamw_step"
+
+    def step(self, rec=None):
+        mark = (lambda k: rec[k].record(self.stream)) if rec is not None else (lambda k: None)
+        mark("x0")
+        for k, g in enumerate(self.micros):
+            self.dps.reduce_scatter(g, last=(k == self.K - 1))
+        mark("n0")
+        self.dps.allreduce_sumsq()
+        mark("s0")
+        self.opt.step()
+        mark("s1")
+        self.dps.all_gather(self.weights)
+        mark("x1")
+        self.t = self.opt.t
+
+    def path_bytes(self):
+        return path_bytes_for(self.args, self.P, self.K, self.total, self.world)
+
+    def report(self, recs):
+        mean = lambda a, c: statistics.mean(r[a].elapsed_time(r[c]) for r in recs)  # noqa: E731
+        parts = {"reduce_scatter": ("x0", "n0"), "allreduce_sumsq": ("n0", "s0"), "adamw_step": ("s0", "s1"),
+                 "all_gather": ("s1", "x1")}
+        kernels = {}
+        for name, (a, c) in parts.items():
+            times = [r[a].elapsed_time(r[c]) for r in recs]
+            kernels[name] = {"ms": mean(a, c), "ms_median": statistics.median(times), "ms_min": min(times),
+                             "ms_max": max(times)}
+        kernels["adamw_step"]["gbs"] = STEP_BYTES_PER_ELEM * self.P / (kernels["adamw_step"]["ms"] * 1e-3) / 1e9
+        kernels["reduce_scatter"]["note"] = ("per micro-batch: %d pack launches, the all-to-all, %d accumulate "
+                                             "call(s)" % (self.world, -(-self.world // self.z.MAX_MICRO)))
+        peak, peak_kind = measured_peaks()
+        achieved = kernels["adamw_step"]["gbs"]
+        traffic, traffic_src = profile_traffic("adamw_step", self.P)
+        roofline = {"bound": "hbm", "kernel": "adamw_step_kernel", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
+                    "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
+                    "frac_of_nominal": achieved / NOMINAL_HBM_GBS, "bytes_per_param": STEP_BYTES_PER_ELEM,
+                    "params_per_launch": self.P}
+        return kernels, roofline
+
+    def launches_per_step(self):
+        per_micro = self.world + -(-self.world // self.z.MAX_MICRO)
+        return self.K * per_micro + 1 + 1 + self.world  # + final reduction, step, unpacks
 
 
 def time_steps(b, args, world, local):
@@ -548,7 +800,7 @@ def time_steps(b, args, world, local):
     the mean of the per-step event pairs; larger steps are timed as one region."""
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     flush = None
-    if b.path_bytes() < 4 * L2_BYTES:
+    if flushes_l2(b.path_bytes()):
         flush = torch.empty(64 << 20, dtype=torch.float32, device=b.dev)  # 256 MB, twice the L2
     for _ in range(args.warmup):
         if flush is not None:
@@ -580,12 +832,9 @@ def time_steps(b, args, world, local):
     clk = clocks.stop()
     if flush is not None:
         ms = statistics.mean(r["t0"].elapsed_time(r["t1"]) for r in recs)
-        note = ("L2 flushed before every step (256 MB write outside the step's events): a step moves %.1f MB "
-                "against the 129 MB L2" % (b.path_bytes() / 1e6))
     else:
         ms = start.elapsed_time(end) / args.steps
-        note = "no flush: each step streams %.1f GB, far above the 129 MB L2" % (b.path_bytes() / 1e9)
-    return recs, max_over_ranks(ms, world), clk, note
+    return recs, max_over_ranks(ms, world), clk, l2_note(b.path_bytes())
 
 
 def kernel_report(b, recs, args):
@@ -619,8 +868,10 @@ def kernel_report(b, recs, args):
         k["ms_median"], k["ms_min"], k["ms_max"] = statistics.median(times), min(times), max(times)
     peak, peak_kind = measured_peaks()
     achieved = kernels[b.step_kernel]["gbs"]
+    traffic, traffic_src = profile_traffic(b.step_kernel, P)
     roofline = {"bound": "hbm", "kernel": b.step_kernel + "_kernel", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "traffic": profile_traffic(b.step_kernel, args.workload),
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "traffic_source": traffic_src,
                 "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
                 "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P}
@@ -630,85 +881,44 @@ def kernel_report(b, recs, args):
 def run_e2e(b, args, world, P_job):
     """The same step end to end through the public API: host gradients in, norm record out.
 
-    Every step's micro-batch gradients start in pinned host memory and are copied to the
-    device by the copy engines on a side stream (cudaMemcpyAsync via Tensor.copy_); every
-    step's 24-byte norm record is copied back and read on the host, one step behind, as a
-    training loop logs it.  Two staging buffers and two gradient arenas let step t+1's
-    transfer (link-bound, on DMA engines) overlap step t's kernels (HBM-bound, on the SMs)."""
-    z, plan, K, stream, dev = b.z, b.plan, b.K, b.stream, b.dev
+    ``HostFedSteps`` (the package's host-fed loop, which the GPU tests check against the
+    synchronous calls and the oracle) copies every step's micro-batch gradients from
+    pinned host memory to the device on a side stream, into two staging sets, so step
+    t+1's transfer (link-bound, on DMA engines) overlaps step t's kernels (HBM-bound, on
+    the SMs); every step's 24-byte norm record is copied back and read on the host, one
+    step behind, as a training loop logs it."""
+    z, stream = b.z, b.stream
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     host_micros = [mb.cpu().pin_memory() for mb in b.micros]
-    stage = [b.micros, [torch.empty_like(mb) for mb in b.micros]]
-    grads = [b.grad, plan.new_arena(torch.float32, dev)]
-    wss = [b.ws, plan.new_workspace(dev)]
-    nouts = [b.nout, z.new_norm_out(dev)]
-    host_rec = [torch.empty(32, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    side = torch.cuda.Stream(dev)
-    copied = [torch.cuda.Event(), torch.cuda.Event()]
-    step_done = [torch.cuda.Event(), torch.cuda.Event()]
-    seen, copy_ev = [], []
-
-    def e2e_steps(n_steps, first_event=None, time_copies=False):
-        for t in range(n_steps):
-            i = t % 2
-            with torch.cuda.stream(side):
-                if t >= 2:
-                    side.wait_event(step_done[i])  # staging buffer i is free once step t-2 is done
-                elif first_event is not None:
-                    side.wait_event(first_event)
-                if time_copies:
-                    copy_ev.append((ev(), ev()))
-                    copy_ev[-1][0].record(side)
-                for k in range(K):
-                    stage[i][k].copy_(host_micros[k], non_blocking=True)
-                if time_copies:
-                    copy_ev[-1][1].record(side)
-                copied[i].record(side)
-            stream.wait_event(copied[i])
-            if args.k_way:
-                z.accumulate_norm(plan, grads[i], stage[i], wss[i], nouts[i], overwrite_first=True, stream=stream)
-            else:
-                for k in range(K - 1):
-                    z.accumulate(plan, grads[i], stage[i][k], overwrite_first=(k == 0), stream=stream)
-                z.accumulate_norm(plan, grads[i], stage[i][K - 1], wss[i], nouts[i], overwrite_first=(K == 1),
-                                  stream=stream)
-            if b.group is not None:
-                z.allreduce_sumsq_(nouts[i], b.group)
-            b.t += 1
-            z.step(plan, b.master, b.m, b.v, grads[i], b.wbf, b.hp, b.t, nouts[i], stream=stream)
-            host_rec[i].copy_(nouts[i], non_blocking=True)  # device -> host, on the step's stream
-            step_done[i].record(stream)
-            if t >= 1:  # read the previous step's result
-                step_done[1 - i].synchronize()
-                seen.append(z.decode_norm(host_rec[1 - i]))
-        step_done[(n_steps - 1) % 2].synchronize()
-        seen.append(z.decode_norm(host_rec[(n_steps - 1) % 2]))
-
-    e2e_steps(2)
+    loop = z.HostFedSteps(b.plan, b.master, b.m, b.v, b.wbf, b.hp, b.K, t=b.t, k_way=args.k_way, group=b.group,
+                          stream=stream, stage0=b.micros, grad0=b.grad, workspace0=b.ws, norm_out0=b.nout)
+    seen = loop.run(host_micros, 2)
     torch.cuda.synchronize()
-    h2d_bytes = sum(mb.numel() * mb.element_size() for mb in host_micros)
+    h2d_bytes = loop.h2d_bytes_per_step
     # the host link's own speed on this box, for reading the e2e number: one plain copy
     c0, c1 = ev(), ev()
     c0.record(stream)
-    for k in range(K):
-        stage[0][k].copy_(host_micros[k], non_blocking=True)
+    for k in range(b.K):
+        loop.stage[0][k].copy_(host_micros[k], non_blocking=True)
     c1.record(stream)
     torch.cuda.synchronize()
     h2d_gbs = h2d_bytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
     barrier(world)
     e0, e1 = ev(), ev()
     e0.record(stream)
-    e2e_steps(args.steps, first_event=e0, time_copies=True)
+    seen += loop.run(host_micros, args.steps, first_event=e0, time_copies=True)
     e1.record(stream)
     torch.cuda.synchronize()
+    b.t = loop.t
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-    copy_ms = statistics.mean(x.elapsed_time(y) for x, y in copy_ev)
+    copy_ms = statistics.mean(x.elapsed_time(y) for x, y in loop.copy_times)
     assert all(r["status"] == 0 for r in seen)
     return {"value": P_job / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
-            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": z.NORM_OUT_BYTES, "h2d_copy_gbs_before": h2d_gbs,
-            "h2d_copy_ms_in_loop": copy_ms, "h2d_copy_gbs_in_loop": h2d_bytes / (copy_ms * 1e-3) / 1e9,
-            "how": "pinned host gradients copied by the DMA engines on a side stream into two staging "
-                   "buffers, overlapping the previous step's kernels; norm record read back every step"}
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": loop.d2h_bytes_per_step,
+            "h2d_copy_gbs_before": h2d_gbs, "h2d_copy_ms_in_loop": copy_ms,
+            "h2d_copy_gbs_in_loop": h2d_bytes / (copy_ms * 1e-3) / 1e9,
+            "how": "HostFedSteps: pinned host gradients copied by the DMA engines on a side stream into two "
+                   "staging sets, overlapping the previous step's kernels; norm record read back every step"}
 
 
 def torch_baseline(b, args):
@@ -751,7 +961,7 @@ def torch_baseline(b, args):
         wbf.copy_(master)
         mark(4)
 
-    flush = torch.empty(64 << 20, dtype=torch.float32, device=b.dev) if b.path_bytes() < 4 * L2_BYTES else None
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=b.dev) if flushes_l2(b.path_bytes()) else None
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -843,20 +1053,34 @@ def main():
     if args.seed is not None:
         w.seed = args.seed
 
+    if args.write_traffic_record:
+        import zero_sharded_mixed_local_gb300 as z
+        local = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank).local_numel  # host-only call
+        kernel = "list_step" if args.tensor_list else "adamw_step"
+        rec = write_traffic_record(args.write_traffic_record, kernel, args.workload, args.traffic_command, local)
+        print(json.dumps(rec))
+        return
+
+    if args.data_parallel:
+        data_parallel_workload(w, int(os.environ.get("WORLD_SIZE", "1")))
+
     if args.impl == "reference":
         run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
 
     import zero_sharded_mixed_local_gb300 as z
 
-    world, rank, local = dist_setup()
+    world, rank, local = dist_setup(one_rank_group=args.data_parallel)
     torch.cuda.set_device(torch.device("cuda", local))
     z.load_library()
-    b = StepBench(args, w, z, world, rank, local)
+    if args.data_parallel:
+        b = DataParallelBench(args, w, z, world, rank, local)
+    else:
+        b = StepBench(args, w, z, world, rank, local)
 
-    recs, ms_step, clk, l2_note = time_steps(b, args, world, local)
+    recs, ms_step, clk, _ = time_steps(b, args, world, local)
     P_job = sum_over_ranks(b.P, world)  # parameters all ranks step per step
-    kernels, roofline = kernel_report(b, recs, args)
+    kernels, roofline = b.report(recs) if args.data_parallel else kernel_report(b, recs, args)
     z.read_norm(b.nout, b.stream)
     path_bytes = b.path_bytes()
 
@@ -881,30 +1105,11 @@ def main():
             "warmup": args.warmup,
             "ms_per_step": ms_step,
             "higher_is_better": True,
-            "scaling": "weak",
+            "scaling": "strong" if args.data_parallel else "weak",
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic",
-            "config": {
-                "workload": w.description,
-                "local_params_per_gpu": b.P,
-                "params_per_step_all_ranks": P_job,
-                "arena_elems": b.plan.arena_numel,
-                "micro_batches": b.K,
-                "dp_size": w.dp_size,
-                "dp_rank": b.dp_rank,
-                "parallelism": "zero1 dp%d shard per GPU" % w.dp_size,
-                "seed": w.seed,
-                "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
-                "accumulate": ("all K micro-batches in one pass (K-way)" if args.k_way
-                               else "one call per micro-batch, as they arrive"),
-                "exchange": ("pack the reduce-scatter input and unpack the bf16 weights, model layout <-> arena"
-                             if b.full_g is not None else "none (the local step only)"),
-                "launch": "one CUDA graph per step (StepGraph)" if b.graph is not None else "eager calls",
-                "layout": ("tensor lists: one allocation per tensor shard, a 16384-element run table"
-                           if b.lists is not None else "arenas: one padded buffer per quantity"),
-                "l2": l2_note,
-            },
+            "config": step_config(args, w, b.P, P_job, b.plan.arena_numel, b.dp_rank),
             "hbm_gbs_step": path_bytes / (ms_step * 1e-3) / 1e9,
             "kernels": kernels,
             "roofline": roofline,
@@ -923,8 +1128,8 @@ def main():
             tb["ours_over_torch"] = out["value"] / tb["value"]
             out["torch_baseline"] = tb
         print(json.dumps(out), flush=True)
-    if world > 1:
-        import torch.distributed as dist
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()
 
 

@@ -266,6 +266,29 @@ int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp
                const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
                const zero1_norm_out* d_norm, void* stream);
 
+/* The whole local step of one rank in one call ("ZeRO-1 风格的 Distributed
+ * Optimizer", section 6.7: every micro-batch's gradient accumulated into the
+ * fp32 .grad, then the reduction and the optimizer step; sections 6.2-6.3 and
+ * 6.6 for the step): zero1_accumulate_norm over all n_micro micro-batches
+ * with the first one overwriting grad, then zero1_step reading the norm
+ * record that pass wrote.  The same kernels in the same order as those two
+ * calls, so the results are theirs bit for bit; it saves a caller, a binding
+ * above all, one crossing of the ABI and its per-call checks, which is what
+ * bounds the step of a small shard.  Every argument of both passes is checked
+ * before the first launch, so an error leaves every buffer unchanged.  There
+ * is no point between the two passes to sum the sum of squares across ranks:
+ * pass the other ranks' share as extra_sumsq when it is known, else use the
+ * two calls.
+ *   grad, micro_bf16, n_micro, grad_divisor, extra_sumsq, workspace,
+ *   workspace_bytes, d_norm       as for zero1_accumulate_norm (d_norm must
+ *                                 not be NULL)
+ *   master, exp_avg, exp_avg_sq, weight_bf16, hp, step_t   as for zero1_step
+ * Errors: those of zero1_accumulate_norm and zero1_step. */
+int zero1_local_step(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16, int32_t n_micro,
+                     double grad_divisor, double extra_sumsq, void* workspace, size_t workspace_bytes,
+                     zero1_norm_out* d_norm, float* master, float* exp_avg, float* exp_avg_sq,
+                     uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t, void* stream);
+
 /* Largest plan zero1_grad_norm_static serves: its fixed scratch holds one
  * 8-byte partial per 16384-element tile, 262144 tiles (2 MiB per GPU), i.e.
  * arenas of up to 2^32 elements. */
@@ -289,7 +312,10 @@ int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp
  * overlap on the GPU (different streams or threads) race on it, so the
  * caller must serialise them.  The first call on each device looks up the
  * array's device address with that device current; make that first call
- * before any stream capture.
+ * before any stream capture.  The address is kept with the ID of the CUDA
+ * context it belongs to and looked up again when another context is current
+ * (after cudaDeviceReset, or a driver-API caller's own context); make the
+ * first call in such a context before any capture too.
  * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ETOOBIG, ZERO1_ECUDA. */
 int zero1_grad_norm_static(const zero1_plan* plan, const float* grad, double extra_sumsq,
                            zero1_norm_out* d_out, void* stream);

@@ -11,6 +11,9 @@ and stays zero under every operation, which the comparison checks too) and
 steps either every arena element or, for the full-size workloads, sampled
 arena indices.
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -91,26 +94,38 @@ def group_counts(idx, plan):
 
 
 CHUNK = 1 << 26  # elements per host pass: bounds host memory on the full-size workloads
+ORACLE_THREADS = max(1, min(8, os.cpu_count() or 1))  # chunks in flight (ctypes releases the GIL)
+
+
+def _oracle_chunk(micros, gpu_grad, c0, c1):
+    g = np.zeros(c1 - c0, np.float32)
+    for k, mb in enumerate(micros):
+        oracle.accumulate(g, u16(mb[c0:c1]), overwrite=(k == 0))
+    gg = gpu_grad[c0:c1].cpu().numpy()
+    bad = None
+    if not np.array_equal(gg.view(np.uint32), g.view(np.uint32)):
+        bad = int(np.nonzero(gg.view(np.uint32) != g.view(np.uint32))[0][0]) + c0
+    return g, bad, oracle.sumsq(g)
 
 
 def oracle_pass(micros, gpu_grad, idx):
     """Oracle accumulation over the whole arena, chunk by chunk: checks the GPU grad
-    arena bit for bit, returns (oracle grad at idx, oracle sum of squares)."""
+    arena bit for bit, returns (oracle grad at idx, oracle sum of squares).  Chunks run
+    on a few host threads; their sums of squares are added in chunk order."""
     n = gpu_grad.numel()
     s = 0.0
     g_idx = np.empty(idx.size, np.float32)
-    for c0 in range(0, n, CHUNK):
-        c1 = min(n, c0 + CHUNK)
-        g = np.zeros(c1 - c0, np.float32)
-        for k, mb in enumerate(micros):
-            oracle.accumulate(g, u16(mb[c0:c1]), overwrite=(k == 0))
-        gg = gpu_grad[c0:c1].cpu().numpy()
-        if not np.array_equal(gg.view(np.uint32), g.view(np.uint32)):
-            bad = int(np.nonzero(gg.view(np.uint32) != g.view(np.uint32))[0][0]) + c0
-            raise AssertionError("grad arena differs from the oracle at element %d" % bad)
-        s += oracle.sumsq(g)
-        lo, hi = np.searchsorted(idx, [c0, c1])
-        g_idx[lo:hi] = g[idx[lo:hi] - c0]
+    bounds = [(c0, min(n, c0 + CHUNK)) for c0 in range(0, n, CHUNK)]
+    with ThreadPoolExecutor(max_workers=ORACLE_THREADS) as ex:
+        futures = [ex.submit(_oracle_chunk, micros, gpu_grad, c0, c1) for c0, c1 in bounds]
+        for j, (c0, c1) in enumerate(bounds):
+            g, bad, part = futures[j].result()
+            futures[j] = None  # the chunk's host arrays go as soon as they are read
+            if bad is not None:
+                raise AssertionError("grad arena differs from the oracle at element %d" % bad)
+            s += part
+            lo, hi = np.searchsorted(idx, [c0, c1])
+            g_idx[lo:hi] = g[idx[lo:hi] - c0]
     return g_idx, s
 
 
@@ -134,8 +149,8 @@ def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda
     report = []
     for t in range(1, steps + 1):
         new_grads = micros is None or fresh_grads
-        if new_grads:
-            micros = pb.gen.micro_grads()
+        if new_grads:  # refill the same buffers: one set of micro-batch arenas at a time
+            micros = pb.gen.micro_grads(out=micros)
         got = pb.gpu_step(micros, t, fused=fused)
         if new_grads:
             g_idx, ref_sumsq = oracle_pass(micros, pb.grad, idx)

@@ -42,6 +42,33 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    # the config record is the GPU arm's own, built from the library's plan of the same shard
+    import zero_sharded_mixed_local_gb300 as z
+    w = get_workload("toy")
+    plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank)
+    assert d["config"] == bench.step_config(_default_args(), w, plan.local_numel, plan.local_numel,
+                                            plan.arena_numel, w.dp_rank)
+    assert d["oracle_sample"]["sample_elements"] > 0 and "sample_elements" not in d["config"]
+
+
+def _default_args():
+    import argparse
+    return argparse.Namespace(k_way=False, unfused=False, exchange=False, graph=False, tensor_list=False)
+
+
+def test_reference_shard_sizes_are_the_plans_for_every_workload_and_rank():
+    """The reference arm derives the shard sizes of its config from the oracle's split; they
+    equal the library plan's local and padded arena sizes, for every workload and for the
+    dp ranks a multi-GPU job steps."""
+    import zero_sharded_mixed_local_gb300 as z
+    from zero_sharded_mixed_local_gb300.workloads import WORKLOADS
+    for name in WORKLOADS:
+        w = get_workload(name)
+        for world in (1, 2, 8):
+            for r in range(min(world, 3)):
+                dp = bench.rank_dp_rank(w, world, r)
+                plan = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, dp)
+                assert bench.oracle_shard_sizes(w, dp) == (plan.local_numel, plan.arena_numel), (name, world, r)
 
 
 def _rank_worker(rank, world, port, q):
@@ -107,3 +134,44 @@ def test_clock_samples_inside_the_timed_region():
     assert got["samples"] == 4 and got["samples_in_timed_region"] == 2
     assert got["sm_mhz"] == 1985.0 and got["sm_max_mhz"] == 2070.0
     assert got["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_record_from_an_ncu_metrics_list(tmp_path):
+    """bench.py --write-traffic-record turns ncu's CSV metrics list into the record the bench
+    scales roofline.traffic from: per-launch DRAM read + write of the step kernel only (other
+    kernels and units ignored), per parameter, with the kernel sources' hash."""
+    head = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+            '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n')
+
+    def row(i, name, metric, unit, value):
+        return ('"%d","1","python3","h","%s","1","7","(256, 1, 1)","(9, 1, 1)","0","10.3",'
+                '"Command line profiler metrics","%s","%s","%s"\n' % (i, name, metric, unit, value))
+
+    step = "void zero1::<unnamed>::adamw_step_kernel<true, false>(zero1::StepParams, long)"
+    lines = ["==PROF== Connected to process 1\n", head]
+    for i, (rd, wr) in enumerate(((1600.0, 1400.0), (1602.0, 1398.0))):
+        lines += [row(2 * i, "void at::fill_kernel(int)", "dram__bytes_read.sum", "byte", "99"),
+                  row(2 * i + 1, step, "dram__bytes_read.sum", "Kbyte", "%.3f" % (rd / 1e3)),
+                  row(2 * i + 1, step, "dram__bytes_write.sum", "byte", "%d" % wr),
+                  row(2 * i + 1, step, "gpu__time_duration.sum", "us", "4.5")]
+    csv_path = tmp_path / "traffic.csv"
+    csv_path.write_text("".join(lines))
+    out = tmp_path / "rec.json"
+    rec = bench.write_traffic_record(str(csv_path), "adamw_step", "tiny", "ncu ...", 100, out=str(out))
+    assert rec["capture"]["launches"] == 2
+    assert rec["dram_read_bytes_per_launch"] == 1601 and rec["dram_write_bytes_per_launch"] == 1399
+    assert rec["traffic_bytes_per_param"] == 30.0 and rec["ncu_duration_us_per_launch"] == 4.5
+    assert rec["kernel_source_sha256_16"] == bench.kernel_source_hash("adamw_step")
+    assert json.loads(out.read_text()) == rec
+
+
+def test_committed_traffic_records_match_the_kernel_sources():
+    """The records bench.py reads were taken on the kernels as they are (else it reports null)."""
+    for kernel in ("adamw_step", "list_step"):
+        path = bench.traffic_record_path(kernel)
+        if path is None:
+            continue
+        rec = json.load(open(path))
+        assert rec["kernel_source_sha256_16"] == bench.kernel_source_hash(kernel), kernel
+        got, src = bench.profile_traffic(kernel, 1_003_782_656)
+        assert got == int(round(rec["traffic_bytes_per_param"] * 1_003_782_656)) and src

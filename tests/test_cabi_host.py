@@ -384,3 +384,21 @@ def test_plan_sizes_are_the_librarys(z):
     assert plan.arena_numel == lib.zero1_plan_arena_numel(h)
     assert plan.workspace_bytes == lib.zero1_workspace_bytes(h)
     assert plan.list_workspace_bytes == lib.zero1_list_workspace_bytes(h)
+
+
+def test_plan_for_rank_is_the_same_list_sharded_for_another_rank():
+    """DataParallelStep builds the other ranks' plans with Plan.for_rank: the same tensors,
+    groups and scales, each rank's own shard (equal to a plan made directly for that rank)."""
+    import zero_sharded_mixed_local_gb300 as z
+    numels = [5000, 17, 64, 3, 999, 1]
+    for kw in ({"no_decay": [0, 1, 0, 1, 0, 0]},
+               {"groups": [3, 0, 3, 1, 2, 0], "lr_scale": [1.0, 0.5, 2.0] + [1.0] * 5,
+                "wd_scale": [1.0, 0.0, 0.25] + [1.0] * 5}):
+        base = z.Plan(numels, dp_size=4, dp_rank=1, **kw)
+        for r in range(4):
+            a, b = base.for_rank(r), z.Plan(numels, dp_size=4, dp_rank=r, **kw)
+            assert (a.dp_size, a.dp_rank, a.local_numel, a.arena_numel) == (4, r, b.local_numel, b.arena_numel)
+            la, lb = a.layout(), b.layout()
+            for f in ("shard_start", "counts", "offsets", "no_decay"):
+                assert np.array_equal(getattr(la, f), getattr(lb, f)), (r, f)
+            assert [a.group_scales(g) for g in range(8)] == [b.group_scales(g) for g in range(8)]

@@ -55,3 +55,17 @@ def test_bench_checkpoint_io_restores_the_state(extra):
     c = d["checkpoint"]
     assert c["restored_bit_exact"] is True and c["bytes"] == 12 * d["config"]["local_params_per_gpu"]
     assert c["save_gbs"] > 0 and c["load_gbs"] > 0 and c["snapshot_gbs"] > 0
+
+
+def test_bench_data_parallel_line():
+    """--data-parallel on one GPU: the whole toy model through DataParallelStep in a one-rank NCCL
+    group (pack, all-to-all, ordered accumulation, all-reduce, step, all-gather, unpack)."""
+    d = _run("--workload", "toy", "--data-parallel", "--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    assert d["scaling"] == "strong" and d["value"] > 0
+    c = d["config"]
+    assert c["dp_size"] == 1 and c["local_params_per_gpu"] == c["params_per_step_all_ranks"] == 3147008
+    assert set(d["kernels"]) == {"reduce_scatter", "allreduce_sumsq", "adamw_step", "all_gather"}
+    # per step, K = 2: a pack and an accumulate for the first micro-batch, a pack and the fused pass
+    # (2 kernels) for the last, the step, the unpack
+    assert d["gpu_launches"] == 3 * 7
+    assert d["roofline"]["kernel"] == "adamw_step_kernel" and d["roofline"]["params_per_launch"] == 3147008

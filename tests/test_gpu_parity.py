@@ -51,7 +51,7 @@ def test_parameter_groups_with_lr_and_wd_scales():
 
 
 def test_smollm135m_mup_groups_full_size_sampled():
-    res = run_parity("smollm135m_mup", fresh_grads=False, sample="sampled")
+    res = run_parity("smollm135m_mup", sample="sampled")
     assert res["local_numel"] > 67_000_000
 
 
@@ -107,24 +107,24 @@ def test_fused_accumulate_norm_equals_separate_calls():
 
 
 def test_smollm135m_full_size_sampled():
-    res = run_parity("smollm135m", fresh_grads=False, sample="sampled")
+    res = run_parity("smollm135m", sample="sampled")
     assert res["local_numel"] == 134_515_008
 
 
 def test_smollm1p7b_full_size_sampled_clip_active():
-    res = run_parity("smollm1p7b", fresh_grads=False, sample="sampled")
+    res = run_parity("smollm1p7b", sample="sampled")
     assert res["local_numel"] == 213_922_048
     t, gpu_norm, ref_norm, coef = res["norms"][0]
     assert 3.0 < ref_norm < 5.0 and coef < 1.0  # the grads were scaled so clipping is active
 
 
 def test_llama8b_full_size_sampled():
-    res = run_parity("llama8b", steps=10, fresh_grads=False, sample="sampled")
+    res = run_parity("llama8b", steps=10, sample="sampled")
     assert res["local_numel"] == 1_003_782_656
 
 
 def test_ragged_full_size_sampled():
-    res = run_parity("ragged", fresh_grads=False, sample="sampled")
+    res = run_parity("ragged", sample="sampled")
     _, gpu_norm, ref_norm, coef = res["norms"][0]
     assert ref_norm > 1.0 and coef < 1.0
 

@@ -6,7 +6,6 @@ raw pointers and forwards the current CUDA stream.  It has no fallback: when
 the library is missing or a call fails it raises.
 """
 import ctypes
-import functools
 import os
 from dataclasses import dataclass
 
@@ -91,6 +90,9 @@ def load_library(path=None):
         "zero1_grad_norm": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
         "zero1_grad_norm_static": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, vp]),
         "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
+        "zero1_local_step": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, ctypes.c_double, ctypes.c_double, vp,
+                                            ctypes.c_size_t, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64,
+                                            vp]),
         "zero1_read_norm": (ctypes.c_int, [vp, vp, ctypes.POINTER(_NormOut)]),
         "zero1_step_scalars_fill": (ctypes.c_int, [vp, ctypes.POINTER(_Hparams), i64, ctypes.POINTER(_StepScalars)]),
         "zero1_step_dev": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
@@ -130,23 +132,31 @@ def _check(code, where):
         raise Zero1Error(code, where)
 
 
+# torch's own accessors of the current device and of its current stream's handle: what
+# torch.cuda.current_device() and current_stream().cuda_stream return, without building a
+# Stream object on every call
+_current_device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
+_current_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_ptr(stream, device):
-    """The stream a call launches on.  The library launches on the current CUDA device, so the
-    tensors' device must be the current one (a kernel given another device's memory or stream
-    would fail); say so here rather than through a CUDA error."""
+    """The stream a call launches on (a cudaStream_t as an int).  The library launches on the
+    current CUDA device, so the tensors' device must be the current one (a kernel given another
+    device's memory or stream would fail); say so here rather than through a CUDA error."""
     if not isinstance(device, torch.device):
         device = torch.device(device)
     index = device.index
-    if index is not None and device.type == "cuda":
-        current = torch.cuda.current_device()
-        if index != current:
-            raise ValueError("the buffers are on %s but the current CUDA device is cuda:%d; call inside "
-                             "torch.cuda.device(%d)" % (device, current, index))
+    current = _current_device()
+    if index is not None and device.type == "cuda" and index != current:
+        raise ValueError("the buffers are on %s but the current CUDA device is cuda:%d; call inside "
+                         "torch.cuda.device(%d)" % (device, current, index))
     if stream is None:
-        stream = torch.cuda.current_stream()  # the current device's, checked above
+        if _current_raw_stream is not None:
+            return _current_raw_stream(current)  # the current device's, checked above
+        stream = torch.cuda.current_stream()
     elif index is not None and stream.device_index != index:
         raise ValueError("stream is on %s, the buffers on %s" % (stream.device, device))
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _ptr(t, dtype, numel, name, device=None, host_ok=False):
@@ -169,14 +179,7 @@ def _ptr(t, dtype, numel, name, device=None, host_ok=False):
     ptr = t.data_ptr()
     if ptr % 16:
         raise ValueError("%s must start on a 16-byte boundary" % name)
-    return ctypes.c_void_p(ptr)
-
-
-@functools.lru_cache(maxsize=256)
-def _hparams_struct(values):
-    """The ctypes zero1_hparams for a tuple of settings (the library only reads it); building
-    one costs more per call than looking it up."""
-    return _Hparams(*values)
+    return ptr  # ctypes passes an int to a c_void_p parameter as the address
 
 
 @dataclass
@@ -191,7 +194,8 @@ class Hparams:
     clip_grad: float = 1.0
 
     def _c(self):
-        return _hparams_struct((self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.clip_grad))
+        """A fresh ctypes zero1_hparams for one call (never shared between calls)."""
+        return _Hparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.clip_grad)
 
 
 @dataclass
@@ -252,6 +256,15 @@ class Plan:
         self._groups = grp.copy()
         self.numels = numels.copy()
         self._layout = None
+        self._grouped = groups is not None
+
+    def for_rank(self, dp_rank):
+        """The same parameter list, groups and scales, sharded for another data-parallel rank."""
+        if self._grouped:
+            lr, wd = self._scales
+            return Plan(self.numels, groups=self._groups, dp_size=self.dp_size, dp_rank=dp_rank, lr_scale=lr,
+                        wd_scale=wd)
+        return Plan(self.numels, self._groups, self.dp_size, dp_rank)
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:
@@ -408,7 +421,7 @@ def _micro_array(plan, micro, dev):
     if not 1 <= len(micro) <= MAX_MICRO:
         raise ValueError("1..%d micro-batch gradients per call" % MAX_MICRO)
     return micro, (ctypes.c_void_p * len(micro))(*[_ptr(mb, torch.bfloat16, plan.arena_numel, "micro[%d]" % k, dev,
-                                                        host_ok=True).value for k, mb in enumerate(micro)])
+                                                        host_ok=True) for k, mb in enumerate(micro)])
 
 
 def accumulate_norm(plan, grad, micro, workspace, norm_out, overwrite_first=True, extra_sumsq=0.0, divisor=1.0,
@@ -472,6 +485,29 @@ def step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, hparams, step_t, 
     hp = hparams._c() if isinstance(hparams, Hparams) else Hparams(**hparams)._c()
     _check(lib.zero1_step(plan.handle, *ptrs, wp, ctypes.byref(hp), int(step_t), npp, _stream_ptr(stream, dev)),
            "zero1_step")
+
+
+def local_step(plan, grad, micro, workspace, norm_out, master, exp_avg, exp_avg_sq, weight_bf16, hparams, step_t,
+               extra_sumsq=0.0, divisor=1.0, stream=None):
+    """zero1_local_step: the whole local step in one call -- every micro-batch accumulated
+    (the first overwriting ``grad``) with the norm in one pass, then clip + AdamW + the bf16
+    copy.  The same results as accumulate_norm(overwrite_first=True) then step()."""
+    lib = load_library()
+    n = plan.arena_numel
+    dev = master.device
+    micro, arr = _micro_array(plan, micro, dev)
+    gp = _ptr(grad, torch.float32, n, "grad", dev)
+    wp = _ptr(workspace, torch.uint8, None, "workspace", dev)
+    if workspace.numel() < plan.workspace_bytes:
+        raise ValueError("workspace has %d bytes, the plan needs %d" % (workspace.numel(), plan.workspace_bytes))
+    op = _norm_ptr(norm_out, device=dev)
+    ptrs = [_ptr(master, torch.float32, n, "master", dev), _ptr(exp_avg, torch.float32, n, "exp_avg", dev),
+            _ptr(exp_avg_sq, torch.float32, n, "exp_avg_sq", dev)]
+    bp = None if weight_bf16 is None else _ptr(weight_bf16, torch.bfloat16, n, "weight_bf16", dev)
+    hp = hparams._c() if isinstance(hparams, Hparams) else Hparams(**hparams)._c()
+    _check(lib.zero1_local_step(plan.handle, gp, arr, len(micro), float(divisor), float(extra_sumsq), wp,
+                                workspace.numel(), op, *ptrs, bp, ctypes.byref(hp), int(step_t),
+                                _stream_ptr(stream, dev)), "zero1_local_step")
 
 
 def step_scalars(plan, hparams, step_t):

@@ -188,15 +188,23 @@ int fill_step_scalars(const zero1_plan* plan, const zero1_hparams* hp, int64_t s
 
 namespace {
 
-// Checks shared by zero1_step and zero1_step_dev, and the launch.
-int launch_checked_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq, const float* grad,
-                        uint16_t* weight_bf16, const zero1_step_scalars* sc, const zero1_step_scalars* d_scalars,
-                        const zero1_norm_out* d_norm, void* stream) {
+// The step's buffer checks (shared by zero1_step, zero1_step_dev and zero1_local_step).
+int check_step_buffers(const zero1_plan* plan, const float* master, const float* exp_avg, const float* exp_avg_sq,
+                       const float* grad, const uint16_t* weight_bf16, const zero1_norm_out* d_norm) {
     if (plan->arena_numel == 0) return ZERO1_OK;  // nothing to do; empty buffers may be NULL
     if (master == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || grad == nullptr) return ZERO1_EINVAL;
     if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) || !aligned16(grad)) return ZERO1_EALIGN;
     if (weight_bf16 != nullptr && !aligned16(weight_bf16)) return ZERO1_EALIGN;
     if (d_norm != nullptr && !aligned16(d_norm)) return ZERO1_EALIGN;
+    return ZERO1_OK;
+}
+
+// Checks shared by zero1_step and zero1_step_dev, and the launch.
+int launch_checked_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq, const float* grad,
+                        uint16_t* weight_bf16, const zero1_step_scalars* sc, const zero1_step_scalars* d_scalars,
+                        const zero1_norm_out* d_norm, void* stream) {
+    const int rc = check_step_buffers(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, d_norm);
+    if (rc != ZERO1_OK || plan->arena_numel == 0) return rc;
     zero1::StepParams p{};
     p.master = master;
     p.m = exp_avg;
@@ -220,6 +228,26 @@ extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg,
     NvtxRange range("zero1_step");
     zero1_step_scalars sc{};
     const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
+    if (rc != ZERO1_OK) return rc;
+    return launch_checked_step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, &sc, nullptr, d_norm, stream);
+}
+
+extern "C" int zero1_local_step(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
+                                int32_t n_micro, double grad_divisor, double extra_sumsq, void* workspace,
+                                size_t workspace_bytes, zero1_norm_out* d_norm, float* master, float* exp_avg,
+                                float* exp_avg_sq, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                                void* stream) {
+    NvtxRange range("zero1_local_step");
+    if (plan == nullptr || d_norm == nullptr) return ZERO1_EINVAL;
+    // Every argument of both passes is checked before the first launch, so a rejected call
+    // leaves every buffer as it was.
+    zero1_step_scalars sc{};
+    int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
+    if (rc != ZERO1_OK) return rc;
+    rc = check_step_buffers(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, d_norm);
+    if (rc != ZERO1_OK) return rc;
+    rc = zero1_accumulate_norm(plan, grad, micro_bf16, n_micro, 1, grad_divisor, extra_sumsq, workspace,
+                               workspace_bytes, d_norm, stream);
     if (rc != ZERO1_OK) return rc;
     return launch_checked_step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, &sc, nullptr, d_norm, stream);
 }

@@ -21,7 +21,13 @@
 //     by the caller.
 //   - The first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, which may load the module) with that device
-//     current; make that first call before any stream capture.
+//     current; make that first call before any stream capture.  The address
+//     is cached per device together with the unique ID of the CUDA context
+//     it was resolved in, and looked up again when the current context is
+//     another one (after cudaDeviceReset, or when a driver-API caller has
+//     made its own context current), so a stale address is never used.
+#include <cuda.h>  // CUcontext and CUresult only: the two driver calls below are
+                   // reached through the runtime, so the library does not link libcuda
 #include <mutex>
 
 #include "zero1_internal.h"
@@ -33,10 +39,47 @@ static __device__ __align__(256) double g_static_norm_partials[ZERO1_STATIC_NORM
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-double* g_partials_addr[kMaxDevices];  // per device, resolved once
 
-// Device address of the array on the current device, or nullptr with *err set.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+struct Resolved {
+    bool valid = false;
+    unsigned long long context_id = 0;  // the context the address belongs to
+    double* address = nullptr;
+};
+
+std::mutex g_lock;
+Resolved g_resolved[kMaxDevices];
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// The two driver entry points, looked up once through the runtime.
+cudaError_t driver_entry_points() {
+    if (g_ctx_get_current != nullptr && g_ctx_get_id != nullptr) return cudaSuccess;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || f == nullptr) return cudaErrorSymbolNotFound;
+    void* g = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &g, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || g == nullptr) return cudaErrorSymbolNotFound;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(g);
+    return cudaSuccess;
+}
+
+// Unique ID of the calling thread's current context; false when none is current.
+bool current_context_id(unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current device's current context, or
+// nullptr with *err set.
 double* static_partials(cudaError_t* err) {
     int dev = 0;
     *err = cudaGetDevice(&dev);
@@ -46,13 +89,22 @@ double* static_partials(cudaError_t* err) {
         return nullptr;
     }
     std::lock_guard<std::mutex> guard(g_lock);
-    if (g_partials_addr[dev] == nullptr) {
-        void* p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_static_norm_partials);
-        if (*err != cudaSuccess) return nullptr;
-        g_partials_addr[dev] = static_cast<double*>(p);
+    *err = driver_entry_points();
+    if (*err != cudaSuccess) return nullptr;
+    Resolved& r = g_resolved[dev];
+    unsigned long long id = 0;
+    if (r.valid && current_context_id(&id) && id == r.context_id) return r.address;
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_static_norm_partials);  // makes the device's context current if none is
+    if (*err != cudaSuccess) return nullptr;
+    if (!current_context_id(&id)) {
+        *err = cudaErrorDeviceUninitialized;  // no context is current after the lookup
+        return nullptr;
     }
-    return g_partials_addr[dev];
+    r.valid = true;
+    r.context_id = id;
+    r.address = static_cast<double*>(p);
+    return r.address;
 }
 
 }  // namespace

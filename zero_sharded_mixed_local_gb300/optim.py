@@ -30,7 +30,7 @@ import math
 import torch
 
 from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, Hparams, list_accumulate,
-                      list_accumulate_norm, list_grad_norm, list_step, list_step_dev, new_norm_out, Plan,
+                      list_accumulate_norm, list_grad_norm, list_step, list_step_dev, local_step, new_norm_out, Plan,
                       PointerLists, read_norm, step, step_dev, step_scalars, STEP_SCALARS_BYTES)
 
 
@@ -105,6 +105,21 @@ class LocalShardAdamW:
         step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
              self.norm_out, stream=stream)
         self._micro_seen = 0
+        return _applied(self, stream) if check_finite else None
+
+    def step_from(self, micro, extra_sumsq=0.0, divisor=1.0, lr=None, stream=None, check_finite=False):
+        """The whole step from micro-batch gradients that are all resident (a bf16 arena or a list
+        of up to MAX_MICRO, in order) in one library call (zero1_local_step): accumulate with the
+        norm in one pass, then clip + AdamW + bf16 copy.  The same result as accumulate(micro,
+        last=True) then step(); no all-reduce can sit between the two passes, so give the other
+        ranks' sum of squares as ``extra_sumsq`` or use those two calls."""
+        self.t += 1
+        hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
+        local_step(self.plan, self.grad, micro, self.workspace, self.norm_out, self.master, self.exp_avg,
+                   self.exp_avg_sq, self.weight_bf16, hp, self.t, extra_sumsq=extra_sumsq, divisor=divisor,
+                   stream=stream)
+        self._micro_seen = 0
+        self._norm_ready = False
         return _applied(self, stream) if check_finite else None
 
     def read_norm(self, stream=None):

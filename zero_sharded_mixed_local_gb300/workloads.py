@@ -215,9 +215,12 @@ class InputGenerator:
     def zeros(self, dtype=torch.float32) -> torch.Tensor:
         return torch.zeros(self.layout.arena_numel, dtype=dtype, device=self.device)
 
-    def micro_grad(self) -> torch.Tensor:
-        """One bf16 micro-batch gradient: N(0, sigma^2) (times the per-tensor scale), RNE to bf16."""
-        out = torch.zeros(self.layout.arena_numel, dtype=torch.bfloat16, device=self.device)
+    def micro_grad(self, out=None) -> torch.Tensor:
+        """One bf16 micro-batch gradient: N(0, sigma^2) (times the per-tensor scale), RNE to bf16.
+        ``out``: an arena this fills instead of a new one (its padding must be zero; only the
+        shards are written)."""
+        if out is None:
+            out = torch.zeros(self.layout.arena_numel, dtype=torch.bfloat16, device=self.device)
         tmp = None
         for i, o, c in self._segments():
             if tmp is None or tmp.numel() < c:
@@ -229,7 +232,10 @@ class InputGenerator:
             out[o:o + c].copy_(t)
         return out
 
-    def micro_grads(self, k=None) -> List[torch.Tensor]:
+    def micro_grads(self, k=None, out=None) -> List[torch.Tensor]:
+        """K micro-batch gradients, drawn in order; ``out`` (a list of arenas) is refilled if given."""
+        if out is not None:
+            return [self.micro_grad(o) for o in out]
         return [self.micro_grad() for _ in range(self.w.micro_batches if k is None else k)]
 
 
