@@ -30,6 +30,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "AdamW shard-step params/sec and HBM GB/s (fraction of GB300 peak), 1 GPU"
+OUT = sys.stdout  # where the JSON line goes (main() keeps the real stdout for it alone)
 STEP_BYTES_PER_ELEM = 30          # adamw_step: grad 4 R, master/m/v 12 R + 12 W, bf16 2 W
 NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e, nominal
 
@@ -66,7 +67,8 @@ def flushes_l2(path_bytes):
 def l2_note(path_bytes):
     if flushes_l2(path_bytes):
         return ("L2 flushed before every step (256 MB write outside the step's events): a step moves %.1f MB "
-                "against the 129 MB L2" % (path_bytes / 1e6))
+                "against the 129 MB L2; the timed steps carry no per-kernel events (a second pass times the "
+                "parts)" % (path_bytes / 1e6))
     return "no flush: each step streams %.1f GB, far above the 129 MB L2" % (path_bytes / 1e9)
 
 
@@ -105,7 +107,9 @@ def step_config(args, w, local, job, arena, dp_rank):
                      "weights" if getattr(args, "data_parallel", False) else
                      "pack the reduce-scatter input and unpack the bf16 weights, model layout <-> arena"
                      if args.exchange else "none (the local step only)"),
-        "launch": "one CUDA graph per step (StepGraph)" if args.graph else "eager calls",
+        "launch": ("one CUDA graph per step (StepGraph)" if args.graph else
+                   "one library call per step (zero1_local_step)" if getattr(args, "one_call", False) else
+                   "eager calls"),
         "layout": ("tensor lists: one allocation per tensor shard, a 16384-element run table"
                    if args.tensor_list else "arenas: one padded buffer per quantity"),
         "l2": l2_note(path_bytes_for(args, local, w.micro_batches, int(sum(w.params.numels)), w.dp_size)),
@@ -490,7 +494,7 @@ def run_reference(args, w, world, rank):
                          "sample": "%d elements drawn like the workload's decayed tensors, per step" % n,
                          "single_core": {"value": value1, "elements": 1 << 22}},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }), flush=True)
+    }), file=OUT, flush=True)
 
 
 # ------------------------------------------------------------------ GPU
@@ -520,6 +524,9 @@ def parse_args():
     ap.add_argument("--k-way", action="store_true",
                     help="accumulate all K micro-batch gradients (already resident) in one fused pass with the "
                          "norm, instead of one call per micro-batch as they arrive")
+    ap.add_argument("--one-call", action="store_true",
+                    help="the whole local step as one library call (zero1_local_step: all K micro-batches, already "
+                         "resident, accumulated with the norm in one pass, then the step); implies --k-way")
     ap.add_argument("--exchange", action="store_true",
                     help="add the copies around the local step: pack the last micro-batch's reduce-scatter input "
                          "from a model-layout bf16 gradient (zero1_shard_gather) and unpack the bf16 weights into "
@@ -542,6 +549,10 @@ def parse_args():
     args = ap.parse_args()
     if args.tensor_list and args.unfused:
         raise SystemExit("--tensor-list runs the fused calls")
+    if args.one_call:
+        if args.unfused or args.graph or args.tensor_list or args.exchange or args.data_parallel:
+            raise SystemExit("--one-call runs the arena step as one eager call")
+        args.k_way = True
     if args.k_way and (args.unfused or args.graph):
         raise SystemExit("--k-way runs the fused eager calls")
     if args.exchange and (args.tensor_list or args.graph):
@@ -685,6 +696,13 @@ class StepBench:
         for k in range(0 if a.k_way else K - 1):
             z.accumulate(plan, self.grad, self.micros[k], overwrite_first=(k == 0), stream=s)
         mark("n0")
+        if a.one_call:  # accumulate + norm and the step in one crossing of the C ABI
+            z.local_step(plan, self.grad, self.micros, self.ws, self.nout, self.master, self.m, self.v, self.wbf,
+                         self.hp, self.t, stream=s)
+            mark("s0")
+            mark("s1")
+            mark("x1")
+            return
         if a.k_way:
             z.accumulate_norm(plan, self.grad, self.micros, self.ws, self.nout, overwrite_first=True, stream=s)
         elif a.unfused:
@@ -822,7 +840,10 @@ def time_steps(b, args, world, local):
         if flush is not None:
             flush.zero_()
         recs[i]["t0"].record(b.stream)
-        b.step(recs[i])
+        # A small step is bound by the host's launches: events recorded inside it would add their
+        # own host time, so its timed steps carry only t0 / t1 and the per-kernel events come
+        # from a second pass below.
+        b.step(None if flush is not None else recs[i])
         recs[i]["t1"].record(b.stream)
     end.record(b.stream)
     b.launches_counted = b.z.launch_count() - launches0  # graph replays launch nothing from the host
@@ -832,6 +853,10 @@ def time_steps(b, args, world, local):
     clk = clocks.stop()
     if flush is not None:
         ms = statistics.mean(r["t0"].elapsed_time(r["t1"]) for r in recs)
+        for i in range(args.steps):  # the breakdown pass: the same steps with every part's events
+            flush.zero_()
+            b.step(recs[i])
+        torch.cuda.synchronize()
     else:
         ms = start.elapsed_time(end) / args.steps
     return recs, max_over_ranks(ms, world), clk, l2_note(b.path_bytes())
@@ -843,6 +868,21 @@ def kernel_report(b, recs, args):
         return None, None
     P, K = b.P, b.K
     mean = lambda a, c: statistics.mean(r[a].elapsed_time(r[c]) for r in recs)  # noqa: E731
+    if args.one_call:  # one call per step: its kernels are not separated by events
+        times = [r["n0"].elapsed_time(r["s0"]) for r in recs]
+        per_param = accumulate_bytes_per_elem(K, True) + STEP_BYTES_PER_ELEM
+        ms = statistics.mean(times)
+        achieved = per_param * P / (ms * 1e-3) / 1e9
+        kernels = {"local_step": {"ms": ms, "gbs": achieved, "launches_per_step": 3, "bytes_per_param": per_param,
+                                  "ms_median": statistics.median(times), "ms_min": min(times), "ms_max": max(times)}}
+        peak, peak_kind = measured_peaks()
+        roofline = {"bound": "hbm", "kernel": "zero1_local_step (accumulate_norm_kway_kernel, sumsq_final_kernel, "
+                                              "adamw_step_kernel)", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": None, "traffic_source": None,
+                    "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
+                    "frac_of_nominal": achieved / NOMINAL_HBM_GBS, "bytes_per_param": per_param,
+                    "params_per_launch": P}
+        return kernels, roofline
     acc_ms, accnorm_ms, step_ms = mean("a0", "n0"), mean("n0", "s0"), mean("s0", "s1")
     norm_bytes = 4 * P if args.unfused else 0
     last_bytes = accumulate_bytes_per_elem(K, True) * P if args.k_way else (6 if K == 1 else 10) * P + norm_bytes
@@ -1043,7 +1083,19 @@ def checkpoint_io(b):
     return out
 
 
+def claim_stdout():
+    """The JSON line is the only thing this program writes to stdout: a duplicate of the real
+    stdout is kept for it, and file descriptor 1 is pointed at stderr, so a library banner
+    (NCCL prints its version from C) cannot add a line."""
+    sys.stdout.flush()
+    out = os.fdopen(os.dup(1), "w")
+    os.dup2(2, 1)
+    return out
+
+
 def main():
+    global OUT
+    OUT = claim_stdout()
     args = parse_args()
     from zero_sharded_mixed_local_gb300.workloads import get_workload
     w = get_workload(args.workload)
@@ -1058,7 +1110,7 @@ def main():
         local = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank).local_numel  # host-only call
         kernel = "list_step" if args.tensor_list else "adamw_step"
         rec = write_traffic_record(args.write_traffic_record, kernel, args.workload, args.traffic_command, local)
-        print(json.dumps(rec))
+        print(json.dumps(rec), file=OUT, flush=True)
         return
 
     if args.data_parallel:
@@ -1127,7 +1179,7 @@ def main():
         if tb is not None:
             tb["ours_over_torch"] = out["value"] / tb["value"]
             out["torch_baseline"] = tb
-        print(json.dumps(out), flush=True)
+        print(json.dumps(out), file=OUT, flush=True)
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()

@@ -69,3 +69,13 @@ def test_bench_data_parallel_line():
     # (2 kernels) for the last, the step, the unpack
     assert d["gpu_launches"] == 3 * 7
     assert d["roofline"]["kernel"] == "adamw_step_kernel" and d["roofline"]["params_per_launch"] == 3147008
+
+
+def test_bench_one_call_line():
+    """--one-call: the whole toy step as one zero1_local_step call (K-way pass, final reduction,
+    step: three launches per step)."""
+    d = _run("--workload", "toy", "--one-call", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-e2e",
+             "--no-torch-baseline")
+    assert d["gpu_launches"] == 3 * 3 and set(d["kernels"]) == {"local_step"}
+    assert d["config"]["launch"] == "one library call per step (zero1_local_step)"
+    assert d["roofline"]["bytes_per_param"] == 2 * 2 + 4 + 30
