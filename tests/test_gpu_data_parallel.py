@@ -1,6 +1,6 @@
 """The whole ZeRO-1 data-parallel step with real collectives (``DataParallelStep``).
 
-Two processes, one per data-parallel rank, each run the library's kernels on
+Two (or three) processes, one per data-parallel rank, each run the library's kernels on
 the one GPU of this machine (independent kernels, nothing waits on the other
 process) while a gloo process group carries the collectives over pinned host
 copies: the all-to-all of the packed bf16 gradients, the one-double all-reduce
@@ -151,6 +151,12 @@ def _check(world, nan_at=None):
 
 def test_two_rank_data_parallel_step_equals_the_unsharded_oracle_step():
     _check(2)
+
+
+def test_three_rank_data_parallel_step_equals_the_unsharded_oracle_step():
+    """With three ranks the order of the owner's fp32 additions matters (two values add the same
+    either way): (micro-batch, rank) order, as the oracle adds them."""
+    _check(3)
 
 
 def test_a_nan_on_one_rank_makes_both_ranks_skip():

@@ -11,7 +11,8 @@ fresh gradients every step, and requires:
     synchronously from device-resident gradients;
   - every step's norm record equal to the synchronous step's;
   - master, m and v within 4 fp32 ulp of the oracle (every element of the toy
-    shard; the usual sample of the full-size SmolLM-135M list), the gradient
+    shard; the usual sample of the full-size SmolLM-135M list and of the
+    1.0B-element Llama-3.1-8B shard the bench's e2e figure runs), the gradient
     of every synchronous step bit-exact against the oracle in full, and the
     bf16 copy the RNE of the master, in full.
 The loop runs in two calls (the bench's warm-up and timed calls, the second
@@ -95,6 +96,12 @@ def test_host_fed_toy_k_way():
 def test_host_fed_smollm135m_sampled():
     recs = _host_fed_vs_sync_and_oracle("smollm135m", steps=4, sampled=True)
     assert len({r["sumsq"] for r in recs}) == 4
+
+
+def test_host_fed_llama8b_sampled():
+    """The bench's own workload for its e2e figure: the 1.0B-element Llama-3.1-8B shard, K = 1."""
+    recs = _host_fed_vs_sync_and_oracle("llama8b", steps=3, sampled=True)
+    assert len({r["sumsq"] for r in recs}) == 3
 
 
 def test_host_fed_rejects_pageable_host_gradients():
