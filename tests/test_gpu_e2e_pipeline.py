@@ -104,6 +104,25 @@ def test_host_fed_llama8b_sampled():
     assert len({r["sumsq"] for r in recs}) == 3
 
 
+def test_host_fed_on_a_stream_that_is_not_the_current_one():
+    """Every copy and kernel of the loop runs on the stream it was given, not on torch's current
+    stream: the same results as the synchronous steps while the current stream stays idle."""
+    sync, pipe = Problem("toy"), Problem("toy")
+    host = []
+    for t in range(1, 5):
+        micros = sync.gen.micro_grads()
+        host.append([mb.cpu().pin_memory() for mb in micros])
+        sync.gpu_step(micros, t)
+    own = torch.cuda.Stream()
+    loop = z.HostFedSteps(pipe.plan, pipe.master, pipe.m, pipe.v, pipe.wbf, pipe.hp, pipe.w.micro_batches,
+                          stream=own)
+    records = loop.run(lambda i: host[i], 4)
+    own.synchronize()
+    assert records[-1] == z.read_norm(sync.nout)
+    for a, b in ((pipe.master, sync.master), (pipe.m, sync.m), (pipe.v, sync.v), (pipe.wbf, sync.wbf)):
+        assert torch.equal(_bits(a), _bits(b))
+
+
 def test_host_fed_rejects_pageable_host_gradients():
     pb = Problem("toy")
     loop = z.HostFedSteps(pb.plan, pb.master, pb.m, pb.v, pb.wbf, pb.hp, pb.w.micro_batches)

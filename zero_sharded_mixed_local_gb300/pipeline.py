@@ -97,8 +97,11 @@ class HostFedSteps:
                     self.copy_times[-1][1].record(side)
                 self.copied[s].record(side)
             stream.wait_event(self.copied[s])
-            self._step(s)
-            self.host_records[s].copy_(self.norm_outs[s], non_blocking=True)  # device -> host, in stream order
+            # the step's kernels, the all-reduce and the record's copy back all in order on `stream`
+            # (the binding and the collective take torch's current stream)
+            with torch.cuda.stream(stream):
+                self._step(s)
+                self.host_records[s].copy_(self.norm_outs[s], non_blocking=True)
             self.step_done[s].record(stream)
             if i >= 1:  # the previous step's record, one step behind
                 self.step_done[1 - s].synchronize()
