@@ -10,6 +10,7 @@
  *   c_abi_step list <out.bin>            the same step through the tensor-list calls, one
  *                                        cudaMalloc per tensor shard; out.bin has the same
  *                                        format (each shard written at its arena offset)
+ *   c_abi_step onecall <out.bin>         the same step as one zero1_local_step call
  *
  * Inputs are a fixed function of the element index, so a test can rebuild them.
  * Test infrastructure: it checks that the C ABI is usable as declared.
@@ -124,7 +125,7 @@ static int run_list(const zero1_plan* plan, const uint16_t* h_g, const float* h_
 
 int main(int argc, char** argv) {
     if (argc < 2) {
-        fprintf(stderr, "usage: %s plan | step <out.bin> | list <out.bin>\n", argv[0]);
+        fprintf(stderr, "usage: %s plan | step <out.bin> | list <out.bin> | onecall <out.bin>\n", argv[0]);
         return 1;
     }
     zero1_plan* plan = NULL;
@@ -142,7 +143,8 @@ int main(int argc, char** argv) {
         return 0;
     }
     const int list_mode = strcmp(argv[1], "list") == 0;
-    if ((strcmp(argv[1], "step") != 0 && !list_mode) || argc < 3) return 1;
+    const int one_call = strcmp(argv[1], "onecall") == 0;
+    if ((strcmp(argv[1], "step") != 0 && !list_mode && !one_call) || argc < 3) return 1;
 
     /* host inputs: the shard elements get values, padding stays zero */
     uint16_t* h_g = calloc((size_t)n, sizeof(uint16_t));
@@ -185,9 +187,14 @@ int main(int argc, char** argv) {
     check_cuda(cudaStreamCreate(&stream), "stream");
     const uint16_t* micro[1] = {d_g};
     zero1_hparams hp = {3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0};
-    check(zero1_accumulate_norm(plan, d_grad, micro, 1, 1, 1.0, 0.0, d_ws, ws_bytes, d_norm, stream),
-          "zero1_accumulate_norm");
-    check(zero1_step(plan, d_p, d_m, d_v, d_grad, d_w, &hp, 1, d_norm, stream), "zero1_step");
+    if (one_call) {
+        check(zero1_local_step(plan, d_grad, micro, 1, 1.0, 0.0, d_ws, ws_bytes, d_norm, d_p, d_m, d_v, d_w, &hp, 1,
+                               stream), "zero1_local_step");
+    } else {
+        check(zero1_accumulate_norm(plan, d_grad, micro, 1, 1, 1.0, 0.0, d_ws, ws_bytes, d_norm, stream),
+              "zero1_accumulate_norm");
+        check(zero1_step(plan, d_p, d_m, d_v, d_grad, d_w, &hp, 1, d_norm, stream), "zero1_step");
+    }
     zero1_norm_out rec;
     check(zero1_read_norm(d_norm, stream, &rec), "zero1_read_norm");
 

@@ -52,9 +52,10 @@ def _inputs(n, offsets, counts):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("mode", ["step", "list"])
+@pytest.mark.parametrize("mode", ["step", "list", "onecall"])
 def test_step_from_c_matches_the_oracle(program, tmp_path, mode):
-    """The arena calls, and the tensor-list calls on one cudaMalloc per tensor shard."""
+    """The arena calls, the tensor-list calls on one cudaMalloc per tensor shard, and the whole
+    step as one zero1_local_step call."""
     outp = str(tmp_path / "out.bin")
     r = subprocess.run([program, mode, outp], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
