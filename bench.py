@@ -301,16 +301,27 @@ class ClockSampler:
 
 
 def dist_setup(one_rank_group=False):
-    """(world, rank, local rank) from the launcher's environment; an NCCL process group when
-    there are several ranks, or with `one_rank_group` a one-rank NCCL group on this GPU."""
+    """(world, rank, device index) from the launcher's environment, and a process group when there
+    are several ranks (or, with `one_rank_group`, a one-rank NCCL group on this GPU).
+
+    The collectives run on NCCL, one rank per GPU.  ZERO1_BENCH_BACKEND=gloo is a functional check
+    of the multi-rank code on a box with fewer GPUs than ranks: the ranks share the visible GPUs
+    round-robin and the collectives run on gloo (no rank's kernel waits for another's).  Its numbers
+    are not a multi-GPU measurement, and the line says which backend ran."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    backend = os.environ.get("ZERO1_BENCH_BACKEND", "nccl")
+    if backend not in ("nccl", "gloo"):
+        raise SystemExit("ZERO1_BENCH_BACKEND must be nccl or gloo")
+    device = local if backend == "nccl" else local % max(1, torch.cuda.device_count())
     if world > 1 or one_rank_group:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        if world > 1:
-            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        torch.cuda.set_device(device)
+        if world > 1 and backend == "gloo":
+            dist.init_process_group("gloo")
+        elif world > 1:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", device))
         else:
             import socket
             sock = socket.socket()
@@ -318,8 +329,8 @@ def dist_setup(one_rank_group=False):
             port = sock.getsockname()[1]
             sock.close()
             dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0, world_size=1,
-                                    device_id=torch.device("cuda", local))
-    return world, rank, local
+                                    device_id=torch.device("cuda", device))
+    return world, rank, device
 
 
 def barrier(world):
@@ -1171,6 +1182,9 @@ def main():
             # counted by the library in eager runs; a graph replays the launches of its one capture
             "gpu_launches": b.launches_counted if b.graph is None else args.steps * b.launches_per_step(),
         }
+        if world > 1 or args.data_parallel:
+            import torch.distributed as dist
+            out["collectives"] = dist.get_backend()
         out["plan"] = {"build_ms": b.plan_ms, "tensors": len(w.params.numels),
                        "list_table_bytes": int(b.z.load_library().zero1_list_table_bytes(b.plan.handle)),
                        "layout_table_bytes": int(b.z.load_library().zero1_layout_table_bytes(b.plan.handle))}

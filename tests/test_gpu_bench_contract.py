@@ -79,3 +79,48 @@ def test_bench_one_call_line():
     assert d["gpu_launches"] == 3 * 3 and set(d["kernels"]) == {"local_step"}
     assert d["config"]["launch"] == "one library call per step (zero1_local_step)"
     assert d["roofline"]["bytes_per_param"] == 2 * 2 + 4 + 30
+
+
+def _torchrun(nproc, *args):
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    env = dict(os.environ, ZERO1_BENCH_BACKEND="gloo")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=%d" % nproc,
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--gpus", str(nproc), *args]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT, env=env)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_bench_multi_rank_path_two_ranks_on_gloo():
+    """The bench's multi-rank code (per-rank dp shards, the summed job size, the slowest rank's
+    time, the sum-of-squares all-reduce on a CUDA record) with two ranks sharing this GPU over
+    gloo: one line from rank 0, weak scaling over dp ranks 0 and 1 of the toy dp4 split."""
+    import zero_sharded_mixed_local_gb300 as z
+    from zero_sharded_mixed_local_gb300.workloads import get_workload
+    d = _torchrun(2, "--workload", "toy", "--steps", "3", "--warmup", "3", "--no-e2e", "--no-torch-baseline")
+    w = get_workload("toy")
+    sizes = [z.Plan(w.params.numels, w.params.no_decay, w.dp_size, r).local_numel for r in (0, 1)]
+    assert d["n_gpus"] == 2 and d["collectives"] == "gloo" and d["scaling"] == "weak"
+    assert d["config"]["params_per_step_all_ranks"] == sum(sizes)
+    assert d["config"]["local_params_per_gpu"] == sizes[0] and d["config"]["dp_rank"] == 0
+    assert d["value"] > 0 and d["cpu_baseline"] is None
+    assert d["gpu_launches"] == 3 * (2 + 2)  # rank 0's own launches
+
+
+def test_bench_data_parallel_two_ranks_on_gloo():
+    """--data-parallel with two ranks: DataParallelStep's host-staged collectives between two
+    processes sharing this GPU (the toy model split dp2)."""
+    d = _torchrun(2, "--workload", "toy", "--data-parallel", "--steps", "3", "--warmup", "3")
+    assert d["n_gpus"] == 2 and d["collectives"] == "gloo" and d["scaling"] == "strong"
+    c = d["config"]
+    assert c["dp_size"] == 2 and c["params_per_step_all_ranks"] == 3147008
+    assert set(d["kernels"]) == {"reduce_scatter", "allreduce_sumsq", "adamw_step", "all_gather"}
+    # rank 0 per step: 2 packs + 1 accumulate call per micro-batch (+1 for the fused pass), the step, 2 unpacks
+    assert d["gpu_launches"] == 3 * (2 * (2 + 1) + 1 + 1 + 2)
