@@ -100,11 +100,12 @@ def _torchrun(nproc, *args):
 
 def test_bench_multi_rank_path_two_ranks_on_gloo():
     """The bench's multi-rank code (per-rank dp shards, the summed job size, the slowest rank's
-    time, the sum-of-squares all-reduce on a CUDA record) with two ranks sharing this GPU over
-    gloo: one line from rank 0, weak scaling over dp ranks 0 and 1 of the toy dp4 split."""
+    time, the sum-of-squares all-reduce on a CUDA record, in the timed steps and inside the
+    host-fed e2e loop) with two ranks sharing this GPU over gloo: one line from rank 0, weak
+    scaling over dp ranks 0 and 1 of the toy dp4 split."""
     import zero_sharded_mixed_local_gb300 as z
     from zero_sharded_mixed_local_gb300.workloads import get_workload
-    d = _torchrun(2, "--workload", "toy", "--steps", "3", "--warmup", "3", "--no-e2e", "--no-torch-baseline")
+    d = _torchrun(2, "--workload", "toy", "--steps", "3", "--warmup", "3", "--no-torch-baseline")
     w = get_workload("toy")
     sizes = [z.Plan(w.params.numels, w.params.no_decay, w.dp_size, r).local_numel for r in (0, 1)]
     assert d["n_gpus"] == 2 and d["collectives"] == "gloo" and d["scaling"] == "weak"
@@ -112,6 +113,8 @@ def test_bench_multi_rank_path_two_ranks_on_gloo():
     assert d["config"]["local_params_per_gpu"] == sizes[0] and d["config"]["dp_rank"] == 0
     assert d["value"] > 0 and d["cpu_baseline"] is None
     assert d["gpu_launches"] == 3 * (2 + 2)  # rank 0's own launches
+    # the e2e leg: HostFedSteps with the all-reduce inside its loop, every step's record read back
+    assert d["e2e"]["value"] > 0 and d["e2e"]["d2h_bytes_per_step"] == 24
 
 
 def test_bench_data_parallel_two_ranks_on_gloo():

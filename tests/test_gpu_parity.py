@@ -106,6 +106,30 @@ def test_fused_accumulate_norm_equals_separate_calls():
     assert z.read_norm(pb.nout) == r1 and torch.equal(g1, pb.grad)
 
 
+def test_wide_and_narrow_gradient_stores_agree():
+    """The passes that write the gradient without reading it first store it with 256-bit accesses
+    when the arena is 32-byte aligned and with two 128-bit ones when it is only 16-byte aligned (the
+    ABI's minimum). Both keep each thread's elements, so the gradient and the norm record must be
+    the same bits: the one-micro-batch fused pass, and the overwriting accumulate with adds after."""
+    pb = Problem(_custom([16384 * 3 + 8 * 5 + 3, 1000, 77], [0, 1, 0], K=3, steps=1, sigma=0.1))
+    micros = pb.gen.micro_grads()
+    wide = pb.plan.new_arena()
+    back = torch.zeros(pb.n + 4, device="cuda")
+    narrow = back[4:]  # 16 bytes past an aligned start
+    assert wide.data_ptr() % 32 == 0 and narrow.data_ptr() % 32 == 16
+    recs = []
+    for g in (wide, narrow):
+        z.accumulate_norm(pb.plan, g, micros[0], pb.ws, pb.nout, overwrite_first=True)
+        recs.append(z.read_norm(pb.nout))
+    assert recs[0] == recs[1]
+    assert torch.equal(wide.view(torch.int32), narrow.view(torch.int32))
+    for g in (wide, narrow):
+        z.accumulate(pb.plan, g, micros, overwrite_first=True)
+    assert torch.equal(wide.view(torch.int32), narrow.view(torch.int32))
+    ref = oracle_grad(pb.n, [u16(m) for m in micros])
+    assert np.array_equal(narrow.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
 def test_smollm135m_full_size_sampled():
     res = run_parity("smollm135m", sample="sampled")
     assert res["local_numel"] == 134_515_008

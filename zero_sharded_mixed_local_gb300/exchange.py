@@ -77,7 +77,9 @@ class DataParallelStep:
             fn(out, inp, group=self.group)
             return
         h_out, h_in = self._host[out_name], self._host[in_name]
-        h_in.copy_(inp)  # synchronous: the device data is complete before the host collective
+        # Synchronous copy: it waits for the stream, so the device data is complete, and so is the
+        # previous call's asynchronous copy out of any pinned buffer before this one rewrites it.
+        h_in.copy_(inp)
         fn(h_out, h_in, group=self.group)
         out.copy_(h_out, non_blocking=True)  # in stream order before the kernels that read it
 
