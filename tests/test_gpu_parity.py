@@ -379,16 +379,18 @@ def test_misaligned_and_wrong_size_buffers_are_rejected():
     assert lib.zero1_accumulate(plan.handle, ctypes.c_void_p(g.data_ptr()), arr, 1, 1, None) == z.ZERO1_EALIGN
 
 
-def test_no_call_writes_outside_its_buffers():
+@pytest.mark.parametrize("guard_bytes", [256, 272])
+def test_no_call_writes_outside_its_buffers(guard_bytes):
     """Every buffer sits between two guard zones filled with a pattern; after every entry point has
-    run on it, the guards are unchanged."""
+    run on it, the guards are unchanged.  256-byte guards leave the buffers 32-byte aligned (the
+    256-bit gradient stores), 272-byte ones only 16-byte aligned (the 128-bit stores)."""
     numels = [1000, 7, 16384 + 9, 33]
     nd = [0, 1, 0, 1]
     plan = z.Plan(numels, nd, 3, 1)
     n, total = plan.arena_numel, plan.total_numel
-    G = 64  # guard elements (a multiple of 8 keeps the buffers 16-byte aligned)
 
     def guarded(count, dtype):
+        G = guard_bytes // torch.empty(0, dtype=dtype).element_size()
         buf = torch.empty(count + 2 * G, dtype=dtype, device="cuda")
         buf.view(torch.uint8).fill_(0xA5)
         return buf, buf[G:G + count]
@@ -413,6 +415,10 @@ def test_no_call_writes_outside_its_buffers():
     bufs["full32"][1].normal_(generator=g)
     bufs["full16"][1].normal_(generator=g)
     B = {k: v[1] for k, v in bufs.items()}
+    assert (B["grad"].data_ptr() % 32 == 0) == (guard_bytes % 32 == 0)
+    z.accumulate_norm(plan, B["grad"], B["mb"], B["ws"], B["nout"])
+    z.local_step(plan, B["grad"], [B["mb"], B["mb"]], B["ws"], B["nout"], B["master"], B["m"], B["v"], B["w"],
+                 z.Hparams(), 1)
     z.accumulate(plan, B["grad"], B["mb"])
     z.accumulate(plan, B["grad"], [B["mb"], B["mb"]], overwrite_first=False)
     z.accumulate_norm(plan, B["grad"], B["mb"], B["ws"], B["nout"], overwrite_first=False)
@@ -427,7 +433,7 @@ def test_no_call_writes_outside_its_buffers():
     for k, (buf, mid) in bufs.items():
         raw = buf.view(torch.uint8)
         eb = buf.element_size()
-        head, tail = raw[:G * eb], raw[(G + mid.numel()) * eb:]
+        head, tail = raw[:guard_bytes], raw[guard_bytes + mid.numel() * eb:]
         assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), k
 
 
