@@ -55,8 +55,17 @@ def path_bytes_for(args, P, K, total=None, world=1):
         total = P if total is None else total
         acc = sum(2 * world + (4 if k == 0 else 8) for k in range(K)) * P
         return K * 8 * total + acc + STEP_BYTES_PER_ELEM * P + 2 * P + 6 * total
+    if uses_micro_step(args, K):  # the norm from the micro-batch (2), the step that writes the gradient (32)
+        return 34 * P
     return ((accumulate_bytes_per_elem(K, args.k_way) + STEP_BYTES_PER_ELEM) * P + (4 * P if args.unfused else 0) +
             (8 * P if args.exchange else 0))
+
+
+def uses_micro_step(args, K):
+    """One micro-batch in the plain arena step: its norm taken from the micro-batch, then the step
+    that writes the gradient (zero1_micro_norm + zero1_step_accumulate), unless asked otherwise."""
+    return (K == 1 and not (getattr(args, "accumulate_first", False) or args.k_way or args.unfused or args.exchange
+                            or args.tensor_list or args.graph or getattr(args, "data_parallel", False)))
 
 
 def flushes_l2(path_bytes):
@@ -99,7 +108,10 @@ def step_config(args, w, local, job, arena, dp_rank):
         "parallelism": ("zero1 data-parallel job, dp%d (one shard per GPU, real collectives)" % w.dp_size
                         if getattr(args, "data_parallel", False) else "zero1 dp%d shard per GPU" % w.dp_size),
         "seed": w.seed,
-        "norm": "separate pass" if args.unfused else "fused into the last micro-batch's accumulation",
+        "norm": ("separate pass" if args.unfused else
+                 "taken from the one micro-batch; the step writes the gradient (zero1_micro_norm + "
+                 "zero1_step_accumulate)" if uses_micro_step(args, w.micro_batches) else
+                 "fused into the last micro-batch's accumulation"),
         "accumulate": ("all K micro-batches in one pass (K-way)" if args.k_way
                        else "one call per micro-batch, as they arrive"),
         "exchange": ("reduce-scatter (pack, all-to-all of bf16 chunks, owner's fp32 sum in (micro-batch, rank) "
@@ -125,8 +137,12 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-TRAFFIC_SOURCES = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "launch.cuh"],
+TRAFFIC_SOURCES = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "launch.cuh", "store8.cuh"],
+                   "adamw_step_accumulate": ["adamw_step.cu", "elementwise.cuh", "launch.cuh", "store8.cuh"],
                    "list_step": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"]}
+# algorithmic bytes per parameter of each step kernel: the one-micro-batch form reads the 2-byte
+# micro-batch instead of the 4-byte gradient and writes the gradient (4)
+STEP_KERNEL_BYTES = {"adamw_step": STEP_BYTES_PER_ELEM, "list_step": STEP_BYTES_PER_ELEM, "adamw_step_accumulate": 32}
 
 
 def kernel_source_hash(kernel):
@@ -145,8 +161,8 @@ def traffic_record_path(kernel, workload=None):
     (None if there is none)."""
     if workload is not None:
         return os.path.join(ROOT, "profiles", "traffic_%s_%s.json" % (kernel, workload))
-    import glob
-    found = sorted(glob.glob(os.path.join(ROOT, "profiles", "traffic_%s_*.json" % kernel)))
+    from zero_sharded_mixed_local_gb300.workloads import WORKLOADS  # kernel names share prefixes
+    found = [p for p in (traffic_record_path(kernel, name) for name in WORKLOADS) if os.path.exists(p)]
     return found[0] if len(found) == 1 else None
 
 
@@ -194,14 +210,15 @@ def parse_ncu_csv(path, kernel):
 def write_traffic_record(csv_path, kernel, workload, command, params, out=None):
     """Summarise an ncu capture of `kernel` on `workload` (`params` parameters per launch) into
     the machine-written record profile_traffic() reads."""
-    launches = parse_ncu_csv(csv_path, kernel + "_kernel")
+    launches = parse_ncu_csv(csv_path, "adamw_step_kernel" if kernel == "adamw_step_accumulate" else kernel + "_kernel")
     if not launches:
         raise SystemExit("no %s_kernel launches in %s" % (kernel, csv_path))
     rd = statistics.mean(x[0] for x in launches)
     wr = statistics.mean(x[1] for x in launches)
     durs = [x[2] for x in launches if x[2] is not None]
     rec = {
-        "kernel": kernel + "_kernel",
+        "kernel": ("adamw_step_kernel, the one-micro-batch form" if kernel == "adamw_step_accumulate"
+                   else kernel + "_kernel"),
         "kernel_source_sha256_16": kernel_source_hash(kernel),
         "capture": {"workload": workload, "params_per_launch": int(params), "launches": len(launches),
                     "command": command, "csv": os.path.basename(csv_path)},
@@ -209,7 +226,7 @@ def write_traffic_record(csv_path, kernel, workload, command, params, out=None):
         "dram_write_bytes_per_launch": int(round(wr)),
         "traffic_bytes_per_launch": int(round(rd + wr)),
         "traffic_bytes_per_param": (rd + wr) / params,
-        "algorithmic_bytes_per_param": STEP_BYTES_PER_ELEM,
+        "algorithmic_bytes_per_param": STEP_KERNEL_BYTES[kernel],
         "ncu_duration_us_per_launch": statistics.mean(durs) / 1e3 if durs else None,
         "note": "cold-cache, serialised ncu launches: use the bytes, not the duration",
     }
@@ -535,6 +552,9 @@ def parse_args():
     ap.add_argument("--k-way", action="store_true",
                     help="accumulate all K micro-batch gradients (already resident) in one fused pass with the "
                          "norm, instead of one call per micro-batch as they arrive")
+    ap.add_argument("--accumulate-first", action="store_true",
+                    help="with one micro-batch, still accumulate it (with the norm) before the step instead of "
+                         "taking the norm from the micro-batch and letting the step write the gradient")
     ap.add_argument("--one-call", action="store_true",
                     help="the whole local step as one library call (zero1_local_step: all K micro-batches, already "
                          "resident, accumulated with the norm in one pass, then the step); implies --k-way")
@@ -663,7 +683,9 @@ class StepBench:
 
     @property
     def step_kernel(self):
-        return "list_step" if self.lists is not None else "adamw_step"
+        if self.lists is not None:
+            return "list_step"
+        return "adamw_step_accumulate" if uses_micro_step(self.args, self.K) else "adamw_step"
 
     def step(self, rec=None):
         """One pass of the hot path; `rec` (a dict of CUDA events, EVENTS) brackets its parts."""
@@ -707,6 +729,16 @@ class StepBench:
         for k in range(0 if a.k_way else K - 1):
             z.accumulate(plan, self.grad, self.micros[k], overwrite_first=(k == 0), stream=s)
         mark("n0")
+        if uses_micro_step(a, K):  # one micro-batch: its norm, then the step that writes the gradient
+            z.micro_norm(plan, self.micros[0], self.ws, self.nout, stream=s)
+            if self.group is not None:
+                z.allreduce_sumsq_(self.nout, self.group)
+            mark("s0")
+            z.step_accumulate(plan, self.master, self.m, self.v, self.grad, self.micros[0], self.wbf, self.hp, self.t,
+                              self.nout, stream=s)
+            mark("s1")
+            mark("x1")
+            return
         if a.one_call:  # accumulate + norm and the step in one crossing of the C ABI
             z.local_step(plan, self.grad, self.micros, self.ws, self.nout, self.master, self.m, self.v, self.wbf,
                          self.hp, self.t, stream=s)
@@ -897,13 +929,17 @@ def kernel_report(b, recs, args):
     acc_ms, accnorm_ms, step_ms = mean("a0", "n0"), mean("n0", "s0"), mean("s0", "s1")
     norm_bytes = 4 * P if args.unfused else 0
     last_bytes = accumulate_bytes_per_elem(K, True) * P if args.k_way else (6 if K == 1 else 10) * P + norm_bytes
+    step_bytes = STEP_KERNEL_BYTES[b.step_kernel]
+    if uses_micro_step(args, K):  # the norm pass reads the micro-batch only
+        last_bytes = 2 * P
     kernels = {
         "accumulate": {"ms": acc_ms, "gbs": (accumulate_bytes_per_elem(K) * P - last_bytes) / (acc_ms * 1e-3) / 1e9
                        if K > 1 and not args.k_way else None, "launches_per_step": 0 if args.k_way else K - 1},
-        ("accumulate+grad_norm" if args.unfused else "accumulate_norm"): {
+        ("accumulate+grad_norm" if args.unfused else "micro_norm" if uses_micro_step(args, K) else
+         "accumulate_norm"): {
             "ms": accnorm_ms, "gbs": last_bytes / (accnorm_ms * 1e-3) / 1e9,
             "launches_per_step": 3 if args.unfused else 2},
-        b.step_kernel: {"ms": step_ms, "gbs": STEP_BYTES_PER_ELEM * P / (step_ms * 1e-3) / 1e9,
+        b.step_kernel: {"ms": step_ms, "gbs": step_bytes * P / (step_ms * 1e-3) / 1e9,
                         "launches_per_step": 1},
     }
     if kernels["accumulate"]["launches_per_step"] == 0:  # K = 1 or K-way: its events bracket nothing
@@ -913,19 +949,22 @@ def kernel_report(b, recs, args):
             ms = mean(x, y)
             kernels[name] = {"ms": ms, "gbs": 4 * P / (ms * 1e-3) / 1e9, "launches_per_step": 1}
     pairs = {"accumulate": ("a0", "n0"), "accumulate_norm": ("n0", "s0"), "accumulate+grad_norm": ("n0", "s0"),
-             b.step_kernel: ("s0", "s1"), "shard_gather": ("x0", "a0"), "shard_scatter": ("s1", "x1")}
+             "micro_norm": ("n0", "s0"), b.step_kernel: ("s0", "s1"), "shard_gather": ("x0", "a0"),
+             "shard_scatter": ("s1", "x1")}
     for name, k in kernels.items():  # "ms" is the mean over the timed steps; the spread beside it
         times = [r[pairs[name][0]].elapsed_time(r[pairs[name][1]]) for r in recs]
         k["ms_median"], k["ms_min"], k["ms_max"] = statistics.median(times), min(times), max(times)
     peak, peak_kind = measured_peaks()
     achieved = kernels[b.step_kernel]["gbs"]
     traffic, traffic_src = profile_traffic(b.step_kernel, P)
-    roofline = {"bound": "hbm", "kernel": b.step_kernel + "_kernel", "achieved": achieved, "peak": peak,
+    roofline = {"bound": "hbm", "kernel": ("adamw_step_kernel (one-micro-batch form)"
+                                           if b.step_kernel == "adamw_step_accumulate" else b.step_kernel + "_kernel"),
+                "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "traffic_source": traffic_src,
                 "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
                 "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
-                "bytes_per_param": STEP_BYTES_PER_ELEM, "params_per_launch": P}
+                "bytes_per_param": step_bytes, "params_per_launch": P}
     return kernels, roofline
 
 
@@ -1119,7 +1158,8 @@ def main():
     if args.write_traffic_record:
         import zero_sharded_mixed_local_gb300 as z
         local = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank).local_numel  # host-only call
-        kernel = "list_step" if args.tensor_list else "adamw_step"
+        kernel = ("list_step" if args.tensor_list else
+                  "adamw_step_accumulate" if uses_micro_step(args, w.micro_batches) else "adamw_step")
         rec = write_traffic_record(args.write_traffic_record, kernel, args.workload, args.traffic_command, local)
         print(json.dumps(rec), file=OUT, flush=True)
         return

@@ -266,19 +266,58 @@ int zero1_step(const zero1_plan* plan, float* master, float* exp_avg, float* exp
                const float* grad, uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
                const zero1_norm_out* d_norm, void* stream);
 
+/* ---- the step of a single micro-batch in two passes ----------------------
+ * With one micro-batch the fp32 gradient is float(micro) / grad_divisor, known
+ * before it is written ("ZeRO-1 风格的 Distributed Optimizer", section 6.7:
+ * the micro-batch gradient goes into .grad, then the reduction and the step).
+ * So the norm can be taken from the 2-byte micro-batch, and the step can read
+ * the micro-batch instead of the 4-byte gradient and write the gradient in
+ * the same pass: 2 + 32 bytes per element instead of 6 + 30 for
+ * zero1_accumulate_norm + zero1_step, with the same gradient, norm record,
+ * master, m, v and bf16 copy, bit for bit. */
+
+/* The norm record zero1_accumulate_norm(n_micro = 1, overwrite_first = 1)
+ * would write, without writing the gradient: the sum of squares of
+ * float(micro[j]) / grad_divisor over the arena, with the same tiles and
+ * summation order, plus extra_sumsq.
+ *   micro_bf16   device bf16 arena (or readable host memory, as for
+ *                zero1_accumulate)
+ *   grad_divisor, extra_sumsq, workspace, workspace_bytes, d_out
+ *                as for zero1_accumulate_norm
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_micro_norm(const zero1_plan* plan, const uint16_t* micro_bf16, double grad_divisor, double extra_sumsq,
+                     void* workspace, size_t workspace_bytes, zero1_norm_out* d_out, void* stream);
+
+/* zero1_step for the gradient of one micro-batch, accumulated in the same
+ * pass: every element's gradient float(micro[j]) / grad_divisor is written to
+ * grad (what zero1_accumulate_norm would write) and feeds that element's
+ * clipped AdamW update and bf16 copy, exactly as zero1_step would.  d_norm is
+ * normally zero1_micro_norm's record of the same micro-batch (its sumsq
+ * possibly summed across ranks).  When the step is skipped (a non-finite
+ * norm) the gradient is still written and nothing else is.
+ *   grad         device fp32 arena, written (not read)
+ *   micro_bf16   device bf16 arena (or readable host memory), read
+ *   grad_divisor as for zero1_accumulate_norm
+ *   master, exp_avg, exp_avg_sq, weight_bf16, hp, step_t, d_norm
+ *                as for zero1_step
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_step_accumulate(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq, float* grad,
+                          const uint16_t* micro_bf16, double grad_divisor, uint16_t* weight_bf16,
+                          const zero1_hparams* hp, int64_t step_t, const zero1_norm_out* d_norm, void* stream);
+
 /* The whole local step of one rank in one call ("ZeRO-1 风格的 Distributed
  * Optimizer", section 6.7: every micro-batch's gradient accumulated into the
  * fp32 .grad, then the reduction and the optimizer step; sections 6.2-6.3 and
  * 6.6 for the step): zero1_accumulate_norm over all n_micro micro-batches
  * with the first one overwriting grad, then zero1_step reading the norm
- * record that pass wrote.  The same kernels in the same order as those two
- * calls, so the results are theirs bit for bit; it saves a caller, a binding
- * above all, one crossing of the ABI and its per-call checks, which is what
- * bounds the step of a small shard.  Every argument of both passes is checked
- * before the first launch, so an error leaves every buffer unchanged.  There
- * is no point between the two passes to sum the sum of squares across ranks:
- * pass the other ranks' share as extra_sumsq when it is known, else use the
- * two calls.
+ * record that pass wrote; for a single micro-batch, zero1_micro_norm then
+ * zero1_step_accumulate instead.  Either way the results are those two calls'
+ * bit for bit; it saves a caller, a binding above all, one crossing of the ABI
+ * and its per-call checks, which is what bounds the step of a small shard.
+ * Every argument of both passes is checked before the first launch, so an
+ * error leaves every buffer unchanged.  There is no point between the two
+ * passes to sum the sum of squares across ranks: pass the other ranks' share
+ * as extra_sumsq when it is known, else use the two calls.
  *   grad, micro_bf16, n_micro, grad_divisor, extra_sumsq, workspace,
  *   workspace_bytes, d_norm       as for zero1_accumulate_norm (d_norm must
  *                                 not be NULL)

@@ -65,9 +65,17 @@ class Problem:
         self.ws = self.plan.new_workspace(self.dev)
         self.nout = z.new_norm_out(self.dev)
 
-    def gpu_step(self, micros, t, extra_sumsq=0.0, fused=True):
+    def gpu_step(self, micros, t, extra_sumsq=0.0, fused=True, micro_step=False):
         """One step as bench.py runs it: the last micro-batch's accumulation takes the norm
-        (fused=True), or separate accumulate and grad_norm calls (fused=False)."""
+        (fused=True), or separate accumulate and grad_norm calls (fused=False); with one
+        micro-batch and micro_step, its norm from the micro-batch and the step that writes the
+        gradient (micro_norm + step_accumulate, the bench's path for K = 1)."""
+        if micro_step:
+            assert len(micros) == 1
+            z.micro_norm(self.plan, micros[0], self.ws, self.nout, extra_sumsq=extra_sumsq)
+            z.step_accumulate(self.plan, self.master, self.m, self.v, self.grad, micros[0], self.wbf, self.hp, t,
+                              self.nout)
+            return z.read_norm(self.nout)
         last = len(micros) - 1
         for k, mb in enumerate(micros[:last] if fused else micros):
             z.accumulate(self.plan, self.grad, mb, overwrite_first=(k == 0))
@@ -129,7 +137,8 @@ def oracle_pass(micros, gpu_grad, idx):
     return g_idx, s
 
 
-def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda", seed=None, fused=True):
+def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda", seed=None, fused=True,
+               micro_step=False):
     """Run `steps` steps on GPU and oracle; assert parity.  `sample`: None compares every
     arena element (padding included), "sampled" the tensor edges, the padding and a
     million random elements; the grad arena and the bf16 copy are checked in full."""
@@ -151,7 +160,7 @@ def run_parity(workload, steps=None, fresh_grads=True, sample=None, device="cuda
         new_grads = micros is None or fresh_grads
         if new_grads:  # refill the same buffers: one set of micro-batch arenas at a time
             micros = pb.gen.micro_grads(out=micros)
-        got = pb.gpu_step(micros, t, fused=fused)
+        got = pb.gpu_step(micros, t, fused=fused, micro_step=micro_step)
         if new_grads:
             g_idx, ref_sumsq = oracle_pass(micros, pb.grad, idx)
         assert got["status"] == 0

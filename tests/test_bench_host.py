@@ -167,10 +167,9 @@ def test_traffic_record_from_an_ncu_metrics_list(tmp_path):
 
 def test_committed_traffic_records_match_the_kernel_sources():
     """The records bench.py reads were taken on the kernels as they are (else it reports null)."""
-    for kernel in ("adamw_step", "list_step"):
+    for kernel in ("adamw_step", "adamw_step_accumulate", "list_step"):
         path = bench.traffic_record_path(kernel)
-        if path is None:
-            continue
+        assert path is not None and os.path.basename(path).startswith("traffic_%s_" % kernel), kernel
         rec = json.load(open(path))
         assert rec["kernel_source_sha256_16"] == bench.kernel_source_hash(kernel), kernel
         got, src = bench.profile_traffic(kernel, 1_003_782_656)

@@ -16,7 +16,7 @@ from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_
                       ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm,
                       exchange_chunk_numel, grad_norm, grad_norm_static, launch_count, list_accumulate,
                       list_accumulate_norm, list_grad_norm, list_step, list_step_dev, load_library, local_step,
-                      new_norm_out,
+                      micro_norm, new_norm_out, step_accumulate,
                       pack_reduce_scatter, read_norm, shard_gather, shard_scatter, step, step_dev, step_scalars,
                       unpack_all_gather)
 from . import checkpoint
@@ -30,7 +30,7 @@ __all__ = [
     "ZERO1_ENOMEM", "ZERO1_ENONFINITE", "ZERO1_ETOOBIG", "ZERO1_OK", "Zero1Error", "load_library",
     # plan and arena calls
     "Hparams", "Plan", "ShardLayout", "accumulate", "accumulate_norm", "grad_norm", "grad_norm_static", "step",
-    "local_step",
+    "local_step", "micro_norm", "step_accumulate",
     "step_dev", "step_scalars", "new_norm_out", "read_norm", "decode_norm", "allreduce_sumsq_",
     # exchanges
     "exchange_chunk_numel", "pack_reduce_scatter", "shard_gather", "shard_scatter", "unpack_all_gather",

@@ -90,6 +90,9 @@ def load_library(path=None):
         "zero1_grad_norm": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
         "zero1_grad_norm_static": (ctypes.c_int, [vp, vp, ctypes.c_double, vp, vp]),
         "zero1_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
+        "zero1_micro_norm": (ctypes.c_int, [vp, vp, ctypes.c_double, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
+        "zero1_step_accumulate": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, ctypes.c_double, vp,
+                                                 ctypes.POINTER(_Hparams), i64, vp, vp]),
         "zero1_local_step": (ctypes.c_int, [vp, vp, ctypes.POINTER(vp), i32, ctypes.c_double, ctypes.c_double, vp,
                                             ctypes.c_size_t, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64,
                                             vp]),
@@ -487,11 +490,43 @@ def step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, hparams, step_t, 
            "zero1_step")
 
 
+def micro_norm(plan, micro, workspace, norm_out, extra_sumsq=0.0, divisor=1.0, stream=None):
+    """zero1_micro_norm: the norm record of one micro-batch's gradient (float(micro) / divisor),
+    without writing the gradient: the record accumulate_norm(overwrite_first=True) would write."""
+    lib = load_library()
+    dev = norm_out.device
+    mp = _ptr(micro, torch.bfloat16, plan.arena_numel, "micro", dev, host_ok=True)
+    wp = _ptr(workspace, torch.uint8, None, "workspace", dev)
+    if workspace.numel() < plan.workspace_bytes:
+        raise ValueError("workspace has %d bytes, the plan needs %d" % (workspace.numel(), plan.workspace_bytes))
+    op = _norm_ptr(norm_out, device=dev)
+    _check(lib.zero1_micro_norm(plan.handle, mp, float(divisor), float(extra_sumsq), wp, workspace.numel(), op,
+                                _stream_ptr(stream, dev)), "zero1_micro_norm")
+
+
+def step_accumulate(plan, master, exp_avg, exp_avg_sq, grad, micro, weight_bf16, hparams, step_t, norm_out=None,
+                    divisor=1.0, stream=None):
+    """zero1_step_accumulate: the step for one micro-batch's gradient, written to ``grad`` in the
+    same pass (the same results as accumulate_norm + step)."""
+    lib = load_library()
+    n = plan.arena_numel
+    dev = master.device
+    ptrs = [_ptr(master, torch.float32, n, "master", dev), _ptr(exp_avg, torch.float32, n, "exp_avg", dev),
+            _ptr(exp_avg_sq, torch.float32, n, "exp_avg_sq", dev), _ptr(grad, torch.float32, n, "grad", dev),
+            _ptr(micro, torch.bfloat16, n, "micro", dev, host_ok=True)]
+    wp = None if weight_bf16 is None else _ptr(weight_bf16, torch.bfloat16, n, "weight_bf16", dev)
+    npp = None if norm_out is None else _norm_ptr(norm_out, device=dev)
+    hp = hparams._c() if isinstance(hparams, Hparams) else Hparams(**hparams)._c()
+    _check(lib.zero1_step_accumulate(plan.handle, *ptrs, float(divisor), wp, ctypes.byref(hp), int(step_t), npp,
+                                     _stream_ptr(stream, dev)), "zero1_step_accumulate")
+
+
 def local_step(plan, grad, micro, workspace, norm_out, master, exp_avg, exp_avg_sq, weight_bf16, hparams, step_t,
                extra_sumsq=0.0, divisor=1.0, stream=None):
     """zero1_local_step: the whole local step in one call -- every micro-batch accumulated
     (the first overwriting ``grad``) with the norm in one pass, then clip + AdamW + the bf16
-    copy.  The same results as accumulate_norm(overwrite_first=True) then step()."""
+    copy (for one micro-batch, micro_norm then step_accumulate).  The same results as
+    accumulate_norm(overwrite_first=True) then step()."""
     lib = load_library()
     n = plan.arena_numel
     dev = master.device

@@ -20,8 +20,19 @@
 // per-tensor table is read.  The rounding-explicit intrinsics (__fmul_rn,
 // __fadd_rn, __fdiv_rn, __fsqrt_rn) are never contracted into FMAs, which
 // keeps the operation order exact (elementwise.cuh).
+//
+// The one-micro-batch form (kFromMicro): with a single micro-batch the gradient
+// is float(micro) / divisor, exactly what the accumulate pass would write, so
+// the step reads the 2-byte micro-batch instead of the 4-byte gradient and
+// writes the gradient itself (a 256-bit store where it is 32-byte aligned).
+// Its norm comes first from a pass that only reads the micro-batch
+// (micro_sumsq_tiles_kernel).  Per element the two passes move 2 + 32 bytes
+// instead of 6 + 30, with the same values: the gradient, the norm record and
+// every state element are bit for bit those of zero1_accumulate_norm +
+// zero1_step.  A skipped step (non-finite norm) still writes the gradient.
 #include "elementwise.cuh"
 #include "launch.cuh"
+#include "store8.cuh"
 #include "zero1_internal.h"
 
 namespace zero1 {
@@ -31,7 +42,9 @@ constexpr int kStepThreads = 256;
 
 // kDevScalars: the scalars come from P.dev_scalars (read by thread 0 into
 // shared memory after the loads are issued) rather than from P.sc.
-template <bool kWriteBf16, bool kDevScalars>
+// kFromMicro: the one-micro-batch form above; kWideGrad: its gradient store
+// is one 256-bit access.
+template <bool kWriteBf16, bool kDevScalars, bool kFromMicro, bool kWideGrad>
 __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_constant__ StepParams P, int64_t first_vec) {
     pdl_enter();
     __shared__ float s_coef;
@@ -42,13 +55,18 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
 
     // Loads first: they do not depend on the clip coefficient.
     float4 ga, gb, pa, pb, ma, mb, va, vb;
+    uint4 raw;
     if (live) {
-        const float4* g4 = reinterpret_cast<const float4*>(P.grad) + 2 * i;
         const float4* p4 = reinterpret_cast<const float4*>(P.master) + 2 * i;
         const float4* m4 = reinterpret_cast<const float4*>(P.m) + 2 * i;
         const float4* v4 = reinterpret_cast<const float4*>(P.v) + 2 * i;
-        ga = g4[0];
-        gb = g4[1];
+        if (kFromMicro) {
+            raw = reinterpret_cast<const uint4*>(P.micro)[i];
+        } else {
+            const float4* g4 = reinterpret_cast<const float4*>(P.grad) + 2 * i;
+            ga = g4[0];
+            gb = g4[1];
+        }
         pa = p4[0];
         pb = p4[1];
         ma = m4[0];
@@ -80,7 +98,27 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
         s_skip = skip;
     }
     __syncthreads();
-    if (s_skip || !live) return;  // a non-finite gradient norm leaves every buffer as it is
+    if (kFromMicro) {
+        if (!live) return;
+        float f[8];
+        widen8(raw, f);
+        if (P.divide) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __fdiv_rn(f[j], P.divisor);
+        }
+        ga = make_float4(f[0], f[1], f[2], f[3]);
+        gb = make_float4(f[4], f[5], f[6], f[7]);
+        if (kWideGrad) {
+            store8_f32(P.grad_out + 8 * i, ga, gb);
+        } else {
+            float4* g4 = reinterpret_cast<float4*>(P.grad_out) + 2 * i;
+            g4[0] = ga;
+            g4[1] = gb;
+        }
+        if (s_skip) return;  // the gradient is written; master, m, v and the bf16 copy stay as they are
+    } else if (s_skip || !live) {
+        return;  // a non-finite gradient norm leaves every buffer as it is
+    }
 
     const float coef = s_coef;
     const zero1_step_scalars& S = kDevScalars ? s_sc : P.sc;
@@ -130,12 +168,21 @@ cudaError_t launch_step(const StepParams& p, cudaStream_t stream) {
         const int64_t n = p.n_vec - first < kMaxGridVectors(kStepThreads) ? p.n_vec - first : kMaxGridVectors(kStepThreads);
         const unsigned grid = static_cast<unsigned>((n + kStepThreads - 1) / kStepThreads);
         cudaError_t e;
-        if (p.dev_scalars != nullptr)
-            e = p.w != nullptr ? launch(adamw_step_kernel<true, true>, grid, kStepThreads, stream, p, first)
-                               : launch(adamw_step_kernel<false, true>, grid, kStepThreads, stream, p, first);
-        else
-            e = p.w != nullptr ? launch(adamw_step_kernel<true, false>, grid, kStepThreads, stream, p, first)
-                               : launch(adamw_step_kernel<false, false>, grid, kStepThreads, stream, p, first);
+        if (p.micro != nullptr) {
+            const bool wide = wide_store_aligned(p.grad_out);
+            if (p.w != nullptr)
+                e = wide ? launch(adamw_step_kernel<true, false, true, true>, grid, kStepThreads, stream, p, first)
+                         : launch(adamw_step_kernel<true, false, true, false>, grid, kStepThreads, stream, p, first);
+            else
+                e = wide ? launch(adamw_step_kernel<false, false, true, true>, grid, kStepThreads, stream, p, first)
+                         : launch(adamw_step_kernel<false, false, true, false>, grid, kStepThreads, stream, p, first);
+        } else if (p.dev_scalars != nullptr) {
+            e = p.w != nullptr ? launch(adamw_step_kernel<true, true, false, false>, grid, kStepThreads, stream, p, first)
+                               : launch(adamw_step_kernel<false, true, false, false>, grid, kStepThreads, stream, p, first);
+        } else {
+            e = p.w != nullptr ? launch(adamw_step_kernel<true, false, false, false>, grid, kStepThreads, stream, p, first)
+                               : launch(adamw_step_kernel<false, false, false, false>, grid, kStepThreads, stream, p, first);
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

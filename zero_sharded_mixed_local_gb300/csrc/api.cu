@@ -232,6 +232,74 @@ extern "C" int zero1_step(const zero1_plan* plan, float* master, float* exp_avg,
     return launch_checked_step(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, &sc, nullptr, d_norm, stream);
 }
 
+extern "C" int zero1_micro_norm(const zero1_plan* plan, const uint16_t* micro_bf16, double grad_divisor,
+                                double extra_sumsq, void* workspace, size_t workspace_bytes, zero1_norm_out* d_out,
+                                void* stream) {
+    NvtxRange range("zero1_micro_norm");
+    if (plan == nullptr || d_out == nullptr) return ZERO1_EINVAL;
+    if (!divisor_ok(grad_divisor)) return ZERO1_EINVAL;
+    if (std::isnan(extra_sumsq) || extra_sumsq < 0.0) return ZERO1_EINVAL;
+    if (!aligned16(d_out)) return ZERO1_EALIGN;
+    const int64_t n_tiles = zero1::norm_tiles(plan->arena_numel);
+    if (n_tiles > 0) {
+        if (micro_bf16 == nullptr || workspace == nullptr) return ZERO1_EINVAL;
+        if (workspace_bytes < static_cast<size_t>(n_tiles) * sizeof(double)) return ZERO1_EINVAL;
+        if (!aligned16(micro_bf16) || !aligned16(workspace)) return ZERO1_EALIGN;
+        const int rc = check_readable(micro_bf16);
+        if (rc != ZERO1_OK) return rc;
+    }
+    const cudaError_t e = zero1::launch_micro_norm(micro_bf16, plan->arena_numel, static_cast<float>(grad_divisor),
+                                                   grad_divisor != 1.0, static_cast<double*>(workspace), n_tiles,
+                                                   extra_sumsq, d_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+namespace {
+
+// zero1_step_accumulate's checks (all before any launch) and launch.
+int step_accumulate(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq, float* grad,
+                    const uint16_t* micro_bf16, double grad_divisor, uint16_t* weight_bf16,
+                    const zero1_step_scalars* sc, const zero1_norm_out* d_norm, void* stream) {
+    if (!divisor_ok(grad_divisor)) return ZERO1_EINVAL;
+    int rc = check_step_buffers(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, d_norm);
+    if (rc != ZERO1_OK || plan->arena_numel == 0) return rc;
+    if (micro_bf16 == nullptr) return ZERO1_EINVAL;
+    if (!aligned16(micro_bf16)) return ZERO1_EALIGN;
+    rc = check_readable(micro_bf16);
+    if (rc != ZERO1_OK) return rc;
+    zero1::StepParams p{};
+    p.master = master;
+    p.m = exp_avg;
+    p.v = exp_avg_sq;
+    p.grad = nullptr;
+    p.w = weight_bf16;
+    p.micro = micro_bf16;
+    p.grad_out = grad;
+    p.divisor = static_cast<float>(grad_divisor);
+    p.divide = grad_divisor != 1.0 ? 1 : 0;
+    p.norm = d_norm;
+    p.n_vec = plan->arena_numel / ZERO1_ARENA_ALIGN;
+    for (int g = 0; g < ZERO1_MAX_GROUPS; ++g) p.group_begin_vec[g] = plan->group_begin[g] / ZERO1_ARENA_ALIGN;
+    p.sc = *sc;
+    p.dev_scalars = nullptr;
+    const cudaError_t e = zero1::launch_step(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int zero1_step_accumulate(const zero1_plan* plan, float* master, float* exp_avg, float* exp_avg_sq,
+                                     float* grad, const uint16_t* micro_bf16, double grad_divisor,
+                                     uint16_t* weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                                     const zero1_norm_out* d_norm, void* stream) {
+    NvtxRange range("zero1_step_accumulate");
+    zero1_step_scalars sc{};
+    const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
+    if (rc != ZERO1_OK) return rc;
+    return step_accumulate(plan, master, exp_avg, exp_avg_sq, grad, micro_bf16, grad_divisor, weight_bf16, &sc,
+                           d_norm, stream);
+}
+
 extern "C" int zero1_local_step(const zero1_plan* plan, float* grad, const uint16_t* const* micro_bf16,
                                 int32_t n_micro, double grad_divisor, double extra_sumsq, void* workspace,
                                 size_t workspace_bytes, zero1_norm_out* d_norm, float* master, float* exp_avg,
@@ -246,6 +314,19 @@ extern "C" int zero1_local_step(const zero1_plan* plan, float* grad, const uint1
     if (rc != ZERO1_OK) return rc;
     rc = check_step_buffers(plan, master, exp_avg, exp_avg_sq, grad, weight_bf16, d_norm);
     if (rc != ZERO1_OK) return rc;
+    if (n_micro == 1 && micro_bf16 != nullptr && plan->arena_numel > 0) {
+        // one micro-batch: the norm from the micro-batch alone, then the step that writes the gradient
+        if (micro_bf16[0] == nullptr) return ZERO1_EINVAL;
+        if (!aligned16(micro_bf16[0])) return ZERO1_EALIGN;
+        if (!divisor_ok(grad_divisor)) return ZERO1_EINVAL;
+        rc = check_readable(micro_bf16[0]);
+        if (rc != ZERO1_OK) return rc;
+        rc = zero1_micro_norm(plan, micro_bf16[0], grad_divisor, extra_sumsq, workspace, workspace_bytes, d_norm,
+                              stream);
+        if (rc != ZERO1_OK) return rc;
+        return step_accumulate(plan, master, exp_avg, exp_avg_sq, grad, micro_bf16[0], grad_divisor, weight_bf16, &sc,
+                               d_norm, stream);
+    }
     rc = zero1_accumulate_norm(plan, grad, micro_bf16, n_micro, 1, grad_divisor, extra_sumsq, workspace,
                                workspace_bytes, d_norm, stream);
     if (rc != ZERO1_OK) return rc;

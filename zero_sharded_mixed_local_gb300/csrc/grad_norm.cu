@@ -22,6 +22,7 @@
 //                 double, adds the other ranks' share and writes
 //                 {sumsq, norm, status}.
 // Memory-bound: 4 bytes read per element.
+#include "elementwise.cuh"
 #include "launch.cuh"
 #include "pair_sum.cuh"
 
@@ -57,6 +58,42 @@ __global__ void __launch_bounds__(kTileThreads)
     if (threadIdx.x == 0) partials[tile] = make_float2(sq.s[0], sq.c[0]);
 }
 
+// The partials of the gradient one micro-batch gives, float(micro) / divisor, without writing it:
+// the same values squared in the same order as accumulate_norm_kernel's one-micro-batch overwrite
+// pass (each thread's vectors r = 0..7 of the tile), so the partials are bit for bit that pass's.
+// Reads 2 bytes per element.
+template <bool kDivide>
+__global__ void __launch_bounds__(kTileThreads)
+    micro_sumsq_tiles_kernel(const uint16_t* __restrict__ micro, int64_t n_vec, float divisor,
+                             float2* __restrict__ partials, int64_t first_tile) {
+    pdl_enter();
+    __shared__ float2 s_warp[kTileThreads / 32];
+    const int64_t tile = first_tile + blockIdx.x;
+    const int64_t v0 = tile * kVecsPerTile;
+    const int64_t nv = n_vec - v0 < kVecsPerTile ? n_vec - v0 : kVecsPerTile;
+    const uint4* m4 = reinterpret_cast<const uint4*>(micro) + v0;
+    uint4 raw[kVecsPerThread];
+#pragma unroll
+    for (int r = 0; r < kVecsPerThread; ++r) {
+        const int v = threadIdx.x + r * kTileThreads;
+        raw[r] = v < nv ? m4[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    SquarePairs sq;
+#pragma unroll
+    for (int r = 0; r < kVecsPerThread; ++r) {
+        float f[8];
+        widen8(raw[r], f);
+        if (kDivide) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __fdiv_rn(f[j], divisor);
+        }
+        sq.add_vec(make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7]));
+    }
+    sq.fold();
+    block_pair_sum<kTileThreads>(sq.s[0], sq.c[0], s_warp);
+    if (threadIdx.x == 0) partials[tile] = make_float2(sq.s[0], sq.c[0]);
+}
+
 __global__ void __launch_bounds__(kFinalThreads)
     sumsq_final_kernel(const float2* __restrict__ partials, int64_t n_tiles, double extra, zero1_norm_out* out) {
     pdl_enter();
@@ -81,6 +118,20 @@ __global__ void __launch_bounds__(kFinalThreads)
 cudaError_t launch_norm_final(const float2* partials, int64_t n_tiles, double extra_sumsq, zero1_norm_out* out,
                               cudaStream_t stream) {
     return launch(sumsq_final_kernel, 1, kFinalThreads, stream, partials, n_tiles, extra_sumsq, out);
+}
+
+cudaError_t launch_micro_norm(const uint16_t* micro, int64_t n, float divisor, bool divide, double* partials,
+                              int64_t n_tiles, double extra_sumsq, zero1_norm_out* out, cudaStream_t stream) {
+    float2* pairs = reinterpret_cast<float2*>(partials);
+    for (int64_t first = 0; first < n_tiles; first += 0x7fffffff) {
+        const int64_t nb = n_tiles - first < 0x7fffffff ? n_tiles - first : 0x7fffffff;
+        const unsigned g = static_cast<unsigned>(nb);
+        const cudaError_t e =
+            divide ? launch(micro_sumsq_tiles_kernel<true>, g, kTileThreads, stream, micro, n / 8, divisor, pairs, first)
+                   : launch(micro_sumsq_tiles_kernel<false>, g, kTileThreads, stream, micro, n / 8, divisor, pairs, first);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_norm_final(pairs, n_tiles, extra_sumsq, out, stream);
 }
 
 cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int64_t n_tiles, double extra_sumsq,

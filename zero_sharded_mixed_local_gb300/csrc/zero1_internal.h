@@ -76,6 +76,12 @@ struct StepParams {
     float* v;
     const float* grad;
     uint16_t* w;
+    // The step that accumulates its one micro-batch (micro != null): the gradient is
+    // float(micro) / divisor (divide: 0 keeps the plain values), written to grad_out.
+    const uint16_t* micro;
+    float* grad_out;
+    float divisor;
+    int32_t divide;
     const zero1_norm_out* norm;  // may be null: no clipping
     int64_t n_vec;               // arena_numel / 8
     int64_t group_begin_vec[ZERO1_MAX_GROUPS];  // first 8-element vector of each group
@@ -92,6 +98,9 @@ cudaError_t launch_grad_norm(const float* grad, int64_t n, double* partials, int
                              double extra_sumsq, zero1_norm_out* out, cudaStream_t stream);
 cudaError_t launch_accumulate_norm(const AccumulateParams& p, double* partials, int64_t n_tiles, double extra_sumsq,
                                    zero1_norm_out* out, cudaStream_t stream);
+// The norm record of float(micro) / divisor (divide: 0 keeps the plain values) without writing it.
+cudaError_t launch_micro_norm(const uint16_t* micro, int64_t n, float divisor, bool divide, double* partials,
+                              int64_t n_tiles, double extra_sumsq, zero1_norm_out* out, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
 
 cudaError_t launch_layout_copy(const LayoutChunk* table, int64_t n_chunks, const void* src, void* dst,

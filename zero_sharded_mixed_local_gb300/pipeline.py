@@ -12,8 +12,9 @@ with the transfer hidden behind the kernels:
 - on the step stream, the step waits for its own copy (an event), then runs the
   path as a training loop does: K-1 ``accumulate`` calls, ``accumulate_norm`` for
   the last micro-batch (or one K-way ``accumulate_norm``), the optional all-reduce
-  of the sum of squares, and ``step``, each kernel launched as a programmatic
-  dependent of the previous one;
+  of the sum of squares, and ``step``; with one micro-batch, ``micro_norm`` and
+  ``step_accumulate`` (the same results, 34 bytes per element instead of 36);
+  each kernel launched as a programmatic dependent of the previous one;
 - every step's 24-byte norm record is copied back to pinned host memory on the
   step stream and read on the host one step behind, as a loop logs it.
 
@@ -26,7 +27,8 @@ micro-batch, then the reduction and the step).
 """
 import torch
 
-from .binding import NORM_OUT_BYTES, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, new_norm_out, step
+from .binding import (NORM_OUT_BYTES, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm, micro_norm,
+                      new_norm_out, step, step_accumulate)
 
 
 class HostFedSteps:
@@ -116,6 +118,14 @@ class HostFedSteps:
     def _step(self, s):
         plan, K, stream = self.plan, self.K, self.stream
         grad, ws, nout, stage = self.grads[s], self.workspaces[s], self.norm_outs[s], self.stage[s]
+        if K == 1 and not self.k_way:  # the norm from the micro-batch; the step writes the gradient
+            micro_norm(plan, stage[0], ws, nout, stream=stream)
+            if self.group is not None:
+                allreduce_sumsq_(nout, self.group)
+            self.t += 1
+            step_accumulate(plan, self.master, self.exp_avg, self.exp_avg_sq, grad, stage[0], self.weight_bf16,
+                            self.hp, self.t, nout, stream=stream)
+            return
         if self.k_way:
             accumulate_norm(plan, grad, stage, ws, nout, overwrite_first=True, stream=stream)
         else:
