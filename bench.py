@@ -65,7 +65,7 @@ def uses_micro_step(args, K):
     """One micro-batch in the plain arena step: its norm taken from the micro-batch, then the step
     that writes the gradient (zero1_micro_norm + zero1_step_accumulate), unless asked otherwise."""
     return (K == 1 and not (getattr(args, "accumulate_first", False) or args.k_way or args.unfused or args.exchange
-                            or args.tensor_list or args.graph or getattr(args, "data_parallel", False)))
+                            or args.graph or getattr(args, "data_parallel", False)))
 
 
 def flushes_l2(path_bytes):
@@ -139,10 +139,17 @@ def measured_peaks():
 
 TRAFFIC_SOURCES = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "launch.cuh", "store8.cuh"],
                    "adamw_step_accumulate": ["adamw_step.cu", "elementwise.cuh", "launch.cuh", "store8.cuh"],
-                   "list_step": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"]}
+                   "list_step": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"],
+                   "list_step_accumulate": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"]}
 # algorithmic bytes per parameter of each step kernel: the one-micro-batch form reads the 2-byte
 # micro-batch instead of the 4-byte gradient and writes the gradient (4)
-STEP_KERNEL_BYTES = {"adamw_step": STEP_BYTES_PER_ELEM, "list_step": STEP_BYTES_PER_ELEM, "adamw_step_accumulate": 32}
+STEP_KERNEL_BYTES = {"adamw_step": STEP_BYTES_PER_ELEM, "list_step": STEP_BYTES_PER_ELEM, "adamw_step_accumulate": 32,
+                     "list_step_accumulate": 32}
+# the kernel each record's launches belong to, and how the roofline names it
+STEP_KERNEL_NAMES = {"adamw_step": ("adamw_step_kernel", "adamw_step_kernel"),
+                     "adamw_step_accumulate": ("adamw_step_kernel", "adamw_step_kernel (one-micro-batch form)"),
+                     "list_step": ("list_step_kernel", "list_step_kernel"),
+                     "list_step_accumulate": ("list_step_kernel", "list_step_kernel (one-micro-batch form)")}
 
 
 def kernel_source_hash(kernel):
@@ -210,15 +217,14 @@ def parse_ncu_csv(path, kernel):
 def write_traffic_record(csv_path, kernel, workload, command, params, out=None):
     """Summarise an ncu capture of `kernel` on `workload` (`params` parameters per launch) into
     the machine-written record profile_traffic() reads."""
-    launches = parse_ncu_csv(csv_path, "adamw_step_kernel" if kernel == "adamw_step_accumulate" else kernel + "_kernel")
+    launches = parse_ncu_csv(csv_path, STEP_KERNEL_NAMES[kernel][0])
     if not launches:
         raise SystemExit("no %s_kernel launches in %s" % (kernel, csv_path))
     rd = statistics.mean(x[0] for x in launches)
     wr = statistics.mean(x[1] for x in launches)
     durs = [x[2] for x in launches if x[2] is not None]
     rec = {
-        "kernel": ("adamw_step_kernel, the one-micro-batch form" if kernel == "adamw_step_accumulate"
-                   else kernel + "_kernel"),
+        "kernel": STEP_KERNEL_NAMES[kernel][1],
         "kernel_source_sha256_16": kernel_source_hash(kernel),
         "capture": {"workload": workload, "params_per_launch": int(params), "launches": len(launches),
                     "command": command, "csv": os.path.basename(csv_path)},
@@ -683,9 +689,8 @@ class StepBench:
 
     @property
     def step_kernel(self):
-        if self.lists is not None:
-            return "list_step"
-        return "adamw_step_accumulate" if uses_micro_step(self.args, self.K) else "adamw_step"
+        return (("list_step" if self.lists is not None else "adamw_step") +
+                ("_accumulate" if uses_micro_step(self.args, self.K) else ""))
 
     def step(self, rec=None):
         """One pass of the hot path; `rec` (a dict of CUDA events, EVENTS) brackets its parts."""
@@ -703,6 +708,16 @@ class StepBench:
         z, a, K, L, s = self.z, self.args, self.K, self.lists, self.stream
         self.t += 1
         mark("a0")
+        if uses_micro_step(a, K):  # one micro-batch: its norm, then the step that writes the gradients
+            mark("n0")
+            z.list_micro_norm(self.plan, self.table, L["micro"][0], self.lws, self.nout, stream=s)
+            if self.group is not None:
+                z.allreduce_sumsq_(self.nout, self.group)
+            mark("s0")
+            z.list_step_accumulate(self.plan, self.table, L["master"], L["m"], L["v"], L["grad"], L["micro"][0], L["w"],
+                                   self.hp, self.t, self.nout, stream=s)
+            mark("s1")
+            return
         for k in range(0 if a.k_way else K - 1):
             z.list_accumulate(self.plan, self.table, L["grad"], L["micro"][k], overwrite_first=(k == 0), stream=s)
         mark("n0")
@@ -957,8 +972,7 @@ def kernel_report(b, recs, args):
     peak, peak_kind = measured_peaks()
     achieved = kernels[b.step_kernel]["gbs"]
     traffic, traffic_src = profile_traffic(b.step_kernel, P)
-    roofline = {"bound": "hbm", "kernel": ("adamw_step_kernel (one-micro-batch form)"
-                                           if b.step_kernel == "adamw_step_accumulate" else b.step_kernel + "_kernel"),
+    roofline = {"bound": "hbm", "kernel": STEP_KERNEL_NAMES[b.step_kernel][1],
                 "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "traffic_source": traffic_src,
@@ -1158,8 +1172,8 @@ def main():
     if args.write_traffic_record:
         import zero_sharded_mixed_local_gb300 as z
         local = z.Plan(w.params.numels, w.params.no_decay, w.dp_size, w.dp_rank).local_numel  # host-only call
-        kernel = ("list_step" if args.tensor_list else
-                  "adamw_step_accumulate" if uses_micro_step(args, w.micro_batches) else "adamw_step")
+        kernel = (("list_step" if args.tensor_list else "adamw_step") +
+                  ("_accumulate" if uses_micro_step(args, w.micro_batches) else ""))
         rec = write_traffic_record(args.write_traffic_record, kernel, args.workload, args.traffic_command, local)
         print(json.dumps(rec), file=OUT, flush=True)
         return

@@ -518,6 +518,17 @@ int zero1_list_accumulate_norm(const zero1_plan* plan, const void* d_table, floa
                                double grad_divisor, double extra_sumsq, void* workspace, size_t workspace_bytes,
                                zero1_norm_out* d_out, void* stream);
 
+/* zero1_micro_norm over the tensor lists: the norm record
+ * zero1_list_accumulate_norm(one micro-batch list, overwrite_first = 1) would
+ * write, without writing the gradient; the same runs and summation order.
+ *   d_micro   one device list of n_tensors bf16 shard pointers
+ *   grad_divisor, extra_sumsq, workspace, workspace_bytes, d_out
+ *             as for zero1_list_accumulate_norm
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_micro_norm(const zero1_plan* plan, const void* d_table, const uint16_t* const* d_micro,
+                          double grad_divisor, double extra_sumsq, void* workspace, size_t workspace_bytes,
+                          zero1_norm_out* d_out, void* stream);
+
 /* zero1_grad_norm over a gradient pointer list (read only).
  * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
 int zero1_list_grad_norm(const zero1_plan* plan, const void* d_table, const float* const* d_grad,
@@ -537,6 +548,21 @@ int zero1_list_step(const zero1_plan* plan, const void* d_table, float* const* d
                     float* const* d_exp_avg, float* const* d_exp_avg_sq, const float* const* d_grad,
                     uint16_t* const* d_weight_bf16, const zero1_hparams* hp, int64_t step_t,
                     const zero1_norm_out* d_norm, void* stream);
+
+/* zero1_step_accumulate over the tensor lists: every shard's gradient
+ * float(micro) / grad_divisor is written to its gradient buffer and feeds the
+ * same clipped AdamW update and bf16 copy as zero1_list_step; a skipped step
+ * still writes the gradient.  The same results as zero1_list_accumulate_norm
+ * (one micro-batch, overwriting) + zero1_list_step, bit for bit, in 34 bytes
+ * per element instead of 36.
+ *   d_grad   the gradient list, written (not read)
+ *   d_micro  one device list of bf16 shard pointers, read
+ *   other arguments as for zero1_list_step and zero1_list_accumulate_norm
+ * Errors: ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ECUDA. */
+int zero1_list_step_accumulate(const zero1_plan* plan, const void* d_table, float* const* d_master,
+                               float* const* d_exp_avg, float* const* d_exp_avg_sq, float* const* d_grad,
+                               const uint16_t* const* d_micro, double grad_divisor, uint16_t* const* d_weight_bf16,
+                               const zero1_hparams* hp, int64_t step_t, const zero1_norm_out* d_norm, void* stream);
 
 /* zero1_list_step with the step's scalars read from DEVICE memory (d_scalars,
  * 16-byte aligned, filled by zero1_step_scalars_fill) when the kernel runs, so

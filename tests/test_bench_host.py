@@ -167,7 +167,7 @@ def test_traffic_record_from_an_ncu_metrics_list(tmp_path):
 
 def test_committed_traffic_records_match_the_kernel_sources():
     """The records bench.py reads were taken on the kernels as they are (else it reports null)."""
-    for kernel in ("adamw_step", "adamw_step_accumulate", "list_step"):
+    for kernel in ("adamw_step", "adamw_step_accumulate", "list_step", "list_step_accumulate"):
         path = bench.traffic_record_path(kernel)
         assert path is not None and os.path.basename(path).startswith("traffic_%s_" % kernel), kernel
         rec = json.load(open(path))

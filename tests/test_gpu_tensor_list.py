@@ -530,3 +530,79 @@ def test_random_list_configurations_match_the_oracle():
         for name, lst, ref in (("master", pb.master, P), ("m", pb.m, M), ("v", pb.v, V)):
             assert _eq(pb.flat(lst).numpy(), ref), (case, name)
         assert np.array_equal(u16(pb.flat(pb.w)), oracle.bf16_rne(P)), case
+
+
+@pytest.mark.parametrize("misaligned", [False, True])
+def test_list_micro_pair_equals_accumulate_norm_and_step(misaligned):
+    """One micro-batch over the tensor lists: list_micro_norm + list_step_accumulate (the norm from
+    the micro-batch, then the step that writes the gradients) against list_accumulate_norm +
+    list_step, bit for bit: every gradient, master, m, v and bf16 shard and the norm record, over
+    three steps with clipping active, with the divisor on the last; the element-wise path when every
+    buffer sits one element off a 16-byte boundary."""
+    a = ListProblem(NUMELS, NO_DECAY, misaligned=misaligned, seed=11, sigma=0.05)
+    b = ListProblem(NUMELS, NO_DECAY, misaligned=misaligned, seed=11, sigma=0.05)
+    hp = z.Hparams(**HP)
+    for t in (1, 2, 3):
+        div = 2.0 if t == 3 else 1.0
+        mb = a.micro()
+        ap, bp = a.opt.plan, b.opt.plan  # the plans whose run tables the optimizers uploaded
+        pa = z.PointerLists(ap, a.micro_like(mb), torch.bfloat16)
+        pb = z.PointerLists(bp, b.micro_like(mb), torch.bfloat16)
+        La, Lb = a.opt.pointer_lists, b.opt.pointer_lists
+        z.list_micro_norm(ap, a.opt.table, pa, a.opt.workspace, a.opt.norm_out, divisor=div)
+        z.list_step_accumulate(ap, a.opt.table, La["master"], La["exp_avg"], La["exp_avg_sq"], La["grad"], pa,
+                               La["weight_bf16"], hp, t, a.opt.norm_out, divisor=div)
+        z.list_accumulate_norm(bp, b.opt.table, Lb["grad"], pb, b.opt.workspace, b.opt.norm_out, divisor=div)
+        z.list_step(bp, b.opt.table, Lb["master"], Lb["exp_avg"], Lb["exp_avg_sq"], Lb["grad"], Lb["weight_bf16"],
+                    hp, t, b.opt.norm_out)
+        torch.cuda.synchronize()
+        assert bytes(a.opt.norm_out[:24].cpu().numpy()) == bytes(b.opt.norm_out[:24].cpu().numpy())
+        assert z.read_norm(a.opt.norm_out)["norm"] > 1.0
+    for name in ("grad", "master", "m", "v"):
+        for x, y in zip(getattr(a, name), getattr(b, name)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), name
+    for x, y in zip(a.w, b.w):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_list_micro_pair_skips_on_a_nonfinite_gradient_and_still_writes_it():
+    a = ListProblem(NUMELS, NO_DECAY, seed=12)
+    mb = a.micro()
+    mb[3][2] = float("nan")
+    before = [t.clone() for t in a.master]
+    assert a.opt.step_from(mb, check_finite=True) is False and a.opt.t == 0
+    for x, y in zip(a.master, before):
+        assert torch.equal(x, y)
+    for g, m in zip(a.grad, mb):
+        assert torch.equal(g.view(torch.int32), m.float().view(torch.int32))  # NaN included
+
+
+def test_step_from_equals_accumulate_then_step_and_the_arena_form():
+    """ShardListAdamW.step_from (one micro-batch, then three) against accumulate(last=True) + step()
+    and, for one micro-batch, against the arena pair on the same values."""
+    a = ListProblem(NUMELS, NO_DECAY, seed=13, sigma=0.05)
+    b = ListProblem(NUMELS, NO_DECAY, seed=13, sigma=0.05)
+    arena = z.LocalShardAdamW(NUMELS, a.no_decay, 3, 1, hparams=a.hp)
+    for t0, o0 in zip(a.master, a.plan.shard_views(arena.master)):
+        o0.copy_(t0)
+    for t in (1, 2):
+        mb = a.micro()
+        a.opt.step_from(mb)
+        b.opt.accumulate(mb, last=True)
+        b.opt.step()
+        am = a.plan.new_arena(torch.bfloat16)
+        for o, x in zip(a.plan.shard_views(am), mb):
+            o.copy_(x)
+        arena.step_from(am)
+    mbs = [a.micro() for _ in range(3)]
+    a.opt.step_from(mbs)
+    b.opt.accumulate(mbs, last=True)
+    b.opt.step()
+    for name in ("grad", "master", "m", "v"):
+        for x, y in zip(getattr(a, name), getattr(b, name)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), name
+    a2 = ListProblem(NUMELS, NO_DECAY, seed=13, sigma=0.05)  # the arena after the two one-micro-batch steps
+    for t in (1, 2):
+        a2.opt.step_from(a2.micro())
+    for x, y in zip(a2.master, a.plan.shard_views(arena.master)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))

@@ -15,8 +15,8 @@ from .binding import (ARENA_ALIGN, MAX_GROUPS, MAX_MICRO, NORM_OUT_BYTES, ZERO1_
                       ZERO1_ENOMEM, ZERO1_ENONFINITE, ZERO1_ETOOBIG, ZERO1_OK, Hparams, Plan, PointerLists,
                       ShardLayout, Zero1Error, accumulate, accumulate_norm, allreduce_sumsq_, decode_norm,
                       exchange_chunk_numel, grad_norm, grad_norm_static, launch_count, list_accumulate,
-                      list_accumulate_norm, list_grad_norm, list_step, list_step_dev, load_library, local_step,
-                      micro_norm, new_norm_out, step_accumulate,
+                      list_accumulate_norm, list_grad_norm, list_micro_norm, list_step, list_step_accumulate,
+                      list_step_dev, load_library, local_step, micro_norm, new_norm_out, step_accumulate,
                       pack_reduce_scatter, read_norm, shard_gather, shard_scatter, step, step_dev, step_scalars,
                       unpack_all_gather)
 from . import checkpoint
@@ -35,7 +35,8 @@ __all__ = [
     # exchanges
     "exchange_chunk_numel", "pack_reduce_scatter", "shard_gather", "shard_scatter", "unpack_all_gather",
     # tensor lists
-    "PointerLists", "list_accumulate", "list_accumulate_norm", "list_grad_norm", "list_step", "list_step_dev",
+    "PointerLists", "list_accumulate", "list_accumulate_norm", "list_grad_norm", "list_micro_norm", "list_step",
+    "list_step_accumulate", "list_step_dev",
     # optimizer objects and helpers
     "LocalShardAdamW", "ShardListAdamW", "StepGraph", "Zero1AdamW", "default_no_decay", "checkpoint", "lr_at",
     "mup_groups", "HostFedSteps",

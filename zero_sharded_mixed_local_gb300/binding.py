@@ -111,6 +111,10 @@ def load_library(path=None):
         "zero1_list_accumulate_norm": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, ctypes.c_double, ctypes.c_double,
                                                       vp, ctypes.c_size_t, vp, vp]),
         "zero1_list_grad_norm": (ctypes.c_int, [vp, vp, vp, ctypes.c_double, vp, ctypes.c_size_t, vp, vp]),
+        "zero1_list_micro_norm": (ctypes.c_int, [vp, vp, vp, ctypes.c_double, ctypes.c_double, vp, ctypes.c_size_t,
+                                                 vp, vp]),
+        "zero1_list_step_accumulate": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, ctypes.c_double, vp,
+                                                      ctypes.POINTER(_Hparams), i64, vp, vp]),
         "zero1_list_step": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(_Hparams), i64, vp, vp]),
         "zero1_list_step_dev": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "zero1_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -785,6 +789,37 @@ def list_grad_norm(plan, table, grads: PointerLists, workspace, norm_out, extra_
     no = _norm_ptr(norm_out, device=dev)
     _check(lib.zero1_list_grad_norm(plan.handle, tp, gp, float(extra_sumsq), ws, workspace.numel(), no, sp),
            "zero1_list_grad_norm")
+
+
+def list_micro_norm(plan, table, micro: PointerLists, workspace, norm_out, extra_sumsq=0.0, divisor=1.0,
+                    stream=None):
+    """zero1_list_micro_norm: the norm record of one micro-batch's gradient over the tensor lists,
+    without writing the gradient (what list_accumulate_norm(overwrite_first=True) would record)."""
+    lib = load_library()
+    dev = micro.device
+    tp, sp = _list_args(plan, table, stream, dev)
+    mp = _lists(plan, micro, "micro", torch.bfloat16, dev)
+    ws = _ptr(workspace, torch.uint8, None, "workspace", dev)
+    no = _norm_ptr(norm_out, device=dev)
+    _check(lib.zero1_list_micro_norm(plan.handle, tp, mp, float(divisor), float(extra_sumsq), ws, workspace.numel(),
+                                     no, sp), "zero1_list_micro_norm")
+
+
+def list_step_accumulate(plan, table, master: PointerLists, exp_avg: PointerLists, exp_avg_sq: PointerLists,
+                         grads: PointerLists, micro: PointerLists, weight_bf16, hparams, step_t, norm_out=None,
+                         divisor=1.0, stream=None):
+    """zero1_list_step_accumulate: list_step for one micro-batch's gradient, written to the gradient
+    lists in the same pass (the results of list_accumulate_norm + list_step)."""
+    lib = load_library()
+    dev = master.device
+    tp, sp = _list_args(plan, table, stream, dev)
+    ptrs = _step_lists(plan, master, exp_avg, exp_avg_sq, grads, weight_bf16, dev)
+    mp = _lists(plan, micro, "micro", torch.bfloat16, dev)
+    hp = hparams if isinstance(hparams, Hparams) else Hparams(**hparams)
+    no = None if norm_out is None else _norm_ptr(norm_out, device=dev)
+    _check(lib.zero1_list_step_accumulate(plan.handle, tp, ptrs[0], ptrs[1], ptrs[2], ptrs[3], mp, float(divisor),
+                                          ptrs[4], ctypes.byref(hp._c()), int(step_t), no, sp),
+           "zero1_list_step_accumulate")
 
 
 def _step_lists(plan, master, exp_avg, exp_avg_sq, grads, weight_bf16, dev):

@@ -477,9 +477,12 @@ int list_grad_checked(const zero1_plan* plan, const void* d_table, float* const*
     }
     if (!divisor_ok(grad_divisor)) return ZERO1_EINVAL;
     const int64_t n_chunks = static_cast<int64_t>(plan->list_chunks.size());
+    const bool uses_grad = mode != zero1::ListGradMode::kMicroNorm;
     if (n_chunks > 0) {
-        if (d_table == nullptr || d_grad == nullptr || (reads_micro && d_micro == nullptr)) return ZERO1_EINVAL;
-        if (!aligned16(d_table) || !aligned16(d_grad) || (reads_micro && !aligned16(d_micro))) return ZERO1_EALIGN;
+        if (d_table == nullptr || (uses_grad && d_grad == nullptr) || (reads_micro && d_micro == nullptr))
+            return ZERO1_EINVAL;
+        if (!aligned16(d_table) || (uses_grad && !aligned16(d_grad)) || (reads_micro && !aligned16(d_micro)))
+            return ZERO1_EALIGN;
         if (norm) {
             if (workspace == nullptr) return ZERO1_EINVAL;
             if (workspace_bytes < static_cast<size_t>(n_chunks) * sizeof(double)) return ZERO1_EINVAL;
@@ -522,6 +525,14 @@ extern "C" int zero1_list_accumulate_norm(const zero1_plan* plan, const void* d_
                              stream);
 }
 
+extern "C" int zero1_list_micro_norm(const zero1_plan* plan, const void* d_table, const uint16_t* const* d_micro,
+                                     double grad_divisor, double extra_sumsq, void* workspace, size_t workspace_bytes,
+                                     zero1_norm_out* d_out, void* stream) {
+    NvtxRange range("zero1_list_micro_norm");
+    return list_grad_checked(plan, d_table, nullptr, d_micro, 1, 1, grad_divisor, zero1::ListGradMode::kMicroNorm,
+                             extra_sumsq, workspace, workspace_bytes, d_out, stream);
+}
+
 extern "C" int zero1_list_grad_norm(const zero1_plan* plan, const void* d_table, const float* const* d_grad,
                                     double extra_sumsq, void* workspace, size_t workspace_bytes,
                                     zero1_norm_out* d_out, void* stream) {
@@ -533,16 +544,20 @@ extern "C" int zero1_list_grad_norm(const zero1_plan* plan, const void* d_table,
 
 namespace {
 
-// Checks shared by zero1_list_step and zero1_list_step_dev, and the launch.
+// Checks shared by zero1_list_step, zero1_list_step_dev and zero1_list_step_accumulate (d_micro:
+// the one-micro-batch form, which writes the gradient list), and the launch.
 int list_step_checked(const zero1_plan* plan, const void* d_table, float* const* d_master, float* const* d_exp_avg,
                       float* const* d_exp_avg_sq, const float* const* d_grad, uint16_t* const* d_weight_bf16,
                       const zero1_step_scalars* sc, const zero1_step_scalars* d_scalars,
-                      const zero1_norm_out* d_norm, void* stream) {
+                      const zero1_norm_out* d_norm, void* stream, const uint16_t* const* d_micro = nullptr,
+                      double grad_divisor = 1.0) {
+    if (!divisor_ok(grad_divisor)) return ZERO1_EINVAL;
     const int64_t n_chunks = static_cast<int64_t>(plan->list_chunks.size());
     if (n_chunks == 0) return ZERO1_OK;  // nothing to do; empty lists may be NULL
     if (d_table == nullptr || d_master == nullptr || d_exp_avg == nullptr || d_exp_avg_sq == nullptr ||
         d_grad == nullptr)
         return ZERO1_EINVAL;
+    if (d_micro != nullptr && !aligned16(d_micro)) return ZERO1_EALIGN;
     if (!aligned16(d_table) || !aligned16(d_master) || !aligned16(d_exp_avg) || !aligned16(d_exp_avg_sq) ||
         !aligned16(d_grad))
         return ZERO1_EALIGN;
@@ -559,6 +574,13 @@ int list_step_checked(const zero1_plan* plan, const void* d_table, float* const*
     p.n_tensors = plan->n_tensors;
     if (sc != nullptr) p.sc = *sc;
     p.dev_scalars = d_scalars;
+    if (d_micro != nullptr) {
+        p.micro = d_micro;
+        p.n_micro = 1;
+        p.micro_step = 1;
+        p.divisor = static_cast<float>(grad_divisor);
+        p.divide = grad_divisor != 1.0 ? 1 : 0;
+    }
     const cudaError_t e = zero1::launch_list_step(p, n_chunks, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ZERO1_OK : cuda_fail(e);
 }
@@ -575,6 +597,20 @@ extern "C" int zero1_list_step(const zero1_plan* plan, const void* d_table, floa
     if (rc != ZERO1_OK) return rc;
     return list_step_checked(plan, d_table, d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_weight_bf16, &sc, nullptr,
                              d_norm, stream);
+}
+
+extern "C" int zero1_list_step_accumulate(const zero1_plan* plan, const void* d_table, float* const* d_master,
+                                          float* const* d_exp_avg, float* const* d_exp_avg_sq, float* const* d_grad,
+                                          const uint16_t* const* d_micro, double grad_divisor,
+                                          uint16_t* const* d_weight_bf16, const zero1_hparams* hp, int64_t step_t,
+                                          const zero1_norm_out* d_norm, void* stream) {
+    NvtxRange range("zero1_list_step_accumulate");
+    zero1_step_scalars sc{};
+    const int rc = zero1::fill_step_scalars(plan, hp, step_t, &sc);
+    if (rc != ZERO1_OK) return rc;
+    if (d_micro == nullptr && !plan->list_chunks.empty()) return ZERO1_EINVAL;
+    return list_step_checked(plan, d_table, d_master, d_exp_avg, d_exp_avg_sq, d_grad, d_weight_bf16, &sc, nullptr,
+                             d_norm, stream, d_micro, grad_divisor);
 }
 
 extern "C" int zero1_list_step_dev(const zero1_plan* plan, const void* d_table, float* const* d_master,

@@ -94,8 +94,9 @@ __device__ __forceinline__ bool run_in_range(const ListChunk& ch, int32_t n_tens
 }
 
 // Gradient passes over the runs: accumulate (as zero1_accumulate), accumulate
-// and take the norm partials (as zero1_accumulate_norm), or the partials alone
-// (as zero1_grad_norm).  One block per run, thread t owning vectors t + 256r
+// and take the norm partials (as zero1_accumulate_norm), the partials alone
+// (as zero1_grad_norm), or the partials of one micro-batch's gradient without
+// writing it (as zero1_micro_norm; kK = 1).  One block per run, thread t owning vectors t + 256r
 // (r = 0..7, the norm's fixed order).  Every thread reads the run descriptor
 // and its buffers' addresses itself (broadcast loads through L1), so nothing
 // waits on a barrier before the data loads go out.  A run whose list entry is
@@ -118,6 +119,8 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
     pdl_enter();
     constexpr bool kReadsMicro = kMode != ListGradMode::kNorm;
     constexpr bool kSumsSquares = kMode != ListGradMode::kAccumulate;
+    constexpr bool kUsesGrad = kMode != ListGradMode::kMicroNorm;
+    constexpr bool kWritesGrad = kMode == ListGradMode::kAccumulate || kMode == ListGradMode::kAccumulateNorm;
     constexpr int kBatch = 2;
     constexpr int kSlots = kK > 0 ? kK : 1;
     __shared__ float2 s_warp[kTileThreads / 32];
@@ -127,8 +130,8 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
         if (kSumsSquares && threadIdx.x == 0) partials[c] = make_float2(0.f, 0.f);
         return;
     }
-    float* grad = P.grad[ch.tensor];
-    bool missing = grad == nullptr, unaligned = false;
+    float* grad = kUsesGrad ? P.grad[ch.tensor] : nullptr;
+    bool missing = kUsesGrad && grad == nullptr, unaligned = false;
     const uint16_t* micro0 = nullptr;
     const uint16_t* mp[kSlots];
     if (kReadsMicro) {
@@ -154,11 +157,13 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
         if (kSumsSquares && threadIdx.x == 0) partials[c] = make_float2(0.f, 0.f);
         return;
     }
-    grad += ch.offset;
-    unaligned |= misaligned16(grad);
+    if (kUsesGrad) {
+        grad += ch.offset;
+        unaligned |= misaligned16(grad);
+    }
     const int len = ch.len;
     const bool overwrite = kK > 0 || (kReadsMicro && P.overwrite_first);
-    const bool divide = kMode == ListGradMode::kAccumulateNorm && P.divide;
+    const bool divide = (kMode == ListGradMode::kAccumulateNorm || kMode == ListGradMode::kMicroNorm) && P.divide;
     const bool full = !unaligned && len == kNormTile;
 
     SquarePairs sq;
@@ -183,8 +188,10 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[j] = __fdiv_rn(acc[j], P.divisor);
             }
-            reinterpret_cast<float4*>(grad)[2 * v] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            reinterpret_cast<float4*>(grad)[2 * v + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (kWritesGrad) {
+                reinterpret_cast<float4*>(grad)[2 * v] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                reinterpret_cast<float4*>(grad)[2 * v + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
             if (kSumsSquares)
                 sq.add_vec(make_float4(acc[0], acc[1], acc[2], acc[3]), make_float4(acc[4], acc[5], acc[6], acc[7]));
         }
@@ -221,8 +228,10 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) acc[j] = __fdiv_rn(acc[j], P.divisor);
                     }
-                    reinterpret_cast<float4*>(grad)[2 * v] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                    reinterpret_cast<float4*>(grad)[2 * v + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                    if (kWritesGrad) {
+                        reinterpret_cast<float4*>(grad)[2 * v] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                        reinterpret_cast<float4*>(grad)[2 * v + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                    }
                     if (kSumsSquares)
                         sq.add_vec(make_float4(acc[0], acc[1], acc[2], acc[3]),
                                    make_float4(acc[4], acc[5], acc[6], acc[7]));
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) acc[j] = __fdiv_rn(acc[j], P.divisor);
                 }
-                store8(grad + e, n, vec, acc);
+                if (kWritesGrad) store8(grad + e, n, vec, acc);
             }
             if (kSumsSquares)
                 sq.add_vec(make_float4(acc[0], acc[1], acc[2], acc[3]), make_float4(acc[4], acc[5], acc[6], acc[7]));
@@ -288,7 +297,10 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
 constexpr int kStepSubBlocks = 4;
 constexpr int kStepVecsPerThread = kVecsPerThread / kStepSubBlocks;  // 2
 
-template <bool kWriteBf16, bool kDevScalars>
+// kFromMicro: the one-micro-batch form (zero1_step_accumulate): the gradient of each element is
+// float(micro) / divisor, read from micro list 0 and written to the gradient list, also when the
+// step is skipped; the arithmetic after that is the same.
+template <bool kWriteBf16, bool kDevScalars, bool kFromMicro>
 __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid_constant__ ListParams P, int64_t first_block) {
     pdl_enter();
     __shared__ float s_coef;
@@ -301,17 +313,20 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
     float* master = P.master[ch.tensor];
     float* m = P.m[ch.tensor];
     float* v = P.v[ch.tensor];
-    const float* grad = P.grad[ch.tensor];
+    float* grad = P.grad[ch.tensor];
+    const uint16_t* micro = kFromMicro ? P.micro[ch.tensor] : nullptr;
     uint16_t* w = kWriteBf16 ? P.w[ch.tensor] : nullptr;
-    if (master == nullptr || m == nullptr || v == nullptr || grad == nullptr || (kWriteBf16 && w == nullptr))
+    if (master == nullptr || m == nullptr || v == nullptr || grad == nullptr || (kWriteBf16 && w == nullptr) ||
+        (kFromMicro && micro == nullptr))
         return;  // the same for every thread of the block
     master += ch.offset;
     m += ch.offset;
     v += ch.offset;
     grad += ch.offset;
+    if (kFromMicro) micro += ch.offset;
     if (kWriteBf16) w += ch.offset;
     const bool aligned = !(misaligned16(master) || misaligned16(m) || misaligned16(v) || misaligned16(grad) ||
-                           (kWriteBf16 && misaligned16(w)));
+                           (kWriteBf16 && misaligned16(w)) || (kFromMicro && misaligned16(micro)));
     const int len = ch.len;
     const int v0 = sub * kStepVecsPerThread * kTileThreads + static_cast<int>(threadIdx.x);
 
@@ -321,7 +336,10 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
     float g[8], p[8], mm[8], vv[8];
     if (e0 < len) {
         const bool vec = aligned && n0 == 8;
-        load8(grad + e0, n0, vec, g);
+        if (kFromMicro)
+            load8_bf16(micro + e0, n0, vec, g);
+        else
+            load8(grad + e0, n0, vec, g);
         load8(master + e0, n0, vec, p);
         load8(m + e0, n0, vec, mm);
         load8(v + e0, n0, vec, vv);
@@ -339,7 +357,7 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
         s_skip = skip;
     }
     __syncthreads();
-    if (s_skip || e0 >= len) return;  // a non-finite gradient norm leaves every buffer as it is
+    if (e0 >= len || (!kFromMicro && s_skip)) return;  // a non-finite norm leaves every buffer as it is
 
     const float coef = s_coef;
     const zero1_step_scalars& S = kDevScalars ? s_sc : P.sc;
@@ -353,10 +371,21 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
         const int n = len - e < 8 ? len - e : 8;
         const bool vec = aligned && n == 8;
         if (r > 0) {
-            load8(grad + e, n, vec, g);
+            if (kFromMicro)
+                load8_bf16(micro + e, n, vec, g);
+            else
+                load8(grad + e, n, vec, g);
             load8(master + e, n, vec, p);
             load8(m + e, n, vec, mm);
             load8(v + e, n, vec, vv);
+        }
+        if (kFromMicro) {
+            if (P.divide) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) g[j] = __fdiv_rn(g[j], P.divisor);
+            }
+            store8(grad + e, n, vec, g);  // the gradient, whether or not the step applies
+            if (s_skip) continue;
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) adamw_elem(p[j], mm[j], vv[j], g[j], coef, dfac, stepsize, sc);
@@ -380,6 +409,8 @@ template <ListGradMode kMode>
 cudaError_t launch_grad_mode(const ListParams& p, unsigned nb, float2* pairs, int64_t first, cudaStream_t stream) {
     if constexpr (kMode == ListGradMode::kNorm) {
         return launch_k<kMode, 0>(p, nb, pairs, first, stream);
+    } else if constexpr (kMode == ListGradMode::kMicroNorm) {
+        return launch_k<kMode, 1>(p, nb, pairs, first, stream);
     } else {
         // the micro-batch count, when the pass overwrites the gradient with their sum
         switch (p.overwrite_first ? p.n_micro : 0) {
@@ -415,6 +446,9 @@ cudaError_t launch_list_grad(const ListParams& p, ListGradMode mode, int64_t n_c
             case ListGradMode::kNorm:
                 e = launch_grad_mode<ListGradMode::kNorm>(p, nb, pairs, first, stream);
                 break;
+            case ListGradMode::kMicroNorm:
+                e = launch_grad_mode<ListGradMode::kMicroNorm>(p, nb, pairs, first, stream);
+                break;
         }
         if (e != cudaSuccess) return e;
     }
@@ -427,12 +461,15 @@ cudaError_t launch_list_step(const ListParams& p, int64_t n_chunks, cudaStream_t
     for (int64_t first = 0; first < n_blocks; first += 0x7fffffff) {
         const unsigned nb = static_cast<unsigned>(n_blocks - first < 0x7fffffff ? n_blocks - first : 0x7fffffff);
         cudaError_t e;
-        if (p.dev_scalars != nullptr)
-            e = p.w != nullptr ? launch(list_step_kernel<true, true>, nb, kTileThreads, stream, p, first)
-                               : launch(list_step_kernel<false, true>, nb, kTileThreads, stream, p, first);
+        if (p.micro_step)
+            e = p.w != nullptr ? launch(list_step_kernel<true, false, true>, nb, kTileThreads, stream, p, first)
+                               : launch(list_step_kernel<false, false, true>, nb, kTileThreads, stream, p, first);
+        else if (p.dev_scalars != nullptr)
+            e = p.w != nullptr ? launch(list_step_kernel<true, true, false>, nb, kTileThreads, stream, p, first)
+                               : launch(list_step_kernel<false, true, false>, nb, kTileThreads, stream, p, first);
         else
-            e = p.w != nullptr ? launch(list_step_kernel<true, false>, nb, kTileThreads, stream, p, first)
-                               : launch(list_step_kernel<false, false>, nb, kTileThreads, stream, p, first);
+            e = p.w != nullptr ? launch(list_step_kernel<true, false, false>, nb, kTileThreads, stream, p, first)
+                               : launch(list_step_kernel<false, false, false>, nb, kTileThreads, stream, p, first);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -122,12 +122,14 @@ struct ListParams {
     int32_t overwrite_first;
     int32_t divide;                // 0: plain sum (divisor unused)
     float divisor;
+    int32_t micro_step;            // the step reads micro list 0 and writes grad (one micro-batch)
     zero1_step_scalars sc;                   // the step's scalars, at launch
     const zero1_step_scalars* dev_scalars;   // or read from device memory when the kernel runs
 };
 
 // What list_grad passes do with the gradient runs.
-enum class ListGradMode { kAccumulate, kAccumulateNorm, kNorm };
+// kMicroNorm: the partials of one micro-batch's gradient without writing it (zero1_micro_norm).
+enum class ListGradMode { kAccumulate, kAccumulateNorm, kNorm, kMicroNorm };
 
 cudaError_t launch_list_grad(const ListParams& p, ListGradMode mode, int64_t n_chunks, double* partials,
                              double extra_sumsq, zero1_norm_out* out, cudaStream_t stream);

@@ -30,8 +30,9 @@ import math
 import torch
 
 from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, Hparams, list_accumulate,
-                      list_accumulate_norm, list_grad_norm, list_step, list_step_dev, local_step, new_norm_out, Plan,
-                      PointerLists, read_norm, step, step_dev, step_scalars, STEP_SCALARS_BYTES)
+                      list_accumulate_norm, list_grad_norm, list_micro_norm, list_step, list_step_accumulate,
+                      list_step_dev, local_step, micro_norm, new_norm_out, Plan, PointerLists, read_norm, step,
+                      step_accumulate, step_dev, step_scalars, STEP_SCALARS_BYTES)
 
 
 def _applied(opt, stream):
@@ -107,17 +108,32 @@ class LocalShardAdamW:
         self._micro_seen = 0
         return _applied(self, stream) if check_finite else None
 
-    def step_from(self, micro, extra_sumsq=0.0, divisor=1.0, lr=None, stream=None, check_finite=False):
+    def step_from(self, micro, extra_sumsq=0.0, divisor=1.0, lr=None, group=None, stream=None, check_finite=False):
         """The whole step from micro-batch gradients that are all resident (a bf16 arena or a list
-        of up to MAX_MICRO, in order) in one library call (zero1_local_step): accumulate with the
-        norm in one pass, then clip + AdamW + bf16 copy.  The same result as accumulate(micro,
-        last=True) then step(); no all-reduce can sit between the two passes, so give the other
-        ranks' sum of squares as ``extra_sumsq`` or use those two calls."""
+        of up to MAX_MICRO, in order): accumulate with the norm in one pass, then clip + AdamW +
+        bf16 copy; for one micro-batch, the norm from the micro-batch and the step that writes the
+        gradient.  The same result as accumulate(micro, last=True) then step().  Without ``group``
+        it is one library call (zero1_local_step); with one, the sum of squares is all-reduced
+        between the two passes."""
         self.t += 1
         hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
-        local_step(self.plan, self.grad, micro, self.workspace, self.norm_out, self.master, self.exp_avg,
-                   self.exp_avg_sq, self.weight_bf16, hp, self.t, extra_sumsq=extra_sumsq, divisor=divisor,
-                   stream=stream)
+        if group is None:
+            local_step(self.plan, self.grad, micro, self.workspace, self.norm_out, self.master, self.exp_avg,
+                       self.exp_avg_sq, self.weight_bf16, hp, self.t, extra_sumsq=extra_sumsq, divisor=divisor,
+                       stream=stream)
+        else:
+            mb = [micro] if isinstance(micro, torch.Tensor) else list(micro)
+            if len(mb) == 1:
+                micro_norm(self.plan, mb[0], self.workspace, self.norm_out, extra_sumsq, divisor, stream=stream)
+                allreduce_sumsq_(self.norm_out, group)
+                step_accumulate(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, mb[0],
+                                self.weight_bf16, hp, self.t, self.norm_out, divisor=divisor, stream=stream)
+            else:
+                accumulate_norm(self.plan, self.grad, mb, self.workspace, self.norm_out, overwrite_first=True,
+                                extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
+                allreduce_sumsq_(self.norm_out, group)
+                step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
+                     self.norm_out, stream=stream)
         self._micro_seen = 0
         self._norm_ready = False
         return _applied(self, stream) if check_finite else None
@@ -322,6 +338,34 @@ class ShardListAdamW:
         self._micro_seen = 0
         return _applied(self, stream) if check_finite else None
 
+    def step_from(self, micro, extra_sumsq=0.0, divisor=1.0, lr=None, group=None, stream=None, check_finite=False):
+        """The whole step from micro-batch gradients that are all resident (as for accumulate):
+        for one micro-batch, the norm from the micro-batch and the step that writes the gradient
+        (34 bytes per element instead of 36); for several, the K-way accumulation with the norm,
+        then the step.  The same result as accumulate(micro, last=True) then step(); ``group``
+        all-reduces the sum of squares in between."""
+        pl = self._micro_lists(micro)
+        L = self._lists
+        hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
+        if pl.n_lists == 1:
+            list_micro_norm(self.plan, self.table, pl, self.workspace, self.norm_out, extra_sumsq, divisor,
+                            stream=stream)
+        else:
+            list_accumulate_norm(self.plan, self.table, L["grad"], pl, self.workspace, self.norm_out,
+                                 overwrite_first=True, extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
+        if group is not None:
+            allreduce_sumsq_(self.norm_out, group)
+        self.t += 1
+        if pl.n_lists == 1:
+            list_step_accumulate(self.plan, self.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], pl,
+                                 L["weight_bf16"], hp, self.t, self.norm_out, divisor=divisor, stream=stream)
+        else:
+            list_step(self.plan, self.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], L["weight_bf16"],
+                      hp, self.t, self.norm_out, stream=stream)
+        self._micro_seen = 0
+        self._norm_ready = False
+        return _applied(self, stream) if check_finite else None
+
     def read_norm(self, stream=None):
         return read_norm(self.norm_out, stream=stream)
 
@@ -421,9 +465,11 @@ class Zero1AdamW:
         """Clip + AdamW on this rank's slices; the bf16 weights land in the model's parameters.
         ``group``: a torch.distributed group whose ranks' sums of squares make the global norm;
         ``check_finite`` as for LocalShardAdamW.step."""
-        if self._pending == 0:
-            self.opt.accumulate(self._grad_lists(), last=True, stream=stream)
-        applied = self.opt.step(lr=lr, group=group, stream=stream, check_finite=check_finite)
+        if self._pending == 0:  # one micro-batch: its norm, then the step that fills the accumulator
+            applied = self.opt.step_from(self._grad_lists(), lr=lr, group=group, stream=stream,
+                                         check_finite=check_finite)
+        else:
+            applied = self.opt.step(lr=lr, group=group, stream=stream, check_finite=check_finite)
         self._pending = 0
         return applied
 
