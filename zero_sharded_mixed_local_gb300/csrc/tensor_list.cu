@@ -32,6 +32,7 @@
 #include "elementwise.cuh"
 #include "launch.cuh"
 #include "pair_sum.cuh"
+#include "store8.cuh"
 
 namespace zero1 {
 namespace {
@@ -327,6 +328,8 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
     if (kWriteBf16) w += ch.offset;
     const bool aligned = !(misaligned16(master) || misaligned16(m) || misaligned16(v) || misaligned16(grad) ||
                            (kWriteBf16 && misaligned16(w)) || (kFromMicro && misaligned16(micro)));
+    // a 32-byte-aligned gradient takes one 256-bit store per vector (whole sectors per warp instruction)
+    const bool wide_grad = kFromMicro && aligned && (reinterpret_cast<uintptr_t>(grad) & 31u) == 0;
     const int len = ch.len;
     const int v0 = sub * kStepVecsPerThread * kTileThreads + static_cast<int>(threadIdx.x);
 
@@ -384,7 +387,11 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
 #pragma unroll
                 for (int j = 0; j < 8; ++j) g[j] = __fdiv_rn(g[j], P.divisor);
             }
-            store8(grad + e, n, vec, g);  // the gradient, whether or not the step applies
+            // the gradient, whether or not the step applies
+            if (wide_grad && n == 8)
+                store8_f32(grad + e, make_float4(g[0], g[1], g[2], g[3]), make_float4(g[4], g[5], g[6], g[7]));
+            else
+                store8(grad + e, n, vec, g);
             if (s_skip) continue;
         }
 #pragma unroll
