@@ -203,3 +203,36 @@ def sample_indices(layout, per_tensor_edge=2048, n_random=1_000_000, seed=0):
     rng = np.random.default_rng(seed)
     parts.append(rng.integers(0, layout.arena_numel, size=min(n_random, layout.arena_numel), dtype=np.int64))
     return np.unique(np.concatenate(parts))
+
+
+def bf16_norm_pattern(x, kind, gen):
+    """Overwrite some of a flat bf16 CUDA tensor's elements, in place, with values that steer the
+    norm kernels between their exact-square form and the general one:
+    "exact" leaves gradient-sized values (every square exact); "outside" scatters bf16 subnormals and
+    values just below the exact range (and its lower end) among them; "zeros" makes 30% of the values
+    and every 37th whole vector zero, with some -0; "large" scatters values near 2^63 and 2^64, whose
+    squares overflow the sums; "inf" places one infinity."""
+    n = x.numel()
+    if n == 0 or kind == "exact":
+        return x
+    b = x.view(torch.int16)
+
+    def put(every, values):
+        k = max(1, n // every)
+        idx = torch.randint(0, n, (k,), generator=gen, device=x.device)
+        vals = torch.tensor(np.array(values, np.uint16).view(np.int16), device=x.device)
+        b[idx] = vals[torch.randint(0, len(values), (k,), generator=gen, device=x.device)]
+
+    if kind == "outside":
+        put(500, [0x0001, 0x0040, 0x807F, 0x1D80, 0x9DFF, 0x1D82, 0x1E00, 0x9E01])
+    elif kind == "zeros":
+        b[torch.rand(n, generator=gen, device=x.device) < 0.3] = 0
+        b[:n - n % 8].view(-1, 8)[::37] = 0
+        put(1000, [0x8000])
+    elif kind == "large":
+        put(5000, [0x5F00, 0xDF7F, 0x5F80])
+    elif kind == "inf":
+        b[n // 2] = 0x7F80
+    else:
+        raise ValueError(kind)
+    return x

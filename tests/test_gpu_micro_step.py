@@ -8,7 +8,9 @@ tensors with ragged tails), with the divisor and another ranks' share of the
 sum of squares, parameter groups, no bf16 copy, 32- and 16-byte-aligned
 gradient arenas, host-resident micro-batches, and a non-finite gradient (the
 step is skipped, the gradient still written). Rejected arguments launch
-nothing.
+nothing. The micro-batch norm's record equals the accumulating pass's and the
+plain norm's on values that take its exact-square form, the general one, or
+both in one tile.
 """
 import ctypes
 
@@ -140,6 +142,39 @@ def test_local_step_with_one_micro_batch_takes_the_micro_pair():
     assert z.launch_count() - before == 3
     _two_calls(b, mb, 1)
     _same(a, b)
+
+
+@pytest.mark.parametrize("kind", ["exact", "outside", "zeros", "large", "inf"])
+@pytest.mark.parametrize("divisor", [1.0, 3.0])
+def test_micro_norm_record_equals_the_accumulating_pass_on_any_bf16_values(kind, divisor):
+    """Without a divisor the micro-batch norm drops the residual of squares it checks to be exact; the
+    record stays the bits of zero1_accumulate_norm's pass and of zero1_grad_norm over the gradient it
+    writes, whatever mix of exact and inexact squares (subnormals, zeros, overflowing sums) a tile
+    holds.  With a divisor every square takes the general form."""
+    from parity import bf16_norm_pattern
+    numels = [16384 * 5 + 77, 1000, 16384 * 2, 3, 40000]
+    plan, master, micro = _setup(numels, [0, 1, 0, 1, 0], sigma=0.05, seed=9)
+    L = plan.layout()
+    mb = bf16_norm_pattern(micro(), kind, torch.Generator(device="cuda").manual_seed(10))
+    keep = torch.zeros(plan.arena_numel, dtype=torch.bool, device="cuda")
+    for o, c in zip(L.offsets, L.counts):
+        keep[int(o):int(o) + int(c)] = True
+    mb[~keep] = 0  # the arena's padding stays zero
+    a, b = _State(plan, master), _State(plan, master)
+    z.micro_norm(plan, mb, a.ws, a.nout, divisor=divisor)
+    z.accumulate_norm(plan, b.grad, mb, b.ws, b.nout, overwrite_first=True, divisor=divisor)
+    c_out = z.new_norm_out()
+    z.grad_norm(plan, b.grad, b.ws, c_out)
+    torch.cuda.synchronize()
+    ra, rb, rc = (bytes(r[:z.NORM_OUT_BYTES].cpu().numpy()) for r in (a.nout, b.nout, c_out))
+    assert ra == rb == rc
+    rec = z.read_norm(a.nout)
+    if kind in ("large", "inf"):
+        assert rec["status"] == z.ZERO1_ENONFINITE
+    else:
+        assert rec["status"] == 0
+        ref = float(np.sum((b.grad.double() ** 2).cpu().numpy()))
+        assert abs(rec["sumsq"] - ref) <= 1e-12 * ref
 
 
 def test_micro_pair_rejects_bad_arguments_before_any_launch():

@@ -565,6 +565,29 @@ def test_list_micro_pair_equals_accumulate_norm_and_step(misaligned):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
 
+@pytest.mark.parametrize("kind", ["exact", "outside", "zeros", "large", "inf"])
+@pytest.mark.parametrize("divisor", [1.0, 3.0])
+def test_list_micro_norm_record_equals_the_accumulating_pass_on_any_bf16_values(kind, divisor):
+    """The list micro-batch norm (exact-square form on full runs without a divisor) gives the record
+    of list_accumulate_norm's one-micro-batch pass, bit for bit, whatever mix of exact and inexact
+    squares the runs hold."""
+    from parity import bf16_norm_pattern
+    a = ListProblem(NUMELS, NO_DECAY, seed=13, sigma=0.05)
+    gen = torch.Generator(device="cuda").manual_seed(14)
+    mb = [bf16_norm_pattern(t, kind, gen) for t in a.micro()]
+    pl = a.opt.plan
+    pm = z.PointerLists(pl, mb, torch.bfloat16)
+    L = a.opt.pointer_lists
+    other = z.new_norm_out()
+    z.list_micro_norm(pl, a.opt.table, pm, a.opt.workspace, a.opt.norm_out, divisor=divisor)
+    torch.cuda.synchronize()
+    z.list_accumulate_norm(pl, a.opt.table, L["grad"], pm, a.opt.workspace, other, divisor=divisor)
+    torch.cuda.synchronize()
+    assert bytes(a.opt.norm_out[:24].cpu().numpy()) == bytes(other[:24].cpu().numpy())
+    rec = z.read_norm(other)
+    assert (rec["status"] == z.ZERO1_ENONFINITE) == (kind in ("large", "inf"))
+
+
 def test_list_micro_pair_skips_on_a_nonfinite_gradient_and_still_writes_it():
     a = ListProblem(NUMELS, NO_DECAY, seed=12)
     mb = a.micro()

@@ -61,7 +61,9 @@ __global__ void __launch_bounds__(kTileThreads)
 // The partials of the gradient one micro-batch gives, float(micro) / divisor, without writing it:
 // the same values squared in the same order as accumulate_norm_kernel's one-micro-batch overwrite
 // pass (each thread's vectors r = 0..7 of the tile), so the partials are bit for bit that pass's.
-// Reads 2 bytes per element.
+// Reads 2 bytes per element.  Bound by the fp32 pipe rather than DRAM (the compensated squares cost
+// about ten operations per element), so without a divisor a thread whose 64 values all square
+// exactly (bf16_squares_exact: integer checks on the raw bits) adds them without the residual term.
 template <bool kDivide>
 __global__ void __launch_bounds__(kTileThreads)
     micro_sumsq_tiles_kernel(const uint16_t* __restrict__ micro, int64_t n_vec, float divisor,
@@ -79,15 +81,25 @@ __global__ void __launch_bounds__(kTileThreads)
         raw[r] = v < nv ? m4[v] : make_uint4(0u, 0u, 0u, 0u);
     }
     SquarePairs sq;
+    if (!kDivide && bf16_squares_exact(raw)) {
+        // every square exact: no residual to add (the same bits; 0.368 -> 0.330 ms on 1.0B elements)
 #pragma unroll
-    for (int r = 0; r < kVecsPerThread; ++r) {
-        float f[8];
-        widen8(raw[r], f);
-        if (kDivide) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = __fdiv_rn(f[j], divisor);
+        for (int r = 0; r < kVecsPerThread; ++r) {
+            float f[8];
+            widen8(raw[r], f);
+            sq.add_vec_exact(make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7]));
         }
-        sq.add_vec(make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7]));
+    } else {
+#pragma unroll
+        for (int r = 0; r < kVecsPerThread; ++r) {
+            float f[8];
+            widen8(raw[r], f);
+            if (kDivide) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = __fdiv_rn(f[j], divisor);
+            }
+            sq.add_vec(make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7]));
+        }
     }
     sq.fold();
     block_pair_sum<kTileThreads>(sq.s[0], sq.c[0], s_warp);

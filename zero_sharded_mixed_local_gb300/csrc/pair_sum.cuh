@@ -88,6 +88,65 @@ __device__ __forceinline__ void add_square2(uint64_t& s, uint64_t& c, float g0, 
     c = add2(c, add2(e, pe));
 }
 
+// add_square2 for squares known to be exact, whose FMA residual is +0: c + (e + 0) is c + e bit for
+// bit, because e is never -0 (a rounded sum is -0 only when both addends are, and neither the running
+// sum s, which starts at +0, nor a square is ever -0).
+__device__ __forceinline__ void add_exact_square2(uint64_t& s, uint64_t& c, float g0, float g1) {
+    const uint64_t g = pack2(g0, g1);
+    const uint64_t p = mul2(g, g);
+    const uint64_t t = add2(s, p);  // two_sum(s, p)
+    const uint64_t bp = sub2(t, s);
+    const uint64_t e = add2(sub2(s, sub2(t, bp)), sub2(p, bp));
+    s = t;
+    c = add2(c, e);
+}
+
+// Exact squares of bf16 values.  A bf16 value with exponent field E (1..254) is M * 2^(E - 134) with
+// M < 2^8, so its square M^2 * 2^(2E - 268) has at most 16 significant bits: it is an fp32 value
+// exactly when 2E - 268 >= -149 (no bits below the smallest subnormal) and it is below 2^128, i.e.
+// for E in 60..190.  In the magnitude bits of the bf16 (E << 7 | mantissa) that is the range below.
+// Zero also squares exactly (+0).  Bf16 subnormals, tiny or huge values, infinities and NaN fall
+// outside it and take add_square2.
+constexpr uint32_t kExactSquareMin = 0x1E00u;  // E = 60, mantissa 0
+constexpr uint32_t kExactSquareMax = 0x5F7Fu;  // E = 190, mantissa 0x7F
+
+// 16-bit SIMD on the two halves of a word (sm_90 and later).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t add_u16x2(uint32_t a, uint32_t b) {  // per half, modulo 2^16
+    uint32_t r;
+    asm("add.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// True when every bf16 value in the vectors (eight per uint4) squares exactly in fp32: the largest
+// magnitude is at most kExactSquareMax and the smallest non-zero one at least kExactSquareMin.  Each
+// half's magnitude minus one (modulo 2^16) sends zeros to 0xFFFF, out of the way of the minimum.
+template <int kN>
+__device__ __forceinline__ bool bf16_squares_exact(const uint4 (&raw)[kN]) {
+    uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int r = 0; r < kN; ++r) {
+        const uint32_t w[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t a = w[k] & 0x7FFF7FFFu;
+            mx = max_u16x2(mx, a);
+            mn = min_u16x2(mn, add_u16x2(a, 0xFFFFFFFFu));
+        }
+    }
+    const uint32_t hi = max(mx & 0xFFFFu, mx >> 16), lo = min(mn & 0xFFFFu, mn >> 16);
+    return hi <= kExactSquareMax && lo >= kExactSquareMin - 1u;
+}
+
 // A thread's four running pairs over its vectors.  While adding they are kept packed, pairs (0, 1)
 // and (2, 3) in two registers each, so every instruction serves two pairs (measured 5% faster on the
 // norm of a bf16 micro-batch, which is bound by instruction issue rather than DRAM); fold() unpacks
@@ -103,6 +162,15 @@ struct SquarePairs {
         add_square2(s23, c23, a.z, a.w);
         add_square2(s01, c01, b.x, b.y);
         add_square2(s23, c23, b.z, b.w);
+    }
+
+    // add_vec for a vector whose squares are exact (bf16_squares_exact): the same bits, two fp32
+    // operations fewer per element.
+    __device__ __forceinline__ void add_vec_exact(const float4& a, const float4& b) {
+        add_exact_square2(s01, c01, a.x, a.y);
+        add_exact_square2(s23, c23, a.z, a.w);
+        add_exact_square2(s01, c01, b.x, b.y);
+        add_exact_square2(s23, c23, b.z, b.w);
     }
 
     // Fold the four pairs into (s[0], c[0]) in a fixed order.

@@ -111,11 +111,11 @@ __device__ __forceinline__ bool run_in_range(const ListChunk& ch, int32_t n_tens
 // before the additions, which run in micro-batch order as in kK separate calls.
 //
 // kK = 1 (grad = the one micro-batch): 6 blocks per SM (registers capped at 40,
-// a few spilled).  Measured on the 1.0B-element shard, fused pass: 0.911 ms,
+// a few spilled); the micro-batch norm form holds all eight vectors and takes 4.  Measured on the 1.0B-element shard, fused pass: 0.911 ms,
 // against 0.978 ms for batches of four at 5 blocks, 1.001 ms uncapped and
 // 0.985 ms for a shared-memory prologue behind a barrier.
 template <ListGradMode kMode, int kK>
-__global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
+__global__ void __launch_bounds__(kTileThreads, kK == 1 && kMode != ListGradMode::kMicroNorm ? 6 : 4)
     list_grad_kernel(const __grid_constant__ ListParams P, float2* __restrict__ partials, int64_t first_chunk) {
     pdl_enter();
     constexpr bool kReadsMicro = kMode != ListGradMode::kNorm;
@@ -195,6 +195,23 @@ __global__ void __launch_bounds__(kTileThreads, kK == 1 ? 6 : 4)
             }
             if (kSumsSquares)
                 sq.add_vec(make_float4(acc[0], acc[1], acc[2], acc[3]), make_float4(acc[4], acc[5], acc[6], acc[7]));
+        }
+    } else if (kMode == ListGradMode::kMicroNorm && full && !divide) {
+        // as the arena micro-batch norm: all eight vectors loaded, then the squares, without the
+        // residual term where all of the thread's squares are exact (the same bits)
+        uint4 raw[kVecsPerThread];
+#pragma unroll
+        for (int r = 0; r < kVecsPerThread; ++r)
+            raw[r] = reinterpret_cast<const uint4*>(micro0)[threadIdx.x + r * kTileThreads];
+        const bool exact = bf16_squares_exact(raw);
+#pragma unroll
+        for (int r = 0; r < kVecsPerThread; ++r) {
+            float f[8];
+            widen8(raw[r], f);
+            if (exact)
+                sq.add_vec_exact(make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7]));
+            else
+                sq.add_vec(make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7]));
         }
     } else if (kK <= 1 && full && (kMode == ListGradMode::kNorm || P.n_micro == 1)) {
 #pragma unroll
