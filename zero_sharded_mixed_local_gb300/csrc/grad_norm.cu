@@ -110,8 +110,19 @@ __global__ void __launch_bounds__(kFinalThreads)
     sumsq_final_kernel(const float2* __restrict__ partials, int64_t n_tiles, double extra, zero1_norm_out* out) {
     pdl_enter();
     __shared__ float2 s_warp[kFinalThreads / 32];
+    // thread t adds tiles t, t + kFinalThreads, ... in that order; the loads of kAhead of them go out
+    // before their additions (the same order, so the same bits, without a load's latency per tile)
+    constexpr int kAhead = 8;
     float s = 0.f, c = 0.f;
-    for (int64_t i = threadIdx.x; i < n_tiles; i += kFinalThreads) {
+    int64_t i = threadIdx.x;
+    for (; i + (kAhead - 1) * static_cast<int64_t>(kFinalThreads) < n_tiles; i += kAhead * kFinalThreads) {
+        float2 x[kAhead];
+#pragma unroll
+        for (int q = 0; q < kAhead; ++q) x[q] = partials[i + q * kFinalThreads];
+#pragma unroll
+        for (int q = 0; q < kAhead; ++q) add_pair(s, c, x[q].x, x[q].y);
+    }
+    for (; i < n_tiles; i += kFinalThreads) {
         const float2 x = partials[i];
         add_pair(s, c, x.x, x.y);
     }

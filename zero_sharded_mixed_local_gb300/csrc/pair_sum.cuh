@@ -149,8 +149,8 @@ __device__ __forceinline__ bool bf16_squares_exact(const uint4 (&raw)[kN]) {
 
 // A thread's four running pairs over its vectors.  While adding they are kept packed, pairs (0, 1)
 // and (2, 3) in two registers each, so every instruction serves two pairs (measured 5% faster on the
-// norm of a bf16 micro-batch, which is bound by instruction issue rather than DRAM); fold() unpacks
-// them into s[] and c[].
+// norm of a bf16 micro-batch, which was then bound by instruction issue rather than DRAM); fold()
+// unpacks them into s[] and c[].
 struct SquarePairs {
     float s[4] = {0.f, 0.f, 0.f, 0.f};
     float c[4] = {0.f, 0.f, 0.f, 0.f};

@@ -111,11 +111,14 @@ __device__ __forceinline__ bool run_in_range(const ListChunk& ch, int32_t n_tens
 // before the additions, which run in micro-batch order as in kK separate calls.
 //
 // kK = 1 (grad = the one micro-batch): 6 blocks per SM (registers capped at 40,
-// a few spilled); the micro-batch norm form holds all eight vectors and takes 4.  Measured on the 1.0B-element shard, fused pass: 0.911 ms,
+// a few spilled).  The micro-batch norm form holds all eight vectors: 5 blocks
+// per SM (48 registers, a few spilled; 0.354 ms on the 1.0B-element shard,
+// against 0.375 at 4 blocks and 0.366 at 6).  Measured on the 1.0B-element shard, fused pass: 0.911 ms,
 // against 0.978 ms for batches of four at 5 blocks, 1.001 ms uncapped and
 // 0.985 ms for a shared-memory prologue behind a barrier.
 template <ListGradMode kMode, int kK>
-__global__ void __launch_bounds__(kTileThreads, kK == 1 && kMode != ListGradMode::kMicroNorm ? 6 : 4)
+__global__ void __launch_bounds__(kTileThreads,
+                                  kMode == ListGradMode::kMicroNorm ? 5 : (kK == 1 ? 6 : 4))
     list_grad_kernel(const __grid_constant__ ListParams P, float2* __restrict__ partials, int64_t first_chunk) {
     pdl_enter();
     constexpr bool kReadsMicro = kMode != ListGradMode::kNorm;
