@@ -223,3 +223,99 @@ def test_one_rank_nccl_group_equals_the_local_step():
     p.join(timeout=120)
     assert got == [True, True, True, True], got
     assert p.exitcode == 0
+
+
+def _step_from_group_worker(rank, world, port, q):
+    """step_from with a process group, on a side stream: the norm pass, the all-reduce of the sums of
+    squares and the step, against the same rank stepping alone with the other rank's sum of squares as
+    ``extra_sumsq`` (two doubles add the same in either order)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import zero_sharded_mixed_local_gb300 as z
+
+    torch.cuda.set_device(0)
+    dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank, world_size=world)
+    try:
+        numels, nd = _model()
+        total = sum(numels)
+        hp = z.Hparams(**HP)
+        side = torch.cuda.Stream()
+        results = []
+        for kind in ("arena", "list"):
+            for k_micro in (1, 3):
+                make = z.LocalShardAdamW if kind == "arena" else z.ShardListAdamW
+                a, b, c = (make(numels, nd, world, rank, hparams=hp) for _ in range(3))
+                plan = a.plan
+                m0 = plan.new_arena()
+                z.shard_gather(plan, _master0(total).cuda(), m0)
+                for o in (a, b):
+                    if kind == "arena":
+                        o.master.copy_(m0)
+                    else:
+                        for dst, src in zip(o.master, plan.shard_views(m0)):
+                            dst.copy_(src)
+                sums = []
+                for t in range(1, STEPS + 1):
+                    micro = []
+                    for k in range(k_micro):
+                        arena = plan.new_arena(torch.bfloat16)
+                        z.shard_gather(plan, _grad(t, rank, k, total, nan=False).cuda(), arena)
+                        micro.append(arena if kind == "arena" else [v.clone() for v in plan.shard_views(arena)])
+                    if kind == "arena" and k_micro == 1:
+                        micro = micro[0]
+                    c.step_from(micro)  # this rank's own sum of squares, read back
+                    own = z.read_norm(c.norm_out)["sumsq"]
+                    got = [torch.zeros(1, dtype=torch.float64) for _ in range(world)]
+                    dist.all_gather(got, torch.tensor([own], dtype=torch.float64))
+                    extra = sum(float(g[0]) for r, g in enumerate(got) if r != rank)
+                    side.wait_stream(torch.cuda.current_stream())
+                    a.step_from(micro, group=dist.group.WORLD, stream=side)
+                    torch.cuda.current_stream().wait_stream(side)
+                    b.step_from(micro, extra_sumsq=extra)
+                    torch.cuda.synchronize()
+                    sums.append(z.read_norm(a.norm_out)["sumsq"] == z.read_norm(b.norm_out)["sumsq"])
+                if kind == "arena":
+                    pairs = [(a.master, b.master), (a.exp_avg, b.exp_avg), (a.exp_avg_sq, b.exp_avg_sq),
+                             (a.grad, b.grad)]
+                else:
+                    pairs = [(torch.cat(list(x)), torch.cat(list(y))) for x, y in
+                             ((a.master, b.master), (a.exp_avg, b.exp_avg), (a.exp_avg_sq, b.exp_avg_sq),
+                              (a.grad, b.grad))]
+                same = [torch.equal(x.view(torch.int32), y.view(torch.int32)) for x, y in pairs]
+                wa = a.weight_bf16 if kind == "arena" else torch.cat(list(a.weight_bf16))
+                wb = b.weight_bf16 if kind == "arena" else torch.cat(list(b.weight_bf16))
+                same.append(torch.equal(wa.view(torch.int16), wb.view(torch.int16)))
+                results.append((kind, k_micro, all(sums), same, a.t))
+        q.put((rank, results))
+    except Exception as e:
+        q.put((rank, "error: %r" % (e,)))
+        raise
+    finally:
+        dist.destroy_process_group()
+
+
+def test_step_from_with_a_group_on_a_side_stream_equals_the_local_step_with_extra_sumsq():
+    """Two gloo ranks, each with its own shard and gradients: LocalShardAdamW.step_from and
+    ShardListAdamW.step_from with the group (one micro-batch: the micro-batch norm, the all-reduce,
+    the step that writes the gradient; three: the accumulating pass, the all-reduce, the step), on a
+    stream that is not the current one, give every rank the global sum of squares and the same
+    master, m, v, gradient and bf16 copy, bit for bit, as its local step given the other rank's
+    share."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_step_from_group_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+    for r in range(2):
+        assert not isinstance(got[r], str), got[r]
+        for kind, k_micro, sums_equal, same, t in got[r]:
+            assert sums_equal, (r, kind, k_micro)
+            assert same == [True] * 5, (r, kind, k_micro, same)
+            assert t == STEPS
+    for p in procs:
+        assert p.exitcode == 0

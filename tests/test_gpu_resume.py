@@ -112,7 +112,7 @@ def test_another_ranks_nonfinite_sum_skips_the_step(kind, monkeypatch):
     and check_finite reports the skip and keeps the step count."""
     import zero_sharded_mixed_local_gb300.optim as optim
 
-    def allreduce_with_an_inf_rank(norm_out, group):  # what the sum over the ranks gives
+    def allreduce_with_an_inf_rank(norm_out, group, stream=None):  # what the sum over the ranks gives
         norm_out[:8].view(torch.float64).fill_(float("inf"))
 
     monkeypatch.setattr(optim, "allreduce_sumsq_", allreduce_with_an_inf_rank)

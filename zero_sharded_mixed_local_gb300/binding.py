@@ -642,17 +642,25 @@ def unpack_all_gather(plans, recv, full, stream=None):
         shard_scatter(pl, flat[r * chunk:r * chunk + pl.arena_numel], full, stream=stream)
 
 
-def allreduce_sumsq_(norm_out, group=None):
+def allreduce_sumsq_(norm_out, group=None, stream=None):
     """Sum the ``sumsq`` field of a norm record across the ranks of ``group``, in place.
 
     This is the step's one exchange: each rank's zero1_grad_norm gives its
     local sum of squares, and after the all-reduce every rank's zero1_step
     clips with the same global norm (and skips if any rank saw inf/NaN).
-    Works for a CUDA record with NCCL and a CPU record with gloo.
+    Works for a CUDA record with NCCL (or gloo) and a CPU record with gloo.
+    A CUDA collective is ordered after the work of torch's current stream, so
+    with ``stream`` (the torch.cuda.Stream the norm kernels ran on, and the step
+    will run on) it is issued with that stream current.
     """
     import torch.distributed as dist
 
-    dist.all_reduce(norm_out[:8].view(torch.float64), op=dist.ReduceOp.SUM, group=group)
+    rec = norm_out[:8].view(torch.float64)
+    if stream is None or not norm_out.is_cuda:
+        dist.all_reduce(rec, op=dist.ReduceOp.SUM, group=group)
+        return
+    with torch.cuda.stream(stream):
+        dist.all_reduce(rec, op=dist.ReduceOp.SUM, group=group)
 
 
 def decode_norm(norm_out_bytes):
@@ -669,7 +677,9 @@ class PointerLists:
     per-tensor shard buffers of one dtype (model order), checked and uploaded by
     zero1_list_ptrs_upload.  With ``keep`` (the default) it holds references to the
     tensors so their memory stays valid while the lists exist.  ``lists`` is one list
-    of tensors or a list of them."""
+    of tensors or a list of them.  The upload is ordered on ``stream`` (a
+    torch.cuda.Stream; the current stream by default): the calls that read the lists
+    run on that stream, or on one that waits for it."""
 
     def __init__(self, plan, lists, dtype, device=None, stream=None, keep=True):
         lib = load_library()
@@ -711,11 +721,16 @@ class PointerLists:
         self.device = torch.device(device)
         self.n_lists = len(lists)
         count = self.n_lists * n
-        self.dev = torch.zeros(max(count, 2), dtype=torch.int64, device=self.device)
+        # Allocated from the pool of the stream that uploads the lists (and whose kernels read them),
+        # with no fill: a fill on another stream could land after the upload, and the allocator
+        # orders a later reuse of the block after that stream's work.
+        up = stream if stream is not None else torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(up):
+            self.dev = torch.empty(max(count, 2), dtype=torch.int64, device=self.device)
         host = (ctypes.c_void_p * max(count, 1))(*ptrs)
         _check(lib.zero1_list_ptrs_upload(plan.handle, host, self.n_lists, 2 if dtype == torch.bfloat16 else 4,
                                           ctypes.c_void_p(self.dev.data_ptr()), self.dev.numel() * 8,
-                                          _stream_ptr(stream, self.device)), "zero1_list_ptrs_upload")
+                                          _stream_ptr(up, self.device)), "zero1_list_ptrs_upload")
         self.tensors = lists if keep else None
         self.dtype = dtype
         self.counts = counts  # the plan's shard sizes: the calls check the lists against their plan

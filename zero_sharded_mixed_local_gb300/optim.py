@@ -29,10 +29,10 @@ import math
 
 import torch
 
-from .binding import (accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, Hparams, list_accumulate,
-                      list_accumulate_norm, list_grad_norm, list_micro_norm, list_step, list_step_accumulate,
-                      list_step_dev, local_step, micro_norm, new_norm_out, Plan, PointerLists, read_norm, step,
-                      step_accumulate, step_dev, step_scalars, STEP_SCALARS_BYTES)
+from .binding import (_stream_ptr, accumulate, accumulate_norm, allreduce_sumsq_, grad_norm, Hparams,
+                      list_accumulate, list_accumulate_norm, list_grad_norm, list_micro_norm, list_step,
+                      list_step_accumulate, list_step_dev, local_step, micro_norm, new_norm_out, Plan, PointerLists,
+                      read_norm, step, step_accumulate, step_dev, step_scalars, STEP_SCALARS_BYTES)
 
 
 def _applied(opt, stream):
@@ -100,7 +100,7 @@ class LocalShardAdamW:
             grad_norm(self.plan, self.grad, self.workspace, self.norm_out, extra_sumsq, stream=stream)
         self._norm_ready = False
         if group is not None:
-            allreduce_sumsq_(self.norm_out, group)
+            allreduce_sumsq_(self.norm_out, group, stream=stream)
         self.t += 1
         hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
         step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
@@ -125,13 +125,13 @@ class LocalShardAdamW:
             mb = [micro] if isinstance(micro, torch.Tensor) else list(micro)
             if len(mb) == 1:
                 micro_norm(self.plan, mb[0], self.workspace, self.norm_out, extra_sumsq, divisor, stream=stream)
-                allreduce_sumsq_(self.norm_out, group)
+                allreduce_sumsq_(self.norm_out, group, stream=stream)
                 step_accumulate(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, mb[0],
                                 self.weight_bf16, hp, self.t, self.norm_out, divisor=divisor, stream=stream)
             else:
                 accumulate_norm(self.plan, self.grad, mb, self.workspace, self.norm_out, overwrite_first=True,
                                 extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
-                allreduce_sumsq_(self.norm_out, group)
+                allreduce_sumsq_(self.norm_out, group, stream=stream)
                 step(self.plan, self.master, self.exp_avg, self.exp_avg_sq, self.grad, self.weight_bf16, hp, self.t,
                      self.norm_out, stream=stream)
         self._micro_seen = 0
@@ -293,25 +293,28 @@ class ShardListAdamW:
         self._micro_seen = 0
         self._norm_ready = False
 
-    def _micro_lists(self, micro):
+    def _micro_lists(self, micro, stream=None):
         if isinstance(micro, PointerLists):
             return micro
         if len(micro) and isinstance(micro[0], torch.Tensor):
             micro = [micro]
         # A cached upload stays valid for tensors at the same addresses with the same lengths
-        # and dtype (what the upload checked); it keeps no reference to them.
-        key = tuple(tuple((t.data_ptr(), t.numel(), t.dtype) for t in lst) for lst in micro)
+        # and dtype (what the upload checked); it keeps no reference to them.  It was ordered on
+        # the stream the kernels then ran on, so the key holds the stream as well.
+        key = (_stream_ptr(stream, self.device),) + tuple(
+            tuple((t.data_ptr(), t.numel(), t.dtype) for t in lst) for lst in micro)
         pl = self._micro_cache.get(key)
         if pl is None:
             if len(self._micro_cache) >= 8:
                 self._micro_cache.clear()
-            pl = self._micro_cache[key] = PointerLists(self.plan, micro, torch.bfloat16, self.device, keep=False)
+            pl = self._micro_cache[key] = PointerLists(self.plan, micro, torch.bfloat16, self.device, stream=stream,
+                                                       keep=False)
         return pl
 
     def accumulate(self, micro, last=False, extra_sumsq=0.0, divisor=1.0, stream=None):
         """Add one micro-batch (a list of bf16 shard tensors), several (a list of such lists), or
         a PointerLists built for them once (no per-call host work)."""
-        pl = self._micro_lists(micro)
+        pl = self._micro_lists(micro, stream)
         first = self._micro_seen == 0
         if last:
             list_accumulate_norm(self.plan, self.table, self._lists["grad"], pl, self.workspace, self.norm_out,
@@ -329,7 +332,7 @@ class ShardListAdamW:
                            stream=stream)
         self._norm_ready = False
         if group is not None:
-            allreduce_sumsq_(self.norm_out, group)
+            allreduce_sumsq_(self.norm_out, group, stream=stream)
         self.t += 1
         hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
         L = self._lists
@@ -344,7 +347,7 @@ class ShardListAdamW:
         (34 bytes per element instead of 36); for several, the K-way accumulation with the norm,
         then the step.  The same result as accumulate(micro, last=True) then step(); ``group``
         all-reduces the sum of squares in between."""
-        pl = self._micro_lists(micro)
+        pl = self._micro_lists(micro, stream)
         L = self._lists
         hp = self.hp if lr is None else dataclasses.replace(self.hp, lr=lr)
         if pl.n_lists == 1:
@@ -354,7 +357,7 @@ class ShardListAdamW:
             list_accumulate_norm(self.plan, self.table, L["grad"], pl, self.workspace, self.norm_out,
                                  overwrite_first=True, extra_sumsq=extra_sumsq, divisor=divisor, stream=stream)
         if group is not None:
-            allreduce_sumsq_(self.norm_out, group)
+            allreduce_sumsq_(self.norm_out, group, stream=stream)
         self.t += 1
         if pl.n_lists == 1:
             list_step_accumulate(self.plan, self.table, L["master"], L["exp_avg"], L["exp_avg_sq"], L["grad"], pl,
@@ -436,12 +439,13 @@ class Zero1AdamW:
     def t(self):
         return self.opt.t
 
-    def _grad_lists(self):
+    def _grad_lists(self, stream=None):
         """Device pointer lists of every parameter's gradient slice.  Slicing thousands of
         gradients costs the host milliseconds per call, so the lists are reused while every
         p.grad is the same tensor at the same address."""
         grads = [p.grad for _, p in self.named]
         ident = [(id(g), g.data_ptr() if g is not None else 0) for g in grads]
+        ident.append(_stream_ptr(stream, self.device))  # the stream the lists were uploaded on
         if ident == self._grad_ident and self._grad_pl is not None:
             return self._grad_pl
         views = []
@@ -452,13 +456,13 @@ class Zero1AdamW:
                 raise ValueError("gradient of %s must be contiguous bf16" % n)
             views.append(g.view(-1)[s:s + c])
         # no reference kept: the identity check above decides whether the addresses still hold
-        self._grad_pl = PointerLists(self.opt.plan, views, torch.bfloat16, self.device, keep=False)
+        self._grad_pl = PointerLists(self.opt.plan, views, torch.bfloat16, self.device, stream=stream, keep=False)
         self._grad_ident = ident
         return self._grad_pl
 
     def accumulate(self, last=False, stream=None):
         """Add every parameter's current bf16 gradient slice into the fp32 accumulator."""
-        self.opt.accumulate(self._grad_lists(), last=last, stream=stream)
+        self.opt.accumulate(self._grad_lists(stream), last=last, stream=stream)
         self._pending += 1
 
     def step(self, lr=None, group=None, stream=None, check_finite=False):
@@ -466,7 +470,7 @@ class Zero1AdamW:
         ``group``: a torch.distributed group whose ranks' sums of squares make the global norm;
         ``check_finite`` as for LocalShardAdamW.step."""
         if self._pending == 0:  # one micro-batch: its norm, then the step that fills the accumulator
-            applied = self.opt.step_from(self._grad_lists(), lr=lr, group=group, stream=stream,
+            applied = self.opt.step_from(self._grad_lists(stream), lr=lr, group=group, stream=stream,
                                          check_finite=check_finite)
         else:
             applied = self.opt.step(lr=lr, group=group, stream=stream, check_finite=check_finite)
