@@ -156,6 +156,52 @@ def test_compute_calls_reject_bad_arguments_before_any_launch(z):
     assert lib.zero1_last_cuda_error().decode() == ""
 
 
+def test_one_micro_batch_calls_reject_bad_arguments_before_any_launch(z):
+    """zero1_micro_norm, zero1_step_accumulate and their tensor-list forms: every case below fails
+    a check that comes before any CUDA call (the addresses are never dereferenced)."""
+    lib = z.load_library()
+    plan = z.Plan([100, 8], [0, 1], 1, 0)
+    h = plan.handle
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    nan = float("nan")
+    hp = z.binding._Hparams(3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    # the arena pair
+    assert lib.zero1_micro_norm(None, fake, 1.0, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_micro_norm(h, fake, 0.0, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL    # divisor
+    assert lib.zero1_micro_norm(h, fake, nan, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_micro_norm(h, fake, 1.0, -1.0, fake, 64, fake, None) == z.ZERO1_EINVAL   # extra_sumsq
+    assert lib.zero1_micro_norm(h, fake, 1.0, 0.0, fake, 64, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_micro_norm(h, fake, 1.0, 0.0, fake, 64, odd, None) == z.ZERO1_EALIGN
+    assert lib.zero1_micro_norm(h, None, 1.0, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_micro_norm(h, fake, 1.0, 0.0, fake, 4, fake, None) == z.ZERO1_EINVAL    # workspace
+    assert lib.zero1_micro_norm(h, odd, 1.0, 0.0, fake, 64, fake, None) == z.ZERO1_EALIGN
+    st = [h, fake, fake, fake, fake]
+    assert lib.zero1_step_accumulate(*st, fake, 1.0, fake, None, 1, None, None) == z.ZERO1_EINVAL   # no hparams
+    assert lib.zero1_step_accumulate(*st, fake, 1.0, fake, ctypes.byref(hp), 0, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_step_accumulate(*st, fake, nan, fake, ctypes.byref(hp), 1, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_step_accumulate(*st, odd, 1.0, fake, ctypes.byref(hp), 1, None, None) == z.ZERO1_EALIGN
+    # the tensor-list pair
+    assert lib.zero1_list_micro_norm(None, fake, fake, 1.0, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_micro_norm(h, fake, fake, 0.0, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_micro_norm(h, fake, fake, 1.0, nan, fake, 64, fake, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_micro_norm(h, fake, fake, 1.0, 0.0, fake, 64, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_micro_norm(h, fake, fake, 1.0, 0.0, fake, 64, odd, None) == z.ZERO1_EALIGN
+    assert lib.zero1_list_micro_norm(h, None, fake, 1.0, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL  # table
+    assert lib.zero1_list_micro_norm(h, fake, None, 1.0, 0.0, fake, 64, fake, None) == z.ZERO1_EINVAL  # lists
+    assert lib.zero1_list_micro_norm(h, fake, odd, 1.0, 0.0, fake, 64, fake, None) == z.ZERO1_EALIGN
+    assert lib.zero1_list_micro_norm(h, fake, fake, 1.0, 0.0, fake, 4, fake, None) == z.ZERO1_EINVAL  # workspace
+    lt = [h, fake, fake, fake, fake, fake]
+    assert lib.zero1_list_step_accumulate(*lt, fake, 1.0, fake, None, 1, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_step_accumulate(*lt, fake, 1.0, fake, ctypes.byref(hp), 0, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_step_accumulate(*lt, None, 1.0, fake, ctypes.byref(hp), 1, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_step_accumulate(*lt, fake, nan, fake, ctypes.byref(hp), 1, None, None) == z.ZERO1_EINVAL
+    assert lib.zero1_list_step_accumulate(*lt, odd, 1.0, fake, ctypes.byref(hp), 1, None, None) == z.ZERO1_EALIGN
+    assert lib.zero1_list_step_accumulate(h, fake, None, fake, fake, fake, fake, 1.0, fake, ctypes.byref(hp), 1,
+                                          None, None) == z.ZERO1_EINVAL   # no master list
+    assert lib.zero1_last_cuda_error().decode() == ""
+
+
 def test_binding_refuses_cpu_tensors(z):
     import torch
     plan = z.Plan([64], [0], 1, 0)
