@@ -74,6 +74,27 @@ def test_pack_and_unpack_helpers():
     assert torch.equal(out, full)
 
 
+def test_pack_on_a_side_stream_fills_the_padding_before_its_gathers():
+    """pack_reduce_scatter on a stream that is not the current one: the padding's zero fill is
+    ordered with the gathers on that stream, so a buffer holding stale values ends up as the pack on
+    the current stream gives it."""
+    numels = [5000, 13, 64, 2049, 1 << 20]
+    nd = [0, 1, 0, 0, 0]
+    dp = 3
+    plans = [z.Plan(numels, nd, dp, r) for r in range(dp)]
+    chunk = z.exchange_chunk_numel(plans)
+    full = torch.arange(sum(numels), device="cuda", dtype=torch.float32)
+    ref = torch.empty((dp, chunk), device="cuda")
+    z.pack_reduce_scatter(plans, full, ref)
+    side = torch.cuda.Stream()
+    for _ in range(3):
+        send = torch.full((dp, chunk), 7.0, device="cuda")  # stale values, written on the current stream
+        side.wait_stream(torch.cuda.current_stream())
+        z.pack_reduce_scatter(plans, full, send, stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        assert torch.equal(send, ref)
+
+
 def _layouts(numels, nd, dp):
     return [z.Plan(numels, nd, dp, r) for r in range(dp)]
 

@@ -625,7 +625,11 @@ def pack_reduce_scatter(plans, full_grad, send, stream=None):
     chunk = exchange_chunk_numel(plans)
     if send.numel() != chunk * len(plans):
         raise ValueError("send must hold %d x %d elements" % (len(plans), chunk))
-    send.zero_()
+    if stream is None:
+        send.zero_()
+    else:
+        with torch.cuda.stream(stream):  # the padding's fill in order before the gathers on that stream
+            send.zero_()
     flat = send.view(-1)
     for r, pl in enumerate(plans):
         shard_gather(pl, full_grad, flat[r * chunk:r * chunk + pl.arena_numel], stream=stream)
