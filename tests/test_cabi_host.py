@@ -82,6 +82,33 @@ def _check_layout(plan, no_decay):
         assert (np.sum((cnts + 7) // 8 * 8) == e - b)
 
 
+def test_plan_matches_oracle_on_random_shape_lists(z):
+    """Two hundred seeded draws: 1-40 tensors of 0-70,000 elements (a fifth under the dp size),
+    random no-decay flags, dp 1-16 and every rank of a few of them.  Shard split, counts, local size
+    and byte accounting as the oracle gives them; arena layout as _check_layout requires; and the
+    ranks' shards tile every tensor exactly."""
+    rng = np.random.default_rng(2024)
+    for draw in range(200):
+        n = int(rng.integers(1, 41))
+        dp = int(rng.integers(1, 17))
+        small = rng.random(n) < 0.2
+        numels = np.where(small, rng.integers(0, dp + 1, n), rng.integers(0, 70001, n)).astype(np.int64)
+        nd = (rng.random(n) < 0.3).astype(np.uint8)
+        ranks = range(dp) if draw % 20 == 0 else [int(rng.integers(0, dp))]
+        covered = np.zeros(n, np.int64)
+        for r in ranks:
+            plan = z.Plan(numels.tolist(), nd.tolist(), dp, r)
+            start, count, local = oracle.plan(numels.tolist(), dp, r)
+            L = plan.layout()
+            assert np.array_equal(L.shard_start, start) and np.array_equal(L.counts, count), (draw, r)
+            assert plan.local_numel == local and plan.total_numel == int(numels.sum())
+            _check_layout(plan, nd)
+            assert plan.bytes(2) == oracle.zero1_bytes(int(numels.sum()), local, 2)
+            covered += L.counts
+        if draw % 20 == 0:
+            assert np.array_equal(covered, numels), draw
+
+
 def test_small_plan_worked_example(z):
     # numels 10, 3, 8 over dp=3; tensor 1 is a norm weight
     plans = [z.Plan([10, 3, 8], [0, 1, 0], 3, r) for r in range(3)]
