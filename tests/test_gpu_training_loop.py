@@ -200,3 +200,37 @@ def test_module_optimizer_follows_reallocated_gradients():
         runs.append([p.detach().clone() for p in model.parameters()])
     for a, b in zip(*runs):
         assert torch.equal(a, b)
+
+
+def test_module_optimizer_on_a_side_stream_equals_the_current_stream():
+    """Zero1AdamW.accumulate / step given a stream that is not the current one: the gradient pointer
+    lists are uploaded on that stream, and the parameters equal those of the same steps on the current
+    stream, with one micro-batch (no accumulate call) and with two."""
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip_grad=1.0)
+    for n_micro in (1, 2):
+        runs = []
+        for use_side in (False, True):
+            side = torch.cuda.Stream() if use_side else None
+            model = _model(6).to(torch.bfloat16)
+            opt = z.Zero1AdamW(model.named_parameters(), hparams=hp)
+            g = torch.Generator(device="cuda").manual_seed(11)
+            for step in range(3):
+                for micro in range(n_micro):
+                    model.zero_grad(set_to_none=True)  # new gradient tensors: new pointer lists every call
+                    x = torch.randn(32, 64, device="cuda", generator=g)
+                    model(x.bfloat16()).float().pow(2).mean().backward()
+                    if side is not None:
+                        side.wait_stream(torch.cuda.current_stream())
+                    if n_micro > 1:
+                        opt.accumulate(last=(micro == n_micro - 1), stream=side)
+                        if side is not None:  # the gradients it read are freed on the current stream next
+                            torch.cuda.current_stream().wait_stream(side)
+                if side is not None:
+                    side.wait_stream(torch.cuda.current_stream())
+                opt.step(stream=side)
+                if side is not None:
+                    torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            runs.append([p.detach().clone() for p in model.parameters()])
+        for a, b in zip(*runs):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), n_micro
