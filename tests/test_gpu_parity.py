@@ -540,7 +540,8 @@ def test_data_parallel_average_emulated_on_one_gpu():
 def test_arena_beyond_2_to_32_elements():
     """Maximum size: one tensor of 2^32 + 2^20 + 5 elements (dp 1; 86 GB resident) and a tiny
     excluded one.  Every gradient element is 2^-8 (exact in bf16), so the sum of squares is
-    N * 2^-16 exactly; elements around 2^31, 2^32 and the tail are stepped by the oracle."""
+    N * 2^-16 exactly; elements around 2^31, 2^32 and the tail are stepped by the oracle.  Through the
+    two-pass calls, then through the one-micro-batch pair on the same buffers."""
     n0 = (1 << 32) + (1 << 20) + 5
     plan = z.Plan([n0, 3], [0, 1], 1, 0)
     n, N = plan.arena_numel, plan.local_numel
@@ -575,6 +576,25 @@ def test_arena_beyond_2_to_32_elements():
     P, M, V = P0.copy(), np.zeros_like(P0), np.zeros_like(P0)
     dec = int(np.sum(idx < n0))
     oracle.adamw(P, M, V, G, [dec, idx.size - dec], [0, 1], hp, 1, coef)
+    for name, t, ref in (("master", master, P), ("m", m, M), ("v", v, V)):
+        assert np.array_equal(t[it].cpu().numpy().view(np.uint32), ref.view(np.uint32)), name
+    assert np.array_equal(u16(wbf[it]), oracle.bf16_rne(P))
+    # the same step through the one-micro-batch pair (norm from the micro-batch, then the step that
+    # writes the gradient), on the same buffers restored to the initial state
+    g = torch.Generator(device=dev).manual_seed(3)
+    master.zero_()
+    master[:n0].normal_(0.0, 0.02, generator=g)
+    master[b1:b1 + 3] = 1.0
+    assert np.array_equal(master[it].cpu().numpy(), P0)
+    m.zero_()
+    v.zero_()
+    grad.fill_(float("nan"))
+    wbf.zero_()
+    z.micro_norm(plan, mb, ws, nout)
+    z.step_accumulate(plan, master, m, v, grad, mb, wbf, z.Hparams(**hp), 1, nout)
+    got = z.read_norm(nout)
+    assert got["status"] == 0 and got["sumsq"] == N * 2.0 ** -16
+    assert np.all(grad[it].cpu().numpy() == np.float32(2.0 ** -8))
     for name, t, ref in (("master", master, P), ("m", m, M), ("v", v, V)):
         assert np.array_equal(t[it].cpu().numpy().view(np.uint32), ref.view(np.uint32)), name
     assert np.array_equal(u16(wbf[it]), oracle.bf16_rne(P))
