@@ -409,7 +409,8 @@ def test_k_way_list_pass_matches_the_oracle(K, misaligned):
 def test_list_tensor_beyond_2_to_32_elements():
     """Maximum size through the list calls: one shard of 2^32 + 2^20 + 5 elements (run offsets
     past 2^32) plus a 3-element excluded one, gradients all 2^-8, so the sum of squares is
-    N * 2^-16 exactly; elements around 2^31, 2^32 and the tail are stepped by the oracle."""
+    N * 2^-16 exactly; elements around 2^31, 2^32 and the tail are stepped by the oracle.  Through
+    the two-pass list calls, then through the list micro-batch pair on the same buffers."""
     n0 = (1 << 32) + (1 << 20) + 5
     plan = z.Plan([n0, 3], [0, 1], 1, 0)
     dev = torch.device("cuda")
@@ -443,6 +444,24 @@ def test_list_tensor_beyond_2_to_32_elements():
         assert np.array_equal(gotv.view(np.uint32), ref.view(np.uint32)), name
     wv = torch.cat([w[0][it], w[1]])
     assert np.array_equal(u16(wv), oracle.bf16_rne(P))
+    # the same step through the list micro-batch pair, on the same buffers restored to the initial state
+    g = torch.Generator(device=dev).manual_seed(4)
+    master[0].normal_(0.0, 0.02, generator=g)
+    master[1].fill_(1.0)
+    assert np.array_equal(np.concatenate([master[0][it].cpu().numpy(), master[1].cpu().numpy()]), P0)
+    for x in m + v + w:
+        x.zero_()
+    for x in grad:
+        x.fill_(float("nan"))
+    z.list_micro_norm(plan, table, ml, ws, nout)
+    z.list_step_accumulate(plan, table, *L, ml, wl, z.Hparams(**HP), 1, nout)
+    got = z.read_norm(nout)
+    assert got["status"] == 0 and got["sumsq"] == N * 2.0 ** -16, got
+    assert np.all(np.concatenate([grad[0][it].cpu().numpy(), grad[1].cpu().numpy()]) == np.float32(2.0 ** -8))
+    for name, lst, ref in (("master", master, P), ("m", m, M), ("v", v, V)):
+        gotv = np.concatenate([lst[0][it].cpu().numpy(), lst[1].cpu().numpy()])
+        assert np.array_equal(gotv.view(np.uint32), ref.view(np.uint32)), name
+    assert np.array_equal(u16(torch.cat([w[0][it], w[1]])), oracle.bf16_rne(P))
     del master, m, v, grad, w, mb, L, wl, ml
     torch.cuda.empty_cache()
 
