@@ -295,8 +295,9 @@ def test_pointer_lists_are_checked():
 
 def test_llama8b_full_size_list_equals_arena():
     """The 1.0B-element Llama-3.1-8B dp8 rank-0 shard (291 tensors), one step through the
-    arena calls and through the list calls on one allocation per tensor shard: every
-    element of every state buffer identical, the norms within 1e-12."""
+    arena calls and through the list calls on one allocation per tensor shard, then a second
+    through both one-micro-batch pairs (the bench's K = 1 path): every element of every state
+    buffer identical after each, the norms within 1e-12."""
     from zero_sharded_mixed_local_gb300.workloads import InputGenerator, Layout, get_workload
     dev = torch.device("cuda")
     w = get_workload("llama8b")
@@ -324,6 +325,20 @@ def test_llama8b_full_size_list_equals_arena():
     for arena, shards in ((grad, lg), (master, lm), (m, lmm), (v, lv), (wbf, lw)):
         for i, (a, b) in enumerate(zip(plan.shard_views(arena), shards)):
             assert torch.equal(a, b), i
+    # step 2 as the bench runs K = 1: the micro-batch norm, then the step that writes the gradient
+    micro = gen.micro_grads()[0]
+    lmic2 = split(micro)
+    ml2 = z.PointerLists(plan, lmic2, torch.bfloat16)
+    z.micro_norm(plan, micro, ws, nout)
+    z.step_accumulate(plan, master, m, v, grad, micro, wbf, hp, 2, nout)
+    a_norm = z.read_norm(nout)
+    z.list_micro_norm(plan, table, ml2, lws, lnout)
+    z.list_step_accumulate(plan, table, *lists, ml2, wl, hp, 2, lnout)
+    l_norm = z.read_norm(lnout)
+    assert abs(a_norm["sumsq"] - l_norm["sumsq"]) <= 1e-12 * a_norm["sumsq"]
+    for arena, shards in ((grad, lg), (master, lm), (m, lmm), (v, lv), (wbf, lw)):
+        for i, (a, b) in enumerate(zip(plan.shard_views(arena), shards)):
+            assert torch.equal(a, b), ("micro pair", i)
 
 
 @pytest.mark.parametrize("guard", [64, 65])
