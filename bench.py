@@ -137,10 +137,11 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-TRAFFIC_SOURCES = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "launch.cuh", "store8.cuh"],
-                   "adamw_step_accumulate": ["adamw_step.cu", "elementwise.cuh", "launch.cuh", "store8.cuh"],
-                   "list_step": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"],
-                   "list_step_accumulate": ["tensor_list.cu", "elementwise.cuh", "launch.cuh"]}
+TRAFFIC_SOURCES = {"adamw_step": ["adamw_step.cu", "elementwise.cuh", "l2_policy.cuh", "launch.cuh", "store8.cuh"],
+                   "adamw_step_accumulate": ["adamw_step.cu", "elementwise.cuh", "l2_policy.cuh", "launch.cuh",
+                                             "store8.cuh"],
+                   "list_step": ["tensor_list.cu", "elementwise.cuh", "l2_policy.cuh", "launch.cuh"],
+                   "list_step_accumulate": ["tensor_list.cu", "elementwise.cuh", "l2_policy.cuh", "launch.cuh"]}
 # algorithmic bytes per parameter of each step kernel: the one-micro-batch form reads the 2-byte
 # micro-batch instead of the 4-byte gradient and writes the gradient (4)
 STEP_KERNEL_BYTES = {"adamw_step": STEP_BYTES_PER_ELEM, "list_step": STEP_BYTES_PER_ELEM, "adamw_step_accumulate": 32,

@@ -31,6 +31,7 @@
 // every state element are bit for bit those of zero1_accumulate_norm +
 // zero1_step.  A skipped step (non-finite norm) still writes the gradient.
 #include "elementwise.cuh"
+#include "l2_policy.cuh"
 #include "launch.cuh"
 #include "store8.cuh"
 #include "zero1_internal.h"
@@ -108,12 +109,13 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
         }
         ga = make_float4(f[0], f[1], f[2], f[3]);
         gb = make_float4(f[4], f[5], f[6], f[7]);
+        const uint64_t pol = l2_evict_last();
         if (kWideGrad) {
-            store8_f32(P.grad_out + 8 * i, ga, gb);
+            store_f32x8(P.grad_out + 8 * i, ga, gb, pol);
         } else {
             float4* g4 = reinterpret_cast<float4*>(P.grad_out) + 2 * i;
-            g4[0] = ga;
-            g4[1] = gb;
+            store_f32x4(g4, ga, pol);
+            store_f32x4(g4 + 1, gb, pol);
         }
         if (s_skip) return;  // the gradient is written; master, m, v and the bf16 copy stay as they are
     } else if (s_skip || !live) {
@@ -144,19 +146,21 @@ __global__ void __launch_bounds__(kStepThreads) adamw_step_kernel(const __grid_c
     float4* p4 = reinterpret_cast<float4*>(P.master) + 2 * i;
     float4* m4 = reinterpret_cast<float4*>(P.m) + 2 * i;
     float4* v4 = reinterpret_cast<float4*>(P.v) + 2 * i;
-    p4[0] = pa;
-    p4[1] = pb;
-    m4[0] = ma;
-    m4[1] = mb;
-    v4[0] = va;
-    v4[1] = vb;
+    // every result with the evict_last L2 priority (l2_policy.cuh)
+    const uint64_t pol = l2_evict_last();
+    store_f32x4(p4, pa, pol);
+    store_f32x4(p4 + 1, pb, pol);
+    store_f32x4(m4, ma, pol);
+    store_f32x4(m4 + 1, mb, pol);
+    store_f32x4(v4, va, pol);
+    store_f32x4(v4 + 1, vb, pol);
     if (kWriteBf16) {
         uint4 w;
         w.x = pack_bf16x2(pa.x, pa.y);
         w.y = pack_bf16x2(pa.z, pa.w);
         w.z = pack_bf16x2(pb.x, pb.y);
         w.w = pack_bf16x2(pb.z, pb.w);
-        reinterpret_cast<uint4*>(P.w)[i] = w;
+        store_u32x4(reinterpret_cast<uint4*>(P.w) + i, w, pol);
     }
 }
 

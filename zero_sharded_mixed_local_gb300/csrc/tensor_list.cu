@@ -31,8 +31,8 @@
 // separate 512-byte-aligned allocations).
 #include "elementwise.cuh"
 #include "launch.cuh"
+#include "l2_policy.cuh"
 #include "pair_sum.cuh"
-#include "store8.cuh"
 
 namespace zero1 {
 namespace {
@@ -61,6 +61,19 @@ __device__ __forceinline__ void store8(float* x, int n, bool vec, const float (&
     }
 }
 
+// store8, and the bf16 rounding of eight values, with the evict_last L2 priority on the vector
+// path (the step's results; l2_policy.cuh).
+__device__ __forceinline__ void store8_last(float* x, int n, bool vec, const float (&f)[8], uint64_t pol) {
+    if (vec) {
+        store_f32x4(reinterpret_cast<float4*>(x), make_float4(f[0], f[1], f[2], f[3]), pol);
+        store_f32x4(reinterpret_cast<float4*>(x) + 1, make_float4(f[4], f[5], f[6], f[7]), pol);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < n) x[j] = f[j];
+    }
+}
+
 __device__ __forceinline__ void load8_bf16(const uint16_t* x, int n, bool vec, float (&f)[8]) {
     if (vec) {
         widen8(*reinterpret_cast<const uint4*>(x), f);
@@ -70,14 +83,14 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* x, int n, bool vec, f
     }
 }
 
-__device__ __forceinline__ void store8_bf16(uint16_t* x, int n, bool vec, const float (&f)[8]) {
+__device__ __forceinline__ void store8_bf16_last(uint16_t* x, int n, bool vec, const float (&f)[8], uint64_t pol) {
     if (vec) {
         uint4 w;
         w.x = pack_bf16x2(f[0], f[1]);
         w.y = pack_bf16x2(f[2], f[3]);
         w.z = pack_bf16x2(f[4], f[5]);
         w.w = pack_bf16x2(f[6], f[7]);
-        *reinterpret_cast<uint4*>(x) = w;
+        store_u32x4(reinterpret_cast<uint4*>(x), w, pol);
     } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -387,6 +400,7 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
     const StepConsts sc{S.b1, S.b2, S.omb1, S.omb2, S.eps, S.sqrtbc2};
     const float dfac = S.dfac[ch.group];
     const float stepsize = S.stepsize[ch.group];
+    const uint64_t pol = l2_evict_last();  // every result with the evict_last L2 priority
 #pragma unroll 1
     for (int r = 0; r < kStepVecsPerThread; ++r) {
         const int e = 8 * (v0 + r * kTileThreads);
@@ -409,17 +423,18 @@ __global__ void __launch_bounds__(kTileThreads, 4) list_step_kernel(const __grid
             }
             // the gradient, whether or not the step applies
             if (wide_grad && n == 8)
-                store8_f32(grad + e, make_float4(g[0], g[1], g[2], g[3]), make_float4(g[4], g[5], g[6], g[7]));
+                store_f32x8(grad + e, make_float4(g[0], g[1], g[2], g[3]), make_float4(g[4], g[5], g[6], g[7]),
+                            pol);
             else
-                store8(grad + e, n, vec, g);
+                store8_last(grad + e, n, vec, g, pol);
             if (s_skip) continue;
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) adamw_elem(p[j], mm[j], vv[j], g[j], coef, dfac, stepsize, sc);
-        store8(master + e, n, vec, p);
-        store8(m + e, n, vec, mm);
-        store8(v + e, n, vec, vv);
-        if (kWriteBf16) store8_bf16(w + e, n, vec, p);
+        store8_last(master + e, n, vec, p, pol);
+        store8_last(m + e, n, vec, mm, pol);
+        store8_last(v + e, n, vec, vv, pol);
+        if (kWriteBf16) store8_bf16_last(w + e, n, vec, p, pol);
     }
 }
 
