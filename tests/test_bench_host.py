@@ -174,3 +174,15 @@ def test_committed_traffic_records_match_the_kernel_sources():
         assert rec["kernel_source_sha256_16"] == bench.kernel_source_hash(kernel), kernel
         got, src = bench.profile_traffic(kernel, 1_003_782_656)
         assert got == int(round(rec["traffic_bytes_per_param"] * 1_003_782_656)) and src
+
+
+def test_clock_rejection_rule():
+    """A hardware or thermal slowdown, or an SM clock well below its maximum with no reason, rejects the
+    timed region's number; sw_power_cap alone does not."""
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.clock_rejection(ok) is None and bench.clock_rejection(None) is None
+    assert bench.clock_rejection(dict(ok, reasons=["sw_power_cap"], sm_mhz=1800.0)) is None
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert r in bench.clock_rejection(dict(ok, reasons=[r, "sw_power_cap"]))
+    assert "no throttle reason" in bench.clock_rejection(dict(ok, sm_mhz=1200.0))
+    assert bench.clock_rejection(dict(ok, sm_mhz=1900.0)) is None  # within 10% of the maximum

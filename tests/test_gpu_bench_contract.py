@@ -37,6 +37,7 @@ def test_bench_line_has_the_contract_keys(extra):
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["sample"]
     assert d["gpu_launches"] == 3 * (2 + 2)  # K=2: one accumulate, the fused pass (2 kernels), the step
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    assert "clocks_rejection" in d  # None when the clocks admit the number, else why they do not
     if not extra:
         e = d["e2e"]
         assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 24
