@@ -72,6 +72,23 @@ def test_bench_data_parallel_line():
     assert d["roofline"]["kernel"] == "adamw_step_kernel" and d["roofline"]["params_per_launch"] == 3147008
 
 
+@pytest.mark.parametrize("extra", [[], ["--tensor-list"]])
+def test_bench_one_micro_batch_line(extra):
+    """K = 1, the bench's default path: the micro-batch norm (2 kernels) and the step that writes the
+    gradient (1 kernel) per step, with the roofline on the step's one-micro-batch form at 32 B/param and
+    its traffic from the committed record."""
+    d = _run("--workload", "toy", "--micro-batches", "1", "--steps", "3", "--warmup", "3", "--no-cpu-baseline",
+             "--no-e2e", "--no-torch-baseline", *extra)
+    step = "list_step_accumulate" if extra else "adamw_step_accumulate"
+    assert d["gpu_launches"] == 3 * 3
+    assert set(d["kernels"]) >= {"micro_norm", step}
+    r = d["roofline"]
+    assert r["kernel"].endswith("(one-micro-batch form)") and r["bytes_per_param"] == 32
+    assert r["traffic"] is not None and r["traffic_source"].startswith("profiles/traffic_" + step + "_")
+    assert d["config"]["micro_batches"] == 1
+    assert d["clocks_rejection"] is None or "remeasured" in d
+
+
 def test_bench_one_call_line():
     """--one-call: the whole toy step as one zero1_local_step call (K-way pass, final reduction,
     step: three launches per step)."""
