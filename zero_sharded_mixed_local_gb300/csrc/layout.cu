@@ -40,8 +40,21 @@ __global__ void __launch_bounds__(kLayoutThreads)
         const int nv = ch.len / kPerVec;
         const uint4* s4 = reinterpret_cast<const uint4*>(s);
         uint4* d4 = reinterpret_cast<uint4*>(d);
-#pragma unroll 4
-        for (int j = threadIdx.x; j < nv; j += kLayoutThreads) d4[j] = s4[j];
+        // eight vectors' loads before their stores: a full bf16 chunk is one round of load latency
+        constexpr int kBatch = 8;
+        for (int j0 = threadIdx.x; j0 < nv; j0 += kBatch * kLayoutThreads) {
+            uint4 r[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int j = j0 + q * kLayoutThreads;
+                if (j < nv) r[q] = s4[j];
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int j = j0 + q * kLayoutThreads;
+                if (j < nv) d4[j] = r[q];
+            }
+        }
         done = nv * kPerVec;
     }
     for (int j = done + threadIdx.x; j < ch.len; j += kLayoutThreads) d[j] = s[j];
