@@ -529,8 +529,10 @@ def test_random_list_configurations_match_the_oracle():
     16-byte boundary. Each has 1-10 tensors of 0 to 50,000 elements (a fifth under 20), a random
     no-decay set, dp 1-8 at a random rank, 1-5 micro-batches, random hyper-parameters and gradient
     scales. Over two steps, the gradient, the norm, master, m, v and the bf16 copy are checked against
-    the oracle fed the shards concatenated in model order."""
+    the oracle fed the shards concatenated in model order. Half of the one-micro-batch draws take
+    ShardListAdamW.step_from (the micro-batch norm and the list step that writes the gradient)."""
     rng = np.random.default_rng(77)
+    n_micro_pair = 0
     for case in range(30):
         nt = int(rng.integers(1, 11))
         small = rng.random(nt) < 0.2
@@ -546,11 +548,16 @@ def test_random_list_configurations_match_the_oracle():
                          sigma=float(10 ** rng.uniform(-4, -1)))
         K = int(rng.integers(1, 6))
         P, M, V = _oracle_state(pb)
+        micro_pair = K == 1 and case % 2 == 0
+        n_micro_pair += micro_pair
         for t in (1, 2):
             micros = [pb.micro_like(pb.micro()) for _ in range(K)]
-            for k, mb in enumerate(micros):
-                pb.opt.accumulate(mb, last=(k == K - 1))
-            pb.opt.step()
+            if micro_pair:  # the micro-batch's norm, then the list step that writes the gradient
+                pb.opt.step_from(micros[0])
+            else:
+                for k, mb in enumerate(micros):
+                    pb.opt.accumulate(mb, last=(k == K - 1))
+                pb.opt.step()
             got = pb.opt.read_norm()
             G = np.zeros(P.size, np.float32)
             for k, mb in enumerate(micros):
@@ -564,6 +571,7 @@ def test_random_list_configurations_match_the_oracle():
         for name, lst, ref in (("master", pb.master, P), ("m", pb.m, M), ("v", pb.v, V)):
             assert _eq(pb.flat(lst).numpy(), ref), (case, name)
         assert np.array_equal(u16(pb.flat(pb.w)), oracle.bf16_rne(P)), case
+    assert n_micro_pair >= 2, n_micro_pair  # draws that take the one-micro-batch list pair
 
 
 @pytest.mark.parametrize("misaligned", [False, True])
