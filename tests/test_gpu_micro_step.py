@@ -211,3 +211,55 @@ def test_micro_pair_matches_the_oracle_on_the_toy_shard_with_one_micro_batch():
     res = run_parity(w, steps=5, micro_step=True)
     assert res["master"] == 0 and res["m"] == 0 and res["v"] == 0
     assert res["norms"][0][3] < 1.0
+
+
+def test_arena_calls_write_nothing_outside_their_buffers():
+    """Every arena buffer sits between 64-element guard zones filled with a pattern (the buffer stays
+    32-byte aligned); after zero1_accumulate (K = 3), the fused and the separate norm, the step, the
+    micro-batch pair and one-call steps, with and without the bf16 copy and with a divisor, every guard
+    is unchanged.  The sizes leave ragged tails in the last norm tile and the last block."""
+    numels = [16384 * 2 + 8 * 3 + 5, 77, 1, 1000]
+    plan, master, micro = _setup(numels, [0, 1, 0, 1], sigma=0.05, seed=12)
+    n = plan.arena_numel
+    G = 64
+
+    def guarded(dtype, fill):
+        back = torch.empty(n + 2 * G, dtype=dtype, device="cuda")
+        back.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).fill_(fill)
+        return back, back[G:G + n]
+
+    bufs = {name: guarded(dt, fill) for name, dt, fill in (
+        ("grad", torch.float32, 0x5A5A5A5A), ("master", torch.float32, 0x3C3C3C3C), ("m", torch.float32, 0x11111111),
+        ("v", torch.float32, 0x22222222), ("w", torch.bfloat16, 0x7777))}
+    for name in ("master", "m", "v", "grad"):
+        bufs[name][1].copy_(master if name == "master" else torch.zeros_like(master))
+    bufs["w"][1].zero_()
+    mbs = [guarded(torch.bfloat16, 0x6666) for _ in range(3)]
+    for (_, view) in mbs:
+        view.copy_(micro())
+    ws_back = torch.full((plan.new_workspace().numel() + 2 * 16,), 0x5B, dtype=torch.uint8, device="cuda")
+    ws = ws_back[16:16 + plan.new_workspace().numel()]
+    nout_back = torch.full((z.NORM_OUT_BYTES + 64,), 0x4D, dtype=torch.uint8, device="cuda")
+    nout = nout_back[16:48]
+    before = {k: b.clone() for k, (b, _) in bufs.items()}
+    mb_before = [b.clone() for b, _ in mbs]
+    ws_before, nout_before = ws_back.clone(), nout_back.clone()
+    g, p, m_, v_, w_ = (bufs[k][1] for k in ("grad", "master", "m", "v", "w"))
+    views = [v for _, v in mbs]
+    z.accumulate(plan, g, views[0], overwrite_first=True)
+    z.accumulate(plan, g, views[1], overwrite_first=False)
+    z.accumulate_norm(plan, g, views[2], ws, nout, overwrite_first=False, divisor=3.0)
+    z.grad_norm(plan, g, ws, nout)
+    z.step(plan, p, m_, v_, g, w_, HP, 1, nout)
+    z.step(plan, p, m_, v_, g, None, HP, 2, nout)
+    z.micro_norm(plan, views[0], ws, nout, divisor=2.0)
+    z.step_accumulate(plan, p, m_, v_, g, views[0], w_, HP, 3, nout, divisor=2.0)
+    z.local_step(plan, g, views, ws, nout, p, m_, v_, w_, HP, 4)
+    z.local_step(plan, g, views[:1], ws, nout, p, m_, v_, None, HP, 5)
+    torch.cuda.synchronize()
+    for k, (b, _) in bufs.items():
+        assert torch.equal(b[:G], before[k][:G]) and torch.equal(b[G + n:], before[k][G + n:]), k
+    for (b, _), b0 in zip(mbs, mb_before):
+        assert torch.equal(b, b0)  # micro-batches are only read
+    assert torch.equal(ws_back[:16], ws_before[:16]) and torch.equal(ws_back[16 + ws.numel():], ws_before[16 + ws.numel():])
+    assert torch.equal(nout_back[:16], nout_before[:16]) and torch.equal(nout_back[48:], nout_before[48:])
