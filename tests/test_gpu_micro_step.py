@@ -261,5 +261,6 @@ def test_arena_calls_write_nothing_outside_their_buffers():
         assert torch.equal(b[:G], before[k][:G]) and torch.equal(b[G + n:], before[k][G + n:]), k
     for (b, _), b0 in zip(mbs, mb_before):
         assert torch.equal(b, b0)  # micro-batches are only read
-    assert torch.equal(ws_back[:16], ws_before[:16]) and torch.equal(ws_back[16 + ws.numel():], ws_before[16 + ws.numel():])
+    end = 16 + ws.numel()
+    assert torch.equal(ws_back[:16], ws_before[:16]) and torch.equal(ws_back[end:], ws_before[end:])
     assert torch.equal(nout_back[:16], nout_before[:16]) and torch.equal(nout_back[48:], nout_before[48:])
