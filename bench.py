@@ -498,8 +498,9 @@ def cpu_baseline(w, target_s=10.0, max_elems=1 << 27):
     n1, value1, steps1, total1 = res[1]
     return {"value": value, "unit": "params/s", "cores": threads, "kind": "oracle",
             "sample": "%d elements drawn like the workload's decayed tensors; %d full steps (K=%d accumulate, norm, "
-                      "AdamW + bf16 copy) of scalar C on %d threads over contiguous ranges, %.1f s (%.0f core-seconds), "
-                      "after one untimed step" % (n, steps, w.micro_batches, threads, total, total * threads),
+                      "AdamW + bf16 copy) of scalar C on %d threads over contiguous ranges, %.1f s "
+                      "(%.0f core-seconds), after one untimed step" % (n, steps, w.micro_batches, threads, total,
+                                                                       total * threads),
             "single_core": {"value": value1, "elements": n1, "steps": steps1, "seconds": total1}}
 
 
