@@ -15,6 +15,19 @@
  * numel into dp_size contiguous shards and lays the local shards out in one
  * flat "arena" per quantity.
  *
+ * The same step in other shapes, each with the same results bit for bit:
+ *   zero1_accumulate_norm        the last micro-batch's pass and the norm together
+ *   zero1_micro_norm,            one micro-batch: the norm from it, then the
+ *   zero1_step_accumulate        step that writes the fp32 gradient it uses
+ *   zero1_local_step             the whole step in one call
+ *   zero1_list_*                 the calls over one buffer per tensor shard
+ *   zero1_step_dev, zero1_list_step_dev
+ *                                the step's scalars read from device memory
+ *                                (CUDA-graph replay)
+ *   zero1_grad_norm_static       the norm without a caller workspace
+ * and around it zero1_shard_gather / zero1_shard_scatter, the model layout <->
+ * arena copies on either side of the data-parallel exchanges.
+ *
  * Conventions (all entry points):
  *   - Plain pointers and sizes only.  Device pointers are CUDA global-memory
  *     addresses on the current device; host pointers are ordinary memory.
