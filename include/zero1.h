@@ -15,7 +15,10 @@
  * numel into dp_size contiguous shards and lays the local shards out in one
  * flat "arena" per quantity.
  *
- * The same step in other shapes, each with the same results bit for bit:
+ * The same step in other shapes (the arena ones give the results of the
+ * three calls bit for bit; the list ones take the norm's partials per run of
+ * a shard, so their sum of squares can differ from the arena's in its last
+ * bits):
  *   zero1_accumulate_norm        the last micro-batch's pass and the norm together
  *   zero1_micro_norm,            one micro-batch: the norm from it, then the
  *   zero1_step_accumulate        step that writes the fp32 gradient it uses
