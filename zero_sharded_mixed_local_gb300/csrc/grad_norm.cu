@@ -64,8 +64,10 @@ __global__ void __launch_bounds__(kTileThreads)
 // Reads 2 bytes per element.  Bound by the fp32 pipe rather than DRAM (the compensated squares cost
 // about ten operations per element), so without a divisor a thread whose 64 values all square
 // exactly (bf16_squares_exact: integer checks on the raw bits) adds them without the residual term.
+// Five blocks per SM without the divisor (48 registers, a few spilled): 0.3256 ms on the 1.0B-element
+// shard against 0.3309 at four.
 template <bool kDivide>
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, kDivide ? 4 : 5)
     micro_sumsq_tiles_kernel(const uint16_t* __restrict__ micro, int64_t n_vec, float divisor,
                              float2* __restrict__ partials, int64_t first_tile) {
     pdl_enter();
